@@ -1,0 +1,475 @@
+"""Benchmark of the 4-bit decode mat-vec on the integer route.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--case NAME]
+
+One step = one pass of the whole hot path over one batch: quantise the f32
+activation to q8 blocks (xq_quantize_q8) and the Q4_K mat-vec (xq_matvec_q4k),
+inputs resident in HBM.  Default workload: the L2-exceeding vocabulary
+projection, Q4_K 128256 x 4096, batch 1 (W = 295.5 MB, larger than the 129 MB
+L2, so no flush is needed between steps).  Steps are replayed from CUDA graphs
+and timed with CUDA events on the launching stream.
+
+Prints ONE JSON line (rank 0): value = achieved GB/s of algorithmic bytes per
+step (all ranks), ms_per_step, a roofline object for the mat-vec kernel timed
+alone, the end-to-end figure through the public API with host buffers, the CPU
+oracle baseline, the SM clocks sampled during the timed region.
+
+--impl reference times the CPU oracle (the plain C reference implementation
+of the same method) on the host cores on a bounded row sample of the same
+workload; it is a deliberately slow baseline.
+
+Multi-GPU: replicas only (every rank runs the same single-GPU workload, no
+collective on the data path); under torchrun the timed region is bracketed by
+barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "achieved HBM GB/s and µs per 4-bit mat-vec (batch 1) vs ~8 TB/s GB300 roofline"
+DEFAULT_CASE = "c5_q4k_128256x4096_b1"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 1024 * 1024
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "matvec_q4k_traffic.json")
+
+
+# ---------------------------------------------------------------- helpers
+def step_bytes(c) -> dict:
+    """Algorithmic bytes: every weight byte once, the f32 activation read once,
+    the q8 blocks written once and read once, y written once."""
+    q8 = c.batch * (c.cols // 256) * 320
+    matvec = c.w_bytes + q8 + 4 * c.batch * c.rows
+    return {"matvec": matvec, "step": matvec + 4 * c.batch * c.cols + q8,
+            "weights": c.w_bytes}
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_decode_mat_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    with open(os.path.join(ROOT, "include", "xq.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_per_launch(case_name: str):
+    """DRAM bytes per mat-vec launch from a committed ncu capture, valid only
+    while the kernel sources are unchanged since the capture."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_digest") != source_digest():
+        return None
+    return rec.get("cases", {}).get(case_name)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons every 100 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples: list[tuple[float, list[str]]] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [v.strip() for v in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        window = [s for t, s in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        scope = "timed region"
+        if not window:
+            window = [s for _, s in self.samples]
+            scope = "whole run (timed region shorter than the sampling period)"
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        sm = [float(s[0]) for s in window if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in window if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in window for i in range(4)
+                          if len(s) > 4 + i and s[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(window), "scope": scope}
+
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, dist) -> float:
+    if dist is None:
+        return value
+    import torch
+    backend = dist.get_backend()
+    dev = "cuda" if backend == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+class OracleRunner:
+    """The CPU oracle as it stands (quantise + Q4_K/codebook mat-vec) on a row
+    sample of a workload, the rows split across a persistent pool of host
+    threads (the C oracle releases the GIL while it runs)."""
+
+    def __init__(self, c, rows: int, threads: int):
+        from concurrent.futures import ThreadPoolExecutor
+
+        import oracle
+        self.o = oracle.get()
+        self.c = c
+        self.rows = max(1, min(rows, c.rows))
+        seed = synthetic.seed_for(c.cfg, "W") + 2 * c.sub
+        W = (synthetic.q4k_weights(self.rows, c.cols, seed) if c.fmt == "q4k"
+             else synthetic.cb4_weights(self.rows, c.cols, seed))
+        self.kv = synthetic.cb4_table()
+        self.x = c.x()
+        self.parts = [np.ascontiguousarray(W[i::threads]) for i in range(threads)]
+        self.parts = [p for p in self.parts if p.shape[0]]
+        self.pool = ThreadPoolExecutor(max_workers=len(self.parts))
+
+    @property
+    def threads(self) -> int:
+        return len(self.parts)
+
+    def _mv(self, part, xq_ref):
+        c = self.c
+        if c.fmt == "q4k":
+            return self.o.matvec_q4k(part, xq_ref, part.shape[0], c.cols, c.batch)
+        return self.o.matvec_cb4(part, self.kv, xq_ref, part.shape[0], c.cols, c.batch)
+
+    def step(self):
+        xq_ref = self.o.quantize_q8(self.x)
+        for f in [self.pool.submit(self._mv, p, xq_ref) for p in self.parts]:
+            f.result()
+
+    def bytes_per_step(self) -> int:
+        c = self.c
+        q8 = c.batch * (c.cols // 256) * 320
+        w = self.rows * (c.cols // 256) * 144
+        return w + 4 * c.batch * c.cols + 2 * q8 + 4 * c.batch * self.rows
+
+    def close(self):
+        self.pool.shutdown()
+
+
+def calibrated_rows(c, threads: int, seconds_per_step: float) -> int:
+    """Rows per step so that one oracle step takes about seconds_per_step."""
+    probe = OracleRunner(c, 32 * threads, threads)
+    probe.step()
+    t0 = time.perf_counter()
+    probe.step()
+    dt = max(time.perf_counter() - t0, 1e-6)
+    probe.close()
+    rows = int(32 * threads * seconds_per_step / dt)
+    return max(threads, min(rows, c.rows))
+
+
+def oracle_rate(c, wall_budget_s: float, threads: int) -> dict:
+    """GB/s of the oracle over a bounded row sample (about wall_budget_s of
+    wall time on `threads` host threads)."""
+    rows = calibrated_rows(c, threads, wall_budget_s / 4)
+    r = OracleRunner(c, rows, threads)
+    r.step()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        r.step()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= wall_budget_s:
+            break
+    sec = el / n
+    out = {"value": r.bytes_per_step() / sec / 1e9, "unit": "GB/s", "cores": r.threads,
+           "kind": "oracle", "sec_per_pass": sec,
+           "sample": f"{r.rows} of {c.rows} rows x {c.cols} cols, batch {c.batch} (quantise + "
+                     f"mat-vec), {r.threads} host threads, {n} passes, {el:.1f} s wall"}
+    r.close()
+    return out
+
+
+def run_reference(args, c):
+    """The reference arm: the CPU oracle, rank 0 only."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    budget = 90.0  # seconds for warm-up + timed steps together
+    rows = calibrated_rows(c, threads, budget / (args.steps + args.warmup))
+    r = OracleRunner(c, rows, threads)
+    for _ in range(args.warmup):
+        r.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r.step()
+    sec = (time.perf_counter() - t0) / args.steps
+    value = r.bytes_per_step() / sec / 1e9
+    sample = (f"{r.rows} of {c.rows} rows x {c.cols} cols, batch {c.batch} per step "
+              f"(quantise + mat-vec), {r.threads} host threads")
+    r.close()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int64 dots + f64 scaling", "data": "synthetic",
+            "config": workload_config(c),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": r.threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(c) -> dict:
+    return {"workload": f"{c.name}: Q4_K {c.rows}x{c.cols} batch {c.batch}"
+                        if c.fmt == "q4k" else f"{c.name}: codebook {c.rows}x{c.cols} batch {c.batch}",
+            "format": c.fmt, "rows": c.rows, "cols": c.cols, "batch": c.batch,
+            "weight_bytes": c.w_bytes,
+            "step": "xq_quantize_q8 + xq_matvec_" + c.fmt,
+            "l2": f"inputs larger than L2 (W {c.w_bytes / 1e6:.1f} MB > 129 MB); no flush"
+                  if c.w_bytes > L2_BYTES else "W fits in L2: hot-L2 timing",
+            "parallelism": "replicas (one independent mat-vec per GPU)"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args, c):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = dist_init(world, "nccl")
+    import quantized_decode_mat_gb300 as xq
+
+    dev = torch.device("cuda", local)
+    W = torch.from_numpy(c.weights()).to(dev)
+    x_np = c.x()
+    x = torch.from_numpy(x_np).to(dev)
+    kv = synthetic.cb4_table()
+    nb = c.cols // 256
+    xq_buf = torch.empty((c.batch, nb, 320), dtype=torch.uint8, device=dev)
+    y = torch.empty((c.batch, c.rows), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def do_matvec():
+        if c.fmt == "q4k":
+            xq.matvec_q4k(W, xq_buf, c.rows, c.cols, out=y)
+        else:
+            xq.matvec_cb4(W, kv, xq_buf, c.rows, c.cols, out=y)
+
+    def do_step():
+        xq.quantize_q8(x, out=xq_buf)
+        do_matvec()
+
+    # eager warm-up: first call per device configures the kernels (before capture)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            do_step()
+    stream.synchronize()
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                fn()
+        return g
+
+    per_graph = max(1, min(args.steps, 100))
+    counts0 = [xq.launch_count(i) for i in range(5)]
+    g_step = capture(do_step, per_graph)
+    launches_per_step = sum(xq.launch_count(i) - counts0[i] for i in range(5)) / per_graph
+    rem = args.steps % per_graph
+    g_rem = capture(do_step, rem) if rem else None
+    g_mv = capture(do_matvec, per_graph)
+    g_mv_rem = capture(do_matvec, rem) if rem else None
+
+    def replay(g, g_r, k):
+        for _ in range(k // per_graph):
+            g.replay()
+        if k % per_graph:
+            g_r.replay()
+
+    # warm-up steps (untimed), then the timed region: exactly K steps
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // per_graph)):
+            g_step.replay()
+    stream.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        replay(g_step, g_rem, args.steps)
+        ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(dist)
+    step_ms = ev0.elapsed_time(ev1) / args.steps
+    step_ms_max = max_over_ranks(step_ms, dist)
+
+    # the mat-vec kernel alone (roofline): K launches, same stream
+    with torch.cuda.stream(stream):
+        g_mv.replay()
+        ev0.record(stream)
+        replay(g_mv, g_mv_rem, args.steps)
+        ev1.record(stream)
+    ev1.synchronize()
+    mv_ms = ev0.elapsed_time(ev1) / args.steps
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, time.time())
+
+    # end to end through the public API with pinned host buffers
+    x_host = torch.from_numpy(x_np).pin_memory()
+    y_host = torch.empty((c.batch, c.rows), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 2000))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            x.copy_(x_host, non_blocking=True)
+            do_step()
+            y_host.copy_(y, non_blocking=True)
+        stream.synchronize()
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            x.copy_(x_host, non_blocking=True)
+            do_step()
+            y_host.copy_(y, non_blocking=True)
+        ev1.record(stream)
+    ev1.synchronize()
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, dist)
+    status = xq.device_status(stream=stream)
+
+    if rank != 0:
+        return
+    nbytes = step_bytes(c)
+    value = world * nbytes["step"] / (step_ms_max * 1e-3) / 1e9
+    achieved = nbytes["matvec"] / (mv_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    cpu = oracle_rate(c, wall_budget_s=args.cpu_seconds, threads=os.cpu_count() or 1)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
+        "us_per_matvec": mv_ms * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8 dp4a (int32 sums) + f32 epilogue",
+        "data": "synthetic (seeded, shapes and distributions of the decode workloads)",
+        "config": workload_config(c),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy",
+                     "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
+                     "traffic": traffic_per_launch(c.name),
+                     "kernel": "xq_matvec_kernel<" + c.fmt + ", batch %d>" % c.batch,
+                     "algorithmic_bytes_per_launch": nbytes["matvec"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "h2d_bytes_per_step": 4 * c.batch * c.cols,
+                "d2h_bytes_per_step": 4 * c.batch * c.rows,
+                "path": "pinned x -> cudaMemcpyAsync -> xq_quantize_q8 -> xq_matvec -> "
+                        "cudaMemcpyAsync -> pinned y, eager calls through the Python binding"},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "launches_per_step": launches_per_step,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--case", default=DEFAULT_CASE, choices=sorted(synthetic.CASES))
+    ap.add_argument("--cpu-seconds", type=float, default=2.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    c = synthetic.CASES[args.case]
+    if args.impl == "reference":
+        run_reference(args, c)
+    else:
+        run_ours(args, c)
+
+
+if __name__ == "__main__":
+    main()

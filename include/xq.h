@@ -1,0 +1,166 @@
+/*
+ * xq.h -- C ABI of the GB300 (sm_103a) 4-bit decode mat-vec library.
+ *
+ * y = W . x for one to eight activation vectors, with W block-quantised to 4
+ * bits and x quantised once per call to q8 blocks, so that every block's dot
+ * product is integer arithmetic and is scaled to float afterwards.  Two
+ * weight formats:
+ *
+ *   Q4_K super-block, 144 bytes per 256 weights (row-major, rows contiguous):
+ *     +0  f16 d            +2  f16 dmin
+ *     +4  12 bytes: eight 6-bit scales sc_s and eight 6-bit mins m_s
+ *         (bytes 0..3: sc_0..3 in the low 6 bits, the top 2 bits of
+ *          sc_4..7; bytes 4..7: m_0..3 likewise with m_4..7; bytes 8..11:
+ *          low nibble = low 4 bits of sc_4..7, high nibble = of m_4..7)
+ *     +16 128 nibble bytes: group g (0..3) = bytes 16+32g..16+32g+31; the
+ *         low nibbles are sub-block 2g, the high nibbles sub-block 2g+1
+ *     weight value w = d*sc_s*q - dmin*m_s (never formed on this route)
+ *     Source: super-block stride 144 and group offset 16+32g, "cajeta.xpu -
+ *     one kernel, any device" section 2.3; the field layout is the Q4_K
+ *     block of the decode workload.
+ *
+ *   Nonlinear 4-bit codebook block, 18 bytes per 32 weights:
+ *     +0 f16 d, +2 16 payload bytes; element j < 16 is kv[qs[j] & 15],
+ *     element j >= 16 is kv[qs[j-16] >> 4]; kv is a 16-entry int8 table.
+ *     Source: "25 - Writing XPU Kernels" section 25.2.1.
+ *
+ *   q8 activation block, 320 bytes per 256 values ("25 - Writing XPU
+ *   Kernels" section 25.2): +0 int8 q[256], +256 int32 sums of each
+ *   32-value sub-block, +288 f32 scale, +292..319 zero.
+ *
+ * Conventions for every entry point
+ *   - Pointers named W, xq, x, y, dots are DEVICE pointers owned by the
+ *     caller; `table` is a HOST pointer read during the call (copied by
+ *     value into the launch).  The library allocates no device memory and
+ *     keeps no state beyond launch counters, the last launch plan of the
+ *     calling thread, a per-device status word and per-thread error text.
+ *   - Layouts are row-major; x is [batch][cols] f32, xq is
+ *     [batch][cols/256][320 B], y is [batch][rows] f32, fully overwritten.
+ *   - Preconditions, all checked on the host before any CUDA call:
+ *     cols > 0 and cols % 256 == 0; 1 <= rows <= 2^31-1; 1 <= batch <= 8;
+ *     W, xq, x 16-byte aligned; y and dots 4-byte aligned; outputs must not
+ *     overlap inputs.  A violation returns XQ_EINVAL / XQ_EALIGN / XQ_ESHAPE
+ *     and launches nothing.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     compute entry point is asynchronous on it: the return code covers
+ *     argument checks and the launch only.  Nothing here synchronises except
+ *     xq_device_status.  No kernel traps or asserts; a bounded wait that
+ *     times out sets the device status word (see xq_device_status).
+ *   - The first call on a device configures the kernels for that device;
+ *     make one call per device before capturing a stream into a CUDA graph.
+ */
+#ifndef XQ_H
+#define XQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    XQ_OK = 0,
+    XQ_EINVAL = 1,  /* null pointer, overlapping buffers, bad argument      */
+    XQ_EALIGN = 2,  /* a base address is not aligned as required          */
+    XQ_ESHAPE = 3,  /* rows, cols or batch out of range                     */
+    XQ_ELAUNCH = 4, /* the CUDA runtime refused a query or the launch       */
+    XQ_EDEVICE = 5  /* the device status word reports a kernel-side error   */
+} xq_status;
+
+/* Bytes of the q8 blocks for `batch` vectors of `cols` values; 0 if the
+ * shape is invalid.  = batch * (cols/256) * 320. */
+size_t xq_q8_bytes(int64_t cols, int64_t batch);
+/* Bytes of a Q4_K matrix: rows * (cols/256) * 144; 0 if invalid. */
+size_t xq_q4k_bytes(int64_t rows, int64_t cols);
+/* Bytes of a codebook matrix: rows * (cols/32) * 18; 0 if invalid. */
+size_t xq_cb4_bytes(int64_t rows, int64_t cols);
+
+/* Quantise x ([batch][cols] f32, device) into q8 blocks xq (device,
+ * xq_q8_bytes(cols, batch) bytes), one 256-value block at a time:
+ * amax = max|x|; d = amax/127; q = round-half-even(x * (127/amax)) clamped
+ * to [-127, 127] (all in f32 with one rounding per operation); an all-zero
+ * block gets d = 0, q = 0; the eight 32-value sums are stored exactly.
+ * Source: "25 - Writing XPU Kernels" section 25.2 (the q8_K block: quantise
+ * the activation once, 256 int8 values, eight sums, one f32 scale); the
+ * scale and rounding rule are this library's reading (the page names no
+ * rule). */
+xq_status xq_quantize_q8(const float *x, void *xq, int64_t cols, int64_t batch, void *stream);
+
+/* y[b][r] = sum over super-blocks k of xs_{b,k} * (d_{r,k} * sum_s sc_s*dot_s
+ *           - dmin_{r,k} * sum_s m_s*bsum_{b,k,s}),
+ * dot_s = sum of 32 (unsigned nibble x signed int8) products, exact.
+ * W: Q4_K rows (device, xq_q4k_bytes(rows, cols)), xq: q8 blocks of the
+ * batch, y: [batch][rows] f32.  Integer dots are exact; the float epilogue
+ * carries a compensation term so y is within a few f32 ulps of the exact
+ * value.  Source: "25 - Writing XPU Kernels" sections 25.2 (integer route,
+ * reduce first then scale once) and 25.5 (the Q4_K mat-vec as 16-byte
+ * vector loads and dp4a); "cajeta.xpu - one kernel, any device" 2.3. */
+xq_status xq_matvec_q4k(const void *W, const void *xq, float *y, int64_t rows, int64_t cols,
+                        int64_t batch, void *stream);
+
+/* y[b][r] = sum over blocks k of d_{r,k} * xs_{b,k/8} * dot_k,
+ * dot_k = sum_j kv[nibble_j] * xq_{b, 32k+j} (signed x signed, exact).
+ * table: HOST pointer to the 16 int8 codebook values, read during the call.
+ * Source: "25 - Writing XPU Kernels" section 25.2.1 (the integer codebook
+ * decode wave: the codebook maps a nibble to int8, one float multiply per
+ * block after the integer dot). */
+xq_status xq_matvec_cb4(const void *W, const int8_t *table, const void *xq, float *y,
+                        int64_t rows, int64_t cols, int64_t batch, void *stream);
+
+/* Test exports: the exact per-sub-block integer dots of the same kernels.
+ * dots: [batch][rows][cols/32] int32 (device).  Q4_K: dots[b][r][8k+s] is
+ * dot_s of super-block k; codebook: dots[b][r][k] is dot_k of block k. */
+xq_status xq_subdots_q4k(const void *W, const void *xq, int32_t *dots, int64_t rows,
+                         int64_t cols, int64_t batch, void *stream);
+xq_status xq_subdots_cb4(const void *W, const int8_t *table, const void *xq, int32_t *dots,
+                         int64_t rows, int64_t cols, int64_t batch, void *stream);
+
+/* Launch plan of the mat-vec kernels (pure host computation; needs no GPU).
+ * sm_count and smem_optin_bytes describe the device (for GB300: 152 SMs,
+ * 232448 bytes).  warps: warps per CTA, each owning a pipeline of `stages`
+ * 4608-byte TMA stages; grid: persistent CTAs; tiles: 32-row tiles. */
+typedef struct {
+    int32_t warps;
+    int32_t stages;
+    int32_t grid;
+    int32_t tiles;
+    int32_t chunks_per_row;
+    int32_t reserved;
+    int64_t smem_bytes;
+} xq_plan;
+
+xq_status xq_plan_matvec(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
+                         int64_t smem_optin_bytes, xq_plan *plan);
+/* Override the automatic plan for sweeps: warps (1..8) and stages (2..16),
+ * 0 = automatic.  Process-wide; not for concurrent use with launches. */
+void xq_set_plan_override(int32_t warps, int32_t stages);
+/* Plan used by the calling thread's last mat-vec or sub-dot launch. */
+xq_status xq_last_plan(xq_plan *plan);
+
+/* Launch counters (process-wide, monotonic) per kernel family. */
+enum {
+    XQ_COUNT_QUANTIZE = 0,
+    XQ_COUNT_MATVEC_Q4K = 1,
+    XQ_COUNT_MATVEC_CB4 = 2,
+    XQ_COUNT_SUBDOTS_Q4K = 3,
+    XQ_COUNT_SUBDOTS_CB4 = 4,
+    XQ_COUNT_N = 5
+};
+uint64_t xq_launch_count(int32_t which);
+
+/* Read (and optionally clear) the current device's status word.  It is 0
+ * unless a kernel's bounded wait timed out (bit 0).  SYNCHRONISES `stream`
+ * (a device-to-host copy of 4 bytes). */
+xq_status xq_device_status(uint32_t *out, int32_t clear, void *stream);
+
+const char *xq_status_string(xq_status s);
+/* Detail text of the calling thread's last failed call ("" if none). */
+const char *xq_last_error(void);
+/* ABI version: 1. */
+int32_t xq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* XQ_H */

@@ -1,0 +1,39 @@
+"""GB300 (sm_103a) 4-bit decode mat-vec on the integer route.
+
+Thin Python binding over the C ABI in ``include/xq.h`` (``_build/libxq.so``):
+argument marshalling only.  Every step of the path runs in the library's
+CUDA kernels; PyTorch supplies device memory and streams.  There is no CPU
+fallback: if the library is missing this package raises on import.
+
+    xq  = quantize_q8(x)                       # x: f32 [batch, cols] on cuda
+    y   = matvec_q4k(W, xq, rows, cols)        # W: uint8 Q4_K rows on cuda
+    y   = matvec_cb4(W, table, xq, rows, cols) # W: uint8 codebook rows
+"""
+from __future__ import annotations
+
+from . import _native
+from ._native import (  # noqa: F401
+    COUNT_MATVEC_CB4,
+    COUNT_MATVEC_Q4K,
+    COUNT_QUANTIZE,
+    COUNT_SUBDOTS_CB4,
+    COUNT_SUBDOTS_Q4K,
+    XQError,
+    cb4_bytes,
+    device_status,
+    last_plan,
+    launch_count,
+    lib_path,
+    matvec_cb4,
+    matvec_q4k,
+    plan_matvec,
+    q4k_bytes,
+    q8_bytes,
+    quantize_q8,
+    set_plan_override,
+    subdots_cb4,
+    subdots_q4k,
+)
+
+__all__ = [n for n in dir(_native) if not n.startswith("_") and n not in ("ctypes", "os",
+                                                                         "np", "torch")]

@@ -1,0 +1,212 @@
+"""ctypes marshalling for libxq.so (the C ABI declared in include/xq.h)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libxq.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"the CUDA library {_LIB_PATH} is missing; build it first "
+        "(python -m quantized_decode_mat_gb300.build, or __graft_entry__.build())")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+_P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [("warps", ctypes.c_int32), ("stages", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("tiles", ctypes.c_int32), ("chunks_per_row", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("smem_bytes", ctypes.c_int64)]
+
+
+def _sig(name, restype, argtypes):
+    fn = getattr(_lib, name)
+    fn.restype = restype
+    fn.argtypes = argtypes
+    return fn
+
+
+_q8_bytes = _sig("xq_q8_bytes", _SZ, [_I64, _I64])
+_q4k_bytes = _sig("xq_q4k_bytes", _SZ, [_I64, _I64])
+_cb4_bytes = _sig("xq_cb4_bytes", _SZ, [_I64, _I64])
+_quantize = _sig("xq_quantize_q8", ctypes.c_int, [_P, _P, _I64, _I64, _P])
+_matvec_q4k = _sig("xq_matvec_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
+_matvec_cb4 = _sig("xq_matvec_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
+_subdots_q4k = _sig("xq_subdots_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
+_subdots_cb4 = _sig("xq_subdots_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
+_plan = _sig("xq_plan_matvec", ctypes.c_int, [_I64, _I64, _I64, _I32, _I64,
+                                             ctypes.POINTER(_Plan)])
+_set_override = _sig("xq_set_plan_override", None, [_I32, _I32])
+_last_plan = _sig("xq_last_plan", ctypes.c_int, [ctypes.POINTER(_Plan)])
+_launch_count = _sig("xq_launch_count", ctypes.c_uint64, [_I32])
+_device_status = _sig("xq_device_status", ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32),
+                                                        _I32, _P])
+_status_string = _sig("xq_status_string", ctypes.c_char_p, [ctypes.c_int])
+_last_error = _sig("xq_last_error", ctypes.c_char_p, [])
+_version = _sig("xq_version", _I32, [])
+
+COUNT_QUANTIZE, COUNT_MATVEC_Q4K, COUNT_MATVEC_CB4, COUNT_SUBDOTS_Q4K, COUNT_SUBDOTS_CB4 = range(5)
+
+
+class XQError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        self.detail = detail
+        super().__init__(f"{_status_string(status).decode()}: {detail}")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise XQError(status, (_last_error() or b"").decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _table(table) -> ctypes.Array:
+    kv = np.asarray(table.cpu() if isinstance(table, torch.Tensor) else table)
+    if kv.size != 16:
+        raise ValueError("the codebook table must have 16 entries")
+    kv = kv.astype(np.int8).reshape(16)
+    return (ctypes.c_int8 * 16)(*[int(v) for v in kv])
+
+
+def q8_bytes(cols: int, batch: int = 1) -> int:
+    return int(_q8_bytes(cols, batch))
+
+
+def q4k_bytes(rows: int, cols: int) -> int:
+    return int(_q4k_bytes(rows, cols))
+
+
+def cb4_bytes(rows: int, cols: int) -> int:
+    return int(_cb4_bytes(rows, cols))
+
+
+def quantize_q8(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """x: f32 [batch, cols] (or [cols]) on CUDA -> uint8 [batch, cols/256, 320]."""
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    batch, cols = x.shape
+    if out is None:
+        out = torch.empty((batch, max(cols // 256, 0), 320), dtype=torch.uint8, device=x.device)
+    _check(_quantize(_dev(x, "x", torch.float32), _dev(out, "xq", torch.uint8), cols, batch,
+                     _stream(stream)))
+    return out
+
+
+def _batch_of(xq: torch.Tensor, cols: int) -> int:
+    per = q8_bytes(cols, 1)
+    if per == 0 or xq.numel() % per:
+        raise ValueError("xq size does not match cols")
+    return xq.numel() // per
+
+
+def matvec_q4k(W: torch.Tensor, xq: torch.Tensor, rows: int, cols: int,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[b, r] for Q4_K rows W (uint8, CUDA) and q8 blocks xq -> f32 [batch, rows]."""
+    batch = _batch_of(xq, cols)
+    if out is None:
+        out = torch.empty((batch, rows), dtype=torch.float32, device=xq.device)
+    _check(_matvec_q4k(_dev(W, "W", torch.uint8), _dev(xq, "xq", torch.uint8),
+                       _dev(out, "y", torch.float32), rows, cols, batch, _stream(stream)))
+    return out
+
+
+def matvec_cb4(W: torch.Tensor, table, xq: torch.Tensor, rows: int, cols: int,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[b, r] for codebook rows W with a host 16-entry int8 table."""
+    batch = _batch_of(xq, cols)
+    if out is None:
+        out = torch.empty((batch, rows), dtype=torch.float32, device=xq.device)
+    _check(_matvec_cb4(_dev(W, "W", torch.uint8), ctypes.cast(_table(table), _P),
+                       _dev(xq, "xq", torch.uint8), _dev(out, "y", torch.float32), rows, cols,
+                       batch, _stream(stream)))
+    return out
+
+
+def subdots_q4k(W: torch.Tensor, xq: torch.Tensor, rows: int, cols: int,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Exact per-sub-block int32 dots, [batch, rows, cols/32]."""
+    batch = _batch_of(xq, cols)
+    if out is None:
+        out = torch.empty((batch, rows, cols // 32), dtype=torch.int32, device=xq.device)
+    _check(_subdots_q4k(_dev(W, "W", torch.uint8), _dev(xq, "xq", torch.uint8),
+                        _dev(out, "dots", torch.int32), rows, cols, batch, _stream(stream)))
+    return out
+
+
+def subdots_cb4(W: torch.Tensor, table, xq: torch.Tensor, rows: int, cols: int,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    batch = _batch_of(xq, cols)
+    if out is None:
+        out = torch.empty((batch, rows, cols // 32), dtype=torch.int32, device=xq.device)
+    _check(_subdots_cb4(_dev(W, "W", torch.uint8), ctypes.cast(_table(table), _P),
+                        _dev(xq, "xq", torch.uint8), _dev(out, "dots", torch.int32), rows, cols,
+                        batch, _stream(stream)))
+    return out
+
+
+def _plan_dict(p: _Plan) -> dict:
+    return {f: getattr(p, f) for f, _ in _Plan._fields_ if f != "reserved"}
+
+
+def plan_matvec(rows: int, cols: int, batch: int = 1, sm_count: int = 152,
+                smem_optin: int = 232448) -> dict:
+    """Host-only launch plan (no GPU needed)."""
+    p = _Plan()
+    _check(_plan(rows, cols, batch, sm_count, smem_optin, ctypes.byref(p)))
+    return _plan_dict(p)
+
+
+def last_plan() -> dict:
+    p = _Plan()
+    _check(_last_plan(ctypes.byref(p)))
+    return _plan_dict(p)
+
+
+def set_plan_override(warps: int = 0, stages: int = 0) -> None:
+    _set_override(warps, stages)
+
+
+def launch_count(which: int) -> int:
+    return int(_launch_count(which))
+
+
+def device_status(clear: bool = False, stream=None) -> int:
+    """Device status word (0 = fine); synchronises the stream."""
+    v = ctypes.c_uint32(0)
+    st = _device_status(ctypes.byref(v), int(clear), _stream(stream))
+    if st not in (0, 5):
+        _check(st)
+    return int(v.value)
+
+
+def version() -> int:
+    return int(_version())

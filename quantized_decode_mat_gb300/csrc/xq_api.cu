@@ -1,0 +1,411 @@
+// C ABI of the decode mat-vec library: argument checks, per-device set-up,
+// TMA descriptor encoding, launch planning, and the q8 activation quantiser.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "xq_internal.h"
+
+namespace xq {
+
+// Device status word: bit 0 = a bounded wait timed out (see xq_ptx.cuh).
+__device__ uint32_t g_status_word;
+
+// ---- q8 activation quantiser ------------------------------------------------------
+// One warp per 256-value block; lane l holds values 8l..8l+7, so lanes 4s..4s+3
+// hold sub-block s.  Rule (one f32 rounding per operation, no contraction):
+//   amax = max|x|; iscale = 127/amax; q = clamp(rint(x*iscale), -127, 127)
+//   (round half to even; a NaN product gives 0); d = amax/127; zero block ->
+//   d = 0, q = 0.  The eight 32-value sums are exact int32.
+// Source: "25 - Writing XPU Kernels" 25.2 (q8_K: 256 int8 values, eight
+// sub-block sums at +256, one f32 scale at +288, 320 bytes).
+__global__ void __launch_bounds__(256) q8_quantize_kernel(const float *__restrict__ x,
+                                                          uint8_t *__restrict__ xq,
+                                                          int64_t nblocks) {
+    const int64_t blk = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (blk >= nblocks) return;  // whole warps leave together
+    const float4 *src = reinterpret_cast<const float4 *>(x + blk * 256 + lane * 8);
+    const float4 u = __ldg(src), v = __ldg(src + 1);
+    const float vals[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float t = fabsf(vals[i]);
+        amax = t > amax ? t : amax;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, amax, off);
+        amax = o > amax ? o : amax;
+    }
+    int q[8];
+    if (amax == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = 0;
+    } else {
+        const float iscale = __fdiv_rn(127.0f, amax);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float t = __fmul_rn(vals[i], iscale);
+            int r;
+            if (t != t)
+                r = 0;
+            else if (t >= 127.0f)
+                r = 127;
+            else if (t <= -127.0f)
+                r = -127;
+            else
+                r = __float2int_rn(t);  // round half to even
+            q[i] = r;
+        }
+    }
+    uint8_t *out = xq + blk * kQ8Bytes;
+    uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        w0 |= (uint32_t)(q[i] & 0xFF) << (8 * i);
+        w1 |= (uint32_t)(q[4 + i] & 0xFF) << (8 * i);
+    }
+    *reinterpret_cast<uint2 *>(out + lane * 8) = make_uint2(w0, w1);
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum += q[i];
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    if ((lane & 3) == 0) *reinterpret_cast<int *>(out + kQ8SumAt + (lane >> 2) * 4) = sum;
+    if (lane == 0) {
+        const float d = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, 127.0f);
+        *reinterpret_cast<float *>(out + kQ8ScaleAt) = d;
+    } else if (lane < 8) {
+        *reinterpret_cast<uint32_t *>(out + kQ8ScaleAt + 4 * lane) = 0u;  // bytes 292..319
+    }
+}
+
+namespace {
+
+thread_local std::string t_error;
+thread_local xq_plan t_last_plan;
+thread_local bool t_have_plan = false;
+std::atomic<uint64_t> g_counts[XQ_COUNT_N];
+std::atomic<int32_t> g_override_warps{0};
+std::atomic<int32_t> g_override_stages{0};
+
+xq_status fail(xq_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+xq_status fail(xq_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_error = buf;
+    return s;
+}
+
+xq_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(XQ_ELAUNCH, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return na && nb && a0 < b0 + nb && b0 < a0 + na;
+}
+
+xq_status check_shape(int64_t rows, int64_t cols, int64_t batch, bool need_rows) {
+    if (cols <= 0 || cols % 256 != 0)
+        return fail(XQ_ESHAPE, "cols=%lld must be a positive multiple of 256", (long long)cols);
+    if (cols > (int64_t)1 << 24)
+        return fail(XQ_ESHAPE, "cols=%lld exceeds 2^24", (long long)cols);
+    if (batch < 1 || batch > 8)
+        return fail(XQ_ESHAPE, "batch=%lld must be in 1..8", (long long)batch);
+    if (need_rows && (rows < 1 || rows > 0x7FFFFFFFLL))
+        return fail(XQ_ESHAPE, "rows=%lld must be in 1..2^31-1", (long long)rows);
+    return XQ_OK;
+}
+
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    const char *what = "";
+    int sm_count = 0;
+    int smem_optin = 0;
+    uint32_t *status = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+
+// Per-device set-up on the first call with that device current: device
+// attributes, the status word's device address, and the kernels' dynamic
+// shared memory limit.
+xq_status device_state(DeviceState **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(XQ_ELAUNCH, "device %d out of range", dev);
+    DeviceState &st = g_dev[dev];
+    std::call_once(st.once, [&st, dev]() {
+        auto step = [&st](cudaError_t r, const char *what) {
+            if (st.err == cudaSuccess && r != cudaSuccess) {
+                st.err = r;
+                st.what = what;
+            }
+        };
+        step(cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev),
+             "cudaDeviceGetAttribute(MultiProcessorCount)");
+        step(cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
+             "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)");
+        void *p = nullptr;
+        step(cudaGetSymbolAddress(&p, g_status_word), "cudaGetSymbolAddress(status word)");
+        st.status = static_cast<uint32_t *>(p);
+        if (st.err == cudaSuccess) step(configure_matvec_q4k(st.smem_optin), "configure Q4_K kernels");
+        if (st.err == cudaSuccess) step(configure_matvec_cb4(st.smem_optin), "configure codebook kernels");
+    });
+    if (st.err != cudaSuccess) return cuda_fail(st.err, st.what);
+    *out = &st;
+    return XQ_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+xq_status encode_rows(CUtensorMap *tmap, const void *W, int64_t rows, int64_t row_bytes) {
+    std::call_once(g_encode_once, []() {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+            g_encode_err = cudaErrorSymbolNotFound;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode_err != cudaSuccess || g_encode == nullptr)
+        return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled entry point");
+    // W viewed as a 2-D byte matrix [rows][row_bytes]; box = 144 bytes x 32 rows.
+    const cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)kChunkBytes, (cuuint32_t)kTileRows};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = g_encode(tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W),
+                               gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(XQ_ELAUNCH, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return XQ_OK;
+}
+
+xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
+                    int64_t smem_optin, xq_plan *p) {
+    const int32_t nb = (int32_t)(cols / 256);
+    int32_t W = nb < kMaxWarps ? nb : kMaxWarps;
+    const int32_t ow = g_override_warps.load(), os = g_override_stages.load();
+    if (ow > 0) W = ow < nb ? ow : nb;
+    if (W > kMaxWarps) W = kMaxWarps;
+    int32_t S = os > 0 ? os : 4;
+    if (S < 2) S = 2;
+    if (S > kMaxStages) S = kMaxStages;
+    const int64_t partials = 2LL * W * batch * 32 * 8;
+    auto bytes = [&](int32_t s) { return (int64_t)W * s * (kStageBytes + 8) + partials + 128; };
+    while (bytes(S) > smem_optin && S > 2) --S;
+    if (bytes(S) > smem_optin)
+        return fail(XQ_ESHAPE, "plan needs %lld bytes of shared memory, device allows %lld",
+                    (long long)bytes(S), (long long)smem_optin);
+    const int64_t tiles = (rows + kTileRows - 1) / kTileRows;
+    p->warps = W;
+    p->stages = S;
+    p->tiles = (int32_t)tiles;
+    p->grid = (int32_t)(tiles < sm_count ? tiles : sm_count);
+    p->chunks_per_row = nb;
+    p->reserved = 0;
+    p->smem_bytes = bytes(S);
+    return XQ_OK;
+}
+
+enum class Op { kMatvecQ4K, kMatvecCB4, kDotsQ4K, kDotsCB4 };
+
+xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *xq, void *out,
+                     int64_t rows, int64_t cols, int64_t batch, void *stream) {
+    const bool cb4 = (op == Op::kMatvecCB4 || op == Op::kDotsCB4);
+    const bool dots = (op == Op::kDotsQ4K || op == Op::kDotsCB4);
+    t_error.clear();
+    if (!W || !xq || !out) return fail(XQ_EINVAL, "null device pointer (W, xq or output)");
+    if (cb4 && !table) return fail(XQ_EINVAL, "null codebook table");
+    if (xq_status s = check_shape(rows, cols, batch, true)) return s;
+    if (!aligned(W, 16)) return fail(XQ_EALIGN, "W must be 16-byte aligned");
+    if (!aligned(xq, 16)) return fail(XQ_EALIGN, "xq must be 16-byte aligned");
+    if (!aligned(out, dots ? 16 : 4))
+        return fail(XQ_EALIGN, dots ? "dots must be 16-byte aligned" : "y must be 4-byte aligned");
+    const int64_t nb = cols / 256;
+    const size_t w_bytes = (size_t)rows * nb * kChunkBytes;
+    const size_t x_bytes = (size_t)batch * nb * kQ8Bytes;
+    const size_t o_bytes = (size_t)batch * rows * (dots ? nb * 8 * 4 : 4);
+    if (overlap(out, o_bytes, W, w_bytes) || overlap(out, o_bytes, xq, x_bytes))
+        return fail(XQ_EINVAL, "output overlaps an input");
+
+    DeviceState *dev = nullptr;
+    if (xq_status s = device_state(&dev)) return s;
+    xq_plan plan;
+    if (xq_status s = make_plan(rows, cols, batch, dev->sm_count, dev->smem_optin, &plan)) return s;
+    CUtensorMap tmap;
+    if (xq_status s = encode_rows(&tmap, W, rows, nb * kChunkBytes)) return s;
+
+    MatvecArgs a;
+    memset(&a, 0, sizeof a);
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.y = dots ? nullptr : static_cast<float *>(out);
+    a.dots = dots ? static_cast<int32_t *>(out) : nullptr;
+    a.status = dev->status;
+    a.rows = rows;
+    a.nb = (int32_t)nb;
+    a.ntiles = plan.tiles;
+    a.stages = plan.stages;
+    if (cb4) {
+        for (int i = 0; i < 4; ++i) {
+            uint32_t w = 0;
+            for (int j = 0; j < 4; ++j) w |= (uint32_t)(uint8_t)table[4 * i + j] << (8 * j);
+            a.kv[i] = w;
+        }
+    }
+    const dim3 grid(plan.grid), block(plan.warps * 32);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cb4 ? launch_matvec_cb4(tmap, a, (int)batch, dots, grid, block,
+                                            (size_t)plan.smem_bytes, s)
+                        : launch_matvec_q4k(tmap, a, (int)batch, dots, grid, block,
+                                            (size_t)plan.smem_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mat-vec launch");
+    t_last_plan = plan;
+    t_have_plan = true;
+    const int which = op == Op::kMatvecQ4K  ? XQ_COUNT_MATVEC_Q4K
+                      : op == Op::kMatvecCB4 ? XQ_COUNT_MATVEC_CB4
+                      : op == Op::kDotsQ4K   ? XQ_COUNT_SUBDOTS_Q4K
+                                             : XQ_COUNT_SUBDOTS_CB4;
+    g_counts[which].fetch_add(1, std::memory_order_relaxed);
+    return XQ_OK;
+}
+
+}  // namespace
+}  // namespace xq
+
+using namespace xq;
+
+extern "C" {
+
+size_t xq_q8_bytes(int64_t cols, int64_t batch) {
+    if (cols <= 0 || cols % 256 || batch < 1) return 0;
+    return (size_t)batch * (size_t)(cols / 256) * kQ8Bytes;
+}
+
+size_t xq_q4k_bytes(int64_t rows, int64_t cols) {
+    if (cols <= 0 || cols % 256 || rows < 0) return 0;
+    return (size_t)rows * (size_t)(cols / 256) * kQ4kBytes;
+}
+
+size_t xq_cb4_bytes(int64_t rows, int64_t cols) {
+    if (cols <= 0 || cols % 256 || rows < 0) return 0;
+    return (size_t)rows * (size_t)(cols / 32) * kCb4Bytes;
+}
+
+xq_status xq_quantize_q8(const float *x, void *xq_out, int64_t cols, int64_t batch, void *stream) {
+    t_error.clear();
+    if (!x || !xq_out) return fail(XQ_EINVAL, "null device pointer (x or xq)");
+    if (xq_status s = check_shape(0, cols, batch, false)) return s;
+    if (!aligned(x, 16)) return fail(XQ_EALIGN, "x must be 16-byte aligned");
+    if (!aligned(xq_out, 16)) return fail(XQ_EALIGN, "xq must be 16-byte aligned");
+    const int64_t nblocks = batch * (cols / 256);
+    if (overlap(xq_out, (size_t)nblocks * kQ8Bytes, x, (size_t)batch * cols * 4))
+        return fail(XQ_EINVAL, "xq overlaps x");
+    DeviceState *dev = nullptr;
+    if (xq_status s = device_state(&dev)) return s;
+    const unsigned grid = (unsigned)((nblocks + 7) / 8);
+    q8_quantize_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        x, static_cast<uint8_t *>(xq_out), nblocks);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
+    g_counts[XQ_COUNT_QUANTIZE].fetch_add(1, std::memory_order_relaxed);
+    return XQ_OK;
+}
+
+xq_status xq_matvec_q4k(const void *W, const void *xq_in, float *y, int64_t rows, int64_t cols,
+                        int64_t batch, void *stream) {
+    return run_matvec(Op::kMatvecQ4K, W, nullptr, xq_in, y, rows, cols, batch, stream);
+}
+
+xq_status xq_matvec_cb4(const void *W, const int8_t *table, const void *xq_in, float *y,
+                        int64_t rows, int64_t cols, int64_t batch, void *stream) {
+    return run_matvec(Op::kMatvecCB4, W, table, xq_in, y, rows, cols, batch, stream);
+}
+
+xq_status xq_subdots_q4k(const void *W, const void *xq_in, int32_t *dots, int64_t rows,
+                         int64_t cols, int64_t batch, void *stream) {
+    return run_matvec(Op::kDotsQ4K, W, nullptr, xq_in, dots, rows, cols, batch, stream);
+}
+
+xq_status xq_subdots_cb4(const void *W, const int8_t *table, const void *xq_in, int32_t *dots,
+                         int64_t rows, int64_t cols, int64_t batch, void *stream) {
+    return run_matvec(Op::kDotsCB4, W, table, xq_in, dots, rows, cols, batch, stream);
+}
+
+xq_status xq_plan_matvec(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
+                         int64_t smem_optin_bytes, xq_plan *plan) {
+    t_error.clear();
+    if (!plan) return fail(XQ_EINVAL, "null plan");
+    if (xq_status s = check_shape(rows, cols, batch, true)) return s;
+    if (sm_count < 1) return fail(XQ_EINVAL, "sm_count must be positive");
+    return make_plan(rows, cols, batch, sm_count, smem_optin_bytes, plan);
+}
+
+void xq_set_plan_override(int32_t warps, int32_t stages) {
+    g_override_warps.store(warps < 0 ? 0 : warps);
+    g_override_stages.store(stages < 0 ? 0 : stages);
+}
+
+xq_status xq_last_plan(xq_plan *plan) {
+    if (!plan) return fail(XQ_EINVAL, "null plan");
+    if (!t_have_plan) return fail(XQ_EINVAL, "no mat-vec launched on this thread yet");
+    *plan = t_last_plan;
+    return XQ_OK;
+}
+
+uint64_t xq_launch_count(int32_t which) {
+    if (which < 0 || which >= XQ_COUNT_N) return 0;
+    return g_counts[which].load(std::memory_order_relaxed);
+}
+
+xq_status xq_device_status(uint32_t *out, int32_t clear, void *stream) {
+    t_error.clear();
+    if (!out) return fail(XQ_EINVAL, "null output");
+    DeviceState *dev = nullptr;
+    if (xq_status s = device_state(&dev)) return s;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(out, dev->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && clear) e = cudaMemsetAsync(dev->status, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess && clear) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    return *out ? XQ_EDEVICE : XQ_OK;
+}
+
+const char *xq_status_string(xq_status s) {
+    switch (s) {
+        case XQ_OK: return "XQ_OK";
+        case XQ_EINVAL: return "XQ_EINVAL: invalid argument";
+        case XQ_EALIGN: return "XQ_EALIGN: misaligned base address";
+        case XQ_ESHAPE: return "XQ_ESHAPE: shape out of range";
+        case XQ_ELAUNCH: return "XQ_ELAUNCH: CUDA runtime error";
+        case XQ_EDEVICE: return "XQ_EDEVICE: device status word set";
+    }
+    return "unknown xq_status";
+}
+
+const char *xq_last_error(void) { return t_error.c_str(); }
+
+int32_t xq_version(void) { return 1; }
+
+}  // extern "C"

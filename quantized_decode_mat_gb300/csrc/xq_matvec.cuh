@@ -1,0 +1,382 @@
+// Persistent TMA-pipelined decode mat-vec for sm_103a, templated on the weight
+// format, the batch (1..8) and whether it also emits the exact integer dots.
+//
+// Mapping (GB300-first; the guide's kernels put one wave on one row and let
+// lanes take consecutive blocks of that row, "25 - Writing XPU Kernels"
+// 25.2 / 25.2.1):
+//   * A row is a run of 256-weight chunks, 144 bytes each in both formats (one
+//     Q4_K super-block, or eight 18-byte codebook blocks).  Chunk c pairs with
+//     q8 activation block c.
+//   * A CTA owns 32-row tiles (persistent, round-robin over the grid).  Its W
+//     warps split each tile's chunks (warp w takes chunks w, w+W, ...); lane l
+//     owns row 32*tile + l.  Each warp streams its [32 rows x 144 B] boxes
+//     through its own ring of TMA stages (cp.async.bulk.tensor.2d into shared
+//     memory, completion on an mbarrier), so the global side is whole-box
+//     bulk copies with many bytes in flight, and the shared-memory side is
+//     one row per lane (144-byte lane stride: 16-byte loads conflict-free).
+//   * Every lane of a warp is on the same chunk, so the activation block is
+//     the same address in all lanes: one broadcast load serves the warp.
+//   * Integer dots with dp4a, reduced to the super-block exactly in int32
+//     ("reduce first, then scale once", 25.2), then an f32 epilogue with an
+//     error-free compensation term (TwoProduct/TwoSum), so the float result
+//     is within a few f32 ulps of the exact one.
+//   * End of tile: each warp's per-row partial (hi, lo) goes to shared memory;
+//     one CTA barrier; the W partials are summed in a fixed order and stored.
+#pragma once
+
+#include "xq_internal.h"
+#include "xq_ptx.cuh"
+
+namespace xq {
+
+// ---- shared epilogue --------------------------------------------------------
+// Adds xs*(d*S1 - dmin*S2) to (hi, lo).  S1, S2 exact integers; |S2| < 2^24;
+// S1 is split into its f32 rounding and an exact residual.
+__device__ __forceinline__ void q4k_epilogue(float xs, float d, float dmin, int S1, int S2,
+                                             float &hi, float &lo) {
+    float ph, pl, qh, ql;
+    two_prod(xs, d, ph, pl);        // xs*d    = ph + pl exactly
+    two_prod(xs, dmin, qh, ql);     // xs*dmin = qh + ql exactly
+    const float f1 = __int2float_rn(S1);
+    const float r1 = __int2float_rn(S1 - __float2int_rn(f1));  // exact, 0 if |S1| <= 2^24
+    const float f2 = __int2float_rn(S2);                       // exact
+    float t1, e1, t2, e2;
+    two_prod(ph, f1, t1, e1);
+    two_prod(-qh, f2, t2, e2);
+    // second-order terms, each below 2^-23 of the main ones
+    float small = __fmaf_rn(pl, f1, __fmaf_rn(ph, r1, __fadd_rn(e1, e2)));
+    small = __fmaf_rn(-ql, f2, small);
+    acc_add(hi, lo, t1, 0.0f);
+    acc_add(hi, lo, t2, small);
+}
+
+// ---- Q4_K chunk ---------------------------------------------------------------------
+// w: this lane's 144-byte super-block in shared memory.  xa: the chunk's q8
+// block of batch 0 in global memory (batch b at xa + b*bstride).
+template <int B, bool DOTS>
+__device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w,
+                                          const uint8_t *__restrict__ xa, int64_t bstride,
+                                          float (&hi)[B], float (&lo)[B], int32_t *dots,
+                                          int64_t dots_bstride) {
+    const uint4 h = *reinterpret_cast<const uint4 *>(w);
+    uint32_t q[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(w + 16 + 16 * i);
+        q[4 * i + 0] = v.x;
+        q[4 * i + 1] = v.y;
+        q[4 * i + 2] = v.z;
+        q[4 * i + 3] = v.w;
+    }
+    const float d = f16_bits_to_f32(h.x);
+    const float dmin = f16_bits_to_f32(h.x >> 16);
+    // six-bit scales and mins: bytes 4..7 (h.y), 8..11 (h.z), 12..15 (h.w)
+    const uint32_t sc_lo = h.y & 0x3F3F3F3Fu;
+    const uint32_t m_lo = h.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+    const uint32_t m_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+    int sc[8], mn[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        sc[j] = (sc_lo >> (8 * j)) & 0xFF;
+        sc[j + 4] = (sc_hi >> (8 * j)) & 0xFF;
+        mn[j] = (m_lo >> (8 * j)) & 0xFF;
+        mn[j + 4] = (m_hi >> (8 * j)) & 0xFF;
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+        const uint4 *xa4 = reinterpret_cast<const uint4 *>(xa + b * bstride);
+        int dot[8];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            // sub-block 2g: activation bytes 64g..64g+31 (low nibbles of group g)
+            // sub-block 2g+1: bytes 64g+32..64g+63 (high nibbles of group g)
+            const uint4 a0 = __ldg(xa4 + 4 * g + 0), a1 = __ldg(xa4 + 4 * g + 1);
+            const uint4 a2 = __ldg(xa4 + 4 * g + 2), a3 = __ldg(xa4 + 4 * g + 3);
+            const uint32_t alo[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t ahi[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+            int d0 = 0, d1 = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t word = q[8 * g + k];
+                d0 = dp4a(word & 0x0F0F0F0Fu, alo[k], d0);
+                d1 = dp4a((word >> 4) & 0x0F0F0F0Fu, ahi[k], d1);
+            }
+            dot[2 * g] = d0;
+            dot[2 * g + 1] = d1;
+        }
+        const uint4 s0 = __ldg(xa4 + 16), s1 = __ldg(xa4 + 17);  // eight int32 sums
+        const float xs = __ldg(reinterpret_cast<const float *>(xa + b * bstride + kQ8ScaleAt));
+        const int bs[8] = {(int)s0.x, (int)s0.y, (int)s0.z, (int)s0.w,
+                           (int)s1.x, (int)s1.y, (int)s1.z, (int)s1.w};
+        int S1 = 0, S2 = 0;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            S1 += sc[s] * dot[s];
+            S2 += mn[s] * bs[s];
+        }
+        q4k_epilogue(xs, d, dmin, S1, S2, hi[b], lo[b]);
+        if (DOTS && dots != nullptr) {
+            int4 *o = reinterpret_cast<int4 *>(dots + b * dots_bstride);
+            o[0] = make_int4(dot[0], dot[1], dot[2], dot[3]);
+            o[1] = make_int4(dot[4], dot[5], dot[6], dot[7]);
+        }
+    }
+}
+
+// ---- codebook chunk -----------------------------------------------------------------
+// Eight nibbles of a payload word -> two words of int8 codebook values, LO for
+// the low nibbles (bytes in order) and HI for the high nibbles.  The table is
+// four registers; prmt looks up 8 entries at a time, so two lookups per half
+// table plus a byte select on nibble bit 3, then a byte shuffle that
+// separates low and high nibbles.  Exact by construction.
+__device__ __forceinline__ void cb4_decode(uint32_t q, const uint32_t (&T)[4], uint32_t &LO,
+                                           uint32_t &HI) {
+    const uint32_t s = q & 0x77777777u;     // entry index within a half table
+    const uint32_t sh = s >> 16;
+    const uint32_t a0 = __byte_perm(T[0], T[1], s);   // kv[0..7] at nibbles 0..3
+    const uint32_t a1 = __byte_perm(T[0], T[1], sh);  // kv[0..7] at nibbles 4..7
+    const uint32_t b0 = __byte_perm(T[2], T[3], s);   // kv[8..15]
+    const uint32_t b1 = __byte_perm(T[2], T[3], sh);
+    // byte n of f0 = kv[nibble n of q] (n = 0..3: L0, H0, L1, H1)
+    const uint32_t f0 = __byte_perm(a0, b0, ((q >> 1) & 0x4444u) | 0x3210u);
+    const uint32_t f1 = __byte_perm(a1, b1, ((q >> 17) & 0x4444u) | 0x3210u);
+    LO = __byte_perm(f0, f1, 0x6420u);  // kv[L0], kv[L1], kv[L2], kv[L3]
+    HI = __byte_perm(f0, f1, 0x7531u);  // kv[H0], kv[H1], kv[H2], kv[H3]
+}
+
+template <int B, bool DOTS>
+__device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w,
+                                          const uint8_t *__restrict__ xa, int64_t bstride,
+                                          const uint32_t (&T)[4], float (&hi)[B], float (&lo)[B],
+                                          int32_t *dots, int64_t dots_bstride) {
+    uint32_t v[36];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        const uint4 t = *reinterpret_cast<const uint4 *>(w + 16 * i);
+        v[4 * i + 0] = t.x;
+        v[4 * i + 1] = t.y;
+        v[4 * i + 2] = t.z;
+        v[4 * i + 3] = t.w;
+    }
+    // Block pair p (blocks 2p, 2p+1) is the 36 bytes at 36p: words 9p..9p+8.
+    // Block 2p: scale = low half of word 9p, payload = bytes 2..17 of the pair
+    // (realigned by 16-bit funnel shifts); block 2p+1: scale = high half of
+    // word 9p+4, payload = words 9p+5..9p+8.
+    float dk[8];
+    uint32_t LO[8][4], HI[8][4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        dk[2 * p] = f16_bits_to_f32(v[9 * p]);
+        dk[2 * p + 1] = f16_bits_to_f32(v[9 * p + 4] >> 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t qa = __funnelshift_r(v[9 * p + i], v[9 * p + i + 1], 16);
+            cb4_decode(qa, T, LO[2 * p][i], HI[2 * p][i]);
+            cb4_decode(v[9 * p + 5 + i], T, LO[2 * p + 1][i], HI[2 * p + 1][i]);
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+        const uint4 *xa4 = reinterpret_cast<const uint4 *>(xa + b * bstride);
+        float ch = 0.0f, cl = 0.0f;  // sum_k d_k * dot_k, compensated
+        int dts[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            // block k: elements 0..15 against bytes 32k..32k+15, 16..31 against 32k+16..
+            const uint4 a0 = __ldg(xa4 + 2 * k), a1 = __ldg(xa4 + 2 * k + 1);
+            int dt = 0;
+            dt = dp4a(LO[k][0], a0.x, dt);
+            dt = dp4a(LO[k][1], a0.y, dt);
+            dt = dp4a(LO[k][2], a0.z, dt);
+            dt = dp4a(LO[k][3], a0.w, dt);
+            dt = dp4a(HI[k][0], a1.x, dt);
+            dt = dp4a(HI[k][1], a1.y, dt);
+            dt = dp4a(HI[k][2], a1.z, dt);
+            dt = dp4a(HI[k][3], a1.w, dt);
+            dts[k] = dt;
+            float p, e;
+            two_prod(dk[k], __int2float_rn(dt), p, e);  // |dt| < 2^20: exact in f32
+            acc_add(ch, cl, p, e);
+        }
+        const float xs = __ldg(reinterpret_cast<const float *>(xa + b * bstride + kQ8ScaleAt));
+        float t, te;
+        two_prod(ch, xs, t, te);
+        acc_add(hi[b], lo[b], t, __fmaf_rn(cl, xs, te));
+        if (DOTS && dots != nullptr) {
+            int4 *o = reinterpret_cast<int4 *>(dots + b * dots_bstride);
+            o[0] = make_int4(dts[0], dts[1], dts[2], dts[3]);
+            o[1] = make_int4(dts[4], dts[5], dts[6], dts[7]);
+        }
+    }
+}
+
+// ---- the kernel ------------------------------------------------------------------------
+// Shared memory: [W][S] stage buffers of 4608 B | [W][S] mbarriers |
+// [2][W][B][32] float2 partials.  Launch: blockDim = 32*W (W <= nb), grid <=
+// ntiles, one CTA per SM.
+template <int FMT, int B, bool DOTS>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1)
+    xq_matvec_kernel(const __grid_constant__ CUtensorMap tmap, const MatvecArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    const int W = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = a.stages;
+    uint8_t *stage0 = smem + (size_t)warp * S * kStageBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)W * S * kStageBytes) + warp * S;
+    float2 *part =
+        reinterpret_cast<float2 *>(smem + (size_t)W * S * kStageBytes + (size_t)W * S * 8);
+
+    const int nb = a.nb;
+    const int nchunk = (nb - warp + W - 1) / W;  // chunks of each tile this warp takes
+    const int G = gridDim.x;
+    const int ntile_cta = (a.ntiles - (int)blockIdx.x + G - 1) / G;
+    const int64_t nitems = (int64_t)ntile_cta * nchunk;
+    const int64_t bstride = (int64_t)nb * kQ8Bytes;
+    const int64_t dots_row = (int64_t)nb * 8;            // dots per row
+    const int64_t dots_bstride = a.rows * dots_row;      // dots per batch vector
+
+    uint32_t T[4] = {a.kv[0], a.kv[1], a.kv[2], a.kv[3]};
+    uint64_t policy = 0;
+
+    auto issue = [&](int64_t i) {
+        const int64_t kt = i / nchunk;
+        const int ci = (int)(i - kt * nchunk);
+        const int tile = (int)blockIdx.x + (int)kt * G;
+        const int chunk = warp + ci * W;
+        const int s = (int)(i % S);
+        mbar_arrive_expect_tx(&bars[s], kStageBytes);
+        tma_load_2d(stage0 + (size_t)s * kStageBytes, &tmap, chunk * kChunkBytes,
+                    tile * kTileRows, &bars[s], policy);
+    };
+
+    if (lane == 0) {
+        prefetch_tensormap(&tmap);
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+        policy = l2_policy_evict_first();
+        const int64_t pre = nitems < S ? nitems : S;
+        for (int64_t i = 0; i < pre; ++i) issue(i);
+    }
+    __syncwarp();
+
+    bool failed = false;
+    int64_t fail_item = nitems;
+    int64_t item = 0;
+    for (int k = 0; k < ntile_cta; ++k) {
+        const int tile = (int)blockIdx.x + k * G;
+        const int64_t row = (int64_t)tile * kTileRows + lane;
+        const bool row_ok = row < a.rows;
+        float hi[B], lo[B];
+#pragma unroll
+        for (int b = 0; b < B; ++b) hi[b] = lo[b] = 0.0f;
+        for (int ci = 0; ci < nchunk; ++ci, ++item) {
+            const int chunk = warp + ci * W;
+            const int s = (int)(item % S);
+            const uint32_t phase = (uint32_t)((item / S) & 1);
+            if (!failed) {
+                const bool ok = mbar_wait_bounded(&bars[s], phase, a.status);
+                if (__any_sync(0xffffffffu, !ok)) {
+                    failed = true;
+                    fail_item = item;
+                }
+            }
+            if (!failed) {
+                const uint8_t *w = stage0 + (size_t)s * kStageBytes + lane * kChunkBytes;
+                const uint8_t *xa = a.xq + (int64_t)chunk * kQ8Bytes;
+                int32_t *dp = (DOTS && row_ok) ? a.dots + row * dots_row + chunk * 8 : nullptr;
+                if (FMT == kQ4K)
+                    q4k_chunk<B, DOTS>(w, xa, bstride, hi, lo, dp, dots_bstride);
+                else
+                    cb4_chunk<B, DOTS>(w, xa, bstride, T, hi, lo, dp, dots_bstride);
+            }
+            __syncwarp();
+            if (lane == 0 && !failed && item + S < nitems) {
+                fence_proxy_async_smem();
+                issue(item + S);
+            }
+        }
+        // tile epilogue: per-warp partials -> fixed-order sum over warps
+        float2 *pb = part + (size_t)(k & 1) * W * B * 32;
+#pragma unroll
+        for (int b = 0; b < B; ++b) pb[(warp * B + b) * 32 + lane] = make_float2(hi[b], lo[b]);
+        __syncthreads();
+        if (!DOTS) {
+            for (int p = threadIdx.x; p < B * 32; p += blockDim.x) {
+                const int b = p >> 5, r = p & 31;
+                const int64_t grow = (int64_t)tile * kTileRows + r;
+                float h = 0.0f, l = 0.0f;
+                for (int ww = 0; ww < W; ++ww) {
+                    const float2 v = pb[(ww * B + b) * 32 + r];
+                    acc_add(h, l, v.x, v.y);
+                }
+                if (grow < a.rows) a.y[(int64_t)b * a.rows + grow] = __fadd_rn(h, l);
+            }
+        }
+    }
+    // After a timed-out wait, let the copies still in flight land (bounded)
+    // before the CTA's shared memory is released.
+    if (failed && lane == 0) {
+        const int64_t end = (fail_item + S < nitems) ? fail_item + S : nitems;
+        for (int64_t i = fail_item; i < end; ++i)
+            mbar_wait_bounded(&bars[(int)(i % S)], (uint32_t)((i / S) & 1), a.status);
+    }
+}
+
+template <int FMT, int B, bool DOTS>
+inline cudaError_t launch_matvec_t(const CUtensorMap &tmap, const MatvecArgs &a, dim3 grid,
+                                   dim3 block, size_t smem, cudaStream_t s) {
+    xq_matvec_kernel<FMT, B, DOTS><<<grid, block, smem, s>>>(tmap, a);
+    return cudaGetLastError();
+}
+
+template <int FMT, int B, bool DOTS>
+inline cudaError_t configure_t(int smem_optin) {
+    return cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+}
+
+template <int FMT>
+inline cudaError_t launch_matvec_fmt(const CUtensorMap &tmap, const MatvecArgs &a, int batch,
+                                     bool dots, dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t s) {
+#define XQ_CASE(BB)                                                                \
+    case BB:                                                               \
+        return dots ? launch_matvec_t<FMT, BB, true>(tmap, a, grid, block, smem, s) \
+                    : launch_matvec_t<FMT, BB, false>(tmap, a, grid, block, smem, s);
+    switch (batch) {
+        XQ_CASE(1)
+        XQ_CASE(2)
+        XQ_CASE(3)
+        XQ_CASE(4)
+        XQ_CASE(5)
+        XQ_CASE(6)
+        XQ_CASE(7)
+        XQ_CASE(8)
+        default:
+            return cudaErrorInvalidValue;
+    }
+#undef XQ_CASE
+}
+
+template <int FMT>
+inline cudaError_t configure_fmt(int smem_optin) {
+    cudaError_t e = cudaSuccess;
+#define XQ_CFG(BB)                                                      \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, false>(smem_optin); \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, true>(smem_optin);
+    XQ_CFG(1)
+    XQ_CFG(2)
+    XQ_CFG(3)
+    XQ_CFG(4)
+    XQ_CFG(5)
+    XQ_CFG(6)
+    XQ_CFG(7)
+    XQ_CFG(8)
+#undef XQ_CFG
+    return e;
+}
+
+}  // namespace xq

@@ -1,0 +1,176 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+include/xq.h declares, and its host-side argument checks, size functions and
+launch planner behave as documented.  Argument checks run before any CUDA
+call, so fake (never dereferenced) pointers are enough here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "xq.h")
+
+P = 0x10000  # a 16-byte aligned fake device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    __graft_entry__._xq_build_module().build()
+    import quantized_decode_mat_gb300 as xq
+    return xq
+
+
+@pytest.fixture(scope="module")
+def raw(lib):
+    return ctypes.CDLL(lib.lib_path())
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(xq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("xq_quantize_q8", "xq_matvec_q4k", "xq_matvec_cb4", "xq_subdots_q4k",
+                 "xq_subdots_cb4", "xq_q8_bytes", "xq_status_string", "xq_last_error"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(raw):
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_sizes_match_the_formats(lib):
+    import oracle
+    assert lib.q8_bytes(256, 1) == oracle.Q8_BYTES == 320
+    assert lib.q8_bytes(4096, 8) == 8 * 16 * 320
+    assert lib.q4k_bytes(1, 256) == oracle.Q4K_BYTES == 144
+    assert lib.cb4_bytes(1, 256) == 8 * oracle.CB4_BYTES
+    assert lib.q4k_bytes(128256, 4096) == 295_501_824
+    assert lib.cb4_bytes(11008, 4096) == 25_362_432
+    assert lib.q8_bytes(100, 1) == 0 and lib.q4k_bytes(4, 0) == 0
+
+
+def _call(raw, name, *args):
+    fn = getattr(raw, name)
+    fn.restype = ctypes.c_int
+    return fn(*args)
+
+
+I64 = ctypes.c_int64
+V = ctypes.c_void_p
+
+
+@pytest.mark.parametrize("args,status", [
+    ((V(0), V(P), V(P), I64(32), I64(256), I64(1), V(0)), 1),         # null W
+    ((V(P), V(P), V(0), I64(32), I64(256), I64(1), V(0)), 1),         # null y
+    ((V(P), V(P), V(P * 8), I64(32), I64(100), I64(1), V(0)), 3),     # cols % 256
+    ((V(P), V(P), V(P * 8), I64(32), I64(0), I64(1), V(0)), 3),       # cols 0
+    ((V(P), V(P), V(P * 8), I64(0), I64(256), I64(1), V(0)), 3),      # rows 0
+    ((V(P), V(P), V(P * 8), I64(32), I64(256), I64(0), V(0)), 3),     # batch 0
+    ((V(P), V(P), V(P * 8), I64(32), I64(256), I64(9), V(0)), 3),     # batch 9
+    ((V(P + 8), V(P), V(P * 8), I64(32), I64(256), I64(1), V(0)), 2),  # W misaligned
+    ((V(P), V(P + 4), V(P * 8), I64(32), I64(256), I64(1), V(0)), 2),  # xq misaligned
+    ((V(P), V(P * 4), V(P + 2), I64(32), I64(256), I64(1), V(0)), 2),  # y misaligned
+    ((V(P), V(P * 4), V(P + 16), I64(32), I64(256), I64(1), V(0)), 1),  # y overlaps W
+])
+def test_matvec_q4k_argument_checks(raw, args, status):
+    assert _call(raw, "xq_matvec_q4k", *args) == status
+    err = ctypes.CDLL(raw._name).xq_last_error
+    err.restype = ctypes.c_char_p
+    assert err()
+
+
+def test_cb4_needs_a_table(raw):
+    assert _call(raw, "xq_matvec_cb4", V(P), V(0), V(P * 2), V(P * 8), I64(32), I64(256),
+                 I64(1), V(0)) == 1
+
+
+def test_quantize_argument_checks(raw):
+    assert _call(raw, "xq_quantize_q8", V(0), V(P), I64(256), I64(1), V(0)) == 1
+    assert _call(raw, "xq_quantize_q8", V(P + 4), V(P * 4), I64(256), I64(1), V(0)) == 2
+    assert _call(raw, "xq_quantize_q8", V(P), V(P * 4), I64(300), I64(1), V(0)) == 3
+    assert _call(raw, "xq_quantize_q8", V(P), V(P + 512), I64(256), I64(1), V(0)) == 1
+
+
+def test_subdots_need_16_byte_aligned_output(raw):
+    assert _call(raw, "xq_subdots_q4k", V(P), V(P * 2), V(P * 8 + 4), I64(32), I64(256),
+                 I64(1), V(0)) == 2
+
+
+def test_status_strings(raw):
+    fn = raw.xq_status_string
+    fn.restype = ctypes.c_char_p
+    for s in range(6):
+        assert fn(s).startswith(b"XQ_")
+    assert raw.xq_version() == 1
+
+
+@pytest.mark.parametrize("rows,cols,batch,warps,grid", [
+    (128256, 4096, 1, 8, 152), (128256, 4096, 8, 8, 152), (4096, 4096, 1, 8, 128),
+    (14336, 4096, 4, 8, 152), (4096, 14336, 8, 8, 128), (256, 1024, 1, 4, 8),
+    (11008, 4096, 1, 8, 152), (33, 256, 2, 1, 2), (1, 512, 1, 2, 1)])
+def test_plan(lib, rows, cols, batch, warps, grid):
+    p = lib.plan_matvec(rows, cols, batch, sm_count=152, smem_optin=232448)
+    assert p["warps"] == warps and p["grid"] == grid
+    assert p["tiles"] == (rows + 31) // 32
+    assert p["chunks_per_row"] == cols // 256
+    assert 2 <= p["stages"] <= 16
+    assert p["smem_bytes"] <= 232448
+    # every warp owns at least one chunk of every tile
+    assert p["warps"] <= p["chunks_per_row"]
+
+
+def test_plan_override_is_clamped(lib):
+    try:
+        lib.set_plan_override(warps=16, stages=64)
+        p = lib.plan_matvec(1000, 1024, 1)
+        assert p["warps"] == 4 and p["stages"] <= 16
+        lib.set_plan_override(warps=2, stages=3)
+        p = lib.plan_matvec(1000, 4096, 1)
+        assert p["warps"] == 2 and p["stages"] == 3
+    finally:
+        lib.set_plan_override(0, 0)
+
+
+def test_python_binding_rejects_host_tensors(lib):
+    import torch
+    with pytest.raises(TypeError):
+        lib.quantize_q8(torch.zeros(1, 256))
+
+
+def test_hot_kernels_do_not_spill(lib):
+    """Spill is invisible to timing ("25 - Writing XPU Kernels" 25.5, the
+    manifest before the wall clock): the batch-1..4 kernels must not spill."""
+    import __graft_entry__
+    rep = __graft_entry__._xq_build_module().ptxas_report()
+    assert rep, "no ptxas report"
+    for name, r in rep.items():
+        m = re.search(r"xq_matvec_kernelILi(\d)ELi(\d)ELb(\d)", name)
+        if m and int(m.group(2)) <= 4:
+            assert r["spill_stores"] == 0 and r["spill_loads"] == 0, (name, r)
+
+
+def test_oracle_and_product_share_no_code():
+    """The oracle and the CUDA path are independent: neither includes or
+    imports the other."""
+    pkg = os.path.join(ROOT, "quantized_decode_mat_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "xq_oracle" not in text, f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c", ".h")):
+            text = open(os.path.join(ROOT, "oracle", f)).read()
+            assert not re.search(r"^\s*(import|from)\s+quantized_decode_mat_gb300\b", text,
+                                 re.M), f
+            assert "xq_internal" not in text and '#include "xq' not in text, f

@@ -1,0 +1,304 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.
+
+Bars (the decode workload's parity rules):
+  * q8 blocks: all 320 bytes bit-exact (the quantiser decides integers in f32
+    on both sides, one rounding per operation).
+  * per-sub-block / per-block int32 dots: bit-exact.
+  * y (f32): |y_gpu - y_ref| <= 1e-5 * |y_ref| + 1e-6 per element, y_ref the
+    oracle's exact-integer / binary64 value.
+Outputs are poisoned with 0xFF (NaN) before each launch and guarded by a
+poisoned tail that must come back unchanged.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+
+pytestmark = pytest.mark.gpu
+
+REL, ABS = 1e-5, 1e-6
+GUARD = 256  # poisoned bytes after every output
+
+
+@pytest.fixture(scope="module")
+def xq():
+    import quantized_decode_mat_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    return m
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda")
+
+
+class Guarded:
+    """An output tensor followed by a poisoned guard band in one allocation."""
+
+    def __init__(self, shape, dtype):
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        self.raw = torch.full((n + GUARD,), 0xFF, dtype=torch.uint8, device="cuda")
+        self.t = self.raw[:n].view(dtype).view(shape)
+
+    def check_guard(self):
+        tail = self.raw[-GUARD:].cpu().numpy()
+        assert np.all(tail == 0xFF), "write past the end of an output"
+
+
+def check_y(y: np.ndarray, y_ref: np.ndarray, what: str):
+    y = y.astype(np.float64)
+    assert not np.isnan(y).any(), f"{what}: NaN in output (unwritten rows?)"
+    err = np.abs(y - y_ref)
+    tol = REL * np.abs(y_ref) + ABS
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {y.size} outside 1e-5 rel + 1e-6 abs; "
+                           f"worst err {err.max():.3e} at |y| {np.abs(y_ref).flat[err.argmax()]:.3e}")
+    assert np.any(y != 0), f"{what}: all-zero output"
+
+
+def run_quantize(xq, x):
+    batch, cols = x.shape
+    out = Guarded((batch, cols // 256, 320), torch.uint8)
+    xq.quantize_q8(dev(x), out=out.t)
+    torch.cuda.synchronize()
+    out.check_guard()
+    return out.t
+
+
+def run_matvec(xq, fmt, W, kv, xq_dev, rows, cols, batch, dots=False):
+    if dots:
+        out = Guarded((batch, rows, cols // 32), torch.int32)
+    else:
+        out = Guarded((batch, rows), torch.float32)
+    Wd = dev(W)
+    if fmt == "q4k":
+        (xq.subdots_q4k if dots else xq.matvec_q4k)(Wd, xq_dev, rows, cols, out=out.t)
+    elif dots:
+        xq.subdots_cb4(Wd, kv, xq_dev, rows, cols, out=out.t)
+    else:
+        xq.matvec_cb4(Wd, kv, xq_dev, rows, cols, out=out.t)
+    torch.cuda.synchronize()
+    out.check_guard()
+    return out.t.cpu().numpy()
+
+
+# ---------------------------------------------------------------- q8 blocks
+def _x_kind(kind, batch, cols, seed):
+    if kind == "normal":
+        return synthetic.activations(batch, cols, seed)
+    if kind == "outliers":
+        return synthetic.activations(batch, cols, seed, outlier_frac=0.001)
+    if kind == "fixture":
+        return np.tile(synthetic.guide_fixture_x(cols), (batch, 1))
+    if kind == "zeros":
+        return np.zeros((batch, cols), np.float32)
+    if kind == "tiny":
+        return (synthetic.activations(batch, cols, seed) * np.float32(1e-33)).astype(np.float32)
+    if kind == "huge":
+        return (synthetic.activations(batch, cols, seed) * np.float32(1e30)).astype(np.float32)
+    if kind == "ties":
+        rng = np.random.Generator(np.random.PCG64(seed))
+        x = (rng.integers(-254, 255, size=(batch, cols)) / 2.0).astype(np.float32)
+        x.reshape(batch, -1, 256)[:, :, 0] = 127.0
+        return x
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("kind", ["normal", "outliers", "fixture", "zeros", "tiny", "huge",
+                                  "ties"])
+@pytest.mark.parametrize("cols,batch", [(256, 1), (1024, 3), (4096, 8), (14336, 2)])
+def test_quantize_bit_exact(xq, orc, kind, cols, batch):
+    x = _x_kind(kind, batch, cols, 1000 + cols + batch)
+    before = xq.launch_count(xq.COUNT_QUANTIZE)
+    got = run_quantize(xq, x).cpu().numpy()
+    assert xq.launch_count(xq.COUNT_QUANTIZE) == before + 1
+    ref = orc.quantize_q8(x)
+    diff = np.argwhere(got != ref)
+    assert diff.size == 0, f"{len(diff)} bytes differ, first at {diff[:4].tolist()}"
+
+
+# ---------------------------------------------------------------- exact dots
+SHAPES = [(1, 256, 1), (31, 512, 2), (32, 1024, 1), (33, 1024, 4), (101, 2304, 3),
+          (300, 4096, 1), (77, 4096, 8), (64, 14336, 2)]
+
+
+def _weights(fmt, rows, cols, seed):
+    return (synthetic.q4k_weights(rows, cols, seed) if fmt == "q4k"
+            else synthetic.cb4_weights(rows, cols, seed))
+
+
+@pytest.mark.parametrize("fmt", ["q4k", "cb4"])
+@pytest.mark.parametrize("rows,cols,batch", SHAPES)
+def test_subdots_bit_exact(xq, orc, fmt, rows, cols, batch):
+    seed = rows * 7 + cols + batch
+    W = _weights(fmt, rows, cols, seed)
+    kv = synthetic.cb4_table()
+    x = synthetic.activations(batch, cols, seed + 1)
+    xq_dev = run_quantize(xq, x)
+    which = xq.COUNT_SUBDOTS_Q4K if fmt == "q4k" else xq.COUNT_SUBDOTS_CB4
+    before = xq.launch_count(which)
+    got = run_matvec(xq, fmt, W, kv, xq_dev, rows, cols, batch, dots=True)
+    assert xq.launch_count(which) == before + 1
+    xq_ref = orc.quantize_q8(x)
+    ref = (orc.subdots_q4k(W, xq_ref, rows, cols, batch) if fmt == "q4k"
+           else orc.subdots_cb4(W, kv, xq_ref, rows, cols, batch))
+    diff = np.argwhere(got != ref)
+    assert diff.size == 0, f"{len(diff)} dots differ, first at {diff[:4].tolist()}"
+
+
+@pytest.mark.parametrize("fmt", ["q4k", "cb4"])
+@pytest.mark.parametrize("rows,cols,batch", SHAPES)
+def test_matvec_within_tolerance(xq, orc, fmt, rows, cols, batch):
+    seed = rows * 11 + cols + batch
+    W = _weights(fmt, rows, cols, seed)
+    kv = synthetic.cb4_table()
+    x = synthetic.activations(batch, cols, seed + 1, outlier_frac=0.001)
+    xq_dev = run_quantize(xq, x)
+    which = xq.COUNT_MATVEC_Q4K if fmt == "q4k" else xq.COUNT_MATVEC_CB4
+    before = xq.launch_count(which)
+    y = run_matvec(xq, fmt, W, kv, xq_dev, rows, cols, batch)
+    assert xq.launch_count(which) == before + 1
+    xq_ref = orc.quantize_q8(x)
+    y_ref = (orc.matvec_q4k(W, xq_ref, rows, cols, batch) if fmt == "q4k"
+             else orc.matvec_cb4(W, kv, xq_ref, rows, cols, batch))
+    check_y(y, y_ref, f"{fmt} {rows}x{cols} b{batch}")
+
+
+# ---------------------------------------------------------------- the configurations
+SMALL_CASES = [k for k in synthetic.CASES if not k.startswith("c5_")]
+
+
+@pytest.mark.parametrize("name", SMALL_CASES)
+def test_config_full(xq, orc, name):
+    """Configurations 1-4 at full size, every output against the oracle."""
+    c = synthetic.CASES[name]
+    W, x = c.weights(), c.x()
+    kv = synthetic.cb4_table()
+    xq_dev = run_quantize(xq, x)
+    assert np.array_equal(xq_dev.cpu().numpy(), orc.quantize_q8(x))
+    y = run_matvec(xq, c.fmt, W, kv, xq_dev, c.rows, c.cols, c.batch)
+    xq_ref = orc.quantize_q8(x)
+    y_ref = (orc.matvec_q4k(W, xq_ref, c.rows, c.cols, c.batch) if c.fmt == "q4k"
+             else orc.matvec_cb4(W, kv, xq_ref, c.rows, c.cols, c.batch))
+    check_y(y, y_ref, name)
+
+
+@pytest.mark.parametrize("name", ["c5_q4k_128256x4096_b1", "c5_q4k_128256x4096_b8"])
+def test_config5_sampled(xq, orc, name):
+    """The L2-exceeding vocabulary projection at full size, in the launch
+    configuration the bench times; the oracle recomputes sampled rows (the
+    first and last tiles, including the ragged end, and 1500 random rows) and
+    every sub-block dot of 64 sampled rows."""
+    c = synthetic.CASES[name]
+    W, x = c.weights(), c.x()
+    xq_dev = run_quantize(xq, x)
+    xq_ref = orc.quantize_q8(x)
+    assert np.array_equal(xq_dev.cpu().numpy(), xq_ref)
+    y = run_matvec(xq, "q4k", W, None, xq_dev, c.rows, c.cols, c.batch)
+    plan = xq.last_plan()
+    assert plan["grid"] == min(plan["tiles"], torch.cuda.get_device_properties(0).multi_processor_count)
+    rng = np.random.Generator(np.random.PCG64(5))
+    sample = np.unique(np.concatenate([np.arange(64), np.arange(c.rows - 70, c.rows),
+                                       rng.choice(c.rows, 1500, replace=False)]))
+    Ws = np.ascontiguousarray(W[sample])
+    y_ref = orc.matvec_q4k(Ws, xq_ref, len(sample), c.cols, c.batch)
+    check_y(y[:, sample], y_ref, name)
+    dots = run_matvec(xq, "q4k", W, None, xq_dev, c.rows, c.cols, c.batch, dots=True)
+    s2 = sample[:: max(1, len(sample) // 64)]
+    ref_d = orc.subdots_q4k(np.ascontiguousarray(W[s2]), xq_ref, len(s2), c.cols, c.batch)
+    assert np.array_equal(dots[:, s2], ref_d)
+
+
+# ---------------------------------------------------------------- degenerate cases
+@pytest.mark.parametrize("fmt", ["q4k", "cb4"])
+def test_zero_weights_and_zero_activations(xq, orc, fmt):
+    rows, cols, batch = 45, 1024, 2
+    kv = synthetic.cb4_table()
+    W0 = np.zeros_like(_weights(fmt, rows, cols, 1))
+    x = synthetic.activations(batch, cols, 2)
+    y = run_matvec(xq, fmt, W0, kv, run_quantize(xq, x), rows, cols, batch)
+    assert np.all(y == 0.0)
+    W = _weights(fmt, rows, cols, 3)
+    y = run_matvec(xq, fmt, W, kv, run_quantize(xq, np.zeros((batch, cols), np.float32)), rows,
+                   cols, batch)
+    assert np.all(y == 0.0)
+
+
+def test_extreme_codes(xq, orc):
+    """All nibbles 15, all six-bit scales/mins 63 and all activations at +-127:
+    the largest integer sums the route can form stay exact."""
+    rows, cols, batch = 40, 2048, 1
+    W = synthetic.q4k_weights(rows, cols, 9)
+    W.reshape(rows, -1, 144)[:, :, 4:] = 0xFF
+    x = np.full((batch, cols), 127.0, np.float32)
+    xq_dev = run_quantize(xq, x)
+    xq_ref = orc.quantize_q8(x)
+    check_y(run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch),
+            orc.matvec_q4k(W, xq_ref, rows, cols, batch), "extreme q4k")
+    assert np.array_equal(run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch, dots=True),
+                          orc.subdots_q4k(W, xq_ref, rows, cols, batch))
+
+
+# ---------------------------------------------------------------- launch plans
+@pytest.mark.parametrize("cols,warps", [(256, 1), (512, 2), (1024, 4), (4096, 8), (14336, 8)])
+def test_plan_fires(xq, orc, cols, warps):
+    rows = 70
+    W = synthetic.q4k_weights(rows, cols, 4)
+    x = synthetic.activations(1, cols, 5)
+    xq_dev = run_quantize(xq, x)
+    run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, 1)
+    p = xq.last_plan()
+    assert p["warps"] == warps and p["tiles"] == 3 and p["grid"] == 3
+
+
+@pytest.mark.parametrize("warps,stages", [(1, 2), (2, 3), (3, 5), (8, 2), (8, 8)])
+def test_plan_overrides_agree(xq, orc, warps, stages):
+    """Every warps/stages split reads the same bytes and forms the same dots;
+    y stays within tolerance of the oracle."""
+    rows, cols, batch = 200, 4096, 2
+    W = synthetic.q4k_weights(rows, cols, 6)
+    x = synthetic.activations(batch, cols, 7)
+    xq_dev = run_quantize(xq, x)
+    xq_ref = orc.quantize_q8(x)
+    try:
+        xq.set_plan_override(warps, stages)
+        dots = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch, dots=True)
+        y = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch)
+        p = xq.last_plan()
+        assert p["warps"] == warps and p["stages"] == stages
+    finally:
+        xq.set_plan_override(0, 0)
+    assert np.array_equal(dots, orc.subdots_q4k(W, xq_ref, rows, cols, batch))
+    check_y(y, orc.matvec_q4k(W, xq_ref, rows, cols, batch), f"override {warps}x{stages}")
+
+
+# ---------------------------------------------------------------- streams and graphs
+def test_side_stream_and_graph_replay(xq, orc):
+    rows, cols, batch = 500, 4096, 1
+    W = dev(synthetic.q4k_weights(rows, cols, 12))
+    x = synthetic.activations(batch, cols, 13)
+    xd = dev(x)
+    xq_buf = torch.empty((batch, cols // 256, 320), dtype=torch.uint8, device="cuda")
+    y = torch.empty((batch, rows), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        xq.quantize_q8(xd, out=xq_buf)
+        xq.matvec_q4k(W, xq_buf, rows, cols, out=y)
+    s.synchronize()
+    eager = y.cpu().numpy().copy()
+    g = torch.cuda.CUDAGraph()
+    y.fill_(float("nan"))
+    with torch.cuda.graph(g):
+        xq.quantize_q8(xd, out=xq_buf)
+        xq.matvec_q4k(W, xq_buf, rows, cols, out=y)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), eager)
+    y_ref = orc.matvec_q4k(W.cpu().numpy(), orc.quantize_q8(x), rows, cols, batch)
+    check_y(eager, y_ref, "stream/graph")
+
+
+def test_device_status_clean(xq):
+    assert xq.device_status(clear=False) == 0
