@@ -19,9 +19,13 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
                  : "memory");
 }
 
-// Makes the barrier initialisation visible to the async (TMA) proxy.
+// Makes the barrier initialisation visible to other threads and to the async
+// (TMA) proxy.  The proxy fence is required: a TMA completion that reaches a
+// barrier whose initialisation the async proxy has not been ordered after
+// raised an illegal-address exception on GB300.
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
