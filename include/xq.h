@@ -38,14 +38,13 @@
  *     [batch][cols/256][320 B], y is [batch][rows] f32, fully overwritten.
  *   - Preconditions, all checked on the host before any CUDA call:
  *     cols > 0 and cols % 256 == 0; 1 <= rows <= 2^31-1; 1 <= batch <= 8;
- *     W, xq, x 16-byte aligned; y and dots 4-byte aligned; outputs must not
+ *     W, xq, x and dots 16-byte aligned; y 4-byte aligned; outputs must not
  *     overlap inputs.  A violation returns XQ_EINVAL / XQ_EALIGN / XQ_ESHAPE
  *     and launches nothing.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *     compute entry point is asynchronous on it: the return code covers
  *     argument checks and the launch only.  Nothing here synchronises except
- *     xq_device_status.  No kernel traps or asserts; a bounded wait that
- *     times out sets the device status word (see xq_device_status).
+ *     xq_device_status.  No kernel traps, asserts or spins.
  *   - The first call on a device configures the kernels for that device;
  *     make one call per device before capturing a stream into a CUDA graph.
  */
@@ -118,8 +117,9 @@ xq_status xq_subdots_cb4(const void *W, const int8_t *table, const void *xq, int
 
 /* Launch plan of the mat-vec kernels (pure host computation; needs no GPU).
  * sm_count and smem_optin_bytes describe the device (for GB300: 152 SMs,
- * 232448 bytes).  warps: warps per CTA, each owning a pipeline of `stages`
- * 4608-byte TMA stages; grid: persistent CTAs; tiles: 32-row tiles. */
+ * 232448 bytes).  warps: warps per CTA, each owning a ring of `stages`
+ * 4608-byte shared-memory stages ([32 rows x 144 B] each); grid: persistent
+ * CTAs; tiles: 32-row tiles. */
 typedef struct {
     int32_t warps;
     int32_t stages;
@@ -132,7 +132,7 @@ typedef struct {
 
 xq_status xq_plan_matvec(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
                          int64_t smem_optin_bytes, xq_plan *plan);
-/* Override the automatic plan for sweeps: warps (1..8) and stages (2..16),
+/* Override the automatic plan for sweeps: warps (1..8) and stages (2..8),
  * 0 = automatic.  Process-wide; not for concurrent use with launches. */
 void xq_set_plan_override(int32_t warps, int32_t stages);
 /* Plan used by the calling thread's last mat-vec or sub-dot launch. */
@@ -149,9 +149,10 @@ enum {
 };
 uint64_t xq_launch_count(int32_t which);
 
-/* Read (and optionally clear) the current device's status word.  It is 0
- * unless a kernel's bounded wait timed out (bit 0).  SYNCHRONISES `stream`
- * (a device-to-host copy of 4 bytes). */
+/* Read (and optionally clear) the current device's status word, where
+ * kernels report errors without trapping; the current kernels have no
+ * failure that sets it, so it reads 0.  SYNCHRONISES `stream` (a
+ * device-to-host copy of 4 bytes). */
 xq_status xq_device_status(uint32_t *out, int32_t clear, void *stream);
 
 const char *xq_status_string(xq_status s);

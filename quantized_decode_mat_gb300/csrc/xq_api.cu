@@ -1,7 +1,5 @@
 // C ABI of the decode mat-vec library: argument checks, per-device set-up,
-// TMA descriptor encoding, launch planning, and the q8 activation quantiser.
-#include <cudaTypedefs.h>
-
+// launch planning, and the q8 activation quantiser.
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -13,7 +11,9 @@
 
 namespace xq {
 
-// Device status word: bit 0 = a bounded wait timed out (see xq_ptx.cuh).
+// Device status word for kernel-side errors reported without trapping.  The
+// current kernels contain no waits that can time out, so it stays 0; it is
+// kept so that callers can check a device once after a sequence of launches.
 __device__ uint32_t g_status_word;
 
 // ---- q8 activation quantiser ------------------------------------------------------
@@ -172,35 +172,6 @@ xq_status device_state(DeviceState **out) {
     return XQ_OK;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-cudaError_t g_encode_err = cudaSuccess;
-
-xq_status encode_rows(CUtensorMap *tmap, const void *W, int64_t rows, int64_t row_bytes) {
-    std::call_once(g_encode_once, []() {
-        cudaDriverEntryPointQueryResult q;
-        void *fn = nullptr;
-        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                        cudaEnableDefault, &q);
-        if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
-            g_encode_err = cudaErrorSymbolNotFound;
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    if (g_encode_err != cudaSuccess || g_encode == nullptr)
-        return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled entry point");
-    // W viewed as a 2-D byte matrix [rows][row_bytes]; box = 144 bytes x 32 rows.
-    const cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-    const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
-    const cuuint32_t box[2] = {(cuuint32_t)kChunkBytes, (cuuint32_t)kTileRows};
-    const cuuint32_t estride[2] = {1, 1};
-    const CUresult r = g_encode(tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W),
-                               gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(XQ_ELAUNCH, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
-    return XQ_OK;
-}
-
 xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
                     int64_t smem_optin, xq_plan *p) {
     const int32_t nb = (int32_t)(cols / 256);
@@ -212,7 +183,7 @@ xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
     if (S < 2) S = 2;
     if (S > kMaxStages) S = kMaxStages;
     const int64_t partials = 2LL * W * batch * 32 * 8;
-    auto bytes = [&](int32_t s) { return (int64_t)W * s * (kStageBytes + 8) + partials + 128; };
+    auto bytes = [&](int32_t s) { return (int64_t)W * s * kStageBytes + partials + 128; };
     while (bytes(S) > smem_optin && S > 2) --S;
     if (bytes(S) > smem_optin)
         return fail(XQ_ESHAPE, "plan needs %lld bytes of shared memory, device allows %lld",
@@ -253,15 +224,12 @@ xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *xq, 
     if (xq_status s = device_state(&dev)) return s;
     xq_plan plan;
     if (xq_status s = make_plan(rows, cols, batch, dev->sm_count, dev->smem_optin, &plan)) return s;
-    CUtensorMap tmap;
-    if (xq_status s = encode_rows(&tmap, W, rows, nb * kChunkBytes)) return s;
-
     MatvecArgs a;
     memset(&a, 0, sizeof a);
+    a.W = static_cast<const uint8_t *>(W);
     a.xq = static_cast<const uint8_t *>(xq);
     a.y = dots ? nullptr : static_cast<float *>(out);
     a.dots = dots ? static_cast<int32_t *>(out) : nullptr;
-    a.status = dev->status;
     a.rows = rows;
     a.nb = (int32_t)nb;
     a.ntiles = plan.tiles;
@@ -275,9 +243,9 @@ xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *xq, 
     }
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cb4 ? launch_matvec_cb4(tmap, a, (int)batch, dots, grid, block,
+    cudaError_t e = cb4 ? launch_matvec_cb4(a, (int)batch, dots, grid, block,
                                             (size_t)plan.smem_bytes, s)
-                        : launch_matvec_q4k(tmap, a, (int)batch, dots, grid, block,
+                        : launch_matvec_q4k(a, (int)batch, dots, grid, block,
                                             (size_t)plan.smem_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "mat-vec launch");
     t_last_plan = plan;

@@ -2,7 +2,6 @@
 // device).  Not part of the public ABI (that is include/xq.h).
 #pragma once
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,29 +20,29 @@ constexpr int kCb4Bytes = 18;       // codebook block
 // q8 activation block.
 constexpr int kChunkBytes = 144;
 constexpr int kTileRows = 32;                       // one row per lane
-constexpr int kStageBytes = kTileRows * kChunkBytes;  // one TMA box: 4608 B
+constexpr int kStageBytes = kTileRows * kChunkBytes;  // one staged box: 4608 B
 constexpr int kMaxWarps = 8;
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 8;
 
 enum Format { kQ4K = 0, kCB4 = 1 };
 
 struct MatvecArgs {
+    const uint8_t *W;       // [rows][nb][144]
     const uint8_t *xq;      // [batch][nb][320]
     float *y;               // [batch][rows]
     int32_t *dots;          // [batch][rows][nb*8] (sub-dot launches only)
-    uint32_t *status;       // device status word
     int64_t rows;
     int32_t nb;             // 256-weight chunks per row
     int32_t ntiles;         // ceil(rows / 32)
-    int32_t stages;         // TMA stages per warp
+    int32_t stages;         // shared-memory stages per warp (2..8)
     uint32_t kv[4];         // codebook bytes kv[0..15], little-endian words
 };
 
 // Launch entry points implemented per format (xq_matvec_q4k.cu / _cb4.cu).
-cudaError_t launch_matvec_q4k(const CUtensorMap &tmap, const MatvecArgs &a, int batch, bool dots,
-                              dim3 grid, dim3 block, size_t smem, cudaStream_t s);
-cudaError_t launch_matvec_cb4(const CUtensorMap &tmap, const MatvecArgs &a, int batch, bool dots,
-                              dim3 grid, dim3 block, size_t smem, cudaStream_t s);
+cudaError_t launch_matvec_q4k(const MatvecArgs &a, int batch, bool dots, dim3 grid, dim3 block,
+                              size_t smem, cudaStream_t s);
+cudaError_t launch_matvec_cb4(const MatvecArgs &a, int batch, bool dots, dim3 grid, dim3 block,
+                              size_t smem, cudaStream_t s);
 // Raise the dynamic shared memory limit of every instantiation of a format.
 cudaError_t configure_matvec_q4k(int smem_optin);
 cudaError_t configure_matvec_cb4(int smem_optin);

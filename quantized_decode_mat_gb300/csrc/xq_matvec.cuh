@@ -1,5 +1,6 @@
-// Persistent TMA-pipelined decode mat-vec for sm_103a, templated on the weight
-// format, the batch (1..8) and whether it also emits the exact integer dots.
+// Persistent, asynchronously staged decode mat-vec for sm_103a, templated on
+// the weight format, the batch (1..8) and whether it also emits the exact
+// integer dots.
 //
 // Mapping (GB300-first; the guide's kernels put one wave on one row and let
 // lanes take consecutive blocks of that row, "25 - Writing XPU Kernels"
@@ -10,10 +11,10 @@
 //   * A CTA owns 32-row tiles (persistent, round-robin over the grid).  Its W
 //     warps split each tile's chunks (warp w takes chunks w, w+W, ...); lane l
 //     owns row 32*tile + l.  Each warp streams its [32 rows x 144 B] boxes
-//     through its own ring of TMA stages (cp.async.bulk.tensor.2d into shared
-//     memory, completion on an mbarrier), so the global side is whole-box
-//     bulk copies with many bytes in flight, and the shared-memory side is
-//     one row per lane (144-byte lane stride: 16-byte loads conflict-free).
+//     through its own ring of shared-memory stages filled by coalesced
+//     16-byte asynchronous copies (cp.async, S-1 boxes in flight per warp),
+//     and the shared-memory side is one row per lane (144-byte lane stride:
+//     16-byte loads take the minimum four wavefronts).
 //   * Every lane of a warp is on the same chunk, so the activation block is
 //     the same address in all lanes: one broadcast load serves the warp.
 //   * Integer dots with dp4a, reduced to the super-block exactly in int32
@@ -212,12 +213,16 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w,
 }
 
 // ---- the kernel ------------------------------------------------------------------------
-// Shared memory: [W][S] stage buffers of 4608 B | [W][S] mbarriers |
-// [2][W][B][32] float2 partials.  Launch: blockDim = 32*W (W <= nb), grid <=
-// ntiles, one CTA per SM.
+// Shared memory: [W][S] stage buffers of 4608 B | [2][W][B][32] float2
+// partials.  Launch: blockDim = 32*W (W <= nb), grid <= ntiles, one CTA per SM.
+//
+// A stage holds one [32 rows x 144 B] box.  The warp fills it with 16-byte
+// cp.async copies: copy p (0..287) moves bytes 16*(p%9).. of row p/9 of the
+// box, so 32 consecutive copies read about four contiguous 144-byte row
+// segments (coalesced) and land at shared offset 16*p (the box is dense in
+// shared memory).  Rows past the end of W are zero-filled (source size 0).
 template <int FMT, int B, bool DOTS>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1)
-    xq_matvec_kernel(const __grid_constant__ CUtensorMap tmap, const MatvecArgs a) {
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) xq_matvec_kernel(const MatvecArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const int W = blockDim.x >> 5;
@@ -225,9 +230,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     const int lane = threadIdx.x & 31;
     const int S = a.stages;
     uint8_t *stage0 = smem + (size_t)warp * S * kStageBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)W * S * kStageBytes) + warp * S;
-    float2 *part =
-        reinterpret_cast<float2 *>(smem + (size_t)W * S * kStageBytes + (size_t)W * S * 8);
+    float2 *part = reinterpret_cast<float2 *>(smem + (size_t)W * S * kStageBytes);
 
     const int nb = a.nb;
     const int nchunk = (nb - warp + W - 1) / W;  // chunks of each tile this warp takes
@@ -237,33 +240,43 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     const int64_t bstride = (int64_t)nb * kQ8Bytes;
     const int64_t dots_row = (int64_t)nb * 8;            // dots per row
     const int64_t dots_bstride = a.rows * dots_row;      // dots per batch vector
+    const int64_t row_bytes = (int64_t)nb * kChunkBytes;
 
     uint32_t T[4] = {a.kv[0], a.kv[1], a.kv[2], a.kv[3]};
-    uint64_t policy = 0;
+
+    // This lane's nine copies of every box: row within the box and the byte
+    // offset of the 16-byte piece within the row's 144-byte chunk.
+    int prow[9];
+    uint32_t poff[9];
+#pragma unroll
+    for (int k = 0; k < 9; ++k) {
+        const int p = lane + 32 * k;
+        prow[k] = p / 9;
+        poff[k] = 16u * (uint32_t)(p - 9 * (p / 9));
+    }
 
     auto issue = [&](int64_t i) {
         const int64_t kt = i / nchunk;
         const int ci = (int)(i - kt * nchunk);
-        const int tile = (int)blockIdx.x + (int)kt * G;
+        const int64_t row0 = ((int64_t)blockIdx.x + kt * G) * kTileRows;
         const int chunk = warp + ci * W;
-        const int s = (int)(i % S);
-        mbar_arrive_expect_tx(&bars[s], kStageBytes);
-        tma_load_2d(stage0 + (size_t)s * kStageBytes, &tmap, chunk * kChunkBytes,
-                    tile * kTileRows, &bars[s], policy);
+        const uint32_t dst = smem_u32(stage0 + (size_t)(i % S) * kStageBytes) + 16u * lane;
+        const uint8_t *base = a.W + (int64_t)chunk * kChunkBytes;
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+            const int64_t r = row0 + prow[k];
+            const bool in = r < a.rows;
+            const uint8_t *src = base + (in ? r : 0) * row_bytes + poff[k];
+            cp_async_16_zfill(dst + 512u * k, src, in ? 16u : 0u);
+        }
     };
 
-    if (lane == 0) {
-        prefetch_tensormap(&tmap);
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
-        policy = l2_policy_evict_first();
-        const int64_t pre = nitems < S ? nitems : S;
-        for (int64_t i = 0; i < pre; ++i) issue(i);
+    // prologue: S-1 boxes in flight
+    for (int j = 0; j < S - 1; ++j) {
+        if (j < nitems) issue(j);
+        cp_async_commit();
     }
-    __syncwarp();
 
-    bool failed = false;
-    int64_t fail_item = nitems;
     int64_t item = 0;
     for (int k = 0; k < ntile_cta; ++k) {
         const int tile = (int)blockIdx.x + k * G;
@@ -274,29 +287,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         for (int b = 0; b < B; ++b) hi[b] = lo[b] = 0.0f;
         for (int ci = 0; ci < nchunk; ++ci, ++item) {
             const int chunk = warp + ci * W;
-            const int s = (int)(item % S);
-            const uint32_t phase = (uint32_t)((item / S) & 1);
-            if (!failed) {
-                const bool ok = mbar_wait_bounded(&bars[s], phase, a.status);
-                if (__any_sync(0xffffffffu, !ok)) {
-                    failed = true;
-                    fail_item = item;
-                }
-            }
-            if (!failed) {
-                const uint8_t *w = stage0 + (size_t)s * kStageBytes + lane * kChunkBytes;
-                const uint8_t *xa = a.xq + (int64_t)chunk * kQ8Bytes;
-                int32_t *dp = (DOTS && row_ok) ? a.dots + row * dots_row + chunk * 8 : nullptr;
-                if (FMT == kQ4K)
-                    q4k_chunk<B, DOTS>(w, xa, bstride, hi, lo, dp, dots_bstride);
-                else
-                    cb4_chunk<B, DOTS>(w, xa, bstride, T, hi, lo, dp, dots_bstride);
-            }
+            // keep S-1 boxes in flight: the stage refilled here, (item-1)%S,
+            // was released by the warp barrier at the end of the last step
+            if (item + S - 1 < nitems) issue(item + S - 1);
+            cp_async_commit();
+            cp_async_wait_pending(S - 1);  // this lane's copies of `item` landed
+            __syncwarp();                  // ... and every other lane's
+            const uint8_t *w = stage0 + (size_t)(item % S) * kStageBytes + lane * kChunkBytes;
+            const uint8_t *xa = a.xq + (int64_t)chunk * kQ8Bytes;
+            int32_t *dp = (DOTS && row_ok) ? a.dots + row * dots_row + chunk * 8 : nullptr;
+            if (FMT == kQ4K)
+                q4k_chunk<B, DOTS>(w, xa, bstride, hi, lo, dp, dots_bstride);
+            else
+                cb4_chunk<B, DOTS>(w, xa, bstride, T, hi, lo, dp, dots_bstride);
             __syncwarp();
-            if (lane == 0 && !failed && item + S < nitems) {
-                fence_proxy_async_smem();
-                issue(item + S);
-            }
         }
         // tile epilogue: per-warp partials -> fixed-order sum over warps
         float2 *pb = part + (size_t)(k & 1) * W * B * 32;
@@ -316,19 +320,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             }
         }
     }
-    // After a timed-out wait, let the copies still in flight land (bounded)
-    // before the CTA's shared memory is released.
-    if (failed && lane == 0) {
-        const int64_t end = (fail_item + S < nitems) ? fail_item + S : nitems;
-        for (int64_t i = fail_item; i < end; ++i)
-            mbar_wait_bounded(&bars[(int)(i % S)], (uint32_t)((i / S) & 1), a.status);
-    }
+    cp_async_wait_all();  // only empty groups can remain; keeps the exit clean
 }
 
 template <int FMT, int B, bool DOTS>
-inline cudaError_t launch_matvec_t(const CUtensorMap &tmap, const MatvecArgs &a, dim3 grid,
-                                   dim3 block, size_t smem, cudaStream_t s) {
-    xq_matvec_kernel<FMT, B, DOTS><<<grid, block, smem, s>>>(tmap, a);
+inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, size_t smem,
+                                   cudaStream_t s) {
+    xq_matvec_kernel<FMT, B, DOTS><<<grid, block, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -339,13 +337,12 @@ inline cudaError_t configure_t(int smem_optin) {
 }
 
 template <int FMT>
-inline cudaError_t launch_matvec_fmt(const CUtensorMap &tmap, const MatvecArgs &a, int batch,
-                                     bool dots, dim3 grid, dim3 block, size_t smem,
-                                     cudaStream_t s) {
+inline cudaError_t launch_matvec_fmt(const MatvecArgs &a, int batch, bool dots, dim3 grid,
+                                     dim3 block, size_t smem, cudaStream_t s) {
 #define XQ_CASE(BB)                                                                \
     case BB:                                                               \
-        return dots ? launch_matvec_t<FMT, BB, true>(tmap, a, grid, block, smem, s) \
-                    : launch_matvec_t<FMT, BB, false>(tmap, a, grid, block, smem, s);
+        return dots ? launch_matvec_t<FMT, BB, true>(a, grid, block, smem, s) \
+                    : launch_matvec_t<FMT, BB, false>(a, grid, block, smem, s);
     switch (batch) {
         XQ_CASE(1)
         XQ_CASE(2)

@@ -4,9 +4,9 @@
 
 namespace xq {
 
-cudaError_t launch_matvec_cb4(const CUtensorMap &tmap, const MatvecArgs &a, int batch, bool dots,
-                              dim3 grid, dim3 block, size_t smem, cudaStream_t s) {
-    return launch_matvec_fmt<kCB4>(tmap, a, batch, dots, grid, block, smem, s);
+cudaError_t launch_matvec_cb4(const MatvecArgs &a, int batch, bool dots, dim3 grid, dim3 block,
+                              size_t smem, cudaStream_t s) {
+    return launch_matvec_fmt<kCB4>(a, batch, dots, grid, block, smem, s);
 }
 
 cudaError_t configure_matvec_cb4(int smem_optin) { return configure_fmt<kCB4>(smem_optin); }

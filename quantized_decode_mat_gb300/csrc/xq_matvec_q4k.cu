@@ -4,9 +4,9 @@
 
 namespace xq {
 
-cudaError_t launch_matvec_q4k(const CUtensorMap &tmap, const MatvecArgs &a, int batch, bool dots,
-                              dim3 grid, dim3 block, size_t smem, cudaStream_t s) {
-    return launch_matvec_fmt<kQ4K>(tmap, a, batch, dots, grid, block, smem, s);
+cudaError_t launch_matvec_q4k(const MatvecArgs &a, int batch, bool dots, dim3 grid, dim3 block,
+                              size_t smem, cudaStream_t s) {
+    return launch_matvec_fmt<kQ4K>(a, batch, dots, grid, block, smem, s);
 }
 
 cudaError_t configure_matvec_q4k(int smem_optin) { return configure_fmt<kQ4K>(smem_optin); }
