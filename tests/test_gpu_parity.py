@@ -253,7 +253,7 @@ def test_plan_fires(xq, orc, cols, warps):
     assert p["warps"] == warps and p["tiles"] == 3 and p["grid"] == 3
 
 
-@pytest.mark.parametrize("warps,stages", [(1, 2), (2, 3), (3, 5), (8, 2), (8, 8)])
+@pytest.mark.parametrize("warps,stages", [(1, 2), (2, 3), (3, 5), (8, 2), (8, 6), (4, 8)])
 def test_plan_overrides_agree(xq, orc, warps, stages):
     """Every warps/stages split reads the same bytes and forms the same dots;
     y stays within tolerance of the oracle."""
@@ -272,6 +272,24 @@ def test_plan_overrides_agree(xq, orc, warps, stages):
         xq.set_plan_override(0, 0)
     assert np.array_equal(dots, orc.subdots_q4k(W, xq_ref, rows, cols, batch))
     check_y(y, orc.matvec_q4k(W, xq_ref, rows, cols, batch), f"override {warps}x{stages}")
+
+
+def test_plan_override_clamped_to_shared_memory(xq, orc):
+    """8 warps x 8 stages do not fit in shared memory: the planner lowers the
+    stage count until they do, and the result is still exact."""
+    rows, cols, batch = 64, 4096, 2
+    W = synthetic.q4k_weights(rows, cols, 8)
+    x = synthetic.activations(batch, cols, 9)
+    xq_dev = run_quantize(xq, x)
+    try:
+        xq.set_plan_override(8, 8)
+        dots = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch, dots=True)
+        p = xq.last_plan()
+    finally:
+        xq.set_plan_override(0, 0)
+    assert p["warps"] == 8 and p["stages"] < 8
+    assert p["smem_bytes"] <= torch.cuda.get_device_properties(0).shared_memory_per_block_optin
+    assert np.array_equal(dots, orc.subdots_q4k(W, orc.quantize_q8(x), rows, cols, batch))
 
 
 # ---------------------------------------------------------------- streams and graphs
