@@ -115,7 +115,11 @@ xq_status xq_subdots_q4k(const void *W, const void *xq, int32_t *dots, int64_t r
 xq_status xq_subdots_cb4(const void *W, const int8_t *table, const void *xq, int32_t *dots,
                          int64_t rows, int64_t cols, int64_t batch, void *stream);
 
+/* Weight formats, for xq_plan_matvec. */
+enum { XQ_FORMAT_Q4K = 0, XQ_FORMAT_CB4 = 1 };
+
 /* Launch plan of the mat-vec kernels (pure host computation; needs no GPU).
+ * format: XQ_FORMAT_Q4K or XQ_FORMAT_CB4.
  * sm_count and smem_optin_bytes describe the device (for GB300: 152 SMs,
  * 232448 bytes).  warps: warps per CTA, each owning a ring of `stages`
  * 4608-byte shared-memory stages ([32 rows x 144 B] each); grid: persistent
@@ -130,9 +134,10 @@ typedef struct {
     int64_t smem_bytes;
 } xq_plan;
 
-xq_status xq_plan_matvec(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
-                         int64_t smem_optin_bytes, xq_plan *plan);
-/* Override the automatic plan for sweeps: warps (1..8) and stages (2..8),
+xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t batch,
+                         int32_t sm_count, int64_t smem_optin_bytes, xq_plan *plan);
+/* Override the automatic plan for sweeps: warps (1..16 for batch-1 Q4_K,
+ * else 1..8) and stages (2..8),
  * 0 = automatic.  Process-wide; not for concurrent use with launches. */
 void xq_set_plan_override(int32_t warps, int32_t stages);
 /* Plan used by the calling thread's last mat-vec or sub-dot launch. */

@@ -41,7 +41,7 @@ _matvec_q4k = _sig("xq_matvec_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64,
 _matvec_cb4 = _sig("xq_matvec_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
 _subdots_q4k = _sig("xq_subdots_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
 _subdots_cb4 = _sig("xq_subdots_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
-_plan = _sig("xq_plan_matvec", ctypes.c_int, [_I64, _I64, _I64, _I32, _I64,
+_plan = _sig("xq_plan_matvec", ctypes.c_int, [_I32, _I64, _I64, _I64, _I32, _I64,
                                              ctypes.POINTER(_Plan)])
 _set_override = _sig("xq_set_plan_override", None, [_I32, _I32])
 _last_plan = _sig("xq_last_plan", ctypes.c_int, [ctypes.POINTER(_Plan)])
@@ -177,11 +177,14 @@ def _plan_dict(p: _Plan) -> dict:
     return {f: getattr(p, f) for f, _ in _Plan._fields_ if f != "reserved"}
 
 
-def plan_matvec(rows: int, cols: int, batch: int = 1, sm_count: int = 152,
+FORMATS = {"q4k": 0, "cb4": 1}
+
+
+def plan_matvec(rows: int, cols: int, batch: int = 1, fmt: str = "q4k", sm_count: int = 152,
                 smem_optin: int = 232448) -> dict:
     """Host-only launch plan (no GPU needed)."""
     p = _Plan()
-    _check(_plan(rows, cols, batch, sm_count, smem_optin, ctypes.byref(p)))
+    _check(_plan(FORMATS[fmt], rows, cols, batch, sm_count, smem_optin, ctypes.byref(p)))
     return _plan_dict(p)
 
 

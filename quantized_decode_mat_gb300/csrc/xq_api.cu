@@ -172,13 +172,24 @@ xq_status device_state(DeviceState **out) {
     return XQ_OK;
 }
 
-xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
+// Warps per CTA: the fewest chunks per warp per tile, reached with the fewest
+// warps (every warp then owns the same number of chunks when nb allows it),
+// within the instantiation's register budget (warps_limit).  Stages: 4, or as
+// many as fit in shared memory (at least 2).
+xq_status make_plan(int32_t fmt, int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
                     int64_t smem_optin, xq_plan *p) {
     const int32_t nb = (int32_t)(cols / 256);
-    int32_t W = nb < kMaxWarps ? nb : kMaxWarps;
+    const int32_t wmax = warps_limit(fmt, batch);
+    const int32_t lim = nb < wmax ? nb : wmax;
+    int32_t W = lim;
+    for (int32_t w = 1; w <= lim; ++w) {
+        if ((nb + w - 1) / w == (nb + lim - 1) / lim) {
+            W = w;
+            break;
+        }
+    }
     const int32_t ow = g_override_warps.load(), os = g_override_stages.load();
-    if (ow > 0) W = ow < nb ? ow : nb;
-    if (W > kMaxWarps) W = kMaxWarps;
+    if (ow > 0) W = ow < lim ? ow : lim;
     int32_t S = os > 0 ? os : 4;
     if (S < 2) S = 2;
     if (S > kMaxStages) S = kMaxStages;
@@ -223,7 +234,9 @@ xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *xq, 
     DeviceState *dev = nullptr;
     if (xq_status s = device_state(&dev)) return s;
     xq_plan plan;
-    if (xq_status s = make_plan(rows, cols, batch, dev->sm_count, dev->smem_optin, &plan)) return s;
+    if (xq_status s = make_plan(cb4 ? kCB4 : kQ4K, rows, cols, batch, dev->sm_count,
+                                dev->smem_optin, &plan))
+        return s;
     MatvecArgs a;
     memset(&a, 0, sizeof a);
     a.W = static_cast<const uint8_t *>(W);
@@ -320,13 +333,16 @@ xq_status xq_subdots_cb4(const void *W, const int8_t *table, const void *xq_in, 
     return run_matvec(Op::kDotsCB4, W, table, xq_in, dots, rows, cols, batch, stream);
 }
 
-xq_status xq_plan_matvec(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
-                         int64_t smem_optin_bytes, xq_plan *plan) {
+xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t batch,
+                         int32_t sm_count, int64_t smem_optin_bytes, xq_plan *plan) {
     t_error.clear();
     if (!plan) return fail(XQ_EINVAL, "null plan");
+    if (format != XQ_FORMAT_Q4K && format != XQ_FORMAT_CB4)
+        return fail(XQ_EINVAL, "format must be XQ_FORMAT_Q4K or XQ_FORMAT_CB4");
     if (xq_status s = check_shape(rows, cols, batch, true)) return s;
     if (sm_count < 1) return fail(XQ_EINVAL, "sm_count must be positive");
-    return make_plan(rows, cols, batch, sm_count, smem_optin_bytes, plan);
+    return make_plan(format == XQ_FORMAT_CB4 ? kCB4 : kQ4K, rows, cols, batch, sm_count,
+                     smem_optin_bytes, plan);
 }
 
 void xq_set_plan_override(int32_t warps, int32_t stages) {

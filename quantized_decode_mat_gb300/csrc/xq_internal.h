@@ -26,6 +26,11 @@ constexpr int kMaxStages = 8;
 
 enum Format { kQ4K = 0, kCB4 = 1 };
 
+// Largest warps per CTA of an instantiation (its register budget allows no more).
+constexpr int warps_limit(int fmt, int64_t batch) {
+    return (fmt == kQ4K && batch == 1) ? 2 * kMaxWarps : kMaxWarps;
+}
+
 struct MatvecArgs {
     const uint8_t *W;       // [rows][nb][144]
     const uint8_t *xq;      // [batch][nb][320]

@@ -96,15 +96,17 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w,
             const uint4 a2 = __ldg(xa4 + 4 * g + 2), a3 = __ldg(xa4 + 4 * g + 3);
             const uint32_t alo[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const uint32_t ahi[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+            // High nibbles are used in place (x16): an unsigned byte 16*q times
+            // a signed byte; the sum is a multiple of 16, so >> 4 is exact.
             int d0 = 0, d1 = 0;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint32_t word = q[8 * g + k];
                 d0 = dp4a(word & 0x0F0F0F0Fu, alo[k], d0);
-                d1 = dp4a((word >> 4) & 0x0F0F0F0Fu, ahi[k], d1);
+                d1 = dp4a_us(word & 0xF0F0F0F0u, ahi[k], d1);
             }
             dot[2 * g] = d0;
-            dot[2 * g + 1] = d1;
+            dot[2 * g + 1] = d1 >> 4;
         }
         const uint4 s0 = __ldg(xa4 + 16), s1 = __ldg(xa4 + 17);  // eight int32 sums
         const float xs = __ldg(reinterpret_cast<const float *>(xa + b * bstride + kQ8ScaleAt));
@@ -221,8 +223,13 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w,
 // box, so 32 consecutive copies read about four contiguous 144-byte row
 // segments (coalesced) and land at shared offset 16*p (the box is dense in
 // shared memory).  Rows past the end of W are zero-filled (source size 0).
+// Batch-1 Q4_K runs up to 16 warps per CTA (at most 128 registers a thread);
+// the other instantiations up to 8.
+template <int FMT, int B>
+constexpr int max_threads() { return warps_limit(FMT, B) * 32; }
+
 template <int FMT, int B, bool DOTS>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) xq_matvec_kernel(const MatvecArgs a) {
+__global__ void __launch_bounds__(max_threads<FMT, B>(), 1) xq_matvec_kernel(const MatvecArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const int W = blockDim.x >> 5;
@@ -230,70 +237,80 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) xq_matvec_kernel(const Matv
     const int lane = threadIdx.x & 31;
     const int S = a.stages;
     uint8_t *stage0 = smem + (size_t)warp * S * kStageBytes;
+    const uint32_t stage0_u32 = smem_u32(stage0);
     float2 *part = reinterpret_cast<float2 *>(smem + (size_t)W * S * kStageBytes);
 
     const int nb = a.nb;
     const int nchunk = (nb - warp + W - 1) / W;  // chunks of each tile this warp takes
     const int G = gridDim.x;
     const int ntile_cta = (a.ntiles - (int)blockIdx.x + G - 1) / G;
-    const int64_t nitems = (int64_t)ntile_cta * nchunk;
+    const int nitems = ntile_cta * nchunk;
     const int64_t bstride = (int64_t)nb * kQ8Bytes;
     const int64_t dots_row = (int64_t)nb * 8;            // dots per row
     const int64_t dots_bstride = a.rows * dots_row;      // dots per batch vector
     const int64_t row_bytes = (int64_t)nb * kChunkBytes;
+    const int64_t rows = a.rows;
 
     uint32_t T[4] = {a.kv[0], a.kv[1], a.kv[2], a.kv[3]};
 
-    // This lane's nine copies of every box: row within the box and the byte
-    // offset of the 16-byte piece within the row's 144-byte chunk.
+    // This lane's nine copies of every box: row within the box, and the byte
+    // offset of the piece from the box's first byte in W.
     int prow[9];
-    uint32_t poff[9];
+    uint32_t roff[9];
 #pragma unroll
     for (int k = 0; k < 9; ++k) {
         const int p = lane + 32 * k;
         prow[k] = p / 9;
-        poff[k] = 16u * (uint32_t)(p - 9 * (p / 9));
+        roff[k] = (uint32_t)(prow[k] * row_bytes) + 16u * (uint32_t)(p - 9 * prow[k]);
     }
 
-    auto issue = [&](int64_t i) {
-        const int64_t kt = i / nchunk;
-        const int ci = (int)(i - kt * nchunk);
-        const int64_t row0 = ((int64_t)blockIdx.x + kt * G) * kTileRows;
-        const int chunk = warp + ci * W;
-        const uint32_t dst = smem_u32(stage0 + (size_t)(i % S) * kStageBytes) + 16u * lane;
-        const uint8_t *base = a.W + (int64_t)chunk * kChunkBytes;
+    // producer cursor: next box to request (tile step, chunk step, stage)
+    int p_k = 0, p_ci = 0, p_stage = 0, issued = 0;
+    auto issue_next = [&]() {
+        const int64_t row0 = ((int64_t)blockIdx.x + (int64_t)p_k * G) * kTileRows;
+        const uint8_t *tb = a.W + row0 * row_bytes + (warp + p_ci * W) * kChunkBytes;
+        const uint32_t dst = stage0_u32 + (uint32_t)p_stage * kStageBytes + 16u * lane;
+        if (row0 + kTileRows <= rows) {
 #pragma unroll
-        for (int k = 0; k < 9; ++k) {
-            const int64_t r = row0 + prow[k];
-            const bool in = r < a.rows;
-            const uint8_t *src = base + (in ? r : 0) * row_bytes + poff[k];
-            cp_async_16_zfill(dst + 512u * k, src, in ? 16u : 0u);
+            for (int k = 0; k < 9; ++k) cp_async_16_zfill(dst + 512u * k, tb + roff[k], 16u);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 9; ++k) {
+                const bool in = row0 + prow[k] < rows;
+                cp_async_16_zfill(dst + 512u * k, in ? tb + roff[k] : a.W, in ? 16u : 0u);
+            }
         }
+        if (++p_ci == nchunk) {
+            p_ci = 0;
+            ++p_k;
+        }
+        if (++p_stage == S) p_stage = 0;
+        ++issued;
     };
 
     // prologue: S-1 boxes in flight
     for (int j = 0; j < S - 1; ++j) {
-        if (j < nitems) issue(j);
+        if (issued < nitems) issue_next();
         cp_async_commit();
     }
 
-    int64_t item = 0;
+    int c_stage = 0;
     for (int k = 0; k < ntile_cta; ++k) {
         const int tile = (int)blockIdx.x + k * G;
         const int64_t row = (int64_t)tile * kTileRows + lane;
-        const bool row_ok = row < a.rows;
+        const bool row_ok = row < rows;
         float hi[B], lo[B];
 #pragma unroll
         for (int b = 0; b < B; ++b) hi[b] = lo[b] = 0.0f;
-        for (int ci = 0; ci < nchunk; ++ci, ++item) {
+        for (int ci = 0; ci < nchunk; ++ci) {
             const int chunk = warp + ci * W;
-            // keep S-1 boxes in flight: the stage refilled here, (item-1)%S,
-            // was released by the warp barrier at the end of the last step
-            if (item + S - 1 < nitems) issue(item + S - 1);
+            // keep S-1 boxes in flight: the stage refilled here was released
+            // by the warp barrier at the end of the previous step
+            if (issued < nitems) issue_next();
             cp_async_commit();
-            cp_async_wait_pending(S - 1);  // this lane's copies of `item` landed
+            cp_async_wait_pending(S - 1);  // this lane's copies of the box landed
             __syncwarp();                  // ... and every other lane's
-            const uint8_t *w = stage0 + (size_t)(item % S) * kStageBytes + lane * kChunkBytes;
+            const uint8_t *w = stage0 + c_stage * kStageBytes + lane * kChunkBytes;
             const uint8_t *xa = a.xq + (int64_t)chunk * kQ8Bytes;
             int32_t *dp = (DOTS && row_ok) ? a.dots + row * dots_row + chunk * 8 : nullptr;
             if (FMT == kQ4K)
@@ -301,6 +318,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) xq_matvec_kernel(const Matv
             else
                 cb4_chunk<B, DOTS>(w, xa, bstride, T, hi, lo, dp, dots_bstride);
             __syncwarp();
+            if (++c_stage == S) c_stage = 0;
         }
         // tile epilogue: per-warp partials -> fixed-order sum over warps
         float2 *pb = part + (size_t)(k & 1) * W * B * 32;
@@ -316,7 +334,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) xq_matvec_kernel(const Matv
                     const float2 v = pb[(ww * B + b) * 32 + r];
                     acc_add(h, l, v.x, v.y);
                 }
-                if (grow < a.rows) a.y[(int64_t)b * a.rows + grow] = __fadd_rn(h, l);
+                if (grow < rows) a.y[(int64_t)b * rows + grow] = __fadd_rn(h, l);
             }
         }
     }

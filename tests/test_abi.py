@@ -113,19 +113,26 @@ def test_status_strings(raw):
     assert raw.xq_version() == 1
 
 
-@pytest.mark.parametrize("rows,cols,batch,warps,grid", [
-    (128256, 4096, 1, 8, 152), (128256, 4096, 8, 8, 152), (4096, 4096, 1, 8, 128),
-    (14336, 4096, 4, 8, 152), (4096, 14336, 8, 8, 128), (256, 1024, 1, 4, 8),
-    (11008, 4096, 1, 8, 152), (33, 256, 2, 1, 2), (1, 512, 1, 2, 1)])
-def test_plan(lib, rows, cols, batch, warps, grid):
-    p = lib.plan_matvec(rows, cols, batch, sm_count=152, smem_optin=232448)
+@pytest.mark.parametrize("fmt,rows,cols,batch,warps,grid", [
+    ("q4k", 128256, 4096, 1, 16, 152), ("q4k", 128256, 4096, 8, 8, 152),
+    ("q4k", 4096, 4096, 1, 16, 128), ("q4k", 14336, 4096, 4, 8, 152),
+    ("q4k", 4096, 14336, 1, 14, 128), ("q4k", 4096, 14336, 8, 8, 128),
+    ("q4k", 256, 1024, 1, 4, 8), ("cb4", 11008, 4096, 1, 8, 152), ("cb4", 4096, 4096, 1, 8, 128),
+    ("q4k", 33, 256, 2, 1, 2), ("q4k", 1, 512, 1, 2, 1), ("q4k", 100, 2304, 1, 9, 4),
+    ("q4k", 100, 2304, 2, 5, 4)])
+def test_plan(lib, fmt, rows, cols, batch, warps, grid):
+    p = lib.plan_matvec(rows, cols, batch, fmt=fmt, sm_count=152, smem_optin=232448)
     assert p["warps"] == warps and p["grid"] == grid
     assert p["tiles"] == (rows + 31) // 32
     assert p["chunks_per_row"] == cols // 256
     assert 2 <= p["stages"] <= 16
     assert p["smem_bytes"] <= 232448
-    # every warp owns at least one chunk of every tile
-    assert p["warps"] <= p["chunks_per_row"]
+    # every warp owns at least one chunk of every tile, and no fewer warps
+    # could give each warp fewer chunks per tile
+    nb = p["chunks_per_row"]
+    assert p["warps"] <= nb
+    per = -(-nb // p["warps"])
+    assert all(-(-nb // w) > per for w in range(1, p["warps"]))  # fewest warps for it
 
 
 def test_plan_override_is_clamped(lib):

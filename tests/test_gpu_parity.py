@@ -242,7 +242,7 @@ def test_extreme_codes(xq, orc):
 
 
 # ---------------------------------------------------------------- launch plans
-@pytest.mark.parametrize("cols,warps", [(256, 1), (512, 2), (1024, 4), (4096, 8), (14336, 8)])
+@pytest.mark.parametrize("cols,warps", [(256, 1), (512, 2), (1024, 4), (4096, 16), (14336, 14)])
 def test_plan_fires(xq, orc, cols, warps):
     rows = 70
     W = synthetic.q4k_weights(rows, cols, 4)
