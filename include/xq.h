@@ -119,18 +119,24 @@ xq_status xq_subdots_cb4(const void *W, const int8_t *table, const void *xq, int
 enum { XQ_FORMAT_Q4K = 0, XQ_FORMAT_CB4 = 1 };
 
 /* Launch plan of the mat-vec kernels (pure host computation; needs no GPU).
- * format: XQ_FORMAT_Q4K or XQ_FORMAT_CB4.
- * sm_count and smem_optin_bytes describe the device (for GB300: 152 SMs,
- * 232448 bytes).  warps: warps per CTA, each owning a ring of `stages`
- * 4608-byte shared-memory stages ([32 rows x 144 B] each); grid: persistent
- * CTAs; tiles: 32-row tiles. */
+ * format: XQ_FORMAT_Q4K or XQ_FORMAT_CB4.  sm_count and smem_optin_bytes
+ * describe the device (for GB300: 152 SMs, 232448 bytes).
+ * A work unit (row group) is rows_per_group rows read as `segments`
+ * contiguous boxes of at most 32 chunks of 256 weights (4608 bytes); lane l
+ * of a warp takes chunk l of a box.  Each of the `warps` warps of the `grid`
+ * persistent CTAs keeps stages-1 boxes in flight.  The batch's q8 blocks are
+ * staged in shared memory; if they do not fit, each call makes `launches`
+ * launches of batch_per_launch vectors (each re-reads W). */
 typedef struct {
     int32_t warps;
     int32_t stages;
     int32_t grid;
-    int32_t tiles;
+    int32_t rows_per_group;
+    int32_t segments;
     int32_t chunks_per_row;
-    int32_t reserved;
+    int64_t groups;
+    int32_t batch_per_launch;
+    int32_t launches;
     int64_t smem_bytes;
 } xq_plan;
 

@@ -22,8 +22,10 @@ _P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_
 
 class _Plan(ctypes.Structure):
     _fields_ = [("warps", ctypes.c_int32), ("stages", ctypes.c_int32), ("grid", ctypes.c_int32),
-                ("tiles", ctypes.c_int32), ("chunks_per_row", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("smem_bytes", ctypes.c_int64)]
+                ("rows_per_group", ctypes.c_int32), ("segments", ctypes.c_int32),
+                ("chunks_per_row", ctypes.c_int32), ("groups", ctypes.c_int64),
+                ("batch_per_launch", ctypes.c_int32), ("launches", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int64)]
 
 
 def _sig(name, restype, argtypes):
@@ -174,7 +176,7 @@ def subdots_cb4(W: torch.Tensor, table, xq: torch.Tensor, rows: int, cols: int,
 
 
 def _plan_dict(p: _Plan) -> dict:
-    return {f: getattr(p, f) for f, _ in _Plan._fields_ if f != "reserved"}
+    return {f: getattr(p, f) for f, _ in _Plan._fields_}
 
 
 FORMATS = {"q4k": 0, "cb4": 1}

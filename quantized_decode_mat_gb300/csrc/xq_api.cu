@@ -172,41 +172,62 @@ xq_status device_state(DeviceState **out) {
     return XQ_OK;
 }
 
-// Warps per CTA: the fewest chunks per warp per tile, reached with the fewest
-// warps (every warp then owns the same number of chunks when nb allows it),
-// within the instantiation's register budget (warps_limit).  Stages: 4, or as
-// many as fit in shared memory (at least 2).
+int64_t align128(int64_t v) { return (v + 127) & ~(int64_t)127; }
+
+// Work units: a row group is 32/nb rows (one contiguous 4608-byte box) when
+// nb is a power of two below 32, else one row streamed in ceil(nb/32) boxes.
+// The batch's q8 blocks are staged in shared memory; when they do not fit
+// beside two stages, the batch is split across launches (each re-reads W).
+// Grid: one CTA per SM, at most one per work unit.  Warps: enough to cover
+// the work units, within the instantiation's register budget.  Stages: 4, or
+// as many as fit (at least 2), then fewer warps if still needed.
 xq_status make_plan(int32_t fmt, int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
                     int64_t smem_optin, xq_plan *p) {
     const int32_t nb = (int32_t)(cols / 256);
-    const int32_t wmax = warps_limit(fmt, batch);
-    const int32_t lim = nb < wmax ? nb : wmax;
-    int32_t W = lim;
-    for (int32_t w = 1; w <= lim; ++w) {
-        if ((nb + w - 1) / w == (nb + lim - 1) / lim) {
-            W = w;
-            break;
-        }
-    }
+    const int32_t R = (nb < 32 && 32 % nb == 0) ? 32 / nb : 1;
+    const int32_t spr = R > 1 ? 1 : (nb + 31) / 32;
+    const int64_t groups = (rows + R - 1) / R;
+    int32_t bl = (int32_t)batch;
+    while (bl > 0 && align128((int64_t)bl * nb * kActStride) + 2LL * kStageBytes + 128 > smem_optin)
+        --bl;
+    if (bl < 1)
+        return fail(XQ_ESHAPE, "cols=%lld: one q8 vector does not fit in shared memory",
+                    (long long)cols);
+    const int64_t act = align128((int64_t)bl * nb * kActStride);
+    const int32_t grid = (int32_t)(groups < sm_count ? groups : sm_count);
+    const int32_t wmax = warps_limit(fmt, bl);
+    const int64_t per_cta = (groups + grid - 1) / grid;
+    int32_t W = (int32_t)(per_cta < wmax ? per_cta : wmax);
     const int32_t ow = g_override_warps.load(), os = g_override_stages.load();
-    if (ow > 0) W = ow < lim ? ow : lim;
+    if (ow > 0) W = ow < wmax ? ow : wmax;
     int32_t S = os > 0 ? os : 4;
     if (S < 2) S = 2;
     if (S > kMaxStages) S = kMaxStages;
-    const int64_t partials = 2LL * W * batch * 32 * 8;
-    auto bytes = [&](int32_t s) { return (int64_t)W * s * kStageBytes + partials + 128; };
-    while (bytes(S) > smem_optin && S > 2) --S;
-    if (bytes(S) > smem_optin)
+    auto bytes = [&](int32_t w, int32_t st) { return act + (int64_t)w * st * kStageBytes + 128; };
+    while (bytes(W, S) > smem_optin) {
+        if (S > 2)
+            --S;
+        else if (W > 1)
+            --W;
+        else
+            break;
+    }
+    if (bytes(W, S) > smem_optin)
         return fail(XQ_ESHAPE, "plan needs %lld bytes of shared memory, device allows %lld",
-                    (long long)bytes(S), (long long)smem_optin);
-    const int64_t tiles = (rows + kTileRows - 1) / kTileRows;
+                    (long long)bytes(W, S), (long long)smem_optin);
+    const int64_t tw = (int64_t)grid * W;
+    if (((groups + tw - 1) / tw) * spr > 0x7FFFFFFFLL)
+        return fail(XQ_ESHAPE, "too many boxes per warp");
     p->warps = W;
     p->stages = S;
-    p->tiles = (int32_t)tiles;
-    p->grid = (int32_t)(tiles < sm_count ? tiles : sm_count);
+    p->grid = grid;
+    p->rows_per_group = R;
+    p->segments = spr;
     p->chunks_per_row = nb;
-    p->reserved = 0;
-    p->smem_bytes = bytes(S);
+    p->groups = groups;
+    p->batch_per_launch = bl;
+    p->launches = (int32_t)((batch + bl - 1) / bl);
+    p->smem_bytes = bytes(W, S);
     return XQ_OK;
 }
 
@@ -240,12 +261,11 @@ xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *xq, 
     MatvecArgs a;
     memset(&a, 0, sizeof a);
     a.W = static_cast<const uint8_t *>(W);
-    a.xq = static_cast<const uint8_t *>(xq);
-    a.y = dots ? nullptr : static_cast<float *>(out);
-    a.dots = dots ? static_cast<int32_t *>(out) : nullptr;
     a.rows = rows;
+    a.groups = plan.groups;
     a.nb = (int32_t)nb;
-    a.ntiles = plan.tiles;
+    a.rows_per_group = plan.rows_per_group;
+    a.segments = plan.segments;
     a.stages = plan.stages;
     if (cb4) {
         for (int i = 0; i < 4; ++i) {
@@ -256,18 +276,24 @@ xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *xq, 
     }
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cb4 ? launch_matvec_cb4(a, (int)batch, dots, grid, block,
-                                            (size_t)plan.smem_bytes, s)
-                        : launch_matvec_q4k(a, (int)batch, dots, grid, block,
-                                            (size_t)plan.smem_bytes, s);
-    if (e != cudaSuccess) return cuda_fail(e, "mat-vec launch");
-    t_last_plan = plan;
-    t_have_plan = true;
     const int which = op == Op::kMatvecQ4K  ? XQ_COUNT_MATVEC_Q4K
                       : op == Op::kMatvecCB4 ? XQ_COUNT_MATVEC_CB4
                       : op == Op::kDotsQ4K   ? XQ_COUNT_SUBDOTS_Q4K
                                              : XQ_COUNT_SUBDOTS_CB4;
-    g_counts[which].fetch_add(1, std::memory_order_relaxed);
+    for (int64_t b0 = 0; b0 < batch; b0 += plan.batch_per_launch) {
+        const int64_t bc = batch - b0 < plan.batch_per_launch ? batch - b0 : plan.batch_per_launch;
+        a.xq = static_cast<const uint8_t *>(xq) + b0 * nb * kQ8Bytes;
+        a.y = dots ? nullptr : static_cast<float *>(out) + b0 * rows;
+        a.dots = dots ? static_cast<int32_t *>(out) + b0 * rows * nb * 8 : nullptr;
+        cudaError_t e = cb4 ? launch_matvec_cb4(a, (int)bc, dots, grid, block,
+                                                (size_t)plan.smem_bytes, s)
+                            : launch_matvec_q4k(a, (int)bc, dots, grid, block,
+                                                (size_t)plan.smem_bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "mat-vec launch");
+        g_counts[which].fetch_add(1, std::memory_order_relaxed);
+    }
+    t_last_plan = plan;
+    t_have_plan = true;
     return XQ_OK;
 }
 

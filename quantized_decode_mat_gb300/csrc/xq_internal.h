@@ -19,8 +19,9 @@ constexpr int kCb4Bytes = 18;       // codebook block
 // super-block, or eight codebook blocks (8 * 18).  It pairs with exactly one
 // q8 activation block.
 constexpr int kChunkBytes = 144;
-constexpr int kTileRows = 32;                       // one row per lane
+constexpr int kTileRows = 32;                       // lanes (chunks) per box
 constexpr int kStageBytes = kTileRows * kChunkBytes;  // one staged box: 4608 B
+constexpr int kActStride = 304;  // shared-memory stride of a staged q8 block (bytes 0..303)
 constexpr int kMaxWarps = 8;
 constexpr int kMaxStages = 8;
 
@@ -37,8 +38,10 @@ struct MatvecArgs {
     float *y;               // [batch][rows]
     int32_t *dots;          // [batch][rows][nb*8] (sub-dot launches only)
     int64_t rows;
+    int64_t groups;         // ceil(rows / rows_per_group)
     int32_t nb;             // 256-weight chunks per row
-    int32_t ntiles;         // ceil(rows / 32)
+    int32_t rows_per_group; // 32/nb if nb is a power of two below 32, else 1
+    int32_t segments;       // boxes per group: 1, or ceil(nb/32) when rows_per_group == 1
     int32_t stages;         // shared-memory stages per warp (2..8)
     uint32_t kv[4];         // codebook bytes kv[0..15], little-endian words
 };

@@ -2,27 +2,11 @@
 // the weight format, the batch (1..8) and whether it also emits the exact
 // integer dots.
 //
-// Mapping (GB300-first; the guide's kernels put one wave on one row and let
-// lanes take consecutive blocks of that row, "25 - Writing XPU Kernels"
-// 25.2 / 25.2.1):
-//   * A row is a run of 256-weight chunks, 144 bytes each in both formats (one
-//     Q4_K super-block, or eight 18-byte codebook blocks).  Chunk c pairs with
-//     q8 activation block c.
-//   * A CTA owns 32-row tiles (persistent, round-robin over the grid).  Its W
-//     warps split each tile's chunks (warp w takes chunks w, w+W, ...); lane l
-//     owns row 32*tile + l.  Each warp streams its [32 rows x 144 B] boxes
-//     through its own ring of shared-memory stages filled by coalesced
-//     16-byte asynchronous copies (cp.async, S-1 boxes in flight per warp),
-//     and the shared-memory side is one row per lane (144-byte lane stride:
-//     16-byte loads take the minimum four wavefronts).
-//   * Every lane of a warp is on the same chunk, so the activation block is
-//     the same address in all lanes: one broadcast load serves the warp.
-//   * Integer dots with dp4a, reduced to the super-block exactly in int32
-//     ("reduce first, then scale once", 25.2), then an f32 epilogue with an
-//     error-free compensation term (TwoProduct/TwoSum), so the float result
-//     is within a few f32 ulps of the exact one.
-//   * End of tile: each warp's per-row partial (hi, lo) goes to shared memory;
-//     one CTA barrier; the W partials are summed in a fixed order and stored.
+// Mapping: see the kernel below.  Integer dots with dp4a, reduced to the
+// super-block exactly in int32 ("reduce first, then scale once", "25 -
+// Writing XPU Kernels" 25.2), then an f32 epilogue with an error-free
+// compensation term (TwoProduct/TwoSum), so the float result is within a few
+// f32 ulps of the exact one.
 #pragma once
 
 #include "xq_internal.h"
@@ -53,7 +37,7 @@ __device__ __forceinline__ void q4k_epilogue(float xs, float d, float dmin, int 
 
 // ---- Q4_K chunk ---------------------------------------------------------------------
 // w: this lane's 144-byte super-block in shared memory.  xa: the chunk's q8
-// block of batch 0 in global memory (batch b at xa + b*bstride).
+// block of batch 0 in shared memory (batch b at xa + b*bstride).
 template <int B, bool DOTS>
 __device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w,
                                           const uint8_t *__restrict__ xa, int64_t bstride,
@@ -92,8 +76,8 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w,
         for (int g = 0; g < 4; ++g) {
             // sub-block 2g: activation bytes 64g..64g+31 (low nibbles of group g)
             // sub-block 2g+1: bytes 64g+32..64g+63 (high nibbles of group g)
-            const uint4 a0 = __ldg(xa4 + 4 * g + 0), a1 = __ldg(xa4 + 4 * g + 1);
-            const uint4 a2 = __ldg(xa4 + 4 * g + 2), a3 = __ldg(xa4 + 4 * g + 3);
+            const uint4 a0 = xa4[4 * g + 0], a1 = xa4[4 * g + 1];
+            const uint4 a2 = xa4[4 * g + 2], a3 = xa4[4 * g + 3];
             const uint32_t alo[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const uint32_t ahi[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
             // High nibbles are used in place (x16): an unsigned byte 16*q times
@@ -108,8 +92,8 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w,
             dot[2 * g] = d0;
             dot[2 * g + 1] = d1 >> 4;
         }
-        const uint4 s0 = __ldg(xa4 + 16), s1 = __ldg(xa4 + 17);  // eight int32 sums
-        const float xs = __ldg(reinterpret_cast<const float *>(xa + b * bstride + kQ8ScaleAt));
+        const uint4 s0 = xa4[16], s1 = xa4[17];  // eight int32 sums
+        const float xs = *reinterpret_cast<const float *>(xa + b * bstride + kQ8ScaleAt);
         const int bs[8] = {(int)s0.x, (int)s0.y, (int)s0.z, (int)s0.w,
                            (int)s1.x, (int)s1.y, (int)s1.z, (int)s1.w};
         int S1 = 0, S2 = 0;
@@ -187,7 +171,7 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w,
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             // block k: elements 0..15 against bytes 32k..32k+15, 16..31 against 32k+16..
-            const uint4 a0 = __ldg(xa4 + 2 * k), a1 = __ldg(xa4 + 2 * k + 1);
+            const uint4 a0 = xa4[2 * k], a1 = xa4[2 * k + 1];
             int dt = 0;
             dt = dp4a(LO[k][0], a0.x, dt);
             dt = dp4a(LO[k][1], a0.y, dt);
@@ -202,7 +186,7 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w,
             two_prod(dk[k], __int2float_rn(dt), p, e);  // |dt| < 2^20: exact in f32
             acc_add(ch, cl, p, e);
         }
-        const float xs = __ldg(reinterpret_cast<const float *>(xa + b * bstride + kQ8ScaleAt));
+        const float xs = *reinterpret_cast<const float *>(xa + b * bstride + kQ8ScaleAt);
         float t, te;
         two_prod(ch, xs, t, te);
         acc_add(hi[b], lo[b], t, __fmaf_rn(cl, xs, te));
@@ -215,14 +199,19 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w,
 }
 
 // ---- the kernel ------------------------------------------------------------------------
-// Shared memory: [W][S] stage buffers of 4608 B | [2][W][B][32] float2
-// partials.  Launch: blockDim = 32*W (W <= nb), grid <= ntiles, one CTA per SM.
+// Work unit: a row group of R rows.  When nb (256-weight chunks per row) is a
+// power of two below 32, R = 32/nb and the group is one contiguous 4608-byte
+// box; otherwise R = 1 and the row is streamed as ceil(nb/32) contiguous
+// segments of up to 32 chunks.  Lane l of the warp takes chunk l of the box
+// ("one wave per row, consecutive lanes read consecutive bytes", 25.2).
 //
-// A stage holds one [32 rows x 144 B] box.  The warp fills it with 16-byte
-// cp.async copies: copy p (0..287) moves bytes 16*(p%9).. of row p/9 of the
-// box, so 32 consecutive copies read about four contiguous 144-byte row
-// segments (coalesced) and land at shared offset 16*p (the box is dense in
-// shared memory).  Rows past the end of W are zero-filled (source size 0).
+// Shared memory: the batch's q8 blocks ([B][nb] blocks at a 304-byte stride,
+// staged once per CTA) | [W][S] box stages of 4608 bytes.  Each warp fills its
+// stages with coalesced 16-byte cp.async copies (copy p moves bytes 16p..16p+15
+// of the box to shared offset 16p; lane l's chunk lands at 144*l), keeping
+// S-1 boxes in flight.  A 304-byte act stride puts the chunks that one
+// instruction reads on distinct bank groups.
+//
 // Batch-1 Q4_K runs up to 16 warps per CTA (at most 128 registers a thread);
 // the other instantiations up to 8.
 template <int FMT, int B>
@@ -236,105 +225,109 @@ __global__ void __launch_bounds__(max_threads<FMT, B>(), 1) xq_matvec_kernel(con
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = a.stages;
-    uint8_t *stage0 = smem + (size_t)warp * S * kStageBytes;
-    const uint32_t stage0_u32 = smem_u32(stage0);
-    float2 *part = reinterpret_cast<float2 *>(smem + (size_t)W * S * kStageBytes);
-
     const int nb = a.nb;
-    const int nchunk = (nb - warp + W - 1) / W;  // chunks of each tile this warp takes
-    const int G = gridDim.x;
-    const int ntile_cta = (a.ntiles - (int)blockIdx.x + G - 1) / G;
-    const int nitems = ntile_cta * nchunk;
-    const int64_t bstride = (int64_t)nb * kQ8Bytes;
-    const int64_t dots_row = (int64_t)nb * 8;            // dots per row
-    const int64_t dots_bstride = a.rows * dots_row;      // dots per batch vector
-    const int64_t row_bytes = (int64_t)nb * kChunkBytes;
+    const int R = a.rows_per_group;
+    const int spr = a.segments;
     const int64_t rows = a.rows;
+    const int64_t ngroups = a.groups;
+    const int64_t row_bytes = (int64_t)nb * kChunkBytes;
+    uint8_t *act = smem;
+    const int act_bytes = (B * nb * kActStride + 127) & ~127;
+    uint8_t *stage0 = smem + act_bytes + (size_t)warp * S * kStageBytes;
+    const uint32_t stage0_u32 = smem_u32(stage0);
 
     uint32_t T[4] = {a.kv[0], a.kv[1], a.kv[2], a.kv[3]};
 
-    // This lane's nine copies of every box: row within the box, and the byte
-    // offset of the piece from the box's first byte in W.
-    int prow[9];
-    uint32_t roff[9];
-#pragma unroll
-    for (int k = 0; k < 9; ++k) {
-        const int p = lane + 32 * k;
-        prow[k] = p / 9;
-        roff[k] = (uint32_t)(prow[k] * row_bytes) + 16u * (uint32_t)(p - 9 * prow[k]);
+    // 1. the activation: bytes 0..303 of every q8 block (values, sums, scale)
+    for (int i = threadIdx.x; i < B * nb * 19; i += blockDim.x) {
+        const int blk = i / 19, piece = i - 19 * blk;
+        *reinterpret_cast<uint4 *>(act + blk * kActStride + 16 * piece) =
+            __ldg(reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes) + piece);
     }
+    __syncthreads();
 
-    // producer cursor: next box to request (tile step, chunk step, stage)
-    int p_k = 0, p_ci = 0, p_stage = 0, issued = 0;
+    // 2. this warp's row groups: gw, gw + TW, ...; every group's spr boxes
+    const int64_t gw = (int64_t)blockIdx.x * W + warp;
+    const int64_t TW = (int64_t)gridDim.x * W;
+    const int64_t my_groups = gw < ngroups ? (ngroups - 1 - gw) / TW + 1 : 0;
+    const int nitems = (int)(my_groups * spr);
+
+    int64_t pg = gw;                 // producer cursor: group, segment, stage
+    int ps = 0, p_stage = 0, issued = 0;
     auto issue_next = [&]() {
-        const int64_t row0 = ((int64_t)blockIdx.x + (int64_t)p_k * G) * kTileRows;
-        const uint8_t *tb = a.W + row0 * row_bytes + (warp + p_ci * W) * kChunkBytes;
-        const uint32_t dst = stage0_u32 + (uint32_t)p_stage * kStageBytes + 16u * lane;
-        if (row0 + kTileRows <= rows) {
-#pragma unroll
-            for (int k = 0; k < 9; ++k) cp_async_16_zfill(dst + 512u * k, tb + roff[k], 16u);
+        const int64_t row0 = pg * R;
+        const uint8_t *src0;
+        int valid;  // bytes of the box that exist in W
+        if (R > 1) {
+            src0 = a.W + row0 * row_bytes;
+            const int64_t rr = rows - row0;
+            valid = (int)((rr < R ? rr : R) * row_bytes);
         } else {
-#pragma unroll
-            for (int k = 0; k < 9; ++k) {
-                const bool in = row0 + prow[k] < rows;
-                cp_async_16_zfill(dst + 512u * k, in ? tb + roff[k] : a.W, in ? 16u : 0u);
-            }
+            const int c0 = ps * 32;
+            src0 = a.W + row0 * row_bytes + c0 * kChunkBytes;
+            valid = (nb - c0 < 32 ? nb - c0 : 32) * kChunkBytes;
         }
-        if (++p_ci == nchunk) {
-            p_ci = 0;
-            ++p_k;
+        const uint32_t dst = stage0_u32 + (uint32_t)p_stage * kStageBytes + 16u * lane;
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+            const int off = 16 * (lane + 32 * k);
+            if (off < valid) cp_async_16_zfill(dst + 512u * k, src0 + off, 16u);
+        }
+        if (++ps == spr) {
+            ps = 0;
+            pg += TW;
         }
         if (++p_stage == S) p_stage = 0;
         ++issued;
     };
 
-    // prologue: S-1 boxes in flight
-    for (int j = 0; j < S - 1; ++j) {
+    for (int j = 0; j < S - 1; ++j) {  // prologue: S-1 boxes in flight
         if (issued < nitems) issue_next();
         cp_async_commit();
     }
 
+    const int64_t act_bstride = (int64_t)nb * kActStride;
+    const int64_t dots_row = (int64_t)nb * 8;
+    const int64_t dots_bstride = rows * dots_row;
+    const int width = R > 1 ? nb : 32;  // lanes that share a row
     int c_stage = 0;
-    for (int k = 0; k < ntile_cta; ++k) {
-        const int tile = (int)blockIdx.x + k * G;
-        const int64_t row = (int64_t)tile * kTileRows + lane;
-        const bool row_ok = row < rows;
+    for (int64_t g = gw; g < ngroups; g += TW) {
+        const int64_t row = g * R + (R > 1 ? lane / nb : 0);
         float hi[B], lo[B];
 #pragma unroll
         for (int b = 0; b < B; ++b) hi[b] = lo[b] = 0.0f;
-        for (int ci = 0; ci < nchunk; ++ci) {
-            const int chunk = warp + ci * W;
-            // keep S-1 boxes in flight: the stage refilled here was released
-            // by the warp barrier at the end of the previous step
+        for (int s = 0; s < spr; ++s) {
             if (issued < nitems) issue_next();
             cp_async_commit();
             cp_async_wait_pending(S - 1);  // this lane's copies of the box landed
             __syncwarp();                  // ... and every other lane's
-            const uint8_t *w = stage0 + c_stage * kStageBytes + lane * kChunkBytes;
-            const uint8_t *xa = a.xq + (int64_t)chunk * kQ8Bytes;
-            int32_t *dp = (DOTS && row_ok) ? a.dots + row * dots_row + chunk * 8 : nullptr;
-            if (FMT == kQ4K)
-                q4k_chunk<B, DOTS>(w, xa, bstride, hi, lo, dp, dots_bstride);
-            else
-                cb4_chunk<B, DOTS>(w, xa, bstride, T, hi, lo, dp, dots_bstride);
+            const int c = R > 1 ? (lane & (nb - 1)) : s * 32 + lane;
+            const bool ok = R > 1 ? row < rows : c < nb;
+            if (ok) {
+                const uint8_t *w = stage0 + c_stage * kStageBytes + lane * kChunkBytes;
+                const uint8_t *xa = act + c * kActStride;
+                int32_t *dp = DOTS ? a.dots + row * dots_row + c * 8 : nullptr;
+                if (FMT == kQ4K)
+                    q4k_chunk<B, DOTS>(w, xa, act_bstride, hi, lo, dp, dots_bstride);
+                else
+                    cb4_chunk<B, DOTS>(w, xa, act_bstride, T, hi, lo, dp, dots_bstride);
+            }
             __syncwarp();
             if (++c_stage == S) c_stage = 0;
         }
-        // tile epilogue: per-warp partials -> fixed-order sum over warps
-        float2 *pb = part + (size_t)(k & 1) * W * B * 32;
-#pragma unroll
-        for (int b = 0; b < B; ++b) pb[(warp * B + b) * 32 + lane] = make_float2(hi[b], lo[b]);
-        __syncthreads();
         if (!DOTS) {
-            for (int p = threadIdx.x; p < B * 32; p += blockDim.x) {
-                const int b = p >> 5, r = p & 31;
-                const int64_t grow = (int64_t)tile * kTileRows + r;
-                float h = 0.0f, l = 0.0f;
-                for (int ww = 0; ww < W; ++ww) {
-                    const float2 v = pb[(ww * B + b) * 32 + r];
-                    acc_add(h, l, v.x, v.y);
+            // compensated butterfly over the row's lanes (aligned groups of `width`)
+            for (int off = width >> 1; off > 0; off >>= 1) {
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    const float oh = __shfl_xor_sync(0xffffffffu, hi[b], off);
+                    const float ol = __shfl_xor_sync(0xffffffffu, lo[b], off);
+                    acc_add(hi[b], lo[b], oh, ol);
                 }
-                if (grow < rows) a.y[(int64_t)b * rows + grow] = __fadd_rn(h, l);
+            }
+            if ((lane & (width - 1)) == 0 && row < rows) {
+#pragma unroll
+                for (int b = 0; b < B; ++b) a.y[(int64_t)b * rows + row] = __fadd_rn(hi[b], lo[b]);
             }
         }
     }

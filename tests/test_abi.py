@@ -113,33 +113,37 @@ def test_status_strings(raw):
     assert raw.xq_version() == 1
 
 
-@pytest.mark.parametrize("fmt,rows,cols,batch,warps,grid", [
-    ("q4k", 128256, 4096, 1, 16, 152), ("q4k", 128256, 4096, 8, 8, 152),
-    ("q4k", 4096, 4096, 1, 16, 128), ("q4k", 14336, 4096, 4, 8, 152),
-    ("q4k", 4096, 14336, 1, 14, 128), ("q4k", 4096, 14336, 8, 8, 128),
-    ("q4k", 256, 1024, 1, 4, 8), ("cb4", 11008, 4096, 1, 8, 152), ("cb4", 4096, 4096, 1, 8, 128),
-    ("q4k", 33, 256, 2, 1, 2), ("q4k", 1, 512, 1, 2, 1), ("q4k", 100, 2304, 1, 9, 4),
-    ("q4k", 100, 2304, 2, 5, 4)])
-def test_plan(lib, fmt, rows, cols, batch, warps, grid):
+@pytest.mark.parametrize("fmt,rows,cols,batch,warps,grid,R,spr,launches", [
+    ("q4k", 128256, 4096, 1, 16, 152, 2, 1, 1), ("q4k", 128256, 4096, 8, 8, 152, 2, 1, 1),
+    ("q4k", 4096, 4096, 1, 14, 152, 2, 1, 1), ("q4k", 14336, 4096, 4, 8, 152, 2, 1, 1),
+    ("q4k", 4096, 14336, 1, 16, 152, 1, 2, 1), ("q4k", 4096, 14336, 8, 8, 152, 1, 2, 1),
+    ("q4k", 256, 1024, 1, 1, 32, 8, 1, 1), ("cb4", 11008, 4096, 1, 8, 152, 2, 1, 1),
+    ("cb4", 4096, 4096, 1, 8, 152, 2, 1, 1), ("q4k", 33, 256, 2, 1, 2, 32, 1, 1),
+    ("q4k", 1, 512, 1, 1, 1, 16, 1, 1), ("q4k", 100, 2304, 1, 1, 100, 1, 1, 1),
+    ("q4k", 1000, 65536, 8, 7, 152, 1, 8, 4)])
+def test_plan(lib, fmt, rows, cols, batch, warps, grid, R, spr, launches):
     p = lib.plan_matvec(rows, cols, batch, fmt=fmt, sm_count=152, smem_optin=232448)
-    assert p["warps"] == warps and p["grid"] == grid
-    assert p["tiles"] == (rows + 31) // 32
-    assert p["chunks_per_row"] == cols // 256
-    assert 2 <= p["stages"] <= 16
+    assert (p["warps"], p["grid"], p["rows_per_group"], p["segments"], p["launches"]) == \
+        (warps, grid, R, spr, launches), p
+    nb = cols // 256
+    assert p["chunks_per_row"] == nb
+    assert p["groups"] == -(-rows // R)
+    # a work unit is whole rows in one 4608-byte box, or one row in 32-chunk boxes
+    assert (R > 1 and R * nb == 32 and spr == 1) or (R == 1 and spr == -(-nb // 32))
+    assert 2 <= p["stages"] <= 8
+    act = -(-p["batch_per_launch"] * nb * 304 // 128) * 128
+    assert p["smem_bytes"] == act + p["warps"] * p["stages"] * 4608 + 128
     assert p["smem_bytes"] <= 232448
-    # every warp owns at least one chunk of every tile, and no fewer warps
-    # could give each warp fewer chunks per tile
-    nb = p["chunks_per_row"]
-    assert p["warps"] <= nb
-    per = -(-nb // p["warps"])
-    assert all(-(-nb // w) > per for w in range(1, p["warps"]))  # fewest warps for it
+    assert p["batch_per_launch"] * (p["launches"] - 1) < batch <= p["batch_per_launch"] * p["launches"]
 
 
 def test_plan_override_is_clamped(lib):
     try:
-        lib.set_plan_override(warps=16, stages=64)
+        lib.set_plan_override(warps=32, stages=64)
         p = lib.plan_matvec(1000, 1024, 1)
-        assert p["warps"] == 4 and p["stages"] <= 16
+        assert p["warps"] == 16 and p["stages"] <= 8 and p["smem_bytes"] <= 232448
+        p = lib.plan_matvec(1000, 1024, 2)
+        assert p["warps"] == 8
         lib.set_plan_override(warps=2, stages=3)
         p = lib.plan_matvec(1000, 4096, 1)
         assert p["warps"] == 2 and p["stages"] == 3

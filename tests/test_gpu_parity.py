@@ -198,7 +198,7 @@ def test_config5_sampled(xq, orc, name):
     assert np.array_equal(xq_dev.cpu().numpy(), xq_ref)
     y = run_matvec(xq, "q4k", W, None, xq_dev, c.rows, c.cols, c.batch)
     plan = xq.last_plan()
-    assert plan["grid"] == min(plan["tiles"], torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["grid"] == min(plan["groups"], torch.cuda.get_device_properties(0).multi_processor_count)
     rng = np.random.Generator(np.random.PCG64(5))
     sample = np.unique(np.concatenate([np.arange(64), np.arange(c.rows - 70, c.rows),
                                        rng.choice(c.rows, 1500, replace=False)]))
@@ -242,15 +242,41 @@ def test_extreme_codes(xq, orc):
 
 
 # ---------------------------------------------------------------- launch plans
-@pytest.mark.parametrize("cols,warps", [(256, 1), (512, 2), (1024, 4), (4096, 16), (14336, 14)])
-def test_plan_fires(xq, orc, cols, warps):
+@pytest.mark.parametrize("cols", [256, 512, 1024, 2048, 4096, 4352, 14336])
+def test_plan_fires(xq, orc, cols):
+    """Each shape takes the work-unit shape meant for it: whole rows in one
+    box when cols/256 is a power of two below 32, else 32-chunk row segments."""
     rows = 70
     W = synthetic.q4k_weights(rows, cols, 4)
     x = synthetic.activations(1, cols, 5)
     xq_dev = run_quantize(xq, x)
-    run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, 1)
+    before = xq.launch_count(xq.COUNT_MATVEC_Q4K)
+    y = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, 1)
+    assert xq.launch_count(xq.COUNT_MATVEC_Q4K) == before + 1
     p = xq.last_plan()
-    assert p["warps"] == warps and p["tiles"] == 3 and p["grid"] == 3
+    nb = cols // 256
+    R = 32 // nb if nb < 32 and 32 % nb == 0 else 1
+    assert p["rows_per_group"] == R and p["segments"] == (1 if R > 1 else -(-nb // 32))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert p["groups"] == -(-rows // R) and p["grid"] == min(p["groups"], sms)
+    check_y(y, orc.matvec_q4k(W, orc.quantize_q8(x), rows, cols, 1), f"plan {cols}")
+
+
+def test_batch_split_when_activations_exceed_shared_memory(xq, orc):
+    """cols = 65536 with 8 vectors: the q8 blocks (8 x 256 x 304 bytes) do not
+    fit in shared memory, so the call makes several launches of fewer vectors."""
+    rows, cols, batch = 37, 65536, 8
+    W = synthetic.q4k_weights(rows, cols, 14)
+    x = synthetic.activations(batch, cols, 15)
+    xq_dev = run_quantize(xq, x)
+    before = xq.launch_count(xq.COUNT_MATVEC_Q4K)
+    y = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch)
+    p = xq.last_plan()
+    assert p["launches"] > 1 and xq.launch_count(xq.COUNT_MATVEC_Q4K) == before + p["launches"]
+    xq_ref = orc.quantize_q8(x)
+    check_y(y, orc.matvec_q4k(W, xq_ref, rows, cols, batch), "batch split")
+    dots = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch, dots=True)
+    assert np.array_equal(dots, orc.subdots_q4k(W, xq_ref, rows, cols, batch))
 
 
 @pytest.mark.parametrize("warps,stages", [(1, 2), (2, 3), (3, 5), (8, 2), (8, 6), (4, 8)])
