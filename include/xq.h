@@ -142,9 +142,9 @@ typedef struct {
 
 xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t batch,
                          int32_t sm_count, int64_t smem_optin_bytes, xq_plan *plan);
-/* Override the automatic plan for sweeps: warps (1..16 for batch-1 Q4_K,
- * else 1..8) and stages (2..8),
- * 0 = automatic.  Process-wide; not for concurrent use with launches. */
+/* Override the automatic plan for sweeps: warps (up to 16 at batch 1, 8
+ * above) and stages (2..8), 0 = automatic.  Process-wide; not for concurrent
+ * use with launches. */
 void xq_set_plan_override(int32_t warps, int32_t stages);
 /* Plan used by the calling thread's last mat-vec or sub-dot launch. */
 xq_status xq_last_plan(xq_plan *plan);

@@ -179,9 +179,9 @@ int64_t align128(int64_t v) { return (v + 127) & ~(int64_t)127; }
 // The batch's q8 blocks are staged in shared memory; when they do not fit
 // beside two stages, the batch is split across launches (each re-reads W).
 // Grid: one CTA per SM, at most one per work unit.  Warps: enough to cover
-// the work units, within the instantiation's register budget.  Stages: 4, or
-// as many as fit (at least 2), then fewer warps if still needed.
-xq_status make_plan(int32_t fmt, int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
+// the work units, within the instantiation's register budget.  Stages: 2
+// (measured best), fewer warps if even that does not fit.
+xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
                     int64_t smem_optin, xq_plan *p) {
     const int32_t nb = (int32_t)(cols / 256);
     const int32_t R = (nb < 32 && 32 % nb == 0) ? 32 / nb : 1;
@@ -195,12 +195,14 @@ xq_status make_plan(int32_t fmt, int64_t rows, int64_t cols, int64_t batch, int3
                     (long long)cols);
     const int64_t act = align128((int64_t)bl * nb * kActStride);
     const int32_t grid = (int32_t)(groups < sm_count ? groups : sm_count);
-    const int32_t wmax = warps_limit(fmt, bl);
+    const int32_t wmax = warps_limit(bl);
     const int64_t per_cta = (groups + grid - 1) / grid;
     int32_t W = (int32_t)(per_cta < wmax ? per_cta : wmax);
     const int32_t ow = g_override_warps.load(), os = g_override_stages.load();
     if (ow > 0) W = ow < wmax ? ow : wmax;
-    int32_t S = os > 0 ? os : 4;
+    // Two stages (one box in flight per warp while the other is consumed) read
+    // fastest on GB300: the warps of the GPU then stream one contiguous window.
+    int32_t S = os > 0 ? os : 2;
     if (S < 2) S = 2;
     if (S > kMaxStages) S = kMaxStages;
     auto bytes = [&](int32_t w, int32_t st) { return act + (int64_t)w * st * kStageBytes + 128; };
@@ -255,8 +257,7 @@ xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *xq, 
     DeviceState *dev = nullptr;
     if (xq_status s = device_state(&dev)) return s;
     xq_plan plan;
-    if (xq_status s = make_plan(cb4 ? kCB4 : kQ4K, rows, cols, batch, dev->sm_count,
-                                dev->smem_optin, &plan))
+    if (xq_status s = make_plan(rows, cols, batch, dev->sm_count, dev->smem_optin, &plan))
         return s;
     MatvecArgs a;
     memset(&a, 0, sizeof a);
@@ -367,8 +368,7 @@ xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t bat
         return fail(XQ_EINVAL, "format must be XQ_FORMAT_Q4K or XQ_FORMAT_CB4");
     if (xq_status s = check_shape(rows, cols, batch, true)) return s;
     if (sm_count < 1) return fail(XQ_EINVAL, "sm_count must be positive");
-    return make_plan(format == XQ_FORMAT_CB4 ? kCB4 : kQ4K, rows, cols, batch, sm_count,
-                     smem_optin_bytes, plan);
+    return make_plan(rows, cols, batch, sm_count, smem_optin_bytes, plan);
 }
 
 void xq_set_plan_override(int32_t warps, int32_t stages) {

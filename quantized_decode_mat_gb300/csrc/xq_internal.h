@@ -21,16 +21,19 @@ constexpr int kCb4Bytes = 18;       // codebook block
 constexpr int kChunkBytes = 144;
 constexpr int kTileRows = 32;                       // lanes (chunks) per box
 constexpr int kStageBytes = kTileRows * kChunkBytes;  // one staged box: 4608 B
-constexpr int kActStride = 304;  // shared-memory stride of a staged q8 block (bytes 0..303)
+// Shared-memory stride of a staged q8 block: bytes 0..303 of the block, then
+// its split sums at 304..319; 336 = 84 words puts 8 consecutive chunks on
+// distinct 4-bank groups.
+constexpr int kActStride = 336;
+constexpr int kActSplitAt = 304;
 constexpr int kMaxWarps = 8;
 constexpr int kMaxStages = 8;
 
 enum Format { kQ4K = 0, kCB4 = 1 };
 
-// Largest warps per CTA of an instantiation (its register budget allows no more).
-constexpr int warps_limit(int fmt, int64_t batch) {
-    return (fmt == kQ4K && batch == 1) ? 2 * kMaxWarps : kMaxWarps;
-}
+// Largest warps per CTA of an instantiation, which its register budget
+// allows no more: 16 at batch 1 (at most 128 registers a thread), 8 above.
+constexpr int warps_limit(int64_t batch) { return batch == 1 ? 2 * kMaxWarps : kMaxWarps; }
 
 struct MatvecArgs {
     const uint8_t *W;       // [rows][nb][144]

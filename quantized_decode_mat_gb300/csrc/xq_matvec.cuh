@@ -2,17 +2,51 @@
 // the weight format, the batch (1..8) and whether it also emits the exact
 // integer dots.
 //
-// Mapping: see the kernel below.  Integer dots with dp4a, reduced to the
-// super-block exactly in int32 ("reduce first, then scale once", "25 -
-// Writing XPU Kernels" 25.2), then an f32 epilogue with an error-free
-// compensation term (TwoProduct/TwoSum), so the float result is within a few
-// f32 ulps of the exact one.
+// Arithmetic: integer dots with dp4a, reduced to the super-block exactly in
+// int32 ("reduce first, then scale once", "25 - Writing XPU Kernels" 25.2),
+// then an f32 epilogue with an error-free compensation term (TwoProduct /
+// TwoSum), so the float result is within a few f32 ulps of the exact one.
 #pragma once
 
 #include "xq_internal.h"
 #include "xq_ptx.cuh"
 
 namespace xq {
+
+// ---- activation views ----------------------------------------------------------------
+// A staged q8 block (one chunk of one activation vector) in shared memory,
+// kActStride bytes apart per chunk and nb*kActStride apart per vector:
+//   [0,256) int8 values   [256,288) int32 sums   [288,292) f32 scale
+//   [304,320) the eight sums split into bytes: low bytes of sums 0..3, of
+//   4..7 (unsigned), then high bytes (sum >> 8, signed) of 0..3, of 4..7.
+struct ActSmem {
+    const uint8_t *p;
+    int64_t bstride;
+    __device__ __forceinline__ uint4 q16(int b, int i) const {  // values 16i..16i+15
+        return reinterpret_cast<const uint4 *>(p + b * bstride)[i];
+    }
+    __device__ __forceinline__ float xs(int b) const {
+        return *reinterpret_cast<const float *>(p + b * bstride + kQ8ScaleAt);
+    }
+    __device__ __forceinline__ uint4 split(int b) const {
+        return *reinterpret_cast<const uint4 *>(p + b * bstride + kActSplitAt);
+    }
+};
+
+// The eight sub-block sums (each |s| <= 127*32) as unsigned low bytes and
+// signed high bytes, so that sum_j m_j*s_j is four dp4a: s = 256*hi + lo.
+__device__ __forceinline__ uint4 split_sums(uint4 s0, uint4 s1) {
+    const uint32_t s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    uint32_t l0 = 0, l1 = 0, h0 = 0, h1 = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        l0 |= (s[j] & 0xFFu) << (8 * j);
+        l1 |= (s[j + 4] & 0xFFu) << (8 * j);
+        h0 |= (((uint32_t)((int)s[j] >> 8)) & 0xFFu) << (8 * j);
+        h1 |= (((uint32_t)((int)s[j + 4] >> 8)) & 0xFFu) << (8 * j);
+    }
+    return make_uint4(l0, l1, h0, h1);
+}
 
 // ---- shared epilogue --------------------------------------------------------
 // Adds xs*(d*S1 - dmin*S2) to (hi, lo).  S1, S2 exact integers; |S2| < 2^24;
@@ -35,12 +69,14 @@ __device__ __forceinline__ void q4k_epilogue(float xs, float d, float dmin, int 
     acc_add(hi, lo, t2, small);
 }
 
+__device__ __forceinline__ int byte_of(uint32_t x, int k) {
+    return (int)__byte_perm(x, 0u, 0x4440u | (uint32_t)k);
+}
+
 // ---- Q4_K chunk ---------------------------------------------------------------------
-// w: this lane's 144-byte super-block in shared memory.  xa: the chunk's q8
-// block of batch 0 in shared memory (batch b at xa + b*bstride).
-template <int B, bool DOTS>
-__device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w,
-                                          const uint8_t *__restrict__ xa, int64_t bstride,
+// w: this lane's 144-byte super-block in shared memory; act: its q8 blocks.
+template <int B, bool DOTS, class Act>
+__device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w, const Act &act,
                                           float (&hi)[B], float (&lo)[B], int32_t *dots,
                                           int64_t dots_bstride) {
     const uint4 h = *reinterpret_cast<const uint4 *>(w);
@@ -55,29 +91,26 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w,
     }
     const float d = f16_bits_to_f32(h.x);
     const float dmin = f16_bits_to_f32(h.x >> 16);
-    // six-bit scales and mins: bytes 4..7 (h.y), 8..11 (h.z), 12..15 (h.w)
+    // six-bit scales and mins, one byte each: bytes 4..7 (h.y), 8..11 (h.z), 12..15 (h.w)
     const uint32_t sc_lo = h.y & 0x3F3F3F3Fu;
     const uint32_t m_lo = h.z & 0x3F3F3F3Fu;
     const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
     const uint32_t m_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
-    int sc[8], mn[8];
+    int sc[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        sc[j] = (sc_lo >> (8 * j)) & 0xFF;
-        sc[j + 4] = (sc_hi >> (8 * j)) & 0xFF;
-        mn[j] = (m_lo >> (8 * j)) & 0xFF;
-        mn[j + 4] = (m_hi >> (8 * j)) & 0xFF;
+        sc[j] = byte_of(sc_lo, j);
+        sc[j + 4] = byte_of(sc_hi, j);
     }
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-        const uint4 *xa4 = reinterpret_cast<const uint4 *>(xa + b * bstride);
         int dot[8];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-            // sub-block 2g: activation bytes 64g..64g+31 (low nibbles of group g)
-            // sub-block 2g+1: bytes 64g+32..64g+63 (high nibbles of group g)
-            const uint4 a0 = xa4[4 * g + 0], a1 = xa4[4 * g + 1];
-            const uint4 a2 = xa4[4 * g + 2], a3 = xa4[4 * g + 3];
+            // sub-block 2g: values 64g..64g+31 (low nibbles of group g);
+            // sub-block 2g+1: values 64g+32..64g+63 (high nibbles of group g)
+            const uint4 a0 = act.q16(b, 4 * g + 0), a1 = act.q16(b, 4 * g + 1);
+            const uint4 a2 = act.q16(b, 4 * g + 2), a3 = act.q16(b, 4 * g + 3);
             const uint32_t alo[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const uint32_t ahi[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
             // High nibbles are used in place (x16): an unsigned byte 16*q times
@@ -92,17 +125,13 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w,
             dot[2 * g] = d0;
             dot[2 * g + 1] = d1 >> 4;
         }
-        const uint4 s0 = xa4[16], s1 = xa4[17];  // eight int32 sums
-        const float xs = *reinterpret_cast<const float *>(xa + b * bstride + kQ8ScaleAt);
-        const int bs[8] = {(int)s0.x, (int)s0.y, (int)s0.z, (int)s0.w,
-                           (int)s1.x, (int)s1.y, (int)s1.z, (int)s1.w};
-        int S1 = 0, S2 = 0;
+        int S1 = 0;
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            S1 += sc[s] * dot[s];
-            S2 += mn[s] * bs[s];
-        }
-        q4k_epilogue(xs, d, dmin, S1, S2, hi[b], lo[b]);
+        for (int s = 0; s < 8; ++s) S1 += sc[s] * dot[s];
+        const uint4 sp = act.split(b);  // sum_j m_j * bsum_j as four byte dots
+        const int S2 = dp4a_uu(m_hi, sp.y, dp4a_uu(m_lo, sp.x, 0)) +
+                       256 * dp4a_us(m_hi, sp.w, dp4a_us(m_lo, sp.z, 0));
+        q4k_epilogue(act.xs(b), d, dmin, S1, S2, hi[b], lo[b]);
         if (DOTS && dots != nullptr) {
             int4 *o = reinterpret_cast<int4 *>(dots + b * dots_bstride);
             o[0] = make_int4(dot[0], dot[1], dot[2], dot[3]);
@@ -132,9 +161,8 @@ __device__ __forceinline__ void cb4_decode(uint32_t q, const uint32_t (&T)[4], u
     HI = __byte_perm(f0, f1, 0x7531u);  // kv[H0], kv[H1], kv[H2], kv[H3]
 }
 
-template <int B, bool DOTS>
-__device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w,
-                                          const uint8_t *__restrict__ xa, int64_t bstride,
+template <int B, bool DOTS, class Act>
+__device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const Act &act,
                                           const uint32_t (&T)[4], float (&hi)[B], float (&lo)[B],
                                           int32_t *dots, int64_t dots_bstride) {
     uint32_t v[36];
@@ -165,13 +193,12 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w,
     }
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-        const uint4 *xa4 = reinterpret_cast<const uint4 *>(xa + b * bstride);
         float ch = 0.0f, cl = 0.0f;  // sum_k d_k * dot_k, compensated
         int dts[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            // block k: elements 0..15 against bytes 32k..32k+15, 16..31 against 32k+16..
-            const uint4 a0 = xa4[2 * k], a1 = xa4[2 * k + 1];
+            // block k: elements 0..15 against values 32k..32k+15, 16..31 against 32k+16..
+            const uint4 a0 = act.q16(b, 2 * k), a1 = act.q16(b, 2 * k + 1);
             int dt = 0;
             dt = dp4a(LO[k][0], a0.x, dt);
             dt = dp4a(LO[k][1], a0.y, dt);
@@ -186,7 +213,7 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w,
             two_prod(dk[k], __int2float_rn(dt), p, e);  // |dt| < 2^20: exact in f32
             acc_add(ch, cl, p, e);
         }
-        const float xs = *reinterpret_cast<const float *>(xa + b * bstride + kQ8ScaleAt);
+        const float xs = act.xs(b);
         float t, te;
         two_prod(ch, xs, t, te);
         acc_add(hi[b], lo[b], t, __fmaf_rn(cl, xs, te));
@@ -204,21 +231,19 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w,
 // box; otherwise R = 1 and the row is streamed as ceil(nb/32) contiguous
 // segments of up to 32 chunks.  Lane l of the warp takes chunk l of the box
 // ("one wave per row, consecutive lanes read consecutive bytes", 25.2).
+// Global warp g (warp-major over CTAs) takes groups g, g + TW, ...
 //
-// Shared memory: the batch's q8 blocks ([B][nb] blocks at a 304-byte stride,
-// staged once per CTA) | [W][S] box stages of 4608 bytes.  Each warp fills its
-// stages with coalesced 16-byte cp.async copies (copy p moves bytes 16p..16p+15
-// of the box to shared offset 16p; lane l's chunk lands at 144*l), keeping
-// S-1 boxes in flight.  A 304-byte act stride puts the chunks that one
-// instruction reads on distinct bank groups.
-//
-// Batch-1 Q4_K runs up to 16 warps per CTA (at most 128 registers a thread);
-// the other instantiations up to 8.
-template <int FMT, int B>
-constexpr int max_threads() { return warps_limit(FMT, B) * 32; }
+// Shared memory: the batch's q8 blocks, staged once per CTA at kActStride
+// bytes per chunk | [W][S] box stages of 4608 bytes.  Each warp fills its
+// stages with coalesced 16-byte cp.async copies (copy p moves bytes
+// 16p..16p+15 of the box to shared offset 16p; lane l's chunk lands at
+// 144*l), keeping S-1 boxes in flight.  The act stride puts the chunks that
+// one instruction reads on distinct bank groups.
+template <int B>
+constexpr int max_threads() { return warps_limit(B) * 32; }
 
 template <int FMT, int B, bool DOTS>
-__global__ void __launch_bounds__(max_threads<FMT, B>(), 1) xq_matvec_kernel(const MatvecArgs a) {
+__global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const MatvecArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const int W = blockDim.x >> 5;
@@ -231,28 +256,31 @@ __global__ void __launch_bounds__(max_threads<FMT, B>(), 1) xq_matvec_kernel(con
     const int64_t rows = a.rows;
     const int64_t ngroups = a.groups;
     const int64_t row_bytes = (int64_t)nb * kChunkBytes;
+    const int64_t act_bstride = (int64_t)nb * kActStride;
+    const int act_bytes = (int)((B * act_bstride + 127) & ~(int64_t)127);
     uint8_t *act = smem;
-    const int act_bytes = (B * nb * kActStride + 127) & ~127;
     uint8_t *stage0 = smem + act_bytes + (size_t)warp * S * kStageBytes;
     const uint32_t stage0_u32 = smem_u32(stage0);
 
     uint32_t T[4] = {a.kv[0], a.kv[1], a.kv[2], a.kv[3]};
 
-    // 1. the activation: bytes 0..303 of every q8 block (values, sums, scale)
-    for (int i = threadIdx.x; i < B * nb * 19; i += blockDim.x) {
-        const int blk = i / 19, piece = i - 19 * blk;
+    // 1. the activation: bytes 0..303 of every q8 block, then its split sums
+    for (int i = threadIdx.x; i < B * nb * 20; i += blockDim.x) {
+        const int blk = i / 20, piece = i - 20 * blk;
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
         *reinterpret_cast<uint4 *>(act + blk * kActStride + 16 * piece) =
-            __ldg(reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes) + piece);
+            piece < 19 ? __ldg(src + piece) : split_sums(__ldg(src + 16), __ldg(src + 17));
     }
     __syncthreads();
 
-    // 2. this warp's row groups: gw, gw + TW, ...; every group's spr boxes
-    const int64_t gw = (int64_t)blockIdx.x * W + warp;
-    const int64_t TW = (int64_t)gridDim.x * W;
+    // 2. this warp's row groups and their boxes
+    const int G = gridDim.x;
+    const int64_t gw = (int64_t)warp * G + blockIdx.x;
+    const int64_t TW = (int64_t)G * W;
     const int64_t my_groups = gw < ngroups ? (ngroups - 1 - gw) / TW + 1 : 0;
     const int nitems = (int)(my_groups * spr);
 
-    int64_t pg = gw;                 // producer cursor: group, segment, stage
+    int64_t pg = gw;  // producer cursor: group, segment, stage
     int ps = 0, p_stage = 0, issued = 0;
     auto issue_next = [&]() {
         const int64_t row0 = pg * R;
@@ -267,11 +295,15 @@ __global__ void __launch_bounds__(max_threads<FMT, B>(), 1) xq_matvec_kernel(con
             src0 = a.W + row0 * row_bytes + c0 * kChunkBytes;
             valid = (nb - c0 < 32 ? nb - c0 : 32) * kChunkBytes;
         }
+        const uint8_t *src = src0 + 16 * lane;
         const uint32_t dst = stage0_u32 + (uint32_t)p_stage * kStageBytes + 16u * lane;
+        if (valid == kStageBytes) {
 #pragma unroll
-        for (int k = 0; k < 9; ++k) {
-            const int off = 16 * (lane + 32 * k);
-            if (off < valid) cp_async_16_zfill(dst + 512u * k, src0 + off, 16u);
+            for (int k = 0; k < 9; ++k) cp_async_16(dst + 512u * k, src + 512 * k);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 9; ++k)
+                if (16 * (lane + 32 * k) < valid) cp_async_16(dst + 512u * k, src + 512 * k);
         }
         if (++ps == spr) {
             ps = 0;
@@ -286,7 +318,6 @@ __global__ void __launch_bounds__(max_threads<FMT, B>(), 1) xq_matvec_kernel(con
         cp_async_commit();
     }
 
-    const int64_t act_bstride = (int64_t)nb * kActStride;
     const int64_t dots_row = (int64_t)nb * 8;
     const int64_t dots_bstride = rows * dots_row;
     const int width = R > 1 ? nb : 32;  // lanes that share a row
@@ -305,12 +336,12 @@ __global__ void __launch_bounds__(max_threads<FMT, B>(), 1) xq_matvec_kernel(con
             const bool ok = R > 1 ? row < rows : c < nb;
             if (ok) {
                 const uint8_t *w = stage0 + c_stage * kStageBytes + lane * kChunkBytes;
-                const uint8_t *xa = act + c * kActStride;
                 int32_t *dp = DOTS ? a.dots + row * dots_row + c * 8 : nullptr;
+                const ActSmem as{act + c * kActStride, act_bstride};
                 if (FMT == kQ4K)
-                    q4k_chunk<B, DOTS>(w, xa, act_bstride, hi, lo, dp, dots_bstride);
+                    q4k_chunk<B, DOTS>(w, as, hi, lo, dp, dots_bstride);
                 else
-                    cb4_chunk<B, DOTS>(w, xa, act_bstride, T, hi, lo, dp, dots_bstride);
+                    cb4_chunk<B, DOTS>(w, as, T, hi, lo, dp, dots_bstride);
             }
             __syncwarp();
             if (++c_stage == S) c_stage = 0;
@@ -350,8 +381,8 @@ inline cudaError_t configure_t(int smem_optin) {
 template <int FMT>
 inline cudaError_t launch_matvec_fmt(const MatvecArgs &a, int batch, bool dots, dim3 grid,
                                      dim3 block, size_t smem, cudaStream_t s) {
-#define XQ_CASE(BB)                                                                \
-    case BB:                                                               \
+#define XQ_CASE(BB)                                                           \
+    case BB:                                                                  \
         return dots ? launch_matvec_t<FMT, BB, true>(a, grid, block, smem, s) \
                     : launch_matvec_t<FMT, BB, false>(a, grid, block, smem, s);
     switch (batch) {

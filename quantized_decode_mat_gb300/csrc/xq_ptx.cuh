@@ -22,6 +22,11 @@ __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void *src,
                  : "memory");
 }
 
+// The same without the source-size operand (a full 16-byte copy).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -56,6 +61,13 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     int d;
     asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
+}
+
+// Four (unsigned byte x unsigned byte) products summed into c.
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    uint32_t d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"((uint32_t)c));
+    return (int)d;
 }
 
 __device__ __forceinline__ float f16_bits_to_f32(uint32_t bits16) {
