@@ -3,9 +3,11 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--case NAME]
 
-One step = one pass of the whole hot path over one batch: quantise the f32
-activation to q8 blocks (xq_quantize_q8) and the Q4_K mat-vec (xq_matvec_q4k),
-inputs resident in HBM.  Default workload: the L2-exceeding vocabulary
+One step = one pass of the whole hot path over one batch: the fused decode
+step xq_linear_q4k (quantise the f32 activation to q8 blocks and the Q4_K
+mat-vec, one launch), inputs resident in HBM.  The two-call path
+(xq_quantize_q8 + xq_matvec_q4k) and the mat-vec alone on q8 input are timed
+beside it for the breakdown.  Default workload: the L2-exceeding vocabulary
 projection, Q4_K 128256 x 4096, batch 1 (W = 295.5 MB, larger than the 129 MB
 L2, so no flush is needed between steps).  Steps are replayed from CUDA graphs
 and timed with CUDA events on the launching stream.
@@ -53,12 +55,15 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "matvec_q4k_traffic.json")
 
 # ---------------------------------------------------------------- helpers
 def step_bytes(c) -> dict:
-    """Algorithmic bytes: every weight byte once, the f32 activation read once,
-    the q8 blocks written once and read once, y written once."""
+    """Algorithmic bytes per call: every weight byte once, y written once, and
+    the activation as each path moves it.  linear: the fused step reads f32 x
+    (its q8 blocks never leave the SM); matvec: the mat-vec on q8 input reads
+    the q8 blocks; two_call: quantise (x in, q8 out) then the mat-vec."""
     q8 = c.batch * (c.cols // 256) * 320
-    matvec = c.w_bytes + q8 + 4 * c.batch * c.rows
-    return {"matvec": matvec, "step": matvec + 4 * c.batch * c.cols + q8,
-            "weights": c.w_bytes}
+    x = 4 * c.batch * c.cols
+    y = 4 * c.batch * c.rows
+    return {"weights": c.w_bytes, "linear": c.w_bytes + x + y,
+            "matvec": c.w_bytes + q8 + y, "two_call": c.w_bytes + x + 2 * q8 + y}
 
 
 def source_digest() -> str:
@@ -82,9 +87,10 @@ def measured_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_per_launch(case_name: str):
-    """DRAM bytes per mat-vec launch from a committed ncu capture, valid only
-    while the kernel sources are unchanged since the capture."""
+def traffic_per_launch(kernel: str, case_name: str):
+    """DRAM bytes per launch of a kernel ("linear" or "matvec") on a case, from
+    a committed ncu capture; None unless the kernel sources are unchanged
+    since that capture."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             rec = json.load(f)
@@ -92,7 +98,7 @@ def traffic_per_launch(case_name: str):
         return None
     if rec.get("source_digest") != source_digest():
         return None
-    return rec.get("cases", {}).get(case_name)
+    return rec.get("cases", {}).get(f"{kernel}/{case_name}")
 
 
 class ClockSampler:
@@ -221,10 +227,11 @@ class OracleRunner:
             f.result()
 
     def bytes_per_step(self) -> int:
+        """Algorithmic bytes of the sample, counted as for the fused step:
+        the weights once, x read once, y written once."""
         c = self.c
-        q8 = c.batch * (c.cols // 256) * 320
         w = self.rows * (c.cols // 256) * 144
-        return w + 4 * c.batch * c.cols + 2 * q8 + 4 * c.batch * self.rows
+        return w + 4 * c.batch * c.cols + 4 * c.batch * self.rows
 
     def close(self):
         self.pool.shutdown()
@@ -300,7 +307,7 @@ def workload_config(c) -> dict:
                         if c.fmt == "q4k" else f"{c.name}: codebook {c.rows}x{c.cols} batch {c.batch}",
             "format": c.fmt, "rows": c.rows, "cols": c.cols, "batch": c.batch,
             "weight_bytes": c.w_bytes,
-            "step": "xq_quantize_q8 + xq_matvec_" + c.fmt,
+            "step": "xq_linear_" + c.fmt + " (quantise + mat-vec, one launch)",
             "l2": f"inputs larger than L2 (W {c.w_bytes / 1e6:.1f} MB > 129 MB); no flush"
                   if c.w_bytes > L2_BYTES else "W fits in L2: hot-L2 timing",
             "parallelism": "replicas (one independent mat-vec per GPU)"}
@@ -325,19 +332,26 @@ def run_ours(args, c):
     y = torch.empty((c.batch, c.rows), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def do_matvec():
+    def do_step():  # the whole hot path in one launch: quantise x, mat-vec
+        if c.fmt == "q4k":
+            xq.linear_q4k(x, W, c.rows, c.cols, out=y)
+        else:
+            xq.linear_cb4(x, W, kv, c.rows, c.cols, out=y)
+
+    def do_matvec():  # the mat-vec alone on q8 input
         if c.fmt == "q4k":
             xq.matvec_q4k(W, xq_buf, c.rows, c.cols, out=y)
         else:
             xq.matvec_cb4(W, kv, xq_buf, c.rows, c.cols, out=y)
 
-    def do_step():
+    def do_two_call():  # xq_quantize_q8, then the mat-vec
         xq.quantize_q8(x, out=xq_buf)
         do_matvec()
 
-    # eager warm-up: first call per device configures the kernels (before capture)
+    # eager warm-up: the first call per device configures the kernels (before capture)
     with torch.cuda.stream(stream):
         for _ in range(3):
+            do_two_call()
             do_step()
     stream.synchronize()
 
@@ -349,51 +363,47 @@ def run_ours(args, c):
         return g
 
     per_graph = max(1, min(args.steps, 100))
-    counts0 = [xq.launch_count(i) for i in range(5)]
-    g_step = capture(do_step, per_graph)
-    launches_per_step = sum(xq.launch_count(i) - counts0[i] for i in range(5)) / per_graph
     rem = args.steps % per_graph
-    g_rem = capture(do_step, rem) if rem else None
-    g_mv = capture(do_matvec, per_graph)
-    g_mv_rem = capture(do_matvec, rem) if rem else None
+    ncount = 7
+    counts0 = [xq.launch_count(i) for i in range(ncount)]
+    graphs = {}
+    for name, fn in (("step", do_step), ("matvec", do_matvec), ("two_call", do_two_call)):
+        graphs[name] = (capture(fn, per_graph), capture(fn, rem) if rem else None)
+        if name == "step":
+            launches_per_step = sum(xq.launch_count(i) - counts0[i]
+                                    for i in range(ncount)) / per_graph
 
-    def replay(g, g_r, k):
-        for _ in range(k // per_graph):
-            g.replay()
-        if k % per_graph:
-            g_r.replay()
+    def timed(name, k):
+        g, g_r = graphs[name]
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(k // per_graph):
+                g.replay()
+            if k % per_graph:
+                g_r.replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        return ev0.elapsed_time(ev1) / k
 
     # warm-up steps (untimed), then the timed region: exactly K steps
     with torch.cuda.stream(stream):
-        for _ in range(max(1, args.warmup // per_graph)):
-            g_step.replay()
+        for _ in range(max(1, -(-args.warmup // per_graph))):
+            graphs["step"][0].replay()
     stream.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        replay(g_step, g_rem, args.steps)
-        ev1.record(stream)
-    ev1.synchronize()
+    step_ms = timed("step", args.steps)
     torch.cuda.synchronize()
-    t_wall1 = time.time()
     barrier(dist)
-    step_ms = ev0.elapsed_time(ev1) / args.steps
     step_ms_max = max_over_ranks(step_ms, dist)
-
-    # the mat-vec kernel alone (roofline): K launches, same stream
-    with torch.cuda.stream(stream):
-        g_mv.replay()
-        ev0.record(stream)
-        replay(g_mv, g_mv_rem, args.steps)
-        ev1.record(stream)
-    ev1.synchronize()
-    mv_ms = ev0.elapsed_time(ev1) / args.steps
+    # the same kernels outside the step, for the breakdown
+    mv_ms = timed("matvec", args.steps)
+    two_ms = timed("two_call", args.steps)
     time.sleep(0.2)
     sampler.stop()
     clocks = sampler.summary(t_wall0, time.time())
@@ -402,6 +412,7 @@ def run_ours(args, c):
     x_host = torch.from_numpy(x_np).pin_memory()
     y_host = torch.empty((c.batch, c.rows), dtype=torch.float32).pin_memory()
     e2e_steps = max(3, min(args.steps, 2000))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for _ in range(3):
             x.copy_(x_host, non_blocking=True)
@@ -421,29 +432,35 @@ def run_ours(args, c):
     if rank != 0:
         return
     nbytes = step_bytes(c)
-    value = world * nbytes["step"] / (step_ms_max * 1e-3) / 1e9
-    achieved = nbytes["matvec"] / (mv_ms * 1e-3) / 1e9
+    value = world * nbytes["linear"] / (step_ms_max * 1e-3) / 1e9
+    achieved = nbytes["linear"] / (step_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
     cpu = oracle_rate(c, wall_budget_s=args.cpu_seconds, threads=os.cpu_count() or 1)
+    fmt = "Q4_K" if c.fmt == "q4k" else "codebook"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
-        "us_per_matvec": mv_ms * 1e3, "higher_is_better": True, "scaling": "weak",
+        "us_per_matvec": step_ms * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8 dp4a (int32 sums) + f32 epilogue",
         "data": "synthetic (seeded, shapes and distributions of the decode workloads)",
         "config": workload_config(c),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy (burst)",
                      "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
-                     "traffic": traffic_per_launch(c.name),
-                     "kernel": "xq_matvec_kernel<" + c.fmt + ", batch %d>" % c.batch,
-                     "algorithmic_bytes_per_launch": nbytes["matvec"]},
+                     "traffic": traffic_per_launch("linear", c.name),
+                     "kernel": f"xq_matvec_kernel<{fmt}, batch {c.batch}, fused quantise>",
+                     "algorithmic_bytes_per_launch": nbytes["linear"]},
+        "breakdown": {
+            "matvec_on_q8_input": {"us": mv_ms * 1e3,
+                                   "GBs": nbytes["matvec"] / (mv_ms * 1e-3) / 1e9},
+            "quantise_then_matvec": {"us": two_ms * 1e3,
+                                     "GBs": nbytes["two_call"] / (two_ms * 1e-3) / 1e9}},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": world * nbytes["linear"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
                 "h2d_bytes_per_step": 4 * c.batch * c.cols,
                 "d2h_bytes_per_step": 4 * c.batch * c.rows,
-                "path": "pinned x -> cudaMemcpyAsync -> xq_quantize_q8 -> xq_matvec -> "
+                "path": "pinned x -> cudaMemcpyAsync -> xq_linear (one launch) -> "
                         "cudaMemcpyAsync -> pinned y, eager calls through the Python binding"},
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "launches_per_step": launches_per_step,

@@ -107,6 +107,18 @@ xq_status xq_matvec_q4k(const void *W, const void *xq, float *y, int64_t rows, i
 xq_status xq_matvec_cb4(const void *W, const int8_t *table, const void *xq, float *y,
                         int64_t rows, int64_t cols, int64_t batch, void *stream);
 
+/* The fused decode step: quantise x ([batch][cols] f32, device) to q8 blocks
+ * exactly as xq_quantize_q8 does, and compute y = W . x as xq_matvec_q4k /
+ * xq_matvec_cb4 do, in one launch and without a q8 buffer: every CTA
+ * quantises the activation into its own shared memory.  y is bit-identical
+ * to the two-call path.  x must be 16-byte aligned.  Source: the fused tail
+ * of "25 - Writing XPU Kernels" 25.5 (chained launches cost round trips; a
+ * fused tail removes the gaps as well as the launches). */
+xq_status xq_linear_q4k(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
+                        int64_t batch, void *stream);
+xq_status xq_linear_cb4(const float *x, const void *W, const int8_t *table, float *y,
+                        int64_t rows, int64_t cols, int64_t batch, void *stream);
+
 /* Test exports: the exact per-sub-block integer dots of the same kernels.
  * dots: [batch][rows][cols/32] int32 (device).  Q4_K: dots[b][r][8k+s] is
  * dot_s of super-block k; codebook: dots[b][r][k] is dot_k of block k. */
@@ -156,7 +168,9 @@ enum {
     XQ_COUNT_MATVEC_CB4 = 2,
     XQ_COUNT_SUBDOTS_Q4K = 3,
     XQ_COUNT_SUBDOTS_CB4 = 4,
-    XQ_COUNT_N = 5
+    XQ_COUNT_LINEAR_Q4K = 5,
+    XQ_COUNT_LINEAR_CB4 = 6,
+    XQ_COUNT_N = 7
 };
 uint64_t xq_launch_count(int32_t which);
 

@@ -8,11 +8,14 @@ fallback: if the library is missing this package raises on import.
     xq  = quantize_q8(x)                       # x: f32 [batch, cols] on cuda
     y   = matvec_q4k(W, xq, rows, cols)        # W: uint8 Q4_K rows on cuda
     y   = matvec_cb4(W, table, xq, rows, cols) # W: uint8 codebook rows
+    y   = linear_q4k(x, W, rows, cols)         # fused: quantise + mat-vec, one launch
 """
 from __future__ import annotations
 
 from . import _native
 from ._native import (  # noqa: F401
+    COUNT_LINEAR_CB4,
+    COUNT_LINEAR_Q4K,
     COUNT_MATVEC_CB4,
     COUNT_MATVEC_Q4K,
     COUNT_QUANTIZE,
@@ -24,6 +27,8 @@ from ._native import (  # noqa: F401
     last_plan,
     launch_count,
     lib_path,
+    linear_cb4,
+    linear_q4k,
     matvec_cb4,
     matvec_q4k,
     plan_matvec,

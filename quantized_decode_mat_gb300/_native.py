@@ -41,6 +41,8 @@ _cb4_bytes = _sig("xq_cb4_bytes", _SZ, [_I64, _I64])
 _quantize = _sig("xq_quantize_q8", ctypes.c_int, [_P, _P, _I64, _I64, _P])
 _matvec_q4k = _sig("xq_matvec_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
 _matvec_cb4 = _sig("xq_matvec_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
+_linear_q4k = _sig("xq_linear_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
+_linear_cb4 = _sig("xq_linear_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
 _subdots_q4k = _sig("xq_subdots_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
 _subdots_cb4 = _sig("xq_subdots_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
 _plan = _sig("xq_plan_matvec", ctypes.c_int, [_I32, _I64, _I64, _I64, _I32, _I64,
@@ -54,7 +56,8 @@ _status_string = _sig("xq_status_string", ctypes.c_char_p, [ctypes.c_int])
 _last_error = _sig("xq_last_error", ctypes.c_char_p, [])
 _version = _sig("xq_version", _I32, [])
 
-COUNT_QUANTIZE, COUNT_MATVEC_Q4K, COUNT_MATVEC_CB4, COUNT_SUBDOTS_Q4K, COUNT_SUBDOTS_CB4 = range(5)
+(COUNT_QUANTIZE, COUNT_MATVEC_Q4K, COUNT_MATVEC_CB4, COUNT_SUBDOTS_Q4K, COUNT_SUBDOTS_CB4,
+ COUNT_LINEAR_Q4K, COUNT_LINEAR_CB4) = range(7)
 
 
 class XQError(RuntimeError):
@@ -150,6 +153,40 @@ def matvec_cb4(W: torch.Tensor, table, xq: torch.Tensor, rows: int, cols: int,
     _check(_matvec_cb4(_dev(W, "W", torch.uint8), ctypes.cast(_table(table), _P),
                        _dev(xq, "xq", torch.uint8), _dev(out, "y", torch.float32), rows, cols,
                        batch, _stream(stream)))
+    return out
+
+
+def _x2d(x: torch.Tensor) -> torch.Tensor:
+    return x.unsqueeze(0) if x.dim() == 1 else x
+
+
+def linear_q4k(x: torch.Tensor, W: torch.Tensor, rows: int, cols: int,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Fused decode step: quantise x (f32 [batch, cols], CUDA) and multiply by
+    the Q4_K rows W in one launch -> f32 [batch, rows]."""
+    x = _x2d(x)
+    batch = x.shape[0]
+    if x.shape[1] != cols:
+        raise ValueError("x has the wrong number of columns")
+    if out is None:
+        out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    _check(_linear_q4k(_dev(x, "x", torch.float32), _dev(W, "W", torch.uint8),
+                       _dev(out, "y", torch.float32), rows, cols, batch, _stream(stream)))
+    return out
+
+
+def linear_cb4(x: torch.Tensor, W: torch.Tensor, table, rows: int, cols: int,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Fused decode step for codebook rows W with a host 16-entry int8 table."""
+    x = _x2d(x)
+    batch = x.shape[0]
+    if x.shape[1] != cols:
+        raise ValueError("x has the wrong number of columns")
+    if out is None:
+        out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    _check(_linear_cb4(_dev(x, "x", torch.float32), _dev(W, "W", torch.uint8),
+                       ctypes.cast(_table(table), _P), _dev(out, "y", torch.float32), rows,
+                       cols, batch, _stream(stream)))
     return out
 
 

@@ -8,6 +8,7 @@
 #include <string>
 
 #include "xq_internal.h"
+#include "xq_q8.cuh"
 
 namespace xq {
 
@@ -17,13 +18,10 @@ namespace xq {
 __device__ uint32_t g_status_word;
 
 // ---- q8 activation quantiser ------------------------------------------------------
-// One warp per 256-value block; lane l holds values 8l..8l+7, so lanes 4s..4s+3
-// hold sub-block s.  Rule (one f32 rounding per operation, no contraction):
-//   amax = max|x|; iscale = 127/amax; q = clamp(rint(x*iscale), -127, 127)
-//   (round half to even; a NaN product gives 0); d = amax/127; zero block ->
-//   d = 0, q = 0.  The eight 32-value sums are exact int32.
-// Source: "25 - Writing XPU Kernels" 25.2 (q8_K: 256 int8 values, eight
-// sub-block sums at +256, one f32 scale at +288, 320 bytes).
+// One warp per 256-value block (the arithmetic is q8_quantize_lane, shared with
+// the fused kernels); lane l holds values 8l..8l+7, so lanes 4s..4s+3 hold
+// sub-block s.  Layout: values @0, int32 sums @256, f32 scale @288, zero
+// bytes 292..319.
 __global__ void __launch_bounds__(256) q8_quantize_kernel(const float *__restrict__ x,
                                                           uint8_t *__restrict__ xq,
                                                           int64_t nblocks) {
@@ -33,58 +31,14 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float *__restric
     const float4 *src = reinterpret_cast<const float4 *>(x + blk * 256 + lane * 8);
     const float4 u = __ldg(src), v = __ldg(src + 1);
     const float vals[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float t = fabsf(vals[i]);
-        amax = t > amax ? t : amax;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, amax, off);
-        amax = o > amax ? o : amax;
-    }
-    int q[8];
-    if (amax == 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = 0;
-    } else {
-        const float iscale = __fdiv_rn(127.0f, amax);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float t = __fmul_rn(vals[i], iscale);
-            int r;
-            if (t != t)
-                r = 0;
-            else if (t >= 127.0f)
-                r = 127;
-            else if (t <= -127.0f)
-                r = -127;
-            else
-                r = __float2int_rn(t);  // round half to even
-            q[i] = r;
-        }
-    }
+    const Q8Lane r = q8_quantize_lane(vals);
     uint8_t *out = xq + blk * kQ8Bytes;
-    uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        w0 |= (uint32_t)(q[i] & 0xFF) << (8 * i);
-        w1 |= (uint32_t)(q[4 + i] & 0xFF) << (8 * i);
-    }
-    *reinterpret_cast<uint2 *>(out + lane * 8) = make_uint2(w0, w1);
-    int sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sum += q[i];
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    if ((lane & 3) == 0) *reinterpret_cast<int *>(out + kQ8SumAt + (lane >> 2) * 4) = sum;
-    if (lane == 0) {
-        const float d = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, 127.0f);
-        *reinterpret_cast<float *>(out + kQ8ScaleAt) = d;
-    } else if (lane < 8) {
+    *reinterpret_cast<uint2 *>(out + lane * 8) = make_uint2(r.w0, r.w1);
+    if ((lane & 3) == 0) *reinterpret_cast<int *>(out + kQ8SumAt + (lane >> 2) * 4) = r.sum;
+    if (lane == 0)
+        *reinterpret_cast<float *>(out + kQ8ScaleAt) = r.d;
+    else if (lane < 8)
         *reinterpret_cast<uint32_t *>(out + kQ8ScaleAt + 4 * lane) = 0u;  // bytes 292..319
-    }
 }
 
 namespace {
@@ -233,25 +187,30 @@ xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
     return XQ_OK;
 }
 
-enum class Op { kMatvecQ4K, kMatvecCB4, kDotsQ4K, kDotsCB4 };
+enum class Op { kMatvecQ4K, kMatvecCB4, kDotsQ4K, kDotsCB4, kLinearQ4K, kLinearCB4 };
 
-xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *xq, void *out,
+// in: q8 blocks (mat-vec and sub-dots) or f32 x (the fused linear ops).
+xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *in, void *out,
                      int64_t rows, int64_t cols, int64_t batch, void *stream) {
-    const bool cb4 = (op == Op::kMatvecCB4 || op == Op::kDotsCB4);
+    const bool cb4 = (op == Op::kMatvecCB4 || op == Op::kDotsCB4 || op == Op::kLinearCB4);
     const bool dots = (op == Op::kDotsQ4K || op == Op::kDotsCB4);
+    const bool fused = (op == Op::kLinearQ4K || op == Op::kLinearCB4);
     t_error.clear();
-    if (!W || !xq || !out) return fail(XQ_EINVAL, "null device pointer (W, xq or output)");
+    if (!W || !in || !out)
+        return fail(XQ_EINVAL, fused ? "null device pointer (x, W or y)"
+                                     : "null device pointer (W, xq or output)");
     if (cb4 && !table) return fail(XQ_EINVAL, "null codebook table");
     if (xq_status s = check_shape(rows, cols, batch, true)) return s;
     if (!aligned(W, 16)) return fail(XQ_EALIGN, "W must be 16-byte aligned");
-    if (!aligned(xq, 16)) return fail(XQ_EALIGN, "xq must be 16-byte aligned");
+    if (!aligned(in, 16)) return fail(XQ_EALIGN, fused ? "x must be 16-byte aligned"
+                                                         : "xq must be 16-byte aligned");
     if (!aligned(out, dots ? 16 : 4))
         return fail(XQ_EALIGN, dots ? "dots must be 16-byte aligned" : "y must be 4-byte aligned");
     const int64_t nb = cols / 256;
     const size_t w_bytes = (size_t)rows * nb * kChunkBytes;
-    const size_t x_bytes = (size_t)batch * nb * kQ8Bytes;
+    const size_t in_bytes = fused ? (size_t)batch * cols * 4 : (size_t)batch * nb * kQ8Bytes;
     const size_t o_bytes = (size_t)batch * rows * (dots ? nb * 8 * 4 : 4);
-    if (overlap(out, o_bytes, W, w_bytes) || overlap(out, o_bytes, xq, x_bytes))
+    if (overlap(out, o_bytes, W, w_bytes) || overlap(out, o_bytes, in, in_bytes))
         return fail(XQ_EINVAL, "output overlaps an input");
 
     DeviceState *dev = nullptr;
@@ -277,18 +236,24 @@ xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *xq, 
     }
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int which = op == Op::kMatvecQ4K  ? XQ_COUNT_MATVEC_Q4K
-                      : op == Op::kMatvecCB4 ? XQ_COUNT_MATVEC_CB4
-                      : op == Op::kDotsQ4K   ? XQ_COUNT_SUBDOTS_Q4K
-                                             : XQ_COUNT_SUBDOTS_CB4;
+    const int kind = dots ? 1 : fused ? 2 : 0;
+    const int which = op == Op::kMatvecQ4K   ? XQ_COUNT_MATVEC_Q4K
+                      : op == Op::kMatvecCB4  ? XQ_COUNT_MATVEC_CB4
+                      : op == Op::kDotsQ4K    ? XQ_COUNT_SUBDOTS_Q4K
+                      : op == Op::kDotsCB4    ? XQ_COUNT_SUBDOTS_CB4
+                      : op == Op::kLinearQ4K  ? XQ_COUNT_LINEAR_Q4K
+                                              : XQ_COUNT_LINEAR_CB4;
     for (int64_t b0 = 0; b0 < batch; b0 += plan.batch_per_launch) {
         const int64_t bc = batch - b0 < plan.batch_per_launch ? batch - b0 : plan.batch_per_launch;
-        a.xq = static_cast<const uint8_t *>(xq) + b0 * nb * kQ8Bytes;
+        if (fused)
+            a.x = static_cast<const float *>(in) + b0 * cols;
+        else
+            a.xq = static_cast<const uint8_t *>(in) + b0 * nb * kQ8Bytes;
         a.y = dots ? nullptr : static_cast<float *>(out) + b0 * rows;
         a.dots = dots ? static_cast<int32_t *>(out) + b0 * rows * nb * 8 : nullptr;
-        cudaError_t e = cb4 ? launch_matvec_cb4(a, (int)bc, dots, grid, block,
+        cudaError_t e = cb4 ? launch_matvec_cb4(a, (int)bc, kind, grid, block,
                                                 (size_t)plan.smem_bytes, s)
-                            : launch_matvec_q4k(a, (int)bc, dots, grid, block,
+                            : launch_matvec_q4k(a, (int)bc, kind, grid, block,
                                                 (size_t)plan.smem_bytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "mat-vec launch");
         g_counts[which].fetch_add(1, std::memory_order_relaxed);
@@ -348,6 +313,16 @@ xq_status xq_matvec_q4k(const void *W, const void *xq_in, float *y, int64_t rows
 xq_status xq_matvec_cb4(const void *W, const int8_t *table, const void *xq_in, float *y,
                         int64_t rows, int64_t cols, int64_t batch, void *stream) {
     return run_matvec(Op::kMatvecCB4, W, table, xq_in, y, rows, cols, batch, stream);
+}
+
+xq_status xq_linear_q4k(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
+                        int64_t batch, void *stream) {
+    return run_matvec(Op::kLinearQ4K, W, nullptr, x, y, rows, cols, batch, stream);
+}
+
+xq_status xq_linear_cb4(const float *x, const void *W, const int8_t *table, float *y,
+                        int64_t rows, int64_t cols, int64_t batch, void *stream) {
+    return run_matvec(Op::kLinearCB4, W, table, x, y, rows, cols, batch, stream);
 }
 
 xq_status xq_subdots_q4k(const void *W, const void *xq_in, int32_t *dots, int64_t rows,

@@ -37,7 +37,8 @@ constexpr int warps_limit(int64_t batch) { return batch == 1 ? 2 * kMaxWarps : k
 
 struct MatvecArgs {
     const uint8_t *W;       // [rows][nb][144]
-    const uint8_t *xq;      // [batch][nb][320]
+    const uint8_t *xq;      // [batch][nb][320] (q8 input)
+    const float *x;         // [batch][cols] (fused quantise + mat-vec input)
     float *y;               // [batch][rows]
     int32_t *dots;          // [batch][rows][nb*8] (sub-dot launches only)
     int64_t rows;
@@ -50,9 +51,11 @@ struct MatvecArgs {
 };
 
 // Launch entry points implemented per format (xq_matvec_q4k.cu / _cb4.cu).
-cudaError_t launch_matvec_q4k(const MatvecArgs &a, int batch, bool dots, dim3 grid, dim3 block,
+// kind: 0 = mat-vec on q8 blocks, 1 = the same with the exact dots,
+// 2 = fused quantise + mat-vec on f32 x.
+cudaError_t launch_matvec_q4k(const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,
                               size_t smem, cudaStream_t s);
-cudaError_t launch_matvec_cb4(const MatvecArgs &a, int batch, bool dots, dim3 grid, dim3 block,
+cudaError_t launch_matvec_cb4(const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,
                               size_t smem, cudaStream_t s);
 // Raise the dynamic shared memory limit of every instantiation of a format.
 cudaError_t configure_matvec_q4k(int smem_optin);

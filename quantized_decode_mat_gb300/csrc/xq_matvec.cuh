@@ -1,6 +1,7 @@
 // Persistent, asynchronously staged decode mat-vec for sm_103a, templated on
-// the weight format, the batch (1..8) and whether it also emits the exact
-// integer dots.
+// the weight format, the batch (1..8), whether it also emits the exact
+// integer dots, and whether it quantises the f32 activation itself (the
+// fused quantise + mat-vec) or reads q8 blocks.
 //
 // Arithmetic: integer dots with dp4a, reduced to the super-block exactly in
 // int32 ("reduce first, then scale once", "25 - Writing XPU Kernels" 25.2),
@@ -10,6 +11,7 @@
 
 #include "xq_internal.h"
 #include "xq_ptx.cuh"
+#include "xq_q8.cuh"
 
 namespace xq {
 
@@ -242,7 +244,7 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const A
 template <int B>
 constexpr int max_threads() { return warps_limit(B) * 32; }
 
-template <int FMT, int B, bool DOTS>
+template <int FMT, int B, bool DOTS, bool FUSED>
 __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const MatvecArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
@@ -264,12 +266,36 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
 
     uint32_t T[4] = {a.kv[0], a.kv[1], a.kv[2], a.kv[3]};
 
-    // 1. the activation: bytes 0..303 of every q8 block, then its split sums
-    for (int i = threadIdx.x; i < B * nb * 20; i += blockDim.x) {
-        const int blk = i / 20, piece = i - 20 * blk;
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
-        *reinterpret_cast<uint4 *>(act + blk * kActStride + 16 * piece) =
-            piece < 19 ? __ldg(src + piece) : split_sums(__ldg(src + 16), __ldg(src + 17));
+    // 1. the activation
+    if (FUSED) {
+        // quantise x here: warp w takes blocks w, w+W, ... of the batch (the
+        // same arithmetic as the standalone quantiser, so the same bytes)
+        for (int blk = warp; blk < B * nb; blk += W) {
+            const float4 *src = reinterpret_cast<const float4 *>(a.x + (int64_t)blk * 256 + lane * 8);
+            const float4 u = __ldg(src), v = __ldg(src + 1);
+            const float vals[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+            const Q8Lane r = q8_quantize_lane(vals);
+            uint8_t *dst = act + blk * kActStride;
+            *reinterpret_cast<uint2 *>(dst + lane * 8) = make_uint2(r.w0, r.w1);
+            if ((lane & 3) == 0) *reinterpret_cast<int *>(dst + kQ8SumAt + (lane >> 2) * 4) = r.sum;
+            uint32_t sums[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sums[j] = (uint32_t)__shfl_sync(0xffffffffu, r.sum, 4 * j);
+            if (lane == 0) {
+                *reinterpret_cast<float *>(dst + kQ8ScaleAt) = r.d;
+                *reinterpret_cast<uint4 *>(dst + kActSplitAt) =
+                    split_sums(make_uint4(sums[0], sums[1], sums[2], sums[3]),
+                               make_uint4(sums[4], sums[5], sums[6], sums[7]));
+            }
+        }
+    } else {
+        // bytes 0..303 of every q8 block, then its split sums
+        for (int i = threadIdx.x; i < B * nb * 20; i += blockDim.x) {
+            const int blk = i / 20, piece = i - 20 * blk;
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
+            *reinterpret_cast<uint4 *>(act + blk * kActStride + 16 * piece) =
+                piece < 19 ? __ldg(src + piece) : split_sums(__ldg(src + 16), __ldg(src + 17));
+        }
     }
     __syncthreads();
 
@@ -365,26 +391,29 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
     cp_async_wait_all();  // only empty groups can remain; keeps the exit clean
 }
 
-template <int FMT, int B, bool DOTS>
+template <int FMT, int B, bool DOTS, bool FUSED>
 inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, size_t smem,
                                    cudaStream_t s) {
-    xq_matvec_kernel<FMT, B, DOTS><<<grid, block, smem, s>>>(a);
+    xq_matvec_kernel<FMT, B, DOTS, FUSED><<<grid, block, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-template <int FMT, int B, bool DOTS>
+template <int FMT, int B, bool DOTS, bool FUSED>
 inline cudaError_t configure_t(int smem_optin) {
-    return cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS>,
+    return cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSED>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
 }
 
+// kind: 0 = mat-vec on q8 blocks, 1 = the same with the exact dots,
+// 2 = fused quantise + mat-vec.
 template <int FMT>
-inline cudaError_t launch_matvec_fmt(const MatvecArgs &a, int batch, bool dots, dim3 grid,
+inline cudaError_t launch_matvec_fmt(const MatvecArgs &a, int batch, int kind, dim3 grid,
                                      dim3 block, size_t smem, cudaStream_t s) {
-#define XQ_CASE(BB)                                                           \
-    case BB:                                                                  \
-        return dots ? launch_matvec_t<FMT, BB, true>(a, grid, block, smem, s) \
-                    : launch_matvec_t<FMT, BB, false>(a, grid, block, smem, s);
+#define XQ_CASE(BB)                                                                    \
+    case BB:                                                                           \
+        return kind == 1   ? launch_matvec_t<FMT, BB, true, false>(a, grid, block, smem, s)  \
+               : kind == 2 ? launch_matvec_t<FMT, BB, false, true>(a, grid, block, smem, s)  \
+                           : launch_matvec_t<FMT, BB, false, false>(a, grid, block, smem, s);
     switch (batch) {
         XQ_CASE(1)
         XQ_CASE(2)
@@ -403,9 +432,10 @@ inline cudaError_t launch_matvec_fmt(const MatvecArgs &a, int batch, bool dots, 
 template <int FMT>
 inline cudaError_t configure_fmt(int smem_optin) {
     cudaError_t e = cudaSuccess;
-#define XQ_CFG(BB)                                                      \
-    if (e == cudaSuccess) e = configure_t<FMT, BB, false>(smem_optin); \
-    if (e == cudaSuccess) e = configure_t<FMT, BB, true>(smem_optin);
+#define XQ_CFG(BB)                                                             \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, false, false>(smem_optin); \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, true, false>(smem_optin);  \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, false, true>(smem_optin);
     XQ_CFG(1)
     XQ_CFG(2)
     XQ_CFG(3)

@@ -1,12 +1,12 @@
-// Codebook instantiations of the mat-vec kernel (batch 1..8, with and without
-// the exact sub-dot export).
+// Codebook instantiations of the mat-vec kernel (batch 1..8; on q8 blocks,
+// with the exact sub-dot export, and fused with the activation quantiser).
 #include "xq_matvec.cuh"
 
 namespace xq {
 
-cudaError_t launch_matvec_cb4(const MatvecArgs &a, int batch, bool dots, dim3 grid, dim3 block,
+cudaError_t launch_matvec_cb4(const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,
                               size_t smem, cudaStream_t s) {
-    return launch_matvec_fmt<kCB4>(a, batch, dots, grid, block, smem, s);
+    return launch_matvec_fmt<kCB4>(a, batch, kind, grid, block, smem, s);
 }
 
 cudaError_t configure_matvec_cb4(int smem_optin) { return configure_fmt<kCB4>(smem_optin); }

@@ -37,7 +37,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for must in ("xq_quantize_q8", "xq_matvec_q4k", "xq_matvec_cb4", "xq_subdots_q4k",
+    for must in ("xq_quantize_q8", "xq_matvec_q4k", "xq_matvec_cb4", "xq_linear_q4k",
+                 "xq_linear_cb4", "xq_subdots_q4k",
                  "xq_subdots_cb4", "xq_q8_bytes", "xq_status_string", "xq_last_error"):
         assert must in names
 
@@ -86,6 +87,19 @@ def test_matvec_q4k_argument_checks(raw, args, status):
     err = ctypes.CDLL(raw._name).xq_last_error
     err.restype = ctypes.c_char_p
     assert err()
+
+
+def test_linear_argument_checks(raw):
+    assert _call(raw, "xq_linear_q4k", V(0), V(P), V(P * 8), I64(32), I64(256), I64(1), V(0)) == 1
+    assert _call(raw, "xq_linear_q4k", V(P + 4), V(P * 4), V(P * 8), I64(32), I64(256), I64(1),
+                 V(0)) == 2
+    assert _call(raw, "xq_linear_q4k", V(P), V(P * 4), V(P * 8), I64(32), I64(300), I64(1),
+                 V(0)) == 3
+    # y overlapping x (1 x 256 f32 = 1024 bytes from P)
+    assert _call(raw, "xq_linear_q4k", V(P), V(P * 4), V(P + 512), I64(32), I64(256), I64(1),
+                 V(0)) == 1
+    assert _call(raw, "xq_linear_cb4", V(P), V(P * 4), V(0), V(P * 8), I64(32), I64(256),
+                 I64(1), V(0)) == 1
 
 
 def test_cb4_needs_a_table(raw):

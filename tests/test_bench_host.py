@@ -94,7 +94,8 @@ def test_algorithmic_bytes():
     b = bench.step_bytes(c)
     assert b["weights"] == 295_501_824
     assert b["matvec"] == 295_501_824 + 16 * 320 + 4 * 128256
-    assert b["step"] == b["matvec"] + 4 * 4096 + 16 * 320
+    assert b["linear"] == 295_501_824 + 4 * 4096 + 4 * 128256
+    assert b["two_call"] == b["matvec"] + 4 * 4096 + 16 * 320
 
 
 def test_warmup_floor():

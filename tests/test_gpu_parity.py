@@ -318,6 +318,37 @@ def test_plan_override_clamped_to_shared_memory(xq, orc):
     assert np.array_equal(dots, orc.subdots_q4k(W, orc.quantize_q8(x), rows, cols, batch))
 
 
+# ---------------------------------------------------------------- fused quantise + mat-vec
+@pytest.mark.parametrize("fmt", ["q4k", "cb4"])
+@pytest.mark.parametrize("rows,cols,batch", [(1, 256, 1), (101, 1024, 2), (77, 4096, 8),
+                                             (300, 4096, 1), (64, 14336, 3), (37, 65536, 8)])
+def test_linear_is_the_two_call_path(xq, orc, fmt, rows, cols, batch):
+    """The fused launch quantises x with the quantiser's own arithmetic, so y
+    is bit-identical to xq_quantize_q8 followed by the mat-vec, and within
+    the tolerance of the oracle."""
+    seed = rows + cols + 3 * batch
+    W = _weights(fmt, rows, cols, seed)
+    kv = synthetic.cb4_table()
+    x = synthetic.activations(batch, cols, seed + 1, outlier_frac=0.001)
+    y2 = run_matvec(xq, fmt, W, kv, run_quantize(xq, x), rows, cols, batch)
+    out = Guarded((batch, rows), torch.float32)
+    which = xq.COUNT_LINEAR_Q4K if fmt == "q4k" else xq.COUNT_LINEAR_CB4
+    before = xq.launch_count(which)
+    if fmt == "q4k":
+        xq.linear_q4k(dev(x), dev(W), rows, cols, out=out.t)
+    else:
+        xq.linear_cb4(dev(x), dev(W), kv, rows, cols, out=out.t)
+    torch.cuda.synchronize()
+    out.check_guard()
+    assert xq.launch_count(which) == before + xq.last_plan()["launches"]
+    y1 = out.t.cpu().numpy()
+    assert np.array_equal(y1, y2)
+    xq_ref = orc.quantize_q8(x)
+    y_ref = (orc.matvec_q4k(W, xq_ref, rows, cols, batch) if fmt == "q4k"
+             else orc.matvec_cb4(W, kv, xq_ref, rows, cols, batch))
+    check_y(y1, y_ref, f"linear {fmt} {rows}x{cols} b{batch}")
+
+
 # ---------------------------------------------------------------- streams and graphs
 def test_side_stream_and_graph_replay(xq, orc):
     rows, cols, batch = 500, 4096, 1
