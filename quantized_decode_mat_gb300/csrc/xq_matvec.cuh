@@ -266,40 +266,8 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
 
     uint32_t T[4] = {a.kv[0], a.kv[1], a.kv[2], a.kv[3]};
 
-    // 1. the activation
-    if (FUSED) {
-        // quantise x here: warp w takes blocks w, w+W, ... of the batch (the
-        // same arithmetic as the standalone quantiser, so the same bytes)
-        for (int blk = warp; blk < B * nb; blk += W) {
-            const float4 *src = reinterpret_cast<const float4 *>(a.x + (int64_t)blk * 256 + lane * 8);
-            const float4 u = __ldg(src), v = __ldg(src + 1);
-            const float vals[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-            const Q8Lane r = q8_quantize_lane(vals);
-            uint8_t *dst = act + blk * kActStride;
-            *reinterpret_cast<uint2 *>(dst + lane * 8) = make_uint2(r.w0, r.w1);
-            if ((lane & 3) == 0) *reinterpret_cast<int *>(dst + kQ8SumAt + (lane >> 2) * 4) = r.sum;
-            uint32_t sums[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) sums[j] = (uint32_t)__shfl_sync(0xffffffffu, r.sum, 4 * j);
-            if (lane == 0) {
-                *reinterpret_cast<float *>(dst + kQ8ScaleAt) = r.d;
-                *reinterpret_cast<uint4 *>(dst + kActSplitAt) =
-                    split_sums(make_uint4(sums[0], sums[1], sums[2], sums[3]),
-                               make_uint4(sums[4], sums[5], sums[6], sums[7]));
-            }
-        }
-    } else {
-        // bytes 0..303 of every q8 block, then its split sums
-        for (int i = threadIdx.x; i < B * nb * 20; i += blockDim.x) {
-            const int blk = i / 20, piece = i - 20 * blk;
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
-            *reinterpret_cast<uint4 *>(act + blk * kActStride + 16 * piece) =
-                piece < 19 ? __ldg(src + piece) : split_sums(__ldg(src + 16), __ldg(src + 17));
-        }
-    }
-    __syncthreads();
-
-    // 2. this warp's row groups and their boxes
+    // 1. this warp's row groups and their boxes; the first S-1 boxes are
+    //    requested before the activation is staged, so the two overlap
     const int G = gridDim.x;
     const int64_t gw = (int64_t)warp * G + blockIdx.x;
     const int64_t TW = (int64_t)G * W;
@@ -343,6 +311,39 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
         if (issued < nitems) issue_next();
         cp_async_commit();
     }
+
+    // 2. the activation (a different region of shared memory than the stages)
+    if (FUSED) {
+        // quantise x here: warp w takes blocks w, w+W, ... of the batch (the
+        // same arithmetic as the standalone quantiser, so the same bytes)
+        for (int blk = warp; blk < B * nb; blk += W) {
+            const float4 *src = reinterpret_cast<const float4 *>(a.x + (int64_t)blk * 256 + lane * 8);
+            const float4 u = __ldg(src), v = __ldg(src + 1);
+            const float vals[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+            const Q8Lane r = q8_quantize_lane(vals);
+            uint8_t *dst = act + blk * kActStride;
+            *reinterpret_cast<uint2 *>(dst + lane * 8) = make_uint2(r.w0, r.w1);
+            if ((lane & 3) == 0) *reinterpret_cast<int *>(dst + kQ8SumAt + (lane >> 2) * 4) = r.sum;
+            uint32_t sums[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sums[j] = (uint32_t)__shfl_sync(0xffffffffu, r.sum, 4 * j);
+            if (lane == 0) {
+                *reinterpret_cast<float *>(dst + kQ8ScaleAt) = r.d;
+                *reinterpret_cast<uint4 *>(dst + kActSplitAt) =
+                    split_sums(make_uint4(sums[0], sums[1], sums[2], sums[3]),
+                               make_uint4(sums[4], sums[5], sums[6], sums[7]));
+            }
+        }
+    } else {
+        // bytes 0..303 of every q8 block, then its split sums
+        for (int i = threadIdx.x; i < B * nb * 20; i += blockDim.x) {
+            const int blk = i / 20, piece = i - 20 * blk;
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
+            *reinterpret_cast<uint4 *>(act + blk * kActStride + 16 * piece) =
+                piece < 19 ? __ldg(src + piece) : split_sums(__ldg(src + 16), __ldg(src + 17));
+        }
+    }
+    __syncthreads();
 
     const int64_t dots_row = (int64_t)nb * 8;
     const int64_t dots_bstride = rows * dots_row;
