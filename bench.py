@@ -364,7 +364,7 @@ def run_ours(args, c):
 
     per_graph = max(1, min(args.steps, 100))
     rem = args.steps % per_graph
-    ncount = 7
+    ncount = xq.COUNT_N
     counts0 = [xq.launch_count(i) for i in range(ncount)]
     graphs = {}
     for name, fn in (("step", do_step), ("matvec", do_matvec), ("two_call", do_two_call)):

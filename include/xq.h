@@ -119,6 +119,23 @@ xq_status xq_linear_q4k(const float *x, const void *W, float *y, int64_t rows, i
 xq_status xq_linear_cb4(const float *x, const void *W, const int8_t *table, float *y,
                         int64_t rows, int64_t cols, int64_t batch, void *stream);
 
+/* Grouped experts ("25 - Writing XPU Kernels" 25.2.2, the mul_mat_vec_id
+ * shape): W is a slab of n_experts experts of rows_per_expert rows each,
+ * contiguous; sel (DEVICE int32[used]) selects the experts.  One launch
+ * computes, for every slot kk < used,
+ *   y[kk*rows_per_expert + r] = (row r of expert sel[kk]) . x_kk,
+ * where x_kk is q8 vector 0 of xq when x_per_slot == 0 (every slot reads the
+ * one decoded token) and q8 vector kk when x_per_slot != 0 (used <= 8).  y is
+ * slot-major, [used][rows_per_expert], and bit-identical to one dense
+ * xq_matvec_* launch per slot.  A slot whose id lies outside [0, n_experts)
+ * reads nothing, gets NaN rows and sets bit 1 of the device status word. */
+xq_status xq_matvec_q4k_id(const void *W, const int32_t *sel, const void *xq, float *y,
+                           int64_t rows_per_expert, int64_t cols, int64_t n_experts, int64_t used,
+                           int32_t x_per_slot, void *stream);
+xq_status xq_matvec_cb4_id(const void *W, const int8_t *table, const int32_t *sel, const void *xq,
+                           float *y, int64_t rows_per_expert, int64_t cols, int64_t n_experts,
+                           int64_t used, int32_t x_per_slot, void *stream);
+
 /* Test exports: the exact per-sub-block integer dots of the same kernels.
  * dots: [batch][rows][cols/32] int32 (device).  Q4_K: dots[b][r][8k+s] is
  * dot_s of super-block k; codebook: dots[b][r][k] is dot_k of block k. */
@@ -170,14 +187,16 @@ enum {
     XQ_COUNT_SUBDOTS_CB4 = 4,
     XQ_COUNT_LINEAR_Q4K = 5,
     XQ_COUNT_LINEAR_CB4 = 6,
-    XQ_COUNT_N = 7
+    XQ_COUNT_MATVEC_ID_Q4K = 7,
+    XQ_COUNT_MATVEC_ID_CB4 = 8,
+    XQ_COUNT_N = 9
 };
 uint64_t xq_launch_count(int32_t which);
 
 /* Read (and optionally clear) the current device's status word, where
- * kernels report errors without trapping; the current kernels have no
- * failure that sets it, so it reads 0.  SYNCHRONISES `stream` (a
- * device-to-host copy of 4 bytes). */
+ * kernels report errors without trapping: bit 1 = a grouped mat-vec met an
+ * expert id outside [0, n_experts).  Returns XQ_EDEVICE when it is non-zero.
+ * SYNCHRONISES `stream` (device-to-host copy of 4 bytes, and a clear). */
 xq_status xq_device_status(uint32_t *out, int32_t clear, void *stream);
 
 const char *xq_status_string(xq_status s);

@@ -17,7 +17,10 @@ from ._native import (  # noqa: F401
     COUNT_LINEAR_CB4,
     COUNT_LINEAR_Q4K,
     COUNT_MATVEC_CB4,
+    COUNT_MATVEC_ID_CB4,
+    COUNT_MATVEC_ID_Q4K,
     COUNT_MATVEC_Q4K,
+    COUNT_N,
     COUNT_QUANTIZE,
     COUNT_SUBDOTS_CB4,
     COUNT_SUBDOTS_Q4K,
@@ -30,6 +33,7 @@ from ._native import (  # noqa: F401
     linear_cb4,
     linear_q4k,
     matvec_cb4,
+    matvec_id,
     matvec_q4k,
     plan_matvec,
     q4k_bytes,

@@ -43,6 +43,10 @@ _matvec_q4k = _sig("xq_matvec_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64,
 _matvec_cb4 = _sig("xq_matvec_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
 _linear_q4k = _sig("xq_linear_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
 _linear_cb4 = _sig("xq_linear_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
+_matvec_q4k_id = _sig("xq_matvec_q4k_id", ctypes.c_int,
+                      [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P])
+_matvec_cb4_id = _sig("xq_matvec_cb4_id", ctypes.c_int,
+                      [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P])
 _subdots_q4k = _sig("xq_subdots_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
 _subdots_cb4 = _sig("xq_subdots_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
 _plan = _sig("xq_plan_matvec", ctypes.c_int, [_I32, _I64, _I64, _I64, _I32, _I64,
@@ -57,7 +61,8 @@ _last_error = _sig("xq_last_error", ctypes.c_char_p, [])
 _version = _sig("xq_version", _I32, [])
 
 (COUNT_QUANTIZE, COUNT_MATVEC_Q4K, COUNT_MATVEC_CB4, COUNT_SUBDOTS_Q4K, COUNT_SUBDOTS_CB4,
- COUNT_LINEAR_Q4K, COUNT_LINEAR_CB4) = range(7)
+ COUNT_LINEAR_Q4K, COUNT_LINEAR_CB4, COUNT_MATVEC_ID_Q4K, COUNT_MATVEC_ID_CB4) = range(9)
+COUNT_N = 9
 
 
 class XQError(RuntimeError):
@@ -187,6 +192,28 @@ def linear_cb4(x: torch.Tensor, W: torch.Tensor, table, rows: int, cols: int,
     _check(_linear_cb4(_dev(x, "x", torch.float32), _dev(W, "W", torch.uint8),
                        ctypes.cast(_table(table), _P), _dev(out, "y", torch.float32), rows,
                        cols, batch, _stream(stream)))
+    return out
+
+
+def matvec_id(fmt: str, W: torch.Tensor, sel: torch.Tensor, xq: torch.Tensor,
+              rows_per_expert: int, cols: int, n_experts: int, table=None,
+              x_per_slot: bool = False, out: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """Grouped experts: y[kk] = W[expert sel[kk]] . x (x = xq vector 0, or
+    vector kk with x_per_slot) -> f32 [used, rows_per_expert]."""
+    used = int(sel.numel())
+    if out is None:
+        out = torch.empty((used, rows_per_expert), dtype=torch.float32, device=xq.device)
+    s = _dev(sel, "sel", torch.int32)
+    if fmt == "q4k":
+        _check(_matvec_q4k_id(_dev(W, "W", torch.uint8), s, _dev(xq, "xq", torch.uint8),
+                              _dev(out, "y", torch.float32), rows_per_expert, cols, n_experts,
+                              used, int(x_per_slot), _stream(stream)))
+    else:
+        _check(_matvec_cb4_id(_dev(W, "W", torch.uint8), ctypes.cast(_table(table), _P), s,
+                              _dev(xq, "xq", torch.uint8), _dev(out, "y", torch.float32),
+                              rows_per_expert, cols, n_experts, used, int(x_per_slot),
+                              _stream(stream)))
     return out
 
 

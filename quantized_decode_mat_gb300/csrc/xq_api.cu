@@ -12,9 +12,8 @@
 
 namespace xq {
 
-// Device status word for kernel-side errors reported without trapping.  The
-// current kernels contain no waits that can time out, so it stays 0; it is
-// kept so that callers can check a device once after a sequence of launches.
+// Device status word for kernel-side errors reported without trapping (bit 1:
+// a grouped mat-vec met an expert id outside [0, n_experts)).
 __device__ uint32_t g_status_word;
 
 // ---- q8 activation quantiser ------------------------------------------------------
@@ -135,12 +134,15 @@ int64_t align128(int64_t v) { return (v + 127) & ~(int64_t)127; }
 // Grid: one CTA per SM, at most one per work unit.  Warps: enough to cover
 // the work units, within the instantiation's register budget.  Stages: 2
 // (measured best), fewer warps if even that does not fit.
+// slots > 0 plans the grouped-expert form: `rows` rows per expert, `slots`
+// selected experts, each group inside one slot, and `batch` staged activation
+// vectors (1 shared, or one per slot).
 xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
-                    int64_t smem_optin, xq_plan *p) {
+                    int64_t smem_optin, xq_plan *p, int64_t slots = 0) {
     const int32_t nb = (int32_t)(cols / 256);
     const int32_t R = (nb < 32 && 32 % nb == 0) ? 32 / nb : 1;
     const int32_t spr = R > 1 ? 1 : (nb + 31) / 32;
-    const int64_t groups = (rows + R - 1) / R;
+    const int64_t groups = slots > 0 ? slots * ((rows + R - 1) / R) : (rows + R - 1) / R;
     int32_t bl = (int32_t)batch;
     while (bl > 0 && align128((int64_t)bl * nb * kActStride) + 2LL * kStageBytes + 128 > smem_optin)
         --bl;
@@ -148,8 +150,10 @@ xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
         return fail(XQ_ESHAPE, "cols=%lld: one q8 vector does not fit in shared memory",
                     (long long)cols);
     const int64_t act = align128((int64_t)bl * nb * kActStride);
+    if (slots > 0 && bl != batch)
+        return fail(XQ_ESHAPE, "the per-slot activations do not fit in shared memory");
     const int32_t grid = (int32_t)(groups < sm_count ? groups : sm_count);
-    const int32_t wmax = warps_limit(bl);
+    const int32_t wmax = warps_limit(slots > 0 ? 1 : bl);
     const int64_t per_cta = (groups + grid - 1) / grid;
     int32_t W = (int32_t)(per_cta < wmax ? per_cta : wmax);
     const int32_t ow = g_override_warps.load(), os = g_override_stages.load();
@@ -263,6 +267,69 @@ xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *in, 
     return XQ_OK;
 }
 
+xq_status run_matvec_id(bool cb4, const void *W, const int8_t *table, const int32_t *sel,
+                        const void *xq_in, float *y, int64_t rpe, int64_t cols,
+                        int64_t n_experts, int64_t used, int32_t x_per_slot, void *stream) {
+    t_error.clear();
+    if (!W || !sel || !xq_in || !y) return fail(XQ_EINVAL, "null device pointer (W, sel, xq or y)");
+    if (cb4 && !table) return fail(XQ_EINVAL, "null codebook table");
+    if (xq_status s = check_shape(rpe, cols, 1, true)) return s;
+    if (n_experts < 1 || n_experts > 0x7FFFFFFFLL || rpe * n_experts > 0x7FFFFFFFLL)
+        return fail(XQ_ESHAPE, "n_experts=%lld out of range", (long long)n_experts);
+    if (used < 1 || used > (1 << 20)) return fail(XQ_ESHAPE, "used=%lld out of range", (long long)used);
+    if (x_per_slot && used > 8) return fail(XQ_ESHAPE, "per-slot activations: used must be <= 8");
+    if (!aligned(W, 16)) return fail(XQ_EALIGN, "W must be 16-byte aligned");
+    if (!aligned(xq_in, 16)) return fail(XQ_EALIGN, "xq must be 16-byte aligned");
+    if (!aligned(sel, 4)) return fail(XQ_EALIGN, "sel must be 4-byte aligned");
+    if (!aligned(y, 4)) return fail(XQ_EALIGN, "y must be 4-byte aligned");
+    const int64_t nb = cols / 256;
+    const int64_t nvec = x_per_slot ? used : 1;
+    const size_t o_bytes = (size_t)used * rpe * 4;
+    if (overlap(y, o_bytes, W, (size_t)n_experts * rpe * nb * kChunkBytes) ||
+        overlap(y, o_bytes, xq_in, (size_t)nvec * nb * kQ8Bytes) ||
+        overlap(y, o_bytes, sel, (size_t)used * 4))
+        return fail(XQ_EINVAL, "output overlaps an input");
+    DeviceState *dev = nullptr;
+    if (xq_status s = device_state(&dev)) return s;
+    xq_plan plan;
+    if (xq_status s = make_plan(rpe, cols, nvec, dev->sm_count, dev->smem_optin, &plan, used))
+        return s;
+    MatvecArgs a;
+    memset(&a, 0, sizeof a);
+    a.W = static_cast<const uint8_t *>(W);
+    a.xq = static_cast<const uint8_t *>(xq_in);
+    a.y = y;
+    a.rows = used * rpe;
+    a.groups = plan.groups;
+    a.nb = (int32_t)nb;
+    a.rows_per_group = plan.rows_per_group;
+    a.segments = plan.segments;
+    a.stages = plan.stages;
+    a.sel = sel;
+    a.rows_per_expert = rpe;
+    a.n_experts = (int32_t)n_experts;
+    a.groups_per_slot = (int32_t)(plan.groups / used);
+    a.act_vectors = (int32_t)nvec;
+    a.status = dev->status;
+    if (cb4) {
+        for (int i = 0; i < 4; ++i) {
+            uint32_t w = 0;
+            for (int j = 0; j < 4; ++j) w |= (uint32_t)(uint8_t)table[4 * i + j] << (8 * j);
+            a.kv[i] = w;
+        }
+    }
+    const dim3 grid(plan.grid), block(plan.warps * 32);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cb4 ? launch_matvec_cb4(a, 1, 3, grid, block, (size_t)plan.smem_bytes, s)
+                        : launch_matvec_q4k(a, 1, 3, grid, block, (size_t)plan.smem_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "grouped mat-vec launch");
+    g_counts[cb4 ? XQ_COUNT_MATVEC_ID_CB4 : XQ_COUNT_MATVEC_ID_Q4K].fetch_add(
+        1, std::memory_order_relaxed);
+    t_last_plan = plan;
+    t_have_plan = true;
+    return XQ_OK;
+}
+
 }  // namespace
 }  // namespace xq
 
@@ -323,6 +390,20 @@ xq_status xq_linear_q4k(const float *x, const void *W, float *y, int64_t rows, i
 xq_status xq_linear_cb4(const float *x, const void *W, const int8_t *table, float *y,
                         int64_t rows, int64_t cols, int64_t batch, void *stream) {
     return run_matvec(Op::kLinearCB4, W, table, x, y, rows, cols, batch, stream);
+}
+
+xq_status xq_matvec_q4k_id(const void *W, const int32_t *sel, const void *xq_in, float *y,
+                           int64_t rows_per_expert, int64_t cols, int64_t n_experts, int64_t used,
+                           int32_t x_per_slot, void *stream) {
+    return run_matvec_id(false, W, nullptr, sel, xq_in, y, rows_per_expert, cols, n_experts, used,
+                         x_per_slot, stream);
+}
+
+xq_status xq_matvec_cb4_id(const void *W, const int8_t *table, const int32_t *sel,
+                           const void *xq_in, float *y, int64_t rows_per_expert, int64_t cols,
+                           int64_t n_experts, int64_t used, int32_t x_per_slot, void *stream) {
+    return run_matvec_id(true, W, table, sel, xq_in, y, rows_per_expert, cols, n_experts, used,
+                         x_per_slot, stream);
 }
 
 xq_status xq_subdots_q4k(const void *W, const void *xq_in, int32_t *dots, int64_t rows,

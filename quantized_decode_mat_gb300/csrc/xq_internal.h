@@ -48,11 +48,21 @@ struct MatvecArgs {
     int32_t segments;       // boxes per group: 1, or ceil(nb/32) when rows_per_group == 1
     int32_t stages;         // shared-memory stages per warp (2..8)
     uint32_t kv[4];         // codebook bytes kv[0..15], little-endian words
+    // grouped-expert form
+    const int32_t *sel;     // [used] expert ids (device)
+    int64_t rows_per_expert;
+    int32_t n_experts;
+    int32_t groups_per_slot;
+    int32_t act_vectors;    // 1: every slot reads vector 0; used: slot kk reads vector kk
+    uint32_t *status;       // device status word
 };
+
+// Status word bits (see xq_device_status).
+constexpr uint32_t kStatusBadExpertId = 2u;
 
 // Launch entry points implemented per format (xq_matvec_q4k.cu / _cb4.cu).
 // kind: 0 = mat-vec on q8 blocks, 1 = the same with the exact dots,
-// 2 = fused quantise + mat-vec on f32 x.
+// 2 = fused quantise + mat-vec on f32 x, 3 = grouped experts.
 cudaError_t launch_matvec_q4k(const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,
                               size_t smem, cudaStream_t s);
 cudaError_t launch_matvec_cb4(const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,

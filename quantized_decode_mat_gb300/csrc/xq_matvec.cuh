@@ -227,6 +227,46 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const A
     }
 }
 
+// ---- work-unit descriptor ---------------------------------------------------------------
+// Row group g of a launch: where its rows start in W, how many exist, where
+// their outputs go and which staged activation vector they use.  In the
+// grouped-expert form (ID), the launch's rows are `used` slots of
+// rows_per_expert rows each; slot kk reads expert sel[kk]'s rows from the
+// slab and writes output rows kk*rows_per_expert.. ("25 - Writing XPU
+// Kernels" 25.2.2); a group never straddles two slots.
+struct GroupInfo {
+    int64_t row0;   // first row in W
+    int64_t out0;   // first output row
+    int valid;      // rows of the group that exist (0..R)
+    int vec;        // staged activation vector
+    bool bad;       // ID form: sel[kk] outside [0, n_experts)
+};
+
+template <bool ID>
+__device__ __forceinline__ GroupInfo group_info(const MatvecArgs &a, int64_t g, int R) {
+    GroupInfo gi;
+    if (!ID) {
+        gi.row0 = g * R;
+        gi.out0 = gi.row0;
+        const int64_t rr = a.rows - gi.row0;
+        gi.valid = (int)(rr < R ? rr : R);
+        gi.vec = 0;
+        gi.bad = false;
+    } else {
+        const int64_t gps = a.groups_per_slot;
+        const int64_t kk = g / gps;
+        const int64_t r0 = (g - kk * gps) * R;  // first row within the slot
+        const int e = __ldg(a.sel + kk);
+        gi.bad = e < 0 || e >= a.n_experts;
+        gi.row0 = (int64_t)(gi.bad ? 0 : e) * a.rows_per_expert + r0;
+        gi.out0 = kk * a.rows_per_expert + r0;
+        const int64_t rr = a.rows_per_expert - r0;
+        gi.valid = (int)(rr < R ? rr : R);
+        gi.vec = a.act_vectors > 1 ? (int)kk : 0;
+    }
+    return gi;
+}
+
 // ---- the kernel ------------------------------------------------------------------------
 // Work unit: a row group of R rows.  When nb (256-weight chunks per row) is a
 // power of two below 32, R = 32/nb and the group is one contiguous 4608-byte
@@ -244,8 +284,9 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const A
 template <int B>
 constexpr int max_threads() { return warps_limit(B) * 32; }
 
-template <int FMT, int B, bool DOTS, bool FUSED>
+template <int FMT, int B, bool DOTS, bool FUSED, bool ID>
 __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const MatvecArgs a) {
+    static_assert(!ID || (B == 1 && !DOTS && !FUSED), "the grouped form is batch 1 on q8 input");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const int W = blockDim.x >> 5;
@@ -259,7 +300,8 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
     const int64_t ngroups = a.groups;
     const int64_t row_bytes = (int64_t)nb * kChunkBytes;
     const int64_t act_bstride = (int64_t)nb * kActStride;
-    const int act_bytes = (int)((B * act_bstride + 127) & ~(int64_t)127);
+    const int nvec = ID ? a.act_vectors : B;  // staged activation vectors
+    const int act_bytes = (int)((nvec * act_bstride + 127) & ~(int64_t)127);
     uint8_t *act = smem;
     uint8_t *stage0 = smem + act_bytes + (size_t)warp * S * kStageBytes;
     const uint32_t stage0_u32 = smem_u32(stage0);
@@ -277,18 +319,18 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
     int64_t pg = gw;  // producer cursor: group, segment, stage
     int ps = 0, p_stage = 0, issued = 0;
     auto issue_next = [&]() {
-        const int64_t row0 = pg * R;
+        const GroupInfo gi = group_info<ID>(a, pg, R);
         const uint8_t *src0;
         int valid;  // bytes of the box that exist in W
         if (R > 1) {
-            src0 = a.W + row0 * row_bytes;
-            const int64_t rr = rows - row0;
-            valid = (int)((rr < R ? rr : R) * row_bytes);
+            src0 = a.W + gi.row0 * row_bytes;
+            valid = gi.valid * (int)row_bytes;
         } else {
             const int c0 = ps * 32;
-            src0 = a.W + row0 * row_bytes + c0 * kChunkBytes;
+            src0 = a.W + gi.row0 * row_bytes + c0 * kChunkBytes;
             valid = (nb - c0 < 32 ? nb - c0 : 32) * kChunkBytes;
         }
+        if (gi.bad) valid = 0;  // an invalid expert id reads nothing
         const uint8_t *src = src0 + 16 * lane;
         const uint32_t dst = stage0_u32 + (uint32_t)p_stage * kStageBytes + 16u * lane;
         if (valid == kStageBytes) {
@@ -336,7 +378,7 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
         }
     } else {
         // bytes 0..303 of every q8 block, then its split sums
-        for (int i = threadIdx.x; i < B * nb * 20; i += blockDim.x) {
+        for (int i = threadIdx.x; i < nvec * nb * 20; i += blockDim.x) {
             const int blk = i / 20, piece = i - 20 * blk;
             const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
             *reinterpret_cast<uint4 *>(act + blk * kActStride + 16 * piece) =
@@ -350,7 +392,9 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
     const int width = R > 1 ? nb : 32;  // lanes that share a row
     int c_stage = 0;
     for (int64_t g = gw; g < ngroups; g += TW) {
-        const int64_t row = g * R + (R > 1 ? lane / nb : 0);
+        const GroupInfo gi = group_info<ID>(a, g, R);
+        const int rig = R > 1 ? lane / nb : 0;  // this lane's row within the group
+        const int64_t row = gi.row0 + rig;      // its row in W (for the dots)
         float hi[B], lo[B];
 #pragma unroll
         for (int b = 0; b < B; ++b) hi[b] = lo[b] = 0.0f;
@@ -360,11 +404,11 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
             cp_async_wait_pending(S - 1);  // this lane's copies of the box landed
             __syncwarp();                  // ... and every other lane's
             const int c = R > 1 ? (lane & (nb - 1)) : s * 32 + lane;
-            const bool ok = R > 1 ? row < rows : c < nb;
+            const bool ok = rig < gi.valid && c < nb && !gi.bad;
             if (ok) {
                 const uint8_t *w = stage0 + c_stage * kStageBytes + lane * kChunkBytes;
                 int32_t *dp = DOTS ? a.dots + row * dots_row + c * 8 : nullptr;
-                const ActSmem as{act + c * kActStride, act_bstride};
+                const ActSmem as{act + gi.vec * act_bstride + c * kActStride, act_bstride};
                 if (FMT == kQ4K)
                     q4k_chunk<B, DOTS>(w, as, hi, lo, dp, dots_bstride);
                 else
@@ -383,33 +427,40 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
                     acc_add(hi[b], lo[b], oh, ol);
                 }
             }
-            if ((lane & (width - 1)) == 0 && row < rows) {
+            if ((lane & (width - 1)) == 0 && rig < gi.valid) {
+                const int64_t orow = gi.out0 + rig;
+                const float nan = __int_as_float(0x7FC00000);
 #pragma unroll
-                for (int b = 0; b < B; ++b) a.y[(int64_t)b * rows + row] = __fadd_rn(hi[b], lo[b]);
+                for (int b = 0; b < B; ++b)
+                    a.y[(int64_t)b * rows + orow] = gi.bad ? nan : __fadd_rn(hi[b], lo[b]);
+                if (ID && gi.bad && rig == 0) atomicOr(a.status, kStatusBadExpertId);
             }
         }
     }
     cp_async_wait_all();  // only empty groups can remain; keeps the exit clean
 }
 
-template <int FMT, int B, bool DOTS, bool FUSED>
+template <int FMT, int B, bool DOTS, bool FUSED, bool ID = false>
 inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, size_t smem,
                                    cudaStream_t s) {
-    xq_matvec_kernel<FMT, B, DOTS, FUSED><<<grid, block, smem, s>>>(a);
+    xq_matvec_kernel<FMT, B, DOTS, FUSED, ID><<<grid, block, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-template <int FMT, int B, bool DOTS, bool FUSED>
+template <int FMT, int B, bool DOTS, bool FUSED, bool ID = false>
 inline cudaError_t configure_t(int smem_optin) {
-    return cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSED>,
+    return cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSED, ID>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
 }
 
 // kind: 0 = mat-vec on q8 blocks, 1 = the same with the exact dots,
-// 2 = fused quantise + mat-vec.
+// 2 = fused quantise + mat-vec, 3 = grouped experts (batch 1, q8 input).
 template <int FMT>
 inline cudaError_t launch_matvec_fmt(const MatvecArgs &a, int batch, int kind, dim3 grid,
                                      dim3 block, size_t smem, cudaStream_t s) {
+    if (kind == 3)
+        return batch == 1 ? launch_matvec_t<FMT, 1, false, false, true>(a, grid, block, smem, s)
+                          : cudaErrorInvalidValue;
 #define XQ_CASE(BB)                                                                    \
     case BB:                                                                           \
         return kind == 1   ? launch_matvec_t<FMT, BB, true, false>(a, grid, block, smem, s)  \
@@ -446,6 +497,7 @@ inline cudaError_t configure_fmt(int smem_optin) {
     XQ_CFG(7)
     XQ_CFG(8)
 #undef XQ_CFG
+    if (e == cudaSuccess) e = configure_t<FMT, 1, false, false, true>(smem_optin);
     return e;
 }
 

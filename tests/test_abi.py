@@ -102,6 +102,19 @@ def test_linear_argument_checks(raw):
                  I64(1), V(0)) == 1
 
 
+def test_matvec_id_argument_checks(raw):
+    fn = "xq_matvec_q4k_id"
+    I32 = ctypes.c_int32
+    # W, sel, xq, y, rows_per_expert, cols, n_experts, used, x_per_slot, stream
+    ok = (V(P), V(P * 2), V(P * 3), V(P * 8), I64(16), I64(256), I64(4), I64(2), I32(0), V(0))
+    assert _call(raw, fn, V(P), V(0), *ok[2:]) == 1                         # null sel
+    assert _call(raw, fn, V(P), V(P * 2 + 2), *ok[2:]) == 2                 # sel misaligned
+    assert _call(raw, fn, *ok[:6], I64(0), *ok[7:]) == 3                    # no experts
+    assert _call(raw, fn, *ok[:7], I64(9), I32(1), V(0)) == 3               # 9 per-slot vectors
+    assert _call(raw, fn, *ok[:7], I64(0), *ok[8:]) == 3                    # used 0
+    assert _call(raw, "xq_matvec_cb4_id", V(P), V(0), *ok[1:]) == 1         # null table
+
+
 def test_cb4_needs_a_table(raw):
     assert _call(raw, "xq_matvec_cb4", V(P), V(0), V(P * 2), V(P * 8), I64(32), I64(256),
                  I64(1), V(0)) == 1

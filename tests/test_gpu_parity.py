@@ -349,6 +349,68 @@ def test_linear_is_the_two_call_path(xq, orc, fmt, rows, cols, batch):
     check_y(y1, y_ref, f"linear {fmt} {rows}x{cols} b{batch}")
 
 
+# ---------------------------------------------------------------- grouped experts
+def _slab(fmt, E, rpe, cols, seed):
+    return np.concatenate([_weights(fmt, rpe, cols, seed + 17 * e) for e in range(E)])
+
+
+@pytest.mark.parametrize("fmt", ["q4k", "cb4"])
+@pytest.mark.parametrize("rpe,cols", [(64, 2048), (45, 4096), (33, 1024), (20, 14336), (64, 256)])
+@pytest.mark.parametrize("x_per_slot", [False, True])
+def test_matvec_id_is_per_expert_launches(xq, orc, fmt, rpe, cols, x_per_slot):
+    """One grouped launch over a six-expert slab equals, bit for bit, one dense
+    launch per selected expert ("25 - Writing XPU Kernels" 25.7.1's gate: ==,
+    never a tolerance); and it is within tolerance of the oracle."""
+    E, ids = 6, [4, 0, 3]
+    used = len(ids)
+    slab = _slab(fmt, E, rpe, cols, rpe + cols)
+    kv = synthetic.cb4_table()
+    nvec = used if x_per_slot else 1
+    x = synthetic.activations(nvec, cols, cols + 1)
+    xq_dev = run_quantize(xq, x)
+    sel = torch.tensor(ids, dtype=torch.int32, device="cuda")
+    out = Guarded((used, rpe), torch.float32)
+    which = xq.COUNT_MATVEC_ID_Q4K if fmt == "q4k" else xq.COUNT_MATVEC_ID_CB4
+    before = xq.launch_count(which)
+    xq.matvec_id(fmt, dev(slab), sel, xq_dev, rpe, cols, E, table=kv, x_per_slot=x_per_slot,
+                 out=out.t)
+    torch.cuda.synchronize()
+    out.check_guard()
+    assert xq.launch_count(which) == before + 1
+    y_id = out.t.cpu().numpy()
+    xq_ref = orc.quantize_q8(x)
+    for kk, e in enumerate(ids):
+        W_e = np.ascontiguousarray(slab[e * rpe:(e + 1) * rpe])
+        v = kk if x_per_slot else 0
+        y_dense = run_matvec(xq, fmt, W_e, kv, xq_dev[v:v + 1].contiguous(), rpe, cols, 1)
+        assert np.array_equal(y_id[kk], y_dense[0]), f"slot {kk}"
+        y_ref = (orc.matvec_q4k(W_e, xq_ref[v:v + 1], rpe, cols, 1) if fmt == "q4k"
+                 else orc.matvec_cb4(W_e, kv, xq_ref[v:v + 1], rpe, cols, 1))
+        check_y(y_id[kk:kk + 1], y_ref, f"id slot {kk}")
+    assert not np.isnan(y_id).any()
+
+
+def test_matvec_id_bad_expert_id_reports_without_trapping(xq, orc):
+    """An id outside [0, n_experts) reads nothing: its slot's rows are NaN, the
+    other slots are exact, and the device status word says so."""
+    E, rpe, cols = 4, 40, 2048
+    slab = _slab("q4k", E, rpe, cols, 5)
+    x = synthetic.activations(1, cols, 6)
+    xq_dev = run_quantize(xq, x)
+    xq.device_status(clear=True)
+    sel = torch.tensor([1, 99, 2, -3], dtype=torch.int32, device="cuda")
+    y = xq.matvec_id("q4k", dev(slab), sel, xq_dev, rpe, cols, E)
+    torch.cuda.synchronize()
+    y = y.cpu().numpy()
+    assert np.isnan(y[1]).all() and np.isnan(y[3]).all()
+    for kk, e in ((0, 1), (2, 2)):
+        y_dense = run_matvec(xq, "q4k", np.ascontiguousarray(slab[e * rpe:(e + 1) * rpe]), None,
+                             xq_dev, rpe, cols, 1)
+        assert np.array_equal(y[kk], y_dense[0])
+    assert xq.device_status(clear=True) == 2
+    assert xq.device_status() == 0
+
+
 # ---------------------------------------------------------------- streams and graphs
 def test_side_stream_and_graph_replay(xq, orc):
     rows, cols, batch = 500, 4096, 1
