@@ -18,6 +18,9 @@ Parity status of each function (all pinned, none "parity unpinned"):
   cb4_unpack/matvec hand-worked golden blocks, half-order pin, brute force,
                    integer-GEMV special case
   f16_to_f64       all 65536 bit patterns against numpy's binary16
+  rmsnorm_q8       hand-derived f32 sums that fix the summation order, the
+                   guide's three-four case, a constant-vector closed form,
+                   the f32 error bound against binary64
 """
 from __future__ import annotations
 
@@ -82,10 +85,15 @@ def _load(fault: int = 0) -> ctypes.CDLL:
         lib.oracle_dequant_cb4.argtypes = [P, P, P, I64, I64]
         lib.oracle_subdots_cb4.argtypes = [P, P, P, P, I64, I64, I64]
         lib.oracle_matvec_cb4.argtypes = [P, P, P, P, P, I64, I64, I64]
+        lib.oracle_rmsnorm_sumsq.restype = ctypes.c_float
+        lib.oracle_rmsnorm_sumsq.argtypes = [P, I64]
+        lib.oracle_rmsnorm_scale.restype = ctypes.c_float
+        lib.oracle_rmsnorm_scale.argtypes = [P, I64]
+        lib.oracle_rmsnorm_q8.argtypes = [P, P, P, I64, I64]
         for fn in ("oracle_quantize_q8", "oracle_dequant_q8", "oracle_q4k_unpack",
                    "oracle_dequant_q4k", "oracle_subdots_q4k", "oracle_matvec_q4k",
                    "oracle_cb4_unpack", "oracle_dequant_cb4", "oracle_subdots_cb4",
-                   "oracle_matvec_cb4"):
+                   "oracle_matvec_cb4", "oracle_rmsnorm_q8"):
             getattr(lib, fn).restype = None
         _libs[fault] = lib
         return lib
@@ -196,6 +204,28 @@ class Oracle:
         self.lib.oracle_matvec_cb4(_ptr(W), _ptr(kv), _ptr(xq), _ptr(y),
                                    _ptr(ya) if with_abs else None, rows, cols, batch)
         return (y, ya) if with_abs else y
+
+
+    # -- RMSNorm + q8 pack ---------------------------------------------------
+    def rmsnorm_sumsq(self, x: np.ndarray) -> float:
+        x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+        return float(self.lib.oracle_rmsnorm_sumsq(_ptr(x), x.size))
+
+    def rmsnorm_scale(self, x: np.ndarray) -> float:
+        x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+        return float(self.lib.oracle_rmsnorm_scale(_ptr(x), x.size))
+
+    def rmsnorm_q8(self, x: np.ndarray):
+        """x: f32 [batch, cols] -> (q8 blocks of y, y = x * scale as f32)."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        if x.ndim == 1:
+            x = x[None, :]
+        batch, cols = x.shape
+        assert cols % 256 == 0
+        xq = np.empty((batch, cols // 256, Q8_BYTES), np.uint8)
+        y = np.empty((batch, cols), np.float32)
+        self.lib.oracle_rmsnorm_q8(_ptr(x), _ptr(xq), _ptr(y), cols, batch)
+        return xq, y
 
 
 _default: Oracle | None = None

@@ -368,3 +368,77 @@ void oracle_matvec_cb4(const uint8_t *W, const int8_t kv[16], const uint8_t *xq,
             if (y_abs) y_abs[b * rows + r] = aab;
         }
 }
+
+/* ---- RMSNorm + q8 pack ([G] 25.2.3 "a sum across the whole workgroup", and
+ * [G] 25.5: a fused tail ends with the next layer's norm and pack) ---------
+ * One workgroup of 256 work-items (eight waves of 32) per vector of n values:
+ *   item t   : ss_t = x_t^2 + x_{t+256}^2 + ..., added in that order from 0
+ *              (the strided loop of the guide's RmsNorm kernel)
+ *   wave w   : its 32 partials are combined by a butterfly over lane offsets
+ *              16, 8, 4, 2, 1 (lane l adds the value of lane l^off; all lanes
+ *              end with the same value, since f32 addition commutes)
+ *   workgroup: from 0, the eight wave partials are added, wave 0 first
+ *   scale    : 1 / sqrt(total / n + 1e-5), then y_i = x_i * scale
+ * Every f32 operation rounds once; nothing is contracted.  The guide fixes
+ * the strided per-item loop and the wave-0-upward order across waves; inside
+ * a wave it calls the reduction the hardware's, and the butterfly above is
+ * this library's reading.  The workgroup size 256 is also a reading. */
+#define ORMS_ITEMS 256
+#define ORMS_WAVE 32
+
+float oracle_rmsnorm_sumsq(const float *x, int64_t n) {
+    float ss[ORMS_ITEMS];
+    for (int t = 0; t < ORMS_ITEMS; ++t) {
+        float s = 0.0f;
+#if ORACLE_FAULT == 11
+        int64_t last = t;                         /* planted: reversed loop  */
+        while (last + ORMS_ITEMS < n) last += ORMS_ITEMS;
+        for (int64_t i = last; i >= t && i < n; i -= ORMS_ITEMS) {
+#else
+        for (int64_t i = t; i < n; i += ORMS_ITEMS) {
+#endif
+            float sq = x[i] * x[i];
+            s = s + sq;
+        }
+        ss[t] = s;
+    }
+    float total = 0.0f;
+    for (int w = 0; w < ORMS_ITEMS / ORMS_WAVE; ++w) {
+        float v[ORMS_WAVE], nv[ORMS_WAVE];
+        for (int l = 0; l < ORMS_WAVE; ++l) v[l] = ss[w * ORMS_WAVE + l];
+#if ORACLE_FAULT == 10
+        float seq = 0.0f;                         /* planted: lanes in order */
+        for (int l = 0; l < ORMS_WAVE; ++l) seq = seq + v[l];
+        v[0] = seq;
+#else
+        for (int off = ORMS_WAVE / 2; off > 0; off >>= 1) {
+            for (int l = 0; l < ORMS_WAVE; ++l) nv[l] = v[l] + v[l ^ off];
+            for (int l = 0; l < ORMS_WAVE; ++l) v[l] = nv[l];
+        }
+#endif
+        total = total + v[0];
+    }
+    return total;
+}
+
+float oracle_rmsnorm_scale(const float *x, int64_t n) {
+    float total = oracle_rmsnorm_sumsq(x, n);
+    float mean = total / (float)n;
+#if ORACLE_FAULT == 9
+    float den = sqrtf(mean);                      /* planted: eps dropped    */
+#else
+    float den = sqrtf(mean + 0.00001f);
+#endif
+    return 1.0f / den;
+}
+
+/* x [batch][cols] -> y = x*scale per vector (f32) and xq = q8 blocks of y. */
+void oracle_rmsnorm_q8(const float *x, uint8_t *xq, float *y, int64_t cols, int64_t batch) {
+    for (int64_t b = 0; b < batch; ++b) {
+        const float *v = x + b * cols;
+        float *yb = y + b * cols;
+        float scale = oracle_rmsnorm_scale(v, cols);
+        for (int64_t i = 0; i < cols; ++i) yb[i] = v[i] * scale;
+        oracle_quantize_q8(yb, xq + b * (cols / OQ8_VALUES) * OQ8_BYTES, cols, 1);
+    }
+}

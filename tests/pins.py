@@ -256,6 +256,97 @@ def pin_cb4_gemv_special(o):
     assert np.array_equal(dots, ref_d)
 
 
+# ---------------------------------------------------------------- RMSNorm + q8
+_EPS32 = float(np.float32(1e-5))
+_U32 = 2.0 ** -24          # unit roundoff of binary32
+
+
+def _sparse_vector(case) -> np.ndarray:
+    x = np.full(case["n"], case.get("x_rest", 0.0), np.float32)
+    for k, v in case["x_sparse"].items():
+        x[int(k)] = v
+    return x
+
+
+def pin_rmsnorm_order(o):
+    """Hand-derived f32 sums of squares whose value depends on the summation
+    order: the strided per-item loop, the butterfly inside a wave and the
+    wave-0-upward order across waves."""
+    for case in _golden("rmsnorm_hand.json")["sums"]:
+        got = o.rmsnorm_sumsq(_sparse_vector(case))
+        assert got == case["total"], (case["name"], got, case["total"])
+
+
+def _scale_bound(n: int) -> float:
+    """Relative error bound of the f32 scale against binary64: each square
+    passes through one product, at most ceil(n/256) loop additions, five
+    butterfly and eight cross-wave additions (positive terms, so the sum's
+    relative error is at most that count times u); then the mean, the eps
+    addition, sqrt (halves the relative error) and the reciprocal."""
+    k = 1 + -(-n // 256) + 5 + 8
+    return ((k + 2) / 2 + 2) * _U32 * 1.01
+
+
+def _scale64(x: np.ndarray) -> float:
+    import math
+    s = math.fsum(float(v) * float(v) for v in x.astype(np.float64))
+    return 1.0 / math.sqrt(s / x.size + _EPS32)
+
+
+def pin_rmsnorm_hand(o):
+    """The three-four case: q codes 95 and 127 whatever the scale's last bits,
+    and the scale within the f32 error bound of the binary64 value."""
+    case = _golden("rmsnorm_hand.json")["cases"][0]
+    x = _sparse_vector(case)
+    xq, y = o.rmsnorm_q8(x[None, :])
+    q = xq[0, 0, :256].view(np.int8).astype(np.int64)
+    want = np.zeros(256, np.int64)
+    for k, v in case["q_sparse"].items():
+        want[int(k)] = v
+    assert np.array_equal(q, want)
+    assert int(_i32(xq[0, 0, 256:260])[0]) == case["bsum0"]
+    ref = _scale64(x)
+    assert abs(o.rmsnorm_scale(x) - ref) <= _scale_bound(x.size) * ref
+    assert abs(float(y[0, 1]) - 4.0 * ref) <= (_scale_bound(x.size) + _U32) * 4.0 * ref
+
+
+def pin_rmsnorm_constant(o):
+    """A constant vector c: the sum of squares n*c^2 is exact in every order
+    (small multiples of a power of two), so the scale is 1/sqrt(c^2 + eps)
+    within four roundings, and every q8 code of y is 127 with sub-block sums
+    32*127."""
+    for c, n in ((0.5, 1024), (2.0, 4096), (1.0, 256)):
+        x = np.full(n, c, np.float32)
+        assert o.rmsnorm_sumsq(x) == n * c * c
+        ref = 1.0 / np.sqrt(c * c + _EPS32)
+        assert abs(o.rmsnorm_scale(x) - ref) <= 4 * _U32 * ref
+        xq, _ = o.rmsnorm_q8(x[None, :])
+        q = xq[0, :, :256].view(np.int8)
+        assert np.all(q == 127)
+        assert np.all(xq[0, :, 256:288].copy().view("<i4") == 32 * 127)
+
+
+def pin_rmsnorm_bound(o):
+    """Seeded vectors of the decode widths (and one with outliers): the f32
+    scale lies within its error bound of the binary64 value, y = x*scale
+    within one more rounding, and the q8 blocks of y meet the block
+    invariants."""
+    cases = [synthetic.activations(2, 4096, 71),
+             synthetic.activations(1, 14336, 72, outlier_frac=0.001),
+             synthetic.activations(3, 768, 73),
+             (synthetic.activations(1, 1024, 74) * np.float32(1e-3)).astype(np.float32)]
+    for x in cases:
+        xq, y = o.rmsnorm_q8(x)
+        for b in range(x.shape[0]):
+            ref = _scale64(x[b])
+            bound = _scale_bound(x.shape[1])
+            assert abs(o.rmsnorm_scale(x[b]) - ref) <= bound * ref
+            err = np.abs(y[b].astype(np.float64) - x[b].astype(np.float64) * ref)
+            assert np.all(err <= (bound + _U32) * 1.01 * np.abs(x[b].astype(np.float64)) * ref)
+        _q8_invariants(y, xq)
+
+
 ALL_PINS = [pin_f16_all_patterns, pin_q8_hand_cases, pin_q8_invariants, pin_q4k_scale_pack,
             pin_q4k_roundtrip, pin_q4k_block_y, pin_q4k_bruteforce, pin_q4k_gemv_special,
-            pin_q4k_min_term, pin_cb4_block_y, pin_cb4_bruteforce, pin_cb4_gemv_special]
+            pin_q4k_min_term, pin_cb4_block_y, pin_cb4_bruteforce, pin_cb4_gemv_special,
+            pin_rmsnorm_order, pin_rmsnorm_hand, pin_rmsnorm_constant, pin_rmsnorm_bound]

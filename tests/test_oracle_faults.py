@@ -16,6 +16,9 @@ FAULTS = {
     6: "q8 sub-block sums in the wrong slot",
     7: "min term sign flipped",
     8: "q8 scale step amax/128",
+    9: "RMSNorm eps dropped",
+    10: "RMSNorm wave lanes added left to right",
+    11: "RMSNorm item loop reversed",
 }
 
 
