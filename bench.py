@@ -348,10 +348,22 @@ def run_ours(args, c):
         xq.quantize_q8(x, out=xq_buf)
         do_matvec()
 
+    def do_norm_linear():  # RMSNorm, quantise and mat-vec in one launch
+        if c.fmt == "q4k":
+            xq.norm_linear_q4k(x, W, c.rows, c.cols, out=y)
+        else:
+            xq.norm_linear_cb4(x, W, kv, c.rows, c.cols, out=y)
+
+    def do_norm_two_call():  # xq_rmsnorm_q8, then the mat-vec
+        xq.rmsnorm_q8(x, out=xq_buf)
+        do_matvec()
+
     # eager warm-up: the first call per device configures the kernels (before capture)
     with torch.cuda.stream(stream):
         for _ in range(3):
             do_two_call()
+            do_norm_two_call()
+            do_norm_linear()
             do_step()
     stream.synchronize()
 
@@ -367,7 +379,8 @@ def run_ours(args, c):
     ncount = xq.COUNT_N
     counts0 = [xq.launch_count(i) for i in range(ncount)]
     graphs = {}
-    for name, fn in (("step", do_step), ("matvec", do_matvec), ("two_call", do_two_call)):
+    for name, fn in (("step", do_step), ("matvec", do_matvec), ("two_call", do_two_call),
+                     ("norm_linear", do_norm_linear), ("norm_two_call", do_norm_two_call)):
         graphs[name] = (capture(fn, per_graph), capture(fn, rem) if rem else None)
         if name == "step":
             launches_per_step = sum(xq.launch_count(i) - counts0[i]
@@ -404,6 +417,8 @@ def run_ours(args, c):
     # the same kernels outside the step, for the breakdown
     mv_ms = timed("matvec", args.steps)
     two_ms = timed("two_call", args.steps)
+    nl_ms = timed("norm_linear", args.steps)
+    n2_ms = timed("norm_two_call", args.steps)
     time.sleep(0.2)
     sampler.stop()
     clocks = sampler.summary(t_wall0, time.time())
@@ -454,7 +469,11 @@ def run_ours(args, c):
             "matvec_on_q8_input": {"us": mv_ms * 1e3,
                                    "GBs": nbytes["matvec"] / (mv_ms * 1e-3) / 1e9},
             "quantise_then_matvec": {"us": two_ms * 1e3,
-                                     "GBs": nbytes["two_call"] / (two_ms * 1e-3) / 1e9}},
+                                     "GBs": nbytes["two_call"] / (two_ms * 1e-3) / 1e9},
+            "rmsnorm_quantise_matvec_fused": {"us": nl_ms * 1e3,
+                                              "GBs": nbytes["linear"] / (nl_ms * 1e-3) / 1e9},
+            "rmsnorm_q8_then_matvec": {"us": n2_ms * 1e3,
+                                       "GBs": nbytes["two_call"] / (n2_ms * 1e-3) / 1e9}},
         "cpu_baseline": cpu,
         "e2e": {"value": world * nbytes["linear"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "steps": e2e_steps,

@@ -119,6 +119,33 @@ xq_status xq_linear_q4k(const float *x, const void *W, float *y, int64_t rows, i
 xq_status xq_linear_cb4(const float *x, const void *W, const int8_t *table, float *y,
                         int64_t rows, int64_t cols, int64_t batch, void *stream);
 
+/* RMSNorm + q8 pack, the producer of the next layer's activation blocks:
+ * for each of the batch vectors x_b ([batch][cols] f32, device),
+ *   scale_b = 1 / sqrt(sum_i x_{b,i}^2 / cols + 1e-5),  y_b = x_b * scale_b,
+ * and xq receives the q8 blocks of y_b exactly as xq_quantize_q8 would write
+ * them.  The f32 sum of squares is taken in one fixed order, that of a
+ * workgroup of 256 items in eight waves of 32: item t adds x_t^2,
+ * x_{t+256}^2, ... in turn, each wave combines its items by an xor
+ * butterfly over lane offsets 16, 8, 4, 2, 1, and the eight wave sums are
+ * added from wave 0 upward; every f32 operation rounds once.  So the scale
+ * and the q8 codes are one defined value, not merely close.  y (device,
+ * [batch][cols] f32, 16-byte aligned) receives y_b when it is non-null.
+ * Shapes as for xq_quantize_q8.  Source: "25 - Writing XPU Kernels" 25.2.3
+ * (a sum across the whole workgroup; the RMSNorm kernel) and 25.5 (a fused
+ * tail ends with the next layer's norm and pack). */
+xq_status xq_rmsnorm_q8(const float *x, void *xq, float *y, int64_t cols, int64_t batch,
+                        void *stream);
+
+/* The fused decode step behind an RMSNorm: y = W . q8(x_b * scale_b), with
+ * scale_b as in xq_rmsnorm_q8, in one launch (every CTA computes the scale
+ * in the same fixed order and quantises into its own shared memory).  y is
+ * bit-identical to xq_rmsnorm_q8 followed by xq_matvec_q4k / xq_matvec_cb4.
+ * x must be 16-byte aligned. */
+xq_status xq_norm_linear_q4k(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
+                             int64_t batch, void *stream);
+xq_status xq_norm_linear_cb4(const float *x, const void *W, const int8_t *table, float *y,
+                             int64_t rows, int64_t cols, int64_t batch, void *stream);
+
 /* Grouped experts ("25 - Writing XPU Kernels" 25.2.2, the mul_mat_vec_id
  * shape): W is a slab of n_experts experts of rows_per_expert rows each,
  * contiguous; sel (DEVICE int32[used]) selects the experts.  One launch
@@ -189,7 +216,10 @@ enum {
     XQ_COUNT_LINEAR_CB4 = 6,
     XQ_COUNT_MATVEC_ID_Q4K = 7,
     XQ_COUNT_MATVEC_ID_CB4 = 8,
-    XQ_COUNT_N = 9
+    XQ_COUNT_RMSNORM_Q8 = 9,
+    XQ_COUNT_NORM_LINEAR_Q4K = 10,
+    XQ_COUNT_NORM_LINEAR_CB4 = 11,
+    XQ_COUNT_N = 12
 };
 uint64_t xq_launch_count(int32_t which);
 

@@ -9,6 +9,8 @@ fallback: if the library is missing this package raises on import.
     y   = matvec_q4k(W, xq, rows, cols)        # W: uint8 Q4_K rows on cuda
     y   = matvec_cb4(W, table, xq, rows, cols) # W: uint8 codebook rows
     y   = linear_q4k(x, W, rows, cols)         # fused: quantise + mat-vec, one launch
+    xq  = rmsnorm_q8(x)                        # RMSNorm + q8 pack of the next input
+    y   = norm_linear_q4k(x, W, rows, cols)    # fused: RMSNorm + quantise + mat-vec
 """
 from __future__ import annotations
 
@@ -21,7 +23,10 @@ from ._native import (  # noqa: F401
     COUNT_MATVEC_ID_Q4K,
     COUNT_MATVEC_Q4K,
     COUNT_N,
+    COUNT_NORM_LINEAR_CB4,
+    COUNT_NORM_LINEAR_Q4K,
     COUNT_QUANTIZE,
+    COUNT_RMSNORM_Q8,
     COUNT_SUBDOTS_CB4,
     COUNT_SUBDOTS_Q4K,
     XQError,
@@ -35,10 +40,13 @@ from ._native import (  # noqa: F401
     matvec_cb4,
     matvec_id,
     matvec_q4k,
+    norm_linear_cb4,
+    norm_linear_q4k,
     plan_matvec,
     q4k_bytes,
     q8_bytes,
     quantize_q8,
+    rmsnorm_q8,
     set_plan_override,
     subdots_cb4,
     subdots_q4k,

@@ -43,6 +43,10 @@ _matvec_q4k = _sig("xq_matvec_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64,
 _matvec_cb4 = _sig("xq_matvec_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
 _linear_q4k = _sig("xq_linear_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
 _linear_cb4 = _sig("xq_linear_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
+_rmsnorm_q8 = _sig("xq_rmsnorm_q8", ctypes.c_int, [_P, _P, _P, _I64, _I64, _P])
+_norm_linear_q4k = _sig("xq_norm_linear_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
+_norm_linear_cb4 = _sig("xq_norm_linear_cb4", ctypes.c_int,
+                        [_P, _P, _P, _P, _I64, _I64, _I64, _P])
 _matvec_q4k_id = _sig("xq_matvec_q4k_id", ctypes.c_int,
                       [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P])
 _matvec_cb4_id = _sig("xq_matvec_cb4_id", ctypes.c_int,
@@ -61,8 +65,9 @@ _last_error = _sig("xq_last_error", ctypes.c_char_p, [])
 _version = _sig("xq_version", _I32, [])
 
 (COUNT_QUANTIZE, COUNT_MATVEC_Q4K, COUNT_MATVEC_CB4, COUNT_SUBDOTS_Q4K, COUNT_SUBDOTS_CB4,
- COUNT_LINEAR_Q4K, COUNT_LINEAR_CB4, COUNT_MATVEC_ID_Q4K, COUNT_MATVEC_ID_CB4) = range(9)
-COUNT_N = 9
+ COUNT_LINEAR_Q4K, COUNT_LINEAR_CB4, COUNT_MATVEC_ID_Q4K, COUNT_MATVEC_ID_CB4,
+ COUNT_RMSNORM_Q8, COUNT_NORM_LINEAR_Q4K, COUNT_NORM_LINEAR_CB4) = range(12)
+COUNT_N = 12
 
 
 class XQError(RuntimeError):
@@ -193,6 +198,47 @@ def linear_cb4(x: torch.Tensor, W: torch.Tensor, table, rows: int, cols: int,
                        ctypes.cast(_table(table), _P), _dev(out, "y", torch.float32), rows,
                        cols, batch, _stream(stream)))
     return out
+
+
+def rmsnorm_q8(x: torch.Tensor, out: torch.Tensor | None = None, y: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """RMSNorm + q8 pack: x f32 [batch, cols] (CUDA) -> the q8 blocks of
+    x * scale (uint8 [batch, cols/256, 320]); writes the f32 x * scale into
+    ``y`` too when it is given."""
+    x = _x2d(x)
+    batch, cols = x.shape
+    if out is None:
+        out = torch.empty((batch, max(cols // 256, 0), 320), dtype=torch.uint8, device=x.device)
+    yp = None if y is None else _dev(y, "y", torch.float32)
+    _check(_rmsnorm_q8(_dev(x, "x", torch.float32), _dev(out, "xq", torch.uint8), yp, cols,
+                       batch, _stream(stream)))
+    return out
+
+
+def _norm_linear(fn, x, W, table, rows, cols, out, stream):
+    x = _x2d(x)
+    batch = x.shape[0]
+    if x.shape[1] != cols:
+        raise ValueError("x has the wrong number of columns")
+    if out is None:
+        out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    args = [_dev(x, "x", torch.float32), _dev(W, "W", torch.uint8)]
+    if table is not None:
+        args.append(ctypes.cast(_table(table), _P))
+    _check(fn(*args, _dev(out, "y", torch.float32), rows, cols, batch, _stream(stream)))
+    return out
+
+
+def norm_linear_q4k(x: torch.Tensor, W: torch.Tensor, rows: int, cols: int,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """RMSNorm, quantise and multiply by the Q4_K rows W in one launch."""
+    return _norm_linear(_norm_linear_q4k, x, W, None, rows, cols, out, stream)
+
+
+def norm_linear_cb4(x: torch.Tensor, W: torch.Tensor, table, rows: int, cols: int,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """RMSNorm, quantise and multiply by the codebook rows W in one launch."""
+    return _norm_linear(_norm_linear_cb4, x, W, table, rows, cols, out, stream)
 
 
 def matvec_id(fmt: str, W: torch.Tensor, sel: torch.Tensor, xq: torch.Tensor,

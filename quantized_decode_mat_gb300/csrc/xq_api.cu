@@ -8,6 +8,7 @@
 #include <string>
 
 #include "xq_internal.h"
+#include "xq_norm.cuh"
 #include "xq_q8.cuh"
 
 namespace xq {
@@ -38,6 +39,46 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float *__restric
         *reinterpret_cast<float *>(out + kQ8ScaleAt) = r.d;
     else if (lane < 8)
         *reinterpret_cast<uint32_t *>(out + kQ8ScaleAt + 4 * lane) = 0u;  // bytes 292..319
+}
+
+// ---- RMSNorm + q8 pack -------------------------------------------------------------
+// One block of 256 threads per vector: warp 0 takes the scale in the fixed
+// order (rms_scale_warp), then warp w takes blocks w, w+8, ... of
+// y = x * scale with q8_quantize_lane, and writes y itself when y is
+// non-null.
+__global__ void __launch_bounds__(256) rmsnorm_q8_kernel(const float *__restrict__ x,
+                                                         uint8_t *__restrict__ xq,
+                                                         float *__restrict__ y, int64_t cols) {
+    __shared__ float s_scale;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float *xv = x + (int64_t)blockIdx.x * cols;
+    if (warp == 0) {
+        const float sc = rms_scale_warp(xv, cols, lane);
+        if (lane == 0) s_scale = sc;
+    }
+    __syncthreads();
+    const float scale = s_scale;
+    const int64_t nb = cols / 256;
+    for (int64_t k = warp; k < nb; k += 8) {
+        const float4 *src = reinterpret_cast<const float4 *>(xv + k * 256 + lane * 8);
+        const float4 u = __ldg(src), v = __ldg(src + 1);
+        float vals[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vals[i] = __fmul_rn(vals[i], scale);
+        if (y) {
+            float4 *dy = reinterpret_cast<float4 *>(y + (int64_t)blockIdx.x * cols + k * 256 + lane * 8);
+            dy[0] = make_float4(vals[0], vals[1], vals[2], vals[3]);
+            dy[1] = make_float4(vals[4], vals[5], vals[6], vals[7]);
+        }
+        const Q8Lane r = q8_quantize_lane(vals);
+        uint8_t *out = xq + ((int64_t)blockIdx.x * nb + k) * kQ8Bytes;
+        *reinterpret_cast<uint2 *>(out + lane * 8) = make_uint2(r.w0, r.w1);
+        if ((lane & 3) == 0) *reinterpret_cast<int *>(out + kQ8SumAt + (lane >> 2) * 4) = r.sum;
+        if (lane == 0)
+            *reinterpret_cast<float *>(out + kQ8ScaleAt) = r.d;
+        else if (lane < 8)
+            *reinterpret_cast<uint32_t *>(out + kQ8ScaleAt + 4 * lane) = 0u;  // bytes 292..319
+    }
 }
 
 namespace {
@@ -191,14 +232,25 @@ xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
     return XQ_OK;
 }
 
-enum class Op { kMatvecQ4K, kMatvecCB4, kDotsQ4K, kDotsCB4, kLinearQ4K, kLinearCB4 };
+enum class Op {
+    kMatvecQ4K,
+    kMatvecCB4,
+    kDotsQ4K,
+    kDotsCB4,
+    kLinearQ4K,
+    kLinearCB4,
+    kNormLinearQ4K,
+    kNormLinearCB4
+};
 
 // in: q8 blocks (mat-vec and sub-dots) or f32 x (the fused linear ops).
 xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *in, void *out,
                      int64_t rows, int64_t cols, int64_t batch, void *stream) {
-    const bool cb4 = (op == Op::kMatvecCB4 || op == Op::kDotsCB4 || op == Op::kLinearCB4);
+    const bool cb4 = (op == Op::kMatvecCB4 || op == Op::kDotsCB4 || op == Op::kLinearCB4 ||
+                      op == Op::kNormLinearCB4);
     const bool dots = (op == Op::kDotsQ4K || op == Op::kDotsCB4);
-    const bool fused = (op == Op::kLinearQ4K || op == Op::kLinearCB4);
+    const bool norm = (op == Op::kNormLinearQ4K || op == Op::kNormLinearCB4);
+    const bool fused = norm || op == Op::kLinearQ4K || op == Op::kLinearCB4;
     t_error.clear();
     if (!W || !in || !out)
         return fail(XQ_EINVAL, fused ? "null device pointer (x, W or y)"
@@ -240,13 +292,15 @@ xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *in, 
     }
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int kind = dots ? 1 : fused ? 2 : 0;
-    const int which = op == Op::kMatvecQ4K   ? XQ_COUNT_MATVEC_Q4K
-                      : op == Op::kMatvecCB4  ? XQ_COUNT_MATVEC_CB4
-                      : op == Op::kDotsQ4K    ? XQ_COUNT_SUBDOTS_Q4K
-                      : op == Op::kDotsCB4    ? XQ_COUNT_SUBDOTS_CB4
-                      : op == Op::kLinearQ4K  ? XQ_COUNT_LINEAR_Q4K
-                                              : XQ_COUNT_LINEAR_CB4;
+    const int kind = dots ? 1 : norm ? 4 : fused ? 2 : 0;
+    const int which = op == Op::kMatvecQ4K      ? XQ_COUNT_MATVEC_Q4K
+                      : op == Op::kMatvecCB4     ? XQ_COUNT_MATVEC_CB4
+                      : op == Op::kDotsQ4K       ? XQ_COUNT_SUBDOTS_Q4K
+                      : op == Op::kDotsCB4       ? XQ_COUNT_SUBDOTS_CB4
+                      : op == Op::kLinearQ4K     ? XQ_COUNT_LINEAR_Q4K
+                      : op == Op::kLinearCB4     ? XQ_COUNT_LINEAR_CB4
+                      : op == Op::kNormLinearQ4K ? XQ_COUNT_NORM_LINEAR_Q4K
+                                                 : XQ_COUNT_NORM_LINEAR_CB4;
     for (int64_t b0 = 0; b0 < batch; b0 += plan.batch_per_launch) {
         const int64_t bc = batch - b0 < plan.batch_per_launch ? batch - b0 : plan.batch_per_launch;
         if (fused)
@@ -372,6 +426,29 @@ xq_status xq_quantize_q8(const float *x, void *xq_out, int64_t cols, int64_t bat
     return XQ_OK;
 }
 
+xq_status xq_rmsnorm_q8(const float *x, void *xq_out, float *y, int64_t cols, int64_t batch,
+                        void *stream) {
+    t_error.clear();
+    if (!x || !xq_out) return fail(XQ_EINVAL, "null device pointer (x or xq)");
+    if (xq_status s = check_shape(0, cols, batch, false)) return s;
+    if (!aligned(x, 16)) return fail(XQ_EALIGN, "x must be 16-byte aligned");
+    if (!aligned(xq_out, 16)) return fail(XQ_EALIGN, "xq must be 16-byte aligned");
+    if (y && !aligned(y, 16)) return fail(XQ_EALIGN, "y must be 16-byte aligned");
+    const size_t x_bytes = (size_t)batch * cols * 4;
+    const size_t q_bytes = (size_t)batch * (cols / 256) * kQ8Bytes;
+    if (overlap(xq_out, q_bytes, x, x_bytes) || (y && overlap(y, x_bytes, x, x_bytes)) ||
+        (y && overlap(y, x_bytes, xq_out, q_bytes)))
+        return fail(XQ_EINVAL, "outputs overlap each other or x");
+    DeviceState *dev = nullptr;
+    if (xq_status s = device_state(&dev)) return s;
+    rmsnorm_q8_kernel<<<(unsigned)batch, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        x, static_cast<uint8_t *>(xq_out), y, cols);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "RMSNorm launch");
+    g_counts[XQ_COUNT_RMSNORM_Q8].fetch_add(1, std::memory_order_relaxed);
+    return XQ_OK;
+}
+
 xq_status xq_matvec_q4k(const void *W, const void *xq_in, float *y, int64_t rows, int64_t cols,
                         int64_t batch, void *stream) {
     return run_matvec(Op::kMatvecQ4K, W, nullptr, xq_in, y, rows, cols, batch, stream);
@@ -390,6 +467,16 @@ xq_status xq_linear_q4k(const float *x, const void *W, float *y, int64_t rows, i
 xq_status xq_linear_cb4(const float *x, const void *W, const int8_t *table, float *y,
                         int64_t rows, int64_t cols, int64_t batch, void *stream) {
     return run_matvec(Op::kLinearCB4, W, table, x, y, rows, cols, batch, stream);
+}
+
+xq_status xq_norm_linear_q4k(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
+                             int64_t batch, void *stream) {
+    return run_matvec(Op::kNormLinearQ4K, W, nullptr, x, y, rows, cols, batch, stream);
+}
+
+xq_status xq_norm_linear_cb4(const float *x, const void *W, const int8_t *table, float *y,
+                             int64_t rows, int64_t cols, int64_t batch, void *stream) {
+    return run_matvec(Op::kNormLinearCB4, W, table, x, y, rows, cols, batch, stream);
 }
 
 xq_status xq_matvec_q4k_id(const void *W, const int32_t *sel, const void *xq_in, float *y,

@@ -23,9 +23,14 @@ constexpr int kTileRows = 32;                       // lanes (chunks) per box
 constexpr int kStageBytes = kTileRows * kChunkBytes;  // one staged box: 4608 B
 // Shared-memory stride of a staged q8 block: bytes 0..303 of the block, then
 // its split sums at 304..319; 336 = 84 words puts 8 consecutive chunks on
-// distinct 4-bank groups.
+// distinct 4-bank groups.  Bytes 320..335 are padding; the fused RMSNorm
+// kernels park a vector's scale there, in its first block.
 constexpr int kActStride = 336;
 constexpr int kActSplitAt = 304;
+constexpr int kActNormAt = 320;
+// q8 blocks whose activation values one warp loads at once in the fused
+// kernels (one L2 round trip per group).
+constexpr int kQuantGroup = 4;
 constexpr int kMaxWarps = 8;
 constexpr int kMaxStages = 8;
 

@@ -11,6 +11,7 @@
 
 #include "xq_internal.h"
 #include "xq_ptx.cuh"
+#include "xq_norm.cuh"
 #include "xq_q8.cuh"
 
 namespace xq {
@@ -279,14 +280,16 @@ __device__ __forceinline__ GroupInfo group_info(const MatvecArgs &a, int64_t g, 
 // bytes per chunk | [W][S] box stages of 4608 bytes.  Each warp fills its
 // stages with coalesced 16-byte cp.async copies (copy p moves bytes
 // 16p..16p+15 of the box to shared offset 16p; lane l's chunk lands at
-// 144*l), keeping S-1 boxes in flight.  The act stride puts the chunks that
-// one instruction reads on distinct bank groups.
+// 144*l), keeping S-1 boxes in flight.  (Requesting all S boxes before the
+// activation is staged measured slower.)  The act stride puts the chunks
+// that one instruction reads on distinct bank groups.
 template <int B>
 constexpr int max_threads() { return warps_limit(B) * 32; }
 
-template <int FMT, int B, bool DOTS, bool FUSED, bool ID>
+template <int FMT, int B, bool DOTS, int FUSE, bool ID>
 __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const MatvecArgs a) {
-    static_assert(!ID || (B == 1 && !DOTS && !FUSED), "the grouped form is batch 1 on q8 input");
+    static_assert(!ID || (B == 1 && !DOTS && FUSE == 0), "the grouped form is batch 1 on q8 input");
+    static_assert(FUSE >= 0 && FUSE <= 2, "FUSE: 0 q8 input, 1 quantise x, 2 RMSNorm then quantise");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const int W = blockDim.x >> 5;
@@ -355,25 +358,57 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
     }
 
     // 2. the activation (a different region of shared memory than the stages)
-    if (FUSED) {
-        // quantise x here: warp w takes blocks w, w+W, ... of the batch (the
-        // same arithmetic as the standalone quantiser, so the same bytes)
-        for (int blk = warp; blk < B * nb; blk += W) {
-            const float4 *src = reinterpret_cast<const float4 *>(a.x + (int64_t)blk * 256 + lane * 8);
-            const float4 u = __ldg(src), v = __ldg(src + 1);
-            const float vals[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-            const Q8Lane r = q8_quantize_lane(vals);
-            uint8_t *dst = act + blk * kActStride;
-            *reinterpret_cast<uint2 *>(dst + lane * 8) = make_uint2(r.w0, r.w1);
-            if ((lane & 3) == 0) *reinterpret_cast<int *>(dst + kQ8SumAt + (lane >> 2) * 4) = r.sum;
-            uint32_t sums[8];
+    if (FUSE != 0) {
+        // FUSE == 2: warp w first takes the RMSNorm scale of vectors w, w+W,
+        // ... and parks it in bytes 320..335 of the vector's first staged
+        // block (stride padding that nothing else reads or writes)
+        if (FUSE == 2) {
+            for (int b = warp; b < B; b += W) {
+                const float sc = rms_scale_warp(a.x + (int64_t)b * nb * 256, (int64_t)nb * 256, lane);
+                if (lane == 0) *reinterpret_cast<float *>(act + b * act_bstride + kActNormAt) = sc;
+            }
+            __syncthreads();
+        }
+        // quantise x (FUSE == 2: y = x * scale) here: warp w takes blocks w,
+        // w+W, ... (vector-major) with the standalone producers' arithmetic,
+        // so the same bytes.  The values of kQuantGroup blocks are loaded
+        // before any of them is processed: one L2 round trip per group.
+        const int nblk = B * nb;
+        for (int k0 = warp; k0 < nblk; k0 += kQuantGroup * W) {
+            float4 u[kQuantGroup], v[kQuantGroup];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) sums[j] = (uint32_t)__shfl_sync(0xffffffffu, r.sum, 4 * j);
-            if (lane == 0) {
-                *reinterpret_cast<float *>(dst + kQ8ScaleAt) = r.d;
-                *reinterpret_cast<uint4 *>(dst + kActSplitAt) =
-                    split_sums(make_uint4(sums[0], sums[1], sums[2], sums[3]),
-                               make_uint4(sums[4], sums[5], sums[6], sums[7]));
+            for (int j = 0; j < kQuantGroup; ++j) {
+                const int blk = k0 + j * W;
+                if (blk < nblk) {
+                    const float4 *src = reinterpret_cast<const float4 *>(a.x + (int64_t)blk * 256 + lane * 8);
+                    u[j] = __ldg(src);
+                    v[j] = __ldg(src + 1);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kQuantGroup; ++j) {
+                const int blk = k0 + j * W;
+                if (blk >= nblk) break;  // warp-uniform
+                float vals[8] = {u[j].x, u[j].y, u[j].z, u[j].w, v[j].x, v[j].y, v[j].z, v[j].w};
+                if (FUSE == 2) {
+                    const int b = blk / nb;
+                    const float ns = *reinterpret_cast<const float *>(act + b * act_bstride + kActNormAt);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) vals[i] = __fmul_rn(vals[i], ns);
+                }
+                const Q8Lane r = q8_quantize_lane(vals);
+                uint8_t *dst = act + blk * kActStride;
+                *reinterpret_cast<uint2 *>(dst + lane * 8) = make_uint2(r.w0, r.w1);
+                if ((lane & 3) == 0) *reinterpret_cast<int *>(dst + kQ8SumAt + (lane >> 2) * 4) = r.sum;
+                uint32_t sums[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) sums[q] = (uint32_t)__shfl_sync(0xffffffffu, r.sum, 4 * q);
+                if (lane == 0) {
+                    *reinterpret_cast<float *>(dst + kQ8ScaleAt) = r.d;
+                    *reinterpret_cast<uint4 *>(dst + kActSplitAt) =
+                        split_sums(make_uint4(sums[0], sums[1], sums[2], sums[3]),
+                                   make_uint4(sums[4], sums[5], sums[6], sums[7]));
+                }
             }
         }
     } else {
@@ -440,32 +475,34 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
     cp_async_wait_all();  // only empty groups can remain; keeps the exit clean
 }
 
-template <int FMT, int B, bool DOTS, bool FUSED, bool ID = false>
+template <int FMT, int B, bool DOTS, int FUSE, bool ID = false>
 inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, size_t smem,
                                    cudaStream_t s) {
-    xq_matvec_kernel<FMT, B, DOTS, FUSED, ID><<<grid, block, smem, s>>>(a);
+    xq_matvec_kernel<FMT, B, DOTS, FUSE, ID><<<grid, block, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-template <int FMT, int B, bool DOTS, bool FUSED, bool ID = false>
+template <int FMT, int B, bool DOTS, int FUSE, bool ID = false>
 inline cudaError_t configure_t(int smem_optin) {
-    return cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSED, ID>,
+    return cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
 }
 
 // kind: 0 = mat-vec on q8 blocks, 1 = the same with the exact dots,
-// 2 = fused quantise + mat-vec, 3 = grouped experts (batch 1, q8 input).
+// 2 = fused quantise + mat-vec, 3 = grouped experts (batch 1, q8 input),
+// 4 = fused RMSNorm + quantise + mat-vec.
 template <int FMT>
 inline cudaError_t launch_matvec_fmt(const MatvecArgs &a, int batch, int kind, dim3 grid,
                                      dim3 block, size_t smem, cudaStream_t s) {
     if (kind == 3)
-        return batch == 1 ? launch_matvec_t<FMT, 1, false, false, true>(a, grid, block, smem, s)
+        return batch == 1 ? launch_matvec_t<FMT, 1, false, 0, true>(a, grid, block, smem, s)
                           : cudaErrorInvalidValue;
 #define XQ_CASE(BB)                                                                    \
     case BB:                                                                           \
-        return kind == 1   ? launch_matvec_t<FMT, BB, true, false>(a, grid, block, smem, s)  \
-               : kind == 2 ? launch_matvec_t<FMT, BB, false, true>(a, grid, block, smem, s)  \
-                           : launch_matvec_t<FMT, BB, false, false>(a, grid, block, smem, s);
+        return kind == 1   ? launch_matvec_t<FMT, BB, true, 0>(a, grid, block, smem, s)  \
+               : kind == 2 ? launch_matvec_t<FMT, BB, false, 1>(a, grid, block, smem, s) \
+               : kind == 4 ? launch_matvec_t<FMT, BB, false, 2>(a, grid, block, smem, s) \
+                           : launch_matvec_t<FMT, BB, false, 0>(a, grid, block, smem, s);
     switch (batch) {
         XQ_CASE(1)
         XQ_CASE(2)
@@ -485,9 +522,10 @@ template <int FMT>
 inline cudaError_t configure_fmt(int smem_optin) {
     cudaError_t e = cudaSuccess;
 #define XQ_CFG(BB)                                                             \
-    if (e == cudaSuccess) e = configure_t<FMT, BB, false, false>(smem_optin); \
-    if (e == cudaSuccess) e = configure_t<FMT, BB, true, false>(smem_optin);  \
-    if (e == cudaSuccess) e = configure_t<FMT, BB, false, true>(smem_optin);
+    if (e == cudaSuccess) e = configure_t<FMT, BB, false, 0>(smem_optin); \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, true, 0>(smem_optin);  \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, false, 1>(smem_optin); \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, false, 2>(smem_optin);
     XQ_CFG(1)
     XQ_CFG(2)
     XQ_CFG(3)
@@ -497,7 +535,7 @@ inline cudaError_t configure_fmt(int smem_optin) {
     XQ_CFG(7)
     XQ_CFG(8)
 #undef XQ_CFG
-    if (e == cudaSuccess) e = configure_t<FMT, 1, false, false, true>(smem_optin);
+    if (e == cudaSuccess) e = configure_t<FMT, 1, false, 0, true>(smem_optin);
     return e;
 }
 

@@ -38,7 +38,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("xq_quantize_q8", "xq_matvec_q4k", "xq_matvec_cb4", "xq_linear_q4k",
-                 "xq_linear_cb4", "xq_subdots_q4k",
+                 "xq_linear_cb4", "xq_rmsnorm_q8", "xq_norm_linear_q4k",
+                 "xq_norm_linear_cb4", "xq_subdots_q4k",
                  "xq_subdots_cb4", "xq_q8_bytes", "xq_status_string", "xq_last_error"):
         assert must in names
 
@@ -125,6 +126,20 @@ def test_quantize_argument_checks(raw):
     assert _call(raw, "xq_quantize_q8", V(P + 4), V(P * 4), I64(256), I64(1), V(0)) == 2
     assert _call(raw, "xq_quantize_q8", V(P), V(P * 4), I64(300), I64(1), V(0)) == 3
     assert _call(raw, "xq_quantize_q8", V(P), V(P + 512), I64(256), I64(1), V(0)) == 1
+
+
+def test_rmsnorm_argument_checks(raw):
+    assert _call(raw, "xq_rmsnorm_q8", V(0), V(P), V(0), I64(256), I64(1), V(0)) == 1
+    assert _call(raw, "xq_rmsnorm_q8", V(P + 4), V(P * 4), V(0), I64(256), I64(1), V(0)) == 2
+    assert _call(raw, "xq_rmsnorm_q8", V(P), V(P * 4), V(P * 8 + 4), I64(256), I64(1), V(0)) == 2
+    assert _call(raw, "xq_rmsnorm_q8", V(P), V(P * 4), V(0), I64(300), I64(1), V(0)) == 3
+    assert _call(raw, "xq_rmsnorm_q8", V(P), V(P * 4), V(0), I64(256), I64(9), V(0)) == 3
+    assert _call(raw, "xq_rmsnorm_q8", V(P), V(P + 512), V(0), I64(256), I64(1), V(0)) == 1
+    assert _call(raw, "xq_rmsnorm_q8", V(P), V(P * 4), V(P + 512), I64(256), I64(1), V(0)) == 1
+    assert _call(raw, "xq_norm_linear_q4k", V(0), V(P), V(P * 8), I64(32), I64(256), I64(1),
+                 V(0)) == 1
+    assert _call(raw, "xq_norm_linear_cb4", V(P), V(P * 4), V(0), V(P * 8), I64(32), I64(256),
+                 I64(1), V(0)) == 1
 
 
 def test_subdots_need_16_byte_aligned_output(raw):

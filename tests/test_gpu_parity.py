@@ -349,6 +349,108 @@ def test_linear_is_the_two_call_path(xq, orc, fmt, rows, cols, batch):
     check_y(y1, y_ref, f"linear {fmt} {rows}x{cols} b{batch}")
 
 
+# ---------------------------------------------------------------- RMSNorm + q8 pack
+def _norm_x(kind, batch, cols, seed):
+    if kind == "order":
+        # the hand-derived order cases: one large square among ones (the
+        # butterfly and the wave order decide the f32 sum), and a large
+        # square last in an item's strided loop
+        x = np.ones((batch, cols), np.float32)
+        x[:, 0] = 4096.0
+        if batch > 1:
+            x[1] = 0.0
+            x[1, 0] = x[1, 256 % cols] = 1.0
+            x[1, 512 % cols] = 4096.0
+        return x
+    return _x_kind(kind, batch, cols, seed)
+
+
+@pytest.mark.parametrize("kind", ["normal", "outliers", "fixture", "zeros", "tiny", "huge",
+                                  "ties", "order"])
+@pytest.mark.parametrize("cols,batch", [(256, 1), (768, 2), (4096, 8), (14336, 2), (65536, 1)])
+def test_rmsnorm_q8_bit_exact(xq, orc, kind, cols, batch):
+    """The scale is summed in the same fixed order on both sides, so y and
+    every byte of the q8 blocks agree bit for bit."""
+    x = _norm_x(kind, batch, cols, cols + batch)
+    xq_ref, y_ref = orc.rmsnorm_q8(x)
+    out = Guarded((batch, cols // 256, 320), torch.uint8)
+    y = Guarded((batch, cols), torch.float32)
+    before = xq.launch_count(xq.COUNT_RMSNORM_Q8)
+    xq.rmsnorm_q8(dev(x), out=out.t, y=y.t)
+    torch.cuda.synchronize()
+    out.check_guard()
+    y.check_guard()
+    assert xq.launch_count(xq.COUNT_RMSNORM_Q8) == before + 1
+    got_y = y.t.cpu().numpy()
+    assert np.array_equal(got_y.view(np.uint32), y_ref.view(np.uint32)), \
+        f"y differs at {np.argwhere(got_y.view(np.uint32) != y_ref.view(np.uint32))[:4]}"
+    got = out.t.cpu().numpy()
+    bad = np.argwhere(got != xq_ref)
+    assert bad.size == 0, f"q8 bytes differ at {bad[:4]}"
+    # without y: the same q8 bytes
+    out2 = Guarded((batch, cols // 256, 320), torch.uint8)
+    xq.rmsnorm_q8(dev(x), out=out2.t)
+    torch.cuda.synchronize()
+    out2.check_guard()
+    assert np.array_equal(out2.t.cpu().numpy(), xq_ref)
+
+
+@pytest.mark.parametrize("fmt", ["q4k", "cb4"])
+@pytest.mark.parametrize("rows,cols,batch", [(1, 256, 1), (101, 1024, 2), (77, 4096, 8),
+                                             (300, 4096, 1), (64, 14336, 3), (37, 65536, 8),
+                                             (4096, 4096, 1)])
+def test_norm_linear_is_rmsnorm_then_matvec(xq, orc, fmt, rows, cols, batch):
+    """Every CTA of the fused launch computes the RMSNorm scale in the same
+    order (whatever its warp count), so y is bit-identical to xq_rmsnorm_q8
+    followed by the mat-vec, and within tolerance of the oracle."""
+    seed = 7 * rows + cols + batch
+    W = _weights(fmt, rows, cols, seed)
+    kv = synthetic.cb4_table()
+    x = synthetic.activations(batch, cols, seed + 1, outlier_frac=0.001)
+    xq2 = Guarded((batch, cols // 256, 320), torch.uint8)
+    xq.rmsnorm_q8(dev(x), out=xq2.t)
+    y2 = run_matvec(xq, fmt, W, kv, xq2.t, rows, cols, batch)
+    out = Guarded((batch, rows), torch.float32)
+    which = xq.COUNT_NORM_LINEAR_Q4K if fmt == "q4k" else xq.COUNT_NORM_LINEAR_CB4
+    before = xq.launch_count(which)
+    if fmt == "q4k":
+        xq.norm_linear_q4k(dev(x), dev(W), rows, cols, out=out.t)
+    else:
+        xq.norm_linear_cb4(dev(x), dev(W), kv, rows, cols, out=out.t)
+    torch.cuda.synchronize()
+    out.check_guard()
+    assert xq.launch_count(which) == before + xq.last_plan()["launches"]
+    y1 = out.t.cpu().numpy()
+    assert np.array_equal(y1, y2)
+    xq_ref, _ = orc.rmsnorm_q8(x)
+    y_ref = (orc.matvec_q4k(W, xq_ref, rows, cols, batch) if fmt == "q4k"
+             else orc.matvec_cb4(W, kv, xq_ref, rows, cols, batch))
+    check_y(y1, y_ref, f"norm linear {fmt} {rows}x{cols} b{batch}")
+
+
+def test_norm_linear_with_few_and_many_warps(xq, orc):
+    """Plans of 1, 3 and 16 warps: one warp takes all eight waves of the
+    reduction, three take them round robin, sixteen leave eight idle."""
+    rows, cols = 2048, 4096
+    W = _weights("q4k", rows, cols, 91)
+    x = synthetic.activations(1, cols, 92)
+    xq_ref, _ = orc.rmsnorm_q8(x)
+    y_ref = orc.matvec_q4k(W, xq_ref, rows, cols, 1)
+    ys = []
+    try:
+        for w in (1, 3, 16):
+            xq.set_plan_override(w, 0)
+            y = xq.norm_linear_q4k(dev(x), dev(W), rows, cols)
+            torch.cuda.synchronize()
+            assert xq.last_plan()["warps"] == w
+            ys.append(y.cpu().numpy())
+    finally:
+        xq.set_plan_override(0, 0)
+    for y in ys:
+        assert np.array_equal(y, ys[0])
+    check_y(ys[0], y_ref, "norm linear warps")
+
+
 # ---------------------------------------------------------------- grouped experts
 def _slab(fmt, E, rpe, cols, seed):
     return np.concatenate([_weights(fmt, rpe, cols, seed + 17 * e) for e in range(E)])
