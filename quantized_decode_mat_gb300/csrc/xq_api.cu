@@ -42,43 +42,48 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float *__restric
 }
 
 // ---- RMSNorm + q8 pack -------------------------------------------------------------
-// One block of 256 threads per vector: warp 0 takes the scale in the fixed
-// order (rms_scale_warp), then warp w takes blocks w, w+8, ... of
-// y = x * scale with q8_quantize_lane, and writes y itself when y is
-// non-null.
+// Grid (ceil(nb/8), batch), 256 threads: block (c, b) owns q8 blocks 8c ..
+// 8c+7 of vector b, one per warp.  Each warp loads its block's values, warp
+// 0 takes the scale in the fixed order (rms_scale_warp; every CTA of the
+// vector gets the same bits), then each warp writes y = x * scale (when y
+// is non-null) and its q8 block via q8_quantize_lane.
 __global__ void __launch_bounds__(256) rmsnorm_q8_kernel(const float *__restrict__ x,
                                                          uint8_t *__restrict__ xq,
                                                          float *__restrict__ y, int64_t cols) {
     __shared__ float s_scale;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float *xv = x + (int64_t)blockIdx.x * cols;
+    const int64_t nb = cols / 256;
+    const int64_t k = (int64_t)blockIdx.x * 8 + warp;  // this warp's q8 block
+    const float *xv = x + (int64_t)blockIdx.y * cols;
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f), v = u;
+    if (k < nb) {
+        const float4 *src = reinterpret_cast<const float4 *>(xv + k * 256 + lane * 8);
+        u = __ldg(src);
+        v = __ldg(src + 1);
+    }
     if (warp == 0) {
         const float sc = rms_scale_warp(xv, cols, lane);
         if (lane == 0) s_scale = sc;
     }
     __syncthreads();
+    if (k >= nb) return;  // whole warps
     const float scale = s_scale;
-    const int64_t nb = cols / 256;
-    for (int64_t k = warp; k < nb; k += 8) {
-        const float4 *src = reinterpret_cast<const float4 *>(xv + k * 256 + lane * 8);
-        const float4 u = __ldg(src), v = __ldg(src + 1);
-        float vals[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+    float vals[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) vals[i] = __fmul_rn(vals[i], scale);
-        if (y) {
-            float4 *dy = reinterpret_cast<float4 *>(y + (int64_t)blockIdx.x * cols + k * 256 + lane * 8);
-            dy[0] = make_float4(vals[0], vals[1], vals[2], vals[3]);
-            dy[1] = make_float4(vals[4], vals[5], vals[6], vals[7]);
-        }
-        const Q8Lane r = q8_quantize_lane(vals);
-        uint8_t *out = xq + ((int64_t)blockIdx.x * nb + k) * kQ8Bytes;
-        *reinterpret_cast<uint2 *>(out + lane * 8) = make_uint2(r.w0, r.w1);
-        if ((lane & 3) == 0) *reinterpret_cast<int *>(out + kQ8SumAt + (lane >> 2) * 4) = r.sum;
-        if (lane == 0)
-            *reinterpret_cast<float *>(out + kQ8ScaleAt) = r.d;
-        else if (lane < 8)
-            *reinterpret_cast<uint32_t *>(out + kQ8ScaleAt + 4 * lane) = 0u;  // bytes 292..319
+    for (int i = 0; i < 8; ++i) vals[i] = __fmul_rn(vals[i], scale);
+    if (y) {
+        float4 *dy = reinterpret_cast<float4 *>(y + (int64_t)blockIdx.y * cols + k * 256 + lane * 8);
+        dy[0] = make_float4(vals[0], vals[1], vals[2], vals[3]);
+        dy[1] = make_float4(vals[4], vals[5], vals[6], vals[7]);
     }
+    const Q8Lane r = q8_quantize_lane(vals);
+    uint8_t *out = xq + ((int64_t)blockIdx.y * nb + k) * kQ8Bytes;
+    *reinterpret_cast<uint2 *>(out + lane * 8) = make_uint2(r.w0, r.w1);
+    if ((lane & 3) == 0) *reinterpret_cast<int *>(out + kQ8SumAt + (lane >> 2) * 4) = r.sum;
+    if (lane == 0)
+        *reinterpret_cast<float *>(out + kQ8ScaleAt) = r.d;
+    else if (lane < 8)
+        *reinterpret_cast<uint32_t *>(out + kQ8ScaleAt + 4 * lane) = 0u;  // bytes 292..319
 }
 
 namespace {
@@ -441,7 +446,8 @@ xq_status xq_rmsnorm_q8(const float *x, void *xq_out, float *y, int64_t cols, in
         return fail(XQ_EINVAL, "outputs overlap each other or x");
     DeviceState *dev = nullptr;
     if (xq_status s = device_state(&dev)) return s;
-    rmsnorm_q8_kernel<<<(unsigned)batch, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    const dim3 grid((unsigned)((cols / 256 + 7) / 8), (unsigned)batch);
+    rmsnorm_q8_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         x, static_cast<uint8_t *>(xq_out), y, cols);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "RMSNorm launch");

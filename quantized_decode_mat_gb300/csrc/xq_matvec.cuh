@@ -359,23 +359,13 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
 
     // 2. the activation (a different region of shared memory than the stages)
     if (FUSE != 0) {
-        // FUSE == 2: warp w first takes the RMSNorm scale of vectors w, w+W,
-        // ... and parks it in bytes 320..335 of the vector's first staged
-        // block (stride padding that nothing else reads or writes)
-        if (FUSE == 2) {
-            for (int b = warp; b < B; b += W) {
-                const float sc = rms_scale_warp(a.x + (int64_t)b * nb * 256, (int64_t)nb * 256, lane);
-                if (lane == 0) *reinterpret_cast<float *>(act + b * act_bstride + kActNormAt) = sc;
-            }
-            __syncthreads();
-        }
         // quantise x (FUSE == 2: y = x * scale) here: warp w takes blocks w,
         // w+W, ... (vector-major) with the standalone producers' arithmetic,
         // so the same bytes.  The values of kQuantGroup blocks are loaded
         // before any of them is processed: one L2 round trip per group.
         const int nblk = B * nb;
-        for (int k0 = warp; k0 < nblk; k0 += kQuantGroup * W) {
-            float4 u[kQuantGroup], v[kQuantGroup];
+        float4 u[kQuantGroup], v[kQuantGroup];
+        auto load_group = [&](int k0) {
 #pragma unroll
             for (int j = 0; j < kQuantGroup; ++j) {
                 const int blk = k0 + j * W;
@@ -385,6 +375,20 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
                     v[j] = __ldg(src + 1);
                 }
             }
+        };
+        load_group(warp);  // in flight while the RMSNorm scale is taken
+        // FUSE == 2: warp w takes the RMSNorm scale of vectors w, w+W, ...
+        // and parks it in bytes 320..335 of the vector's first staged block
+        // (stride padding that nothing else reads or writes)
+        if (FUSE == 2) {
+            for (int b = warp; b < B; b += W) {
+                const float sc = rms_scale_warp(a.x + (int64_t)b * nb * 256, (int64_t)nb * 256, lane);
+                if (lane == 0) *reinterpret_cast<float *>(act + b * act_bstride + kActNormAt) = sc;
+            }
+            __syncthreads();
+        }
+        for (int k0 = warp; k0 < nblk; k0 += kQuantGroup * W) {
+            if (k0 != warp) load_group(k0);
 #pragma unroll
             for (int j = 0; j < kQuantGroup; ++j) {
                 const int blk = k0 + j * W;
