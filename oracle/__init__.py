@@ -18,6 +18,8 @@ Parity status of each function (all pinned, none "parity unpinned"):
   cb4_unpack/matvec hand-worked golden blocks, half-order pin, brute force,
                    integer-GEMV special case
   f16_to_f64       all 65536 bit patterns against numpy's binary16
+  repack_cb4 /     literal hand-written resident bytes (whole and chunked),
+  dequant_cb4r     chunking invariance, same weights as the raw matrix
   rmsnorm_q8       hand-derived f32 sums that fix the summation order, the
                    guide's three-four case, a constant-vector closed form,
                    the f32 error bound against binary64
@@ -90,10 +92,17 @@ def _load(fault: int = 0) -> ctypes.CDLL:
         lib.oracle_rmsnorm_scale.restype = ctypes.c_float
         lib.oracle_rmsnorm_scale.argtypes = [P, I64]
         lib.oracle_rmsnorm_q8.argtypes = [P, P, P, I64, I64]
+        lib.oracle_cb4r_prefix.restype = I64
+        lib.oracle_cb4r_prefix.argtypes = [I64]
+        lib.oracle_cb4r_row_bytes.restype = I64
+        lib.oracle_cb4r_row_bytes.argtypes = [I64]
+        lib.oracle_repack_cb4.argtypes = [P, P, I64, I64, I64]
+        lib.oracle_dequant_cb4r.argtypes = [P, P, P, I64, I64]
         for fn in ("oracle_quantize_q8", "oracle_dequant_q8", "oracle_q4k_unpack",
                    "oracle_dequant_q4k", "oracle_subdots_q4k", "oracle_matvec_q4k",
                    "oracle_cb4_unpack", "oracle_dequant_cb4", "oracle_subdots_cb4",
-                   "oracle_matvec_cb4", "oracle_rmsnorm_q8"):
+                   "oracle_matvec_cb4", "oracle_rmsnorm_q8", "oracle_repack_cb4",
+                   "oracle_dequant_cb4r"):
             getattr(lib, fn).restype = None
         _libs[fault] = lib
         return lib
@@ -226,6 +235,33 @@ class Oracle:
         y = np.empty((batch, cols), np.float32)
         self.lib.oracle_rmsnorm_q8(_ptr(x), _ptr(xq), _ptr(y), cols, batch)
         return xq, y
+
+    # -- resident codebook rows ---------------------------------------------------
+    def cb4r_row_bytes(self, cols: int) -> int:
+        return int(self.lib.oracle_cb4r_row_bytes(cols // 32))
+
+    def cb4r_prefix(self, cols: int) -> int:
+        return int(self.lib.oracle_cb4r_prefix(cols // 32))
+
+    def repack_cb4(self, src_blocks: np.ndarray, dst: np.ndarray, block_base: int,
+                   n_blocks: int, cols: int) -> np.ndarray:
+        """Moves raw blocks block_base.. (src holds exactly n_blocks of 18
+        bytes) into the resident matrix dst (uint8, modified in place)."""
+        src = _u8(src_blocks).reshape(-1)
+        assert src.size >= 18 * n_blocks and dst.flags["C_CONTIGUOUS"] and dst.dtype == np.uint8
+        self.lib.oracle_repack_cb4(_ptr(src), _ptr(dst), block_base, n_blocks, cols)
+        return dst
+
+    def repack_cb4_whole(self, W: np.ndarray, rows: int, cols: int) -> np.ndarray:
+        dst = np.zeros(rows * self.cb4r_row_bytes(cols), np.uint8)
+        return self.repack_cb4(W, dst, 0, rows * (cols // 32), cols)
+
+    def dequant_cb4r(self, Wr, kv, rows: int, cols: int) -> np.ndarray:
+        Wr = _u8(Wr)
+        kv = np.ascontiguousarray(kv, dtype=np.int8)
+        out = np.empty((rows, cols), np.float64)
+        self.lib.oracle_dequant_cb4r(_ptr(Wr), _ptr(kv), _ptr(out), rows, cols)
+        return out
 
 
 _default: Oracle | None = None

@@ -442,3 +442,58 @@ void oracle_rmsnorm_q8(const float *x, uint8_t *xq, float *y, int64_t cols, int6
         oracle_quantize_q8(yb, xq + b * (cols / OQ8_VALUES) * OQ8_BYTES, cols, 1);
     }
 }
+
+/* ---- resident row layout of the codebook format ([G] 25.4 "one layout, and
+ * the copy that reads the lines"; [G] 25.2.1 walks it) -----------------------
+ * A resident row holds the f16 scales of its bpr blocks (block j's at byte
+ * 2j), padded to a whole dword, then the blocks' 16-byte payloads (block j's
+ * at prefix + 16j):
+ *   prefix = ((2*bpr + 3) / 4) * 4,   row_bytes = prefix + 16*bpr.
+ * The repack is chunked as on the page: a call moves blocks block_base ..
+ * block_base + n_blocks - 1 of the row-major raw matrix (src holds exactly
+ * those blocks, 18 bytes each) into the resident matrix dst.  Pad bytes
+ * (bpr odd) are left as they are. */
+int64_t oracle_cb4r_prefix(int64_t bpr) { return ((bpr * 2 + 3) / 4) * 4; }
+
+int64_t oracle_cb4r_row_bytes(int64_t bpr) { return oracle_cb4r_prefix(bpr) + 16 * bpr; }
+
+void oracle_repack_cb4(const uint8_t *src, uint8_t *dst, int64_t block_base, int64_t n_blocks,
+                       int64_t cols) {
+    int64_t bpr = cols / OCB4_WEIGHTS;
+    int64_t prefix = oracle_cb4r_prefix(bpr), row_bytes = oracle_cb4r_row_bytes(bpr);
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        int64_t gb = block_base + b;
+        int64_t row = gb / bpr, j = gb % bpr;
+        const uint8_t *blk = src + b * OCB4_BYTES;
+        uint8_t *rp = dst + row * row_bytes;
+#if ORACLE_FAULT == 13
+        rp[2 * j] = blk[1];                       /* planted: scale bytes swapped */
+        rp[2 * j + 1] = blk[0];
+#else
+        rp[2 * j] = blk[0];
+        rp[2 * j + 1] = blk[1];
+#endif
+#if ORACLE_FAULT == 12
+        memcpy(rp + 16 * j, blk + 2, 16);         /* planted: prefix not skipped  */
+#else
+        memcpy(rp + prefix + 16 * j, blk + 2, 16);
+#endif
+    }
+}
+
+/* Dequantised resident matrix, read the way [G] 25.2.1's kernel walks it. */
+void oracle_dequant_cb4r(const uint8_t *Wr, const int8_t kv[16], double *out, int64_t rows,
+                         int64_t cols) {
+    int64_t bpr = cols / OCB4_WEIGHTS;
+    int64_t prefix = oracle_cb4r_prefix(bpr), row_bytes = oracle_cb4r_row_bytes(bpr);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < bpr; ++j) {
+            const uint8_t *rp = Wr + r * row_bytes;
+            double d = oracle_f16_to_f64(rd_u16(rp + 2 * j));
+            const uint8_t *qs = rp + prefix + 16 * j;
+            for (int m = 0; m < 16; ++m) {
+                out[r * cols + 32 * j + m] = d * kv[qs[m] & 15];
+                out[r * cols + 32 * j + 16 + m] = d * kv[qs[m] >> 4];
+            }
+        }
+}

@@ -346,7 +346,56 @@ def pin_rmsnorm_bound(o):
         _q8_invariants(y, xq)
 
 
+# ---------------------------------------------------------------- resident codebook rows
+def _raw_from_rule(scale_lo) -> np.ndarray:
+    blocks = []
+    for j, lo in enumerate(scale_lo):
+        blocks.append(np.array([lo, 60] + [(16 * j + m) % 256 for m in range(16)], np.uint8))
+    return np.concatenate(blocks)
+
+
+def pin_cb4r_literal(o):
+    """Hand-written resident bytes for three small matrices, one of them
+    repacked in two chunks that cross a row boundary and one with a padded
+    prefix."""
+    for case in _golden("cb4_resident.json")["cases"]:
+        rows, cols = case["rows"], case["cols"]
+        raw = _raw_from_rule(case["scale_lo"])
+        rb = sum(len(r["prefix"]) + r["payload_count"] for r in case["expect_rows"]) // rows
+        assert o.cb4r_row_bytes(cols) == rb, (case["name"], o.cb4r_row_bytes(cols), rb)
+        dst = np.full(rows * rb, case["fill"], np.uint8)
+        for base, n in case["chunks"]:
+            o.repack_cb4(raw[18 * base:18 * (base + n)], dst, base, n, cols)
+        for r, want in enumerate(case["expect_rows"]):
+            row = dst[r * rb:(r + 1) * rb]
+            npf = len(want["prefix"])
+            assert list(row[:npf]) == want["prefix"], (case["name"], r, list(row[:npf]))
+            pay = np.arange(want["payload_from"], want["payload_from"] + want["payload_count"])
+            assert np.array_equal(row[npf:], (pay % 256).astype(np.uint8)), (case["name"], r)
+
+
+def pin_cb4r_chunks_and_weights(o):
+    """Any chunking gives the same resident bytes, and the resident matrix
+    holds the same weights as the raw one (the raw dequantisation is pinned
+    separately)."""
+    rng = np.random.Generator(np.random.PCG64(81))
+    kv = synthetic.cb4_table()
+    for rows, cols in ((3, 256), (5, 96), (4, 1024), (2, 4096)):
+        W = synthetic.cb4_weights(rows, cols, seed=rows + cols).reshape(-1)
+        whole = o.repack_cb4_whole(W, rows, cols)
+        nblk = rows * (cols // 32)
+        cuts = np.sort(rng.choice(np.arange(1, nblk), size=min(4, nblk - 1), replace=False))
+        bounds = [0, *cuts.tolist(), nblk]
+        dst = np.zeros_like(whole)
+        for a, b in zip(bounds[:-1], bounds[1:]):
+            o.repack_cb4(W[18 * a:18 * b], dst, a, b - a, cols)
+        assert np.array_equal(dst, whole), (rows, cols)
+        assert np.array_equal(o.dequant_cb4r(whole, kv, rows, cols),
+                              o.dequant_cb4(W, kv, rows, cols)), (rows, cols)
+
+
 ALL_PINS = [pin_f16_all_patterns, pin_q8_hand_cases, pin_q8_invariants, pin_q4k_scale_pack,
             pin_q4k_roundtrip, pin_q4k_block_y, pin_q4k_bruteforce, pin_q4k_gemv_special,
             pin_q4k_min_term, pin_cb4_block_y, pin_cb4_bruteforce, pin_cb4_gemv_special,
-            pin_rmsnorm_order, pin_rmsnorm_hand, pin_rmsnorm_constant, pin_rmsnorm_bound]
+            pin_rmsnorm_order, pin_rmsnorm_hand, pin_rmsnorm_constant, pin_rmsnorm_bound,
+            pin_cb4r_literal, pin_cb4r_chunks_and_weights]

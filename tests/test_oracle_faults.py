@@ -19,6 +19,8 @@ FAULTS = {
     9: "RMSNorm eps dropped",
     10: "RMSNorm wave lanes added left to right",
     11: "RMSNorm item loop reversed",
+    12: "resident payload written without the prefix offset",
+    13: "resident scale bytes swapped",
 }
 
 
