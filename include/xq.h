@@ -163,6 +163,52 @@ xq_status xq_matvec_cb4_id(const void *W, const int8_t *table, const int32_t *se
                            float *y, int64_t rows_per_expert, int64_t cols, int64_t n_experts,
                            int64_t used, int32_t x_per_slot, void *stream);
 
+/* ---- Resident codebook rows ("25 - Writing XPU Kernels" 25.4, one resident
+ * layout read by every kernel, and the 25.2.1 kernel that walks it) --------
+ * A resident row of a codebook matrix holds the f16 scales of its
+ * bpr = cols/32 blocks first (block j's at byte 2j), padded to a whole dword,
+ * then the blocks' 16-byte payloads (block j's at prefix + 16j), so every
+ * payload is a 16-byte aligned run:
+ *   prefix = ceil(2*bpr / 4) * 4 bytes,  row bytes = prefix + 16*bpr.
+ * With cols % 256 == 0 (this library's shapes) prefix = cols/16 and a row is
+ * 144*cols/256 bytes, the size of the raw row, and both are multiples of 16.
+ * The payload bytes are the raw block's bytes 2..17 unchanged.
+ *
+ * Bytes of a resident matrix: rows * (prefix + 16*bpr); 0 if invalid. */
+size_t xq_cb4r_bytes(int64_t rows, int64_t cols);
+
+/* Repack raw codebook blocks into resident rows: src (DEVICE, any alignment)
+ * holds n_blocks consecutive raw 18-byte blocks, blocks block_base ..
+ * block_base + n_blocks - 1 of the row-major raw matrix (block g is block
+ * g % bpr of row g / bpr); each is written into the resident matrix Wr
+ * (DEVICE, 16-byte aligned, xq_cb4r_bytes(rows, cols) bytes): its scale to
+ * the row's prefix, its payload to the row's payload run.  A chunk may start
+ * and end anywhere, including mid-row; bytes of Wr that the chunk does not
+ * cover are left as they are, so chunks can be repacked in any order.  One
+ * launch moves the scales and the payloads together (the page's separate
+ * scale pass re-reads every block's line for two bytes).  n_blocks == 0 is a
+ * no-op that launches nothing.  Preconditions (host-checked): cols as for
+ * the mat-vec; 0 <= block_base, block_base + n_blocks <= rows*cols/32; src
+ * and Wr do not overlap. */
+xq_status xq_repack_cb4(const void *src, void *Wr, int64_t block_base, int64_t n_blocks,
+                        int64_t rows, int64_t cols, void *stream);
+
+/* The codebook entry points on resident rows Wr (same arguments, results and
+ * preconditions as their raw-layout twins above; y is bit-identical to the
+ * twin's on the same weights, because only the staging of the bytes
+ * differs). */
+xq_status xq_matvec_cb4r(const void *Wr, const int8_t *table, const void *xq, float *y,
+                         int64_t rows, int64_t cols, int64_t batch, void *stream);
+xq_status xq_linear_cb4r(const float *x, const void *Wr, const int8_t *table, float *y,
+                         int64_t rows, int64_t cols, int64_t batch, void *stream);
+xq_status xq_norm_linear_cb4r(const float *x, const void *Wr, const int8_t *table, float *y,
+                              int64_t rows, int64_t cols, int64_t batch, void *stream);
+xq_status xq_matvec_cb4r_id(const void *Wr, const int8_t *table, const int32_t *sel,
+                            const void *xq, float *y, int64_t rows_per_expert, int64_t cols,
+                            int64_t n_experts, int64_t used, int32_t x_per_slot, void *stream);
+xq_status xq_subdots_cb4r(const void *Wr, const int8_t *table, const void *xq, int32_t *dots,
+                          int64_t rows, int64_t cols, int64_t batch, void *stream);
+
 /* Test exports: the exact per-sub-block integer dots of the same kernels.
  * dots: [batch][rows][cols/32] int32 (device).  Q4_K: dots[b][r][8k+s] is
  * dot_s of super-block k; codebook: dots[b][r][k] is dot_k of block k. */
@@ -172,10 +218,10 @@ xq_status xq_subdots_cb4(const void *W, const int8_t *table, const void *xq, int
                          int64_t rows, int64_t cols, int64_t batch, void *stream);
 
 /* Weight formats, for xq_plan_matvec. */
-enum { XQ_FORMAT_Q4K = 0, XQ_FORMAT_CB4 = 1 };
+enum { XQ_FORMAT_Q4K = 0, XQ_FORMAT_CB4 = 1, XQ_FORMAT_CB4R = 2 };
 
 /* Launch plan of the mat-vec kernels (pure host computation; needs no GPU).
- * format: XQ_FORMAT_Q4K or XQ_FORMAT_CB4.  sm_count and smem_optin_bytes
+ * format: XQ_FORMAT_Q4K, XQ_FORMAT_CB4 or XQ_FORMAT_CB4R.  sm_count and smem_optin_bytes
  * describe the device (for GB300: 152 SMs, 232448 bytes).
  * A work unit (row group) is rows_per_group rows read as `segments`
  * contiguous boxes of at most 32 chunks of 256 weights (4608 bytes); lane l
@@ -219,7 +265,13 @@ enum {
     XQ_COUNT_RMSNORM_Q8 = 9,
     XQ_COUNT_NORM_LINEAR_Q4K = 10,
     XQ_COUNT_NORM_LINEAR_CB4 = 11,
-    XQ_COUNT_N = 12
+    XQ_COUNT_REPACK_CB4 = 12,
+    XQ_COUNT_MATVEC_CB4R = 13,
+    XQ_COUNT_SUBDOTS_CB4R = 14,
+    XQ_COUNT_LINEAR_CB4R = 15,
+    XQ_COUNT_NORM_LINEAR_CB4R = 16,
+    XQ_COUNT_MATVEC_ID_CB4R = 17,
+    XQ_COUNT_N = 18
 };
 uint64_t xq_launch_count(int32_t which);
 

@@ -11,6 +11,8 @@ fallback: if the library is missing this package raises on import.
     y   = linear_q4k(x, W, rows, cols)         # fused: quantise + mat-vec, one launch
     xq  = rmsnorm_q8(x)                        # RMSNorm + q8 pack of the next input
     y   = norm_linear_q4k(x, W, rows, cols)    # fused: RMSNorm + quantise + mat-vec
+    Wr  = repack_cb4(W, rows, cols)            # codebook rows -> resident rows
+    y   = matvec_cb4r(Wr, table, xq, rows, cols)
 """
 from __future__ import annotations
 
@@ -26,11 +28,23 @@ from ._native import (  # noqa: F401
     COUNT_NORM_LINEAR_CB4,
     COUNT_NORM_LINEAR_Q4K,
     COUNT_QUANTIZE,
+    COUNT_REPACK_CB4,
+    COUNT_MATVEC_CB4R,
+    COUNT_SUBDOTS_CB4R,
+    COUNT_LINEAR_CB4R,
+    COUNT_NORM_LINEAR_CB4R,
+    COUNT_MATVEC_ID_CB4R,
     COUNT_RMSNORM_Q8,
     COUNT_SUBDOTS_CB4,
     COUNT_SUBDOTS_Q4K,
     XQError,
     cb4_bytes,
+    cb4r_bytes,
+    repack_cb4,
+    matvec_cb4r,
+    linear_cb4r,
+    norm_linear_cb4r,
+    subdots_cb4r,
     device_status,
     last_plan,
     launch_count,

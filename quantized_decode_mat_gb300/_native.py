@@ -51,6 +51,15 @@ _matvec_q4k_id = _sig("xq_matvec_q4k_id", ctypes.c_int,
                       [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P])
 _matvec_cb4_id = _sig("xq_matvec_cb4_id", ctypes.c_int,
                       [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P])
+_cb4r_bytes = _sig("xq_cb4r_bytes", _SZ, [_I64, _I64])
+_repack_cb4 = _sig("xq_repack_cb4", ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _P])
+_matvec_cb4r = _sig("xq_matvec_cb4r", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
+_linear_cb4r = _sig("xq_linear_cb4r", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
+_norm_linear_cb4r = _sig("xq_norm_linear_cb4r", ctypes.c_int,
+                         [_P, _P, _P, _P, _I64, _I64, _I64, _P])
+_matvec_cb4r_id = _sig("xq_matvec_cb4r_id", ctypes.c_int,
+                       [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P])
+_subdots_cb4r = _sig("xq_subdots_cb4r", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
 _subdots_q4k = _sig("xq_subdots_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
 _subdots_cb4 = _sig("xq_subdots_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
 _plan = _sig("xq_plan_matvec", ctypes.c_int, [_I32, _I64, _I64, _I64, _I32, _I64,
@@ -66,8 +75,10 @@ _version = _sig("xq_version", _I32, [])
 
 (COUNT_QUANTIZE, COUNT_MATVEC_Q4K, COUNT_MATVEC_CB4, COUNT_SUBDOTS_Q4K, COUNT_SUBDOTS_CB4,
  COUNT_LINEAR_Q4K, COUNT_LINEAR_CB4, COUNT_MATVEC_ID_Q4K, COUNT_MATVEC_ID_CB4,
- COUNT_RMSNORM_Q8, COUNT_NORM_LINEAR_Q4K, COUNT_NORM_LINEAR_CB4) = range(12)
-COUNT_N = 12
+ COUNT_RMSNORM_Q8, COUNT_NORM_LINEAR_Q4K, COUNT_NORM_LINEAR_CB4, COUNT_REPACK_CB4,
+ COUNT_MATVEC_CB4R, COUNT_SUBDOTS_CB4R, COUNT_LINEAR_CB4R, COUNT_NORM_LINEAR_CB4R,
+ COUNT_MATVEC_ID_CB4R) = range(18)
+COUNT_N = 18
 
 
 class XQError(RuntimeError):
@@ -246,7 +257,8 @@ def matvec_id(fmt: str, W: torch.Tensor, sel: torch.Tensor, xq: torch.Tensor,
               x_per_slot: bool = False, out: torch.Tensor | None = None,
               stream=None) -> torch.Tensor:
     """Grouped experts: y[kk] = W[expert sel[kk]] . x (x = xq vector 0, or
-    vector kk with x_per_slot) -> f32 [used, rows_per_expert]."""
+    vector kk with x_per_slot) -> f32 [used, rows_per_expert].  fmt: "q4k",
+    "cb4" (raw codebook rows) or "cb4r" (resident codebook rows)."""
     used = int(sel.numel())
     if out is None:
         out = torch.empty((used, rows_per_expert), dtype=torch.float32, device=xq.device)
@@ -256,10 +268,12 @@ def matvec_id(fmt: str, W: torch.Tensor, sel: torch.Tensor, xq: torch.Tensor,
                               _dev(out, "y", torch.float32), rows_per_expert, cols, n_experts,
                               used, int(x_per_slot), _stream(stream)))
     else:
-        _check(_matvec_cb4_id(_dev(W, "W", torch.uint8), ctypes.cast(_table(table), _P), s,
-                              _dev(xq, "xq", torch.uint8), _dev(out, "y", torch.float32),
-                              rows_per_expert, cols, n_experts, used, int(x_per_slot),
-                              _stream(stream)))
+        fn = _matvec_cb4_id if fmt == "cb4" else _matvec_cb4r_id
+        if fmt not in ("cb4", "cb4r"):
+            raise ValueError(f"unknown format {fmt!r}")
+        _check(fn(_dev(W, "W", torch.uint8), ctypes.cast(_table(table), _P), s,
+                  _dev(xq, "xq", torch.uint8), _dev(out, "y", torch.float32),
+                  rows_per_expert, cols, n_experts, used, int(x_per_slot), _stream(stream)))
     return out
 
 
@@ -285,11 +299,78 @@ def subdots_cb4(W: torch.Tensor, table, xq: torch.Tensor, rows: int, cols: int,
     return out
 
 
+# ---------------------------------------------------------------- resident codebook rows
+def cb4r_bytes(rows: int, cols: int) -> int:
+    return int(_cb4r_bytes(rows, cols))
+
+
+def repack_cb4(src: torch.Tensor, rows: int, cols: int, out: torch.Tensor | None = None,
+               block_base: int = 0, n_blocks: int | None = None, src_offset: int = 0,
+               stream=None) -> torch.Tensor:
+    """Repack raw codebook blocks (uint8, CUDA; the n_blocks blocks starting at
+    byte src_offset of src, which are blocks block_base.. of the matrix) into
+    the resident rows ``out`` (uint8 [cb4r_bytes(rows, cols)], CUDA)."""
+    if n_blocks is None:
+        n_blocks = rows * (cols // 32) - block_base
+    if out is None:
+        out = torch.zeros(cb4r_bytes(rows, cols), dtype=torch.uint8, device=src.device)
+    base = _dev(src, "src", torch.uint8)
+    if src_offset < 0 or src_offset + 18 * n_blocks > src.numel():
+        raise ValueError("src is too small for the chunk")
+    _check(_repack_cb4(base + src_offset, _dev(out, "Wr", torch.uint8), block_base, n_blocks,
+                       rows, cols, _stream(stream)))
+    return out
+
+
+def matvec_cb4r(Wr: torch.Tensor, table, xq: torch.Tensor, rows: int, cols: int,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[b, r] for resident codebook rows Wr with a host 16-entry int8 table."""
+    batch = _batch_of(xq, cols)
+    if out is None:
+        out = torch.empty((batch, rows), dtype=torch.float32, device=xq.device)
+    _check(_matvec_cb4r(_dev(Wr, "Wr", torch.uint8), ctypes.cast(_table(table), _P),
+                        _dev(xq, "xq", torch.uint8), _dev(out, "y", torch.float32), rows, cols,
+                        batch, _stream(stream)))
+    return out
+
+
+def linear_cb4r(x: torch.Tensor, Wr: torch.Tensor, table, rows: int, cols: int,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Fused decode step (quantise + mat-vec, one launch) on resident codebook rows."""
+    x = _x2d(x)
+    batch = x.shape[0]
+    if x.shape[1] != cols:
+        raise ValueError("x has the wrong number of columns")
+    if out is None:
+        out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    _check(_linear_cb4r(_dev(x, "x", torch.float32), _dev(Wr, "Wr", torch.uint8),
+                        ctypes.cast(_table(table), _P), _dev(out, "y", torch.float32), rows,
+                        cols, batch, _stream(stream)))
+    return out
+
+
+def norm_linear_cb4r(x: torch.Tensor, Wr: torch.Tensor, table, rows: int, cols: int,
+                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """RMSNorm, quantise and multiply by resident codebook rows in one launch."""
+    return _norm_linear(_norm_linear_cb4r, x, Wr, table, rows, cols, out, stream)
+
+
+def subdots_cb4r(Wr: torch.Tensor, table, xq: torch.Tensor, rows: int, cols: int,
+                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    batch = _batch_of(xq, cols)
+    if out is None:
+        out = torch.empty((batch, rows, cols // 32), dtype=torch.int32, device=xq.device)
+    _check(_subdots_cb4r(_dev(Wr, "Wr", torch.uint8), ctypes.cast(_table(table), _P),
+                         _dev(xq, "xq", torch.uint8), _dev(out, "dots", torch.int32), rows,
+                         cols, batch, _stream(stream)))
+    return out
+
+
 def _plan_dict(p: _Plan) -> dict:
     return {f: getattr(p, f) for f, _ in _Plan._fields_}
 
 
-FORMATS = {"q4k": 0, "cb4": 1}
+FORMATS = {"q4k": 0, "cb4": 1, "cb4r": 2}
 
 
 def plan_matvec(rows: int, cols: int, batch: int = 1, fmt: str = "q4k", sm_count: int = 152,

@@ -86,6 +86,50 @@ __global__ void __launch_bounds__(256) rmsnorm_q8_kernel(const float *__restrict
         *reinterpret_cast<uint32_t *>(out + kQ8ScaleAt + 4 * lane) = 0u;  // bytes 292..319
 }
 
+// ---- resident repack of codebook blocks ---------------------------------------------
+// CTA t (256 threads) takes blocks 256t .. 256t+255 of the chunk.  The tile's
+// raw bytes are read with coalesced loads into shared memory (16-byte loads
+// when the source is 16-byte aligned, byte loads otherwise); then thread i
+// writes block i's f16 scale into its row's prefix and its 16 payload bytes
+// as one 16-byte store into the row's payload run, so consecutive threads
+// store consecutive bytes of a row.  The scale and payload of a block move in
+// the same pass ("25 - Writing XPU Kernels" 25.4: a separate pass over the
+// scales pulls a line per block for two useful bytes).
+__global__ void __launch_bounds__(256) repack_cb4_kernel(const uint8_t *__restrict__ src,
+                                                         uint8_t *__restrict__ Wr,
+                                                         int64_t block_base, int64_t n_blocks,
+                                                         int64_t bpr, int64_t prefix,
+                                                         int64_t row_bytes, int src_vec16) {
+    __shared__ __align__(16) uint8_t tile[256 * kCb4Bytes];
+    const int64_t b0 = (int64_t)blockIdx.x * 256;
+    const int64_t left = n_blocks - b0;
+    const int nblk = left < 256 ? (int)left : 256;
+    const int nbytes = nblk * kCb4Bytes;
+    const uint8_t *s = src + b0 * kCb4Bytes;
+    int done = 0;
+    if (src_vec16) {  // s is 16-byte aligned: 4608 * blockIdx.x is a multiple of 16
+        const int n16 = nbytes >> 4;
+        for (int i = threadIdx.x; i < n16; i += 256)
+            reinterpret_cast<uint4 *>(tile)[i] = __ldg(reinterpret_cast<const uint4 *>(s) + i);
+        done = n16 << 4;
+    }
+    for (int i = done + threadIdx.x; i < nbytes; i += 256) tile[i] = __ldg(s + i);
+    __syncthreads();
+    const int t = threadIdx.x;
+    if (t >= nblk) return;
+    const int64_t g = block_base + b0 + t;
+    const int64_t row = g / bpr, j = g - row * bpr;
+    uint8_t *rp = Wr + row * row_bytes;
+    const uint16_t *h = reinterpret_cast<const uint16_t *>(tile + t * kCb4Bytes);  // even offset
+    reinterpret_cast<uint16_t *>(rp)[j] = h[0];
+    uint4 p;
+    p.x = (uint32_t)h[1] | ((uint32_t)h[2] << 16);
+    p.y = (uint32_t)h[3] | ((uint32_t)h[4] << 16);
+    p.z = (uint32_t)h[5] | ((uint32_t)h[6] << 16);
+    p.w = (uint32_t)h[7] | ((uint32_t)h[8] << 16);
+    *reinterpret_cast<uint4 *>(rp + prefix + 16 * j) = p;
+}
+
 namespace {
 
 thread_local std::string t_error;
@@ -165,6 +209,8 @@ xq_status device_state(DeviceState **out) {
         st.status = static_cast<uint32_t *>(p);
         if (st.err == cudaSuccess) step(configure_matvec_q4k(st.smem_optin), "configure Q4_K kernels");
         if (st.err == cudaSuccess) step(configure_matvec_cb4(st.smem_optin), "configure codebook kernels");
+        if (st.err == cudaSuccess)
+            step(configure_matvec_cb4r(st.smem_optin), "configure resident codebook kernels");
     });
     if (st.err != cudaSuccess) return cuda_fail(st.err, st.what);
     *out = &st;
@@ -237,25 +283,36 @@ xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
     return XQ_OK;
 }
 
-enum class Op {
-    kMatvecQ4K,
-    kMatvecCB4,
-    kDotsQ4K,
-    kDotsCB4,
-    kLinearQ4K,
-    kLinearCB4,
-    kNormLinearQ4K,
-    kNormLinearCB4
+enum class Kind { kMatvec, kDots, kLinear, kNormLinear };
+
+struct OpInfo {
+    int fmt;    // kQ4K, kCB4 or kCB4R
+    Kind kind;
+    int count;  // launch counter
 };
 
+cudaError_t launch_fmt(int fmt, const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t s) {
+    return fmt == kQ4K   ? launch_matvec_q4k(a, batch, kind, grid, block, smem, s)
+           : fmt == kCB4 ? launch_matvec_cb4(a, batch, kind, grid, block, smem, s)
+                         : launch_matvec_cb4r(a, batch, kind, grid, block, smem, s);
+}
+
+void pack_table(const int8_t *table, uint32_t (&kv)[4]) {
+    for (int i = 0; i < 4; ++i) {
+        uint32_t w = 0;
+        for (int j = 0; j < 4; ++j) w |= (uint32_t)(uint8_t)table[4 * i + j] << (8 * j);
+        kv[i] = w;
+    }
+}
+
 // in: q8 blocks (mat-vec and sub-dots) or f32 x (the fused linear ops).
-xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *in, void *out,
+xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *in, void *out,
                      int64_t rows, int64_t cols, int64_t batch, void *stream) {
-    const bool cb4 = (op == Op::kMatvecCB4 || op == Op::kDotsCB4 || op == Op::kLinearCB4 ||
-                      op == Op::kNormLinearCB4);
-    const bool dots = (op == Op::kDotsQ4K || op == Op::kDotsCB4);
-    const bool norm = (op == Op::kNormLinearQ4K || op == Op::kNormLinearCB4);
-    const bool fused = norm || op == Op::kLinearQ4K || op == Op::kLinearCB4;
+    const bool cb4 = op.fmt != kQ4K;
+    const bool dots = op.kind == Kind::kDots;
+    const bool norm = op.kind == Kind::kNormLinear;
+    const bool fused = norm || op.kind == Kind::kLinear;
     t_error.clear();
     if (!W || !in || !out)
         return fail(XQ_EINVAL, fused ? "null device pointer (x, W or y)"
@@ -288,24 +345,10 @@ xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *in, 
     a.rows_per_group = plan.rows_per_group;
     a.segments = plan.segments;
     a.stages = plan.stages;
-    if (cb4) {
-        for (int i = 0; i < 4; ++i) {
-            uint32_t w = 0;
-            for (int j = 0; j < 4; ++j) w |= (uint32_t)(uint8_t)table[4 * i + j] << (8 * j);
-            a.kv[i] = w;
-        }
-    }
+    if (cb4) pack_table(table, a.kv);
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int kind = dots ? 1 : norm ? 4 : fused ? 2 : 0;
-    const int which = op == Op::kMatvecQ4K      ? XQ_COUNT_MATVEC_Q4K
-                      : op == Op::kMatvecCB4     ? XQ_COUNT_MATVEC_CB4
-                      : op == Op::kDotsQ4K       ? XQ_COUNT_SUBDOTS_Q4K
-                      : op == Op::kDotsCB4       ? XQ_COUNT_SUBDOTS_CB4
-                      : op == Op::kLinearQ4K     ? XQ_COUNT_LINEAR_Q4K
-                      : op == Op::kLinearCB4     ? XQ_COUNT_LINEAR_CB4
-                      : op == Op::kNormLinearQ4K ? XQ_COUNT_NORM_LINEAR_Q4K
-                                                 : XQ_COUNT_NORM_LINEAR_CB4;
     for (int64_t b0 = 0; b0 < batch; b0 += plan.batch_per_launch) {
         const int64_t bc = batch - b0 < plan.batch_per_launch ? batch - b0 : plan.batch_per_launch;
         if (fused)
@@ -314,21 +357,20 @@ xq_status run_matvec(Op op, const void *W, const int8_t *table, const void *in, 
             a.xq = static_cast<const uint8_t *>(in) + b0 * nb * kQ8Bytes;
         a.y = dots ? nullptr : static_cast<float *>(out) + b0 * rows;
         a.dots = dots ? static_cast<int32_t *>(out) + b0 * rows * nb * 8 : nullptr;
-        cudaError_t e = cb4 ? launch_matvec_cb4(a, (int)bc, kind, grid, block,
-                                                (size_t)plan.smem_bytes, s)
-                            : launch_matvec_q4k(a, (int)bc, kind, grid, block,
-                                                (size_t)plan.smem_bytes, s);
+        cudaError_t e = launch_fmt(op.fmt, a, (int)bc, kind, grid, block,
+                                   (size_t)plan.smem_bytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "mat-vec launch");
-        g_counts[which].fetch_add(1, std::memory_order_relaxed);
+        g_counts[op.count].fetch_add(1, std::memory_order_relaxed);
     }
     t_last_plan = plan;
     t_have_plan = true;
     return XQ_OK;
 }
 
-xq_status run_matvec_id(bool cb4, const void *W, const int8_t *table, const int32_t *sel,
+xq_status run_matvec_id(int fmt, const void *W, const int8_t *table, const int32_t *sel,
                         const void *xq_in, float *y, int64_t rpe, int64_t cols,
                         int64_t n_experts, int64_t used, int32_t x_per_slot, void *stream) {
+    const bool cb4 = fmt != kQ4K;
     t_error.clear();
     if (!W || !sel || !xq_in || !y) return fail(XQ_EINVAL, "null device pointer (W, sel, xq or y)");
     if (cb4 && !table) return fail(XQ_EINVAL, "null codebook table");
@@ -370,20 +412,15 @@ xq_status run_matvec_id(bool cb4, const void *W, const int8_t *table, const int3
     a.groups_per_slot = (int32_t)(plan.groups / used);
     a.act_vectors = (int32_t)nvec;
     a.status = dev->status;
-    if (cb4) {
-        for (int i = 0; i < 4; ++i) {
-            uint32_t w = 0;
-            for (int j = 0; j < 4; ++j) w |= (uint32_t)(uint8_t)table[4 * i + j] << (8 * j);
-            a.kv[i] = w;
-        }
-    }
+    if (cb4) pack_table(table, a.kv);
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cb4 ? launch_matvec_cb4(a, 1, 3, grid, block, (size_t)plan.smem_bytes, s)
-                        : launch_matvec_q4k(a, 1, 3, grid, block, (size_t)plan.smem_bytes, s);
+    cudaError_t e = launch_fmt(fmt, a, 1, 3, grid, block, (size_t)plan.smem_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "grouped mat-vec launch");
-    g_counts[cb4 ? XQ_COUNT_MATVEC_ID_CB4 : XQ_COUNT_MATVEC_ID_Q4K].fetch_add(
-        1, std::memory_order_relaxed);
+    const int which = fmt == kQ4K   ? XQ_COUNT_MATVEC_ID_Q4K
+                      : fmt == kCB4 ? XQ_COUNT_MATVEC_ID_CB4
+                                    : XQ_COUNT_MATVEC_ID_CB4R;
+    g_counts[which].fetch_add(1, std::memory_order_relaxed);
     t_last_plan = plan;
     t_have_plan = true;
     return XQ_OK;
@@ -457,64 +494,126 @@ xq_status xq_rmsnorm_q8(const float *x, void *xq_out, float *y, int64_t cols, in
 
 xq_status xq_matvec_q4k(const void *W, const void *xq_in, float *y, int64_t rows, int64_t cols,
                         int64_t batch, void *stream) {
-    return run_matvec(Op::kMatvecQ4K, W, nullptr, xq_in, y, rows, cols, batch, stream);
+    return run_matvec({kQ4K, Kind::kMatvec, XQ_COUNT_MATVEC_Q4K}, W, nullptr, xq_in, y, rows, cols, batch, stream);
 }
 
 xq_status xq_matvec_cb4(const void *W, const int8_t *table, const void *xq_in, float *y,
                         int64_t rows, int64_t cols, int64_t batch, void *stream) {
-    return run_matvec(Op::kMatvecCB4, W, table, xq_in, y, rows, cols, batch, stream);
+    return run_matvec({kCB4, Kind::kMatvec, XQ_COUNT_MATVEC_CB4}, W, table, xq_in, y, rows, cols, batch, stream);
 }
 
 xq_status xq_linear_q4k(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
                         int64_t batch, void *stream) {
-    return run_matvec(Op::kLinearQ4K, W, nullptr, x, y, rows, cols, batch, stream);
+    return run_matvec({kQ4K, Kind::kLinear, XQ_COUNT_LINEAR_Q4K}, W, nullptr, x, y, rows, cols, batch, stream);
 }
 
 xq_status xq_linear_cb4(const float *x, const void *W, const int8_t *table, float *y,
                         int64_t rows, int64_t cols, int64_t batch, void *stream) {
-    return run_matvec(Op::kLinearCB4, W, table, x, y, rows, cols, batch, stream);
+    return run_matvec({kCB4, Kind::kLinear, XQ_COUNT_LINEAR_CB4}, W, table, x, y, rows, cols, batch, stream);
 }
 
 xq_status xq_norm_linear_q4k(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
                              int64_t batch, void *stream) {
-    return run_matvec(Op::kNormLinearQ4K, W, nullptr, x, y, rows, cols, batch, stream);
+    return run_matvec({kQ4K, Kind::kNormLinear, XQ_COUNT_NORM_LINEAR_Q4K}, W, nullptr, x, y, rows, cols, batch, stream);
 }
 
 xq_status xq_norm_linear_cb4(const float *x, const void *W, const int8_t *table, float *y,
                              int64_t rows, int64_t cols, int64_t batch, void *stream) {
-    return run_matvec(Op::kNormLinearCB4, W, table, x, y, rows, cols, batch, stream);
+    return run_matvec({kCB4, Kind::kNormLinear, XQ_COUNT_NORM_LINEAR_CB4}, W, table, x, y, rows, cols, batch, stream);
 }
 
 xq_status xq_matvec_q4k_id(const void *W, const int32_t *sel, const void *xq_in, float *y,
                            int64_t rows_per_expert, int64_t cols, int64_t n_experts, int64_t used,
                            int32_t x_per_slot, void *stream) {
-    return run_matvec_id(false, W, nullptr, sel, xq_in, y, rows_per_expert, cols, n_experts, used,
+    return run_matvec_id(kQ4K, W, nullptr, sel, xq_in, y, rows_per_expert, cols, n_experts, used,
                          x_per_slot, stream);
 }
 
 xq_status xq_matvec_cb4_id(const void *W, const int8_t *table, const int32_t *sel,
                            const void *xq_in, float *y, int64_t rows_per_expert, int64_t cols,
                            int64_t n_experts, int64_t used, int32_t x_per_slot, void *stream) {
-    return run_matvec_id(true, W, table, sel, xq_in, y, rows_per_expert, cols, n_experts, used,
+    return run_matvec_id(kCB4, W, table, sel, xq_in, y, rows_per_expert, cols, n_experts, used,
                          x_per_slot, stream);
 }
 
 xq_status xq_subdots_q4k(const void *W, const void *xq_in, int32_t *dots, int64_t rows,
                          int64_t cols, int64_t batch, void *stream) {
-    return run_matvec(Op::kDotsQ4K, W, nullptr, xq_in, dots, rows, cols, batch, stream);
+    return run_matvec({kQ4K, Kind::kDots, XQ_COUNT_SUBDOTS_Q4K}, W, nullptr, xq_in, dots, rows, cols, batch, stream);
 }
 
 xq_status xq_subdots_cb4(const void *W, const int8_t *table, const void *xq_in, int32_t *dots,
                          int64_t rows, int64_t cols, int64_t batch, void *stream) {
-    return run_matvec(Op::kDotsCB4, W, table, xq_in, dots, rows, cols, batch, stream);
+    return run_matvec({kCB4, Kind::kDots, XQ_COUNT_SUBDOTS_CB4}, W, table, xq_in, dots, rows, cols, batch, stream);
+}
+
+size_t xq_cb4r_bytes(int64_t rows, int64_t cols) { return xq_cb4_bytes(rows, cols); }
+
+xq_status xq_repack_cb4(const void *src, void *Wr, int64_t block_base, int64_t n_blocks,
+                        int64_t rows, int64_t cols, void *stream) {
+    t_error.clear();
+    if (!src || !Wr) return fail(XQ_EINVAL, "null device pointer (src or Wr)");
+    if (xq_status s = check_shape(rows, cols, 1, true)) return s;
+    if (!aligned(Wr, 16)) return fail(XQ_EALIGN, "Wr must be 16-byte aligned");
+    const int64_t bpr = cols / 32;
+    if (block_base < 0 || n_blocks < 0 || block_base > rows * bpr ||
+        n_blocks > rows * bpr - block_base)
+        return fail(XQ_ESHAPE, "blocks %lld..%lld+%lld outside the matrix's %lld blocks",
+                    (long long)block_base, (long long)block_base, (long long)n_blocks,
+                    (long long)(rows * bpr));
+    if ((n_blocks + 255) / 256 > 0x7FFFFFFFLL) return fail(XQ_ESHAPE, "chunk too large");
+    const int64_t prefix = ((2 * bpr + 3) / 4) * 4, row_bytes = prefix + 16 * bpr;
+    if (overlap(src, (size_t)n_blocks * kCb4Bytes, Wr, (size_t)(rows * row_bytes)))
+        return fail(XQ_EINVAL, "src overlaps Wr");
+    if (n_blocks == 0) return XQ_OK;
+    DeviceState *dev = nullptr;
+    if (xq_status s = device_state(&dev)) return s;
+    const unsigned grid = (unsigned)((n_blocks + 255) / 256);
+    repack_cb4_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(src), static_cast<uint8_t *>(Wr), block_base, n_blocks, bpr,
+        prefix, row_bytes, aligned(src, 16) ? 1 : 0);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "repack launch");
+    g_counts[XQ_COUNT_REPACK_CB4].fetch_add(1, std::memory_order_relaxed);
+    return XQ_OK;
+}
+
+xq_status xq_matvec_cb4r(const void *Wr, const int8_t *table, const void *xq_in, float *y,
+                         int64_t rows, int64_t cols, int64_t batch, void *stream) {
+    return run_matvec({kCB4R, Kind::kMatvec, XQ_COUNT_MATVEC_CB4R}, Wr, table, xq_in, y, rows,
+                      cols, batch, stream);
+}
+
+xq_status xq_linear_cb4r(const float *x, const void *Wr, const int8_t *table, float *y,
+                         int64_t rows, int64_t cols, int64_t batch, void *stream) {
+    return run_matvec({kCB4R, Kind::kLinear, XQ_COUNT_LINEAR_CB4R}, Wr, table, x, y, rows, cols,
+                      batch, stream);
+}
+
+xq_status xq_norm_linear_cb4r(const float *x, const void *Wr, const int8_t *table, float *y,
+                              int64_t rows, int64_t cols, int64_t batch, void *stream) {
+    return run_matvec({kCB4R, Kind::kNormLinear, XQ_COUNT_NORM_LINEAR_CB4R}, Wr, table, x, y,
+                      rows, cols, batch, stream);
+}
+
+xq_status xq_matvec_cb4r_id(const void *Wr, const int8_t *table, const int32_t *sel,
+                            const void *xq_in, float *y, int64_t rows_per_expert, int64_t cols,
+                            int64_t n_experts, int64_t used, int32_t x_per_slot, void *stream) {
+    return run_matvec_id(kCB4R, Wr, table, sel, xq_in, y, rows_per_expert, cols, n_experts, used,
+                         x_per_slot, stream);
+}
+
+xq_status xq_subdots_cb4r(const void *Wr, const int8_t *table, const void *xq_in, int32_t *dots,
+                          int64_t rows, int64_t cols, int64_t batch, void *stream) {
+    return run_matvec({kCB4R, Kind::kDots, XQ_COUNT_SUBDOTS_CB4R}, Wr, table, xq_in, dots, rows,
+                      cols, batch, stream);
 }
 
 xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t batch,
                          int32_t sm_count, int64_t smem_optin_bytes, xq_plan *plan) {
     t_error.clear();
     if (!plan) return fail(XQ_EINVAL, "null plan");
-    if (format != XQ_FORMAT_Q4K && format != XQ_FORMAT_CB4)
-        return fail(XQ_EINVAL, "format must be XQ_FORMAT_Q4K or XQ_FORMAT_CB4");
+    if (format != XQ_FORMAT_Q4K && format != XQ_FORMAT_CB4 && format != XQ_FORMAT_CB4R)
+        return fail(XQ_EINVAL, "format must be XQ_FORMAT_Q4K, XQ_FORMAT_CB4 or XQ_FORMAT_CB4R");
     if (xq_status s = check_shape(rows, cols, batch, true)) return s;
     if (sm_count < 1) return fail(XQ_EINVAL, "sm_count must be positive");
     return make_plan(rows, cols, batch, sm_count, smem_optin_bytes, plan);

@@ -34,7 +34,10 @@ constexpr int kQuantGroup = 4;
 constexpr int kMaxWarps = 8;
 constexpr int kMaxStages = 8;
 
-enum Format { kQ4K = 0, kCB4 = 1 };
+// kCB4R: codebook blocks in resident rows (scale prefix, then 16-byte
+// payloads).  A 256-weight chunk is then 16 bytes of scales in the prefix and
+// 128 bytes of payloads, 144 bytes in all, as in the raw layout.
+enum Format { kQ4K = 0, kCB4 = 1, kCB4R = 2 };
 
 // Largest warps per CTA of an instantiation, which its register budget
 // allows no more: 16 at batch 1 (at most 128 registers a thread), 8 above.
@@ -67,7 +70,8 @@ constexpr uint32_t kStatusBadExpertId = 2u;
 
 // Launch entry points implemented per format (xq_matvec_q4k.cu / _cb4.cu).
 // kind: 0 = mat-vec on q8 blocks, 1 = the same with the exact dots,
-// 2 = fused quantise + mat-vec on f32 x, 3 = grouped experts.
+// 2 = fused quantise + mat-vec on f32 x, 3 = grouped experts, 4 = fused
+// RMSNorm + quantise + mat-vec.
 cudaError_t launch_matvec_q4k(const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,
                               size_t smem, cudaStream_t s);
 cudaError_t launch_matvec_cb4(const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,
@@ -75,5 +79,8 @@ cudaError_t launch_matvec_cb4(const MatvecArgs &a, int batch, int kind, dim3 gri
 // Raise the dynamic shared memory limit of every instantiation of a format.
 cudaError_t configure_matvec_q4k(int smem_optin);
 cudaError_t configure_matvec_cb4(int smem_optin);
+cudaError_t launch_matvec_cb4r(const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,
+                               size_t smem, cudaStream_t s);
+cudaError_t configure_matvec_cb4r(int smem_optin);
 
 }  // namespace xq

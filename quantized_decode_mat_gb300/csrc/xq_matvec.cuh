@@ -164,36 +164,17 @@ __device__ __forceinline__ void cb4_decode(uint32_t q, const uint32_t (&T)[4], u
     HI = __byte_perm(f0, f1, 0x7531u);  // kv[H0], kv[H1], kv[H2], kv[H3]
 }
 
+// Eight codebook blocks of one chunk: scales dk[k] and payload words P[k][0..3]
+// (block k's 16 payload bytes, little-endian), against q8 block `act`.
 template <int B, bool DOTS, class Act>
-__device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const Act &act,
-                                          const uint32_t (&T)[4], float (&hi)[B], float (&lo)[B],
-                                          int32_t *dots, int64_t dots_bstride) {
-    uint32_t v[36];
-#pragma unroll
-    for (int i = 0; i < 9; ++i) {
-        const uint4 t = *reinterpret_cast<const uint4 *>(w + 16 * i);
-        v[4 * i + 0] = t.x;
-        v[4 * i + 1] = t.y;
-        v[4 * i + 2] = t.z;
-        v[4 * i + 3] = t.w;
-    }
-    // Block pair p (blocks 2p, 2p+1) is the 36 bytes at 36p: words 9p..9p+8.
-    // Block 2p: scale = low half of word 9p, payload = bytes 2..17 of the pair
-    // (realigned by 16-bit funnel shifts); block 2p+1: scale = high half of
-    // word 9p+4, payload = words 9p+5..9p+8.
-    float dk[8];
+__device__ __forceinline__ void cb4_blocks(const float (&dk)[8], const uint32_t (&P)[8][4],
+                                           const Act &act, const uint32_t (&T)[4], float (&hi)[B],
+                                           float (&lo)[B], int32_t *dots, int64_t dots_bstride) {
     uint32_t LO[8][4], HI[8][4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        dk[2 * p] = f16_bits_to_f32(v[9 * p]);
-        dk[2 * p + 1] = f16_bits_to_f32(v[9 * p + 4] >> 16);
+    for (int k = 0; k < 8; ++k)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t qa = __funnelshift_r(v[9 * p + i], v[9 * p + i + 1], 16);
-            cb4_decode(qa, T, LO[2 * p][i], HI[2 * p][i]);
-            cb4_decode(v[9 * p + 5 + i], T, LO[2 * p + 1][i], HI[2 * p + 1][i]);
-        }
-    }
+        for (int i = 0; i < 4; ++i) cb4_decode(P[k][i], T, LO[k][i], HI[k][i]);
 #pragma unroll
     for (int b = 0; b < B; ++b) {
         float ch = 0.0f, cl = 0.0f;  // sum_k d_k * dot_k, compensated
@@ -226,6 +207,70 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const A
             o[1] = make_int4(dts[4], dts[5], dts[6], dts[7]);
         }
     }
+}
+
+// Raw layout: w is this lane's 144-byte chunk (eight 18-byte blocks) in
+// shared memory.
+template <int B, bool DOTS, class Act>
+__device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const Act &act,
+                                          const uint32_t (&T)[4], float (&hi)[B], float (&lo)[B],
+                                          int32_t *dots, int64_t dots_bstride) {
+    uint32_t v[36];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        const uint4 t = *reinterpret_cast<const uint4 *>(w + 16 * i);
+        v[4 * i + 0] = t.x;
+        v[4 * i + 1] = t.y;
+        v[4 * i + 2] = t.z;
+        v[4 * i + 3] = t.w;
+    }
+    // Block pair p (blocks 2p, 2p+1) is the 36 bytes at 36p: words 9p..9p+8.
+    // Block 2p: scale = low half of word 9p, payload = bytes 2..17 of the pair
+    // (realigned by 16-bit funnel shifts); block 2p+1: scale = high half of
+    // word 9p+4, payload = words 9p+5..9p+8.
+    float dk[8];
+    uint32_t P[8][4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        dk[2 * p] = f16_bits_to_f32(v[9 * p]);
+        dk[2 * p + 1] = f16_bits_to_f32(v[9 * p + 4] >> 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            P[2 * p][i] = __funnelshift_r(v[9 * p + i], v[9 * p + i + 1], 16);
+            P[2 * p + 1][i] = v[9 * p + 5 + i];
+        }
+    }
+    cb4_blocks<B, DOTS>(dk, P, act, T, hi, lo, dots, dots_bstride);
+}
+
+// ---- resident codebook rows: the staged slot map ------------------------------------
+// A box of resident rows is staged so that slot l (the chunk lane l takes)
+// has its 16 scale bytes at 16l and its eight 16-byte payloads at
+// 512 + 128l, payload i rotated to piece (i + l) & 7: eight lanes reading
+// their payload i then touch eight distinct 4-bank groups.
+__device__ __forceinline__ uint32_t cb4r_scale_slot(int slot) { return 16u * (uint32_t)slot; }
+__device__ __forceinline__ uint32_t cb4r_payload_slot(int slot, int i) {
+    return 512u + 128u * (uint32_t)slot + 16u * (uint32_t)((i + slot) & 7);
+}
+
+template <int B, bool DOTS, class Act>
+__device__ __forceinline__ void cb4r_chunk(const uint8_t *__restrict__ st, int slot,
+                                           const Act &act, const uint32_t (&T)[4], float (&hi)[B],
+                                           float (&lo)[B], int32_t *dots, int64_t dots_bstride) {
+    const uint4 sc = *reinterpret_cast<const uint4 *>(st + cb4r_scale_slot(slot));
+    const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
+    float dk[8];
+    uint32_t P[8][4];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        dk[k] = f16_bits_to_f32(sw[k >> 1] >> (16 * (k & 1)));
+        const uint4 t = *reinterpret_cast<const uint4 *>(st + cb4r_payload_slot(slot, k));
+        P[k][0] = t.x;
+        P[k][1] = t.y;
+        P[k][2] = t.z;
+        P[k][3] = t.w;
+    }
+    cb4_blocks<B, DOTS>(dk, P, act, T, hi, lo, dots, dots_bstride);
 }
 
 // ---- work-unit descriptor ---------------------------------------------------------------
@@ -321,28 +366,73 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
 
     int64_t pg = gw;  // producer cursor: group, segment, stage
     int ps = 0, p_stage = 0, issued = 0;
+    // Resident rows: where each of this lane's nine 16-byte copies of a box
+    // lands in the stage (the same for every box of the launch).  With whole
+    // rows in the box (R > 1), copy k moves piece q = lane + 32k of the
+    // contiguous box; with row segments (R == 1), copy 0 moves the scales of
+    // chunk c0 + lane and copy k >= 1 payload piece 32(k-1) + lane of the
+    // segment's 32 chunks.
+    uint32_t dmap[9];
+    if (FMT == kCB4R) {
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+            if (R > 1) {
+                const int q = lane + 32 * k, rp = 9 * nb;  // pieces per resident row
+                const int rig = q / rp, r = q - rig * rp;
+                dmap[k] = r < nb ? cb4r_scale_slot(rig * nb + r)
+                                 : cb4r_payload_slot(rig * nb + ((r - nb) >> 3), (r - nb) & 7);
+            } else {
+                const int pp = 32 * (k - 1) + lane;
+                dmap[k] = k == 0 ? cb4r_scale_slot(lane) : cb4r_payload_slot(pp >> 3, pp & 7);
+            }
+        }
+    }
     auto issue_next = [&]() {
         const GroupInfo gi = group_info<ID>(a, pg, R);
-        const uint8_t *src0;
-        int valid;  // bytes of the box that exist in W
-        if (R > 1) {
-            src0 = a.W + gi.row0 * row_bytes;
-            valid = gi.valid * (int)row_bytes;
-        } else {
-            const int c0 = ps * 32;
-            src0 = a.W + gi.row0 * row_bytes + c0 * kChunkBytes;
-            valid = (nb - c0 < 32 ? nb - c0 : 32) * kChunkBytes;
-        }
-        if (gi.bad) valid = 0;  // an invalid expert id reads nothing
-        const uint8_t *src = src0 + 16 * lane;
-        const uint32_t dst = stage0_u32 + (uint32_t)p_stage * kStageBytes + 16u * lane;
-        if (valid == kStageBytes) {
+        const uint32_t dst_stage = stage0_u32 + (uint32_t)p_stage * kStageBytes;
+        if (FMT == kCB4R) {
+            const uint8_t *rowp = a.W + gi.row0 * row_bytes;
+            if (gi.bad) {
+                // an invalid expert id reads nothing
+            } else if (R > 1) {
+                const int valid = gi.valid * (int)row_bytes;
 #pragma unroll
-            for (int k = 0; k < 9; ++k) cp_async_16(dst + 512u * k, src + 512 * k);
-        } else {
+                for (int k = 0; k < 9; ++k)
+                    if (16 * (lane + 32 * k) < valid)
+                        cp_async_16(dst_stage + dmap[k], rowp + 16 * (lane + 32 * k));
+            } else {
+                const int c0 = ps * 32;
+                const int n = nb - c0 < 32 ? nb - c0 : 32;  // chunks of this segment
+                if (lane < n) cp_async_16(dst_stage + dmap[0], rowp + 16 * (c0 + lane));
+                const uint8_t *pay = rowp + 16 * nb + 128 * c0;
 #pragma unroll
-            for (int k = 0; k < 9; ++k)
-                if (16 * (lane + 32 * k) < valid) cp_async_16(dst + 512u * k, src + 512 * k);
+                for (int k = 1; k < 9; ++k) {
+                    const int pp = 32 * (k - 1) + lane;
+                    if ((pp >> 3) < n) cp_async_16(dst_stage + dmap[k], pay + 16 * pp);
+                }
+            }
+        } else {
+            const uint8_t *src0;
+            int valid;  // bytes of the box that exist in W
+            if (R > 1) {
+                src0 = a.W + gi.row0 * row_bytes;
+                valid = gi.valid * (int)row_bytes;
+            } else {
+                const int c0 = ps * 32;
+                src0 = a.W + gi.row0 * row_bytes + c0 * kChunkBytes;
+                valid = (nb - c0 < 32 ? nb - c0 : 32) * kChunkBytes;
+            }
+            if (gi.bad) valid = 0;  // an invalid expert id reads nothing
+            const uint8_t *src = src0 + 16 * lane;
+            const uint32_t dst = dst_stage + 16u * lane;
+            if (valid == kStageBytes) {
+#pragma unroll
+                for (int k = 0; k < 9; ++k) cp_async_16(dst + 512u * k, src + 512 * k);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 9; ++k)
+                    if (16 * (lane + 32 * k) < valid) cp_async_16(dst + 512u * k, src + 512 * k);
+            }
         }
         if (++ps == spr) {
             ps = 0;
@@ -445,13 +535,16 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
             const int c = R > 1 ? (lane & (nb - 1)) : s * 32 + lane;
             const bool ok = rig < gi.valid && c < nb && !gi.bad;
             if (ok) {
-                const uint8_t *w = stage0 + c_stage * kStageBytes + lane * kChunkBytes;
+                const uint8_t *st = stage0 + c_stage * kStageBytes;
+                const uint8_t *w = st + lane * kChunkBytes;
                 int32_t *dp = DOTS ? a.dots + row * dots_row + c * 8 : nullptr;
                 const ActSmem as{act + gi.vec * act_bstride + c * kActStride, act_bstride};
                 if (FMT == kQ4K)
                     q4k_chunk<B, DOTS>(w, as, hi, lo, dp, dots_bstride);
-                else
+                else if (FMT == kCB4)
                     cb4_chunk<B, DOTS>(w, as, T, hi, lo, dp, dots_bstride);
+                else
+                    cb4r_chunk<B, DOTS>(st, lane, as, T, hi, lo, dp, dots_bstride);
             }
             __syncwarp();
             if (++c_stage == S) c_stage = 0;

@@ -105,7 +105,7 @@ def guide_fixture_x(cols: int) -> np.ndarray:
 @dataclass(frozen=True)
 class MatvecCase:
     name: str
-    fmt: str            # "q4k" or "cb4"
+    fmt: str            # "q4k", "cb4", or "cb4r" (the codebook matrix, held in resident rows)
     rows: int
     cols: int
     batch: int
@@ -141,6 +141,10 @@ CASES = {
     "c4_cb4_4096x4096_b1": MatvecCase("c4_cb4_4096x4096_b1", "cb4", 4096, 4096, 1, 4),
     "c4_cb4_11008x4096_b1": MatvecCase("c4_cb4_11008x4096_b1", "cb4", 11008, 4096, 1, 4,
                                          sub=1),
+    # the same codebook matrices, repacked into resident rows by the library
+    "c4_cb4r_4096x4096_b1": MatvecCase("c4_cb4r_4096x4096_b1", "cb4r", 4096, 4096, 1, 4),
+    "c4_cb4r_11008x4096_b1": MatvecCase("c4_cb4r_11008x4096_b1", "cb4r", 11008, 4096, 1, 4,
+                                          sub=1),
     "c5_q4k_128256x4096_b1": MatvecCase("c5_q4k_128256x4096_b1", "q4k", 128256, 4096, 1, 5),
     "c5_q4k_128256x4096_b8": MatvecCase("c5_q4k_128256x4096_b8", "q4k", 128256, 4096, 8, 5),
 }

@@ -227,3 +227,50 @@ def test_oracle_and_product_share_no_code():
             assert not re.search(r"^\s*(import|from)\s+quantized_decode_mat_gb300\b", text,
                                  re.M), f
             assert "xq_internal" not in text and '#include "xq' not in text, f
+
+
+def test_repack_argument_checks(raw):
+    fn = "xq_repack_cb4"
+    # src, Wr, block_base, n_blocks, rows, cols, stream; the 4 x 256 matrix has 32 blocks
+    ok = dict(src=P * 64, wr=P, base=0, n=32, rows=4, cols=256)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return _call(raw, fn, V(a["src"]), V(a["wr"]), I64(a["base"]), I64(a["n"]),
+                     I64(a["rows"]), I64(a["cols"]), V(0))
+    assert call(src=0) == 1                       # null src
+    assert call(wr=0) == 1                        # null Wr
+    assert call(wr=P + 4) == 2                    # Wr misaligned
+    assert call(cols=300) == 3                    # cols % 256
+    assert call(base=-1) == 3                     # chunk before the matrix
+    assert call(base=1, n=32) == 3                # chunk past the end
+    assert call(n=-1) == 3
+    assert call(src=P + 100) == 1                 # src inside Wr
+    # an empty chunk is accepted and launches nothing (no GPU is touched)
+    before = raw.xq_launch_count(12)
+    assert call(n=0) == 0
+    assert raw.xq_launch_count(12) == before
+
+
+def test_resident_entry_points_check_arguments(raw):
+    assert _call(raw, "xq_matvec_cb4r", V(P), V(0), V(P * 2), V(P * 8), I64(32), I64(256),
+                 I64(1), V(0)) == 1
+    tbl = (ctypes.c_int8 * 16)()
+    assert _call(raw, "xq_matvec_cb4r", V(P + 8), tbl, V(P * 2), V(P * 8), I64(32), I64(256),
+                 I64(1), V(0)) == 2
+    assert _call(raw, "xq_linear_cb4r", V(P), V(P * 4), tbl, V(P * 8), I64(32), I64(300),
+                 I64(1), V(0)) == 3
+    assert _call(raw, "xq_norm_linear_cb4r", V(0), V(P * 4), tbl, V(P * 8), I64(32), I64(256),
+                 I64(1), V(0)) == 1
+    assert _call(raw, "xq_subdots_cb4r", V(P), tbl, V(P * 2), V(P * 8 + 4), I64(32), I64(256),
+                 I64(1), V(0)) == 2
+
+
+def test_resident_sizes(lib):
+    import oracle
+    o = oracle.get()
+    for rows, cols in ((1, 256), (7, 4096), (11008, 4096), (3, 14336)):
+        assert lib.cb4r_bytes(rows, cols) == rows * o.cb4r_row_bytes(cols) == \
+            lib.cb4_bytes(rows, cols)
+    p = lib.plan_matvec(11008, 4096, 1, fmt="cb4r")
+    assert p == lib.plan_matvec(11008, 4096, 1, fmt="cb4")
