@@ -221,14 +221,17 @@ xq_status xq_subdots_cb4(const void *W, const int8_t *table, const void *xq, int
 enum { XQ_FORMAT_Q4K = 0, XQ_FORMAT_CB4 = 1, XQ_FORMAT_CB4R = 2 };
 
 /* Launch plan of the mat-vec kernels (pure host computation; needs no GPU).
- * format: XQ_FORMAT_Q4K, XQ_FORMAT_CB4 or XQ_FORMAT_CB4R.  sm_count and smem_optin_bytes
- * describe the device (for GB300: 152 SMs, 232448 bytes).
+ * format: XQ_FORMAT_Q4K, XQ_FORMAT_CB4 or XQ_FORMAT_CB4R.  sm_count and
+ * smem_optin_bytes describe the device (for GB300: 152 SMs, 232448 bytes).
  * A work unit (row group) is rows_per_group rows read as `segments`
  * contiguous boxes of at most 32 chunks of 256 weights (4608 bytes); lane l
- * of a warp takes chunk l of a box.  Each of the `warps` warps of the `grid`
- * persistent CTAs keeps stages-1 boxes in flight.  The batch's q8 blocks are
- * staged in shared memory; if they do not fit, each call makes `launches`
- * launches of batch_per_launch vectors (each re-reads W). */
+ * of a warp takes chunk l of a box.  A warp works on row_block row groups at
+ * once (2 for Q4_K with two or more activation vectors: each activation load
+ * then serves two chunks of one column), one stage holding row_block boxes.
+ * Each of the `warps` warps of the `grid` persistent CTAs keeps stages-1
+ * stages in flight.  The batch's q8 blocks are staged in shared memory; if
+ * they do not fit, each call makes `launches` launches of batch_per_launch
+ * vectors (each re-reads W). */
 typedef struct {
     int32_t warps;
     int32_t stages;
@@ -240,6 +243,7 @@ typedef struct {
     int32_t batch_per_launch;
     int32_t launches;
     int64_t smem_bytes;
+    int32_t row_block;
 } xq_plan;
 
 xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t batch,
@@ -248,6 +252,10 @@ xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t bat
  * above) and stages (2..8), 0 = automatic.  Process-wide; not for concurrent
  * use with launches. */
 void xq_set_plan_override(int32_t warps, int32_t stages);
+/* Override the row groups a warp works on at once: 1, or 2 where the
+ * automatic plan would use 2 (Q4_K at batch >= 2); 0 = automatic.
+ * Process-wide, for sweeps and tests, like xq_set_plan_override. */
+void xq_set_row_block_override(int32_t row_block);
 /* Plan used by the calling thread's last mat-vec or sub-dot launch. */
 xq_status xq_last_plan(xq_plan *plan);
 

@@ -62,6 +62,7 @@ from ._native import (  # noqa: F401
     quantize_q8,
     rmsnorm_q8,
     set_plan_override,
+    set_row_block_override,
     subdots_cb4,
     subdots_q4k,
 )

@@ -25,7 +25,7 @@ class _Plan(ctypes.Structure):
                 ("rows_per_group", ctypes.c_int32), ("segments", ctypes.c_int32),
                 ("chunks_per_row", ctypes.c_int32), ("groups", ctypes.c_int64),
                 ("batch_per_launch", ctypes.c_int32), ("launches", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int64)]
+                ("smem_bytes", ctypes.c_int64), ("row_block", ctypes.c_int32)]
 
 
 def _sig(name, restype, argtypes):
@@ -65,6 +65,7 @@ _subdots_cb4 = _sig("xq_subdots_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64,
 _plan = _sig("xq_plan_matvec", ctypes.c_int, [_I32, _I64, _I64, _I64, _I32, _I64,
                                              ctypes.POINTER(_Plan)])
 _set_override = _sig("xq_set_plan_override", None, [_I32, _I32])
+_set_row_block = _sig("xq_set_row_block_override", None, [_I32])
 _last_plan = _sig("xq_last_plan", ctypes.c_int, [ctypes.POINTER(_Plan)])
 _launch_count = _sig("xq_launch_count", ctypes.c_uint64, [_I32])
 _device_status = _sig("xq_device_status", ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32),
@@ -389,6 +390,11 @@ def last_plan() -> dict:
 
 def set_plan_override(warps: int = 0, stages: int = 0) -> None:
     _set_override(warps, stages)
+
+
+def set_row_block_override(row_block: int = 0) -> None:
+    """1 forces one row group per warp unit; 0 restores the automatic plan."""
+    _set_row_block(row_block)
 
 
 def launch_count(which: int) -> int:

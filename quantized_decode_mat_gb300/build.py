@@ -1,6 +1,6 @@
 """Builds the CUDA library ``_build/libxq.so`` in-tree with nvcc for sm_103a.
 
-Four translation units are compiled in parallel (one -gencode each), then
+The translation units are compiled in parallel (one -gencode each), then
 linked into one shared library with the CUDA runtime linked statically, so the
 library needs only the NVIDIA driver at run time.  ptxas resource reports are
 kept beside the objects (``_build/*.ptxas.log``) for the spill gate.
@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libxq.so")
-SOURCES = ["xq_api.cu", "xq_matvec_q4k.cu", "xq_matvec_cb4.cu", "xq_matvec_cb4r.cu"]
+SOURCES = ["xq_api.cu", "xq_matvec_q4k.cu", "xq_matvec_q4k_rb2.cu", "xq_matvec_cb4.cu",
+           "xq_matvec_cb4r.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               f"-I{INCLUDE}"]

@@ -138,6 +138,7 @@ thread_local bool t_have_plan = false;
 std::atomic<uint64_t> g_counts[XQ_COUNT_N];
 std::atomic<int32_t> g_override_warps{0};
 std::atomic<int32_t> g_override_stages{0};
+std::atomic<int32_t> g_override_row_block{0};
 
 xq_status fail(xq_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 xq_status fail(xq_status s, const char *fmt, ...) {
@@ -219,17 +220,17 @@ xq_status device_state(DeviceState **out) {
 
 int64_t align128(int64_t v) { return (v + 127) & ~(int64_t)127; }
 
-// Work units: a row group is 32/nb rows (one contiguous 4608-byte box) when
-// nb is a power of two below 32, else one row streamed in ceil(nb/32) boxes.
-// The batch's q8 blocks are staged in shared memory; when they do not fit
-// beside two stages, the batch is split across launches (each re-reads W).
-// Grid: one CTA per SM, at most one per work unit.  Warps: enough to cover
-// the work units, within the instantiation's register budget.  Stages: 2
-// (measured best), fewer warps if even that does not fit.
-// slots > 0 plans the grouped-expert form: `rows` rows per expert, `slots`
-// selected experts, each group inside one slot, and `batch` staged activation
-// vectors (1 shared, or one per slot).
-xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
+// Row groups: 32/nb rows (one contiguous 4608-byte box) when nb is a power
+// of two below 32, else one row streamed in ceil(nb/32) boxes.  A warp's work
+// unit is row_block consecutive row groups (see the kernel).  The batch's q8
+// blocks are staged in shared memory; when they do not fit beside two stages,
+// the batch is split across launches (each re-reads W).  Grid: one CTA per
+// SM, at most one per work unit.  Warps: enough to cover the work units,
+// within the instantiation's register budget.  Stages: 2 (measured best),
+// fewer warps if even that does not fit.  slots > 0 plans the grouped-expert
+// form: `rows` rows per expert, `slots` selected experts, each group inside
+// one slot, and `batch` staged activation vectors (1 shared, or one per slot).
+xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
                     int64_t smem_optin, xq_plan *p, int64_t slots = 0) {
     const int32_t nb = (int32_t)(cols / 256);
     const int32_t R = (nb < 32 && 32 % nb == 0) ? 32 / nb : 1;
@@ -244,19 +245,29 @@ xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
     const int64_t act = align128((int64_t)bl * nb * kActStride);
     if (slots > 0 && bl != batch)
         return fail(XQ_ESHAPE, "the per-slot activations do not fit in shared memory");
-    const int32_t grid = (int32_t)(groups < sm_count ? groups : sm_count);
     const int32_t wmax = warps_limit(slots > 0 ? 1 : bl);
-    const int64_t per_cta = (groups + grid - 1) / grid;
-    int32_t W = (int32_t)(per_cta < wmax ? per_cta : wmax);
     const int32_t ow = g_override_warps.load(), os = g_override_stages.load();
-    if (ow > 0) W = ow < wmax ? ow : wmax;
+    const int32_t om = g_override_row_block.load();
     // Two stages (one box in flight per warp while the other is consumed) read
     // fastest on GB300: the warps of the GPU then stream one contiguous window.
-    int32_t S = os > 0 ? os : 2;
-    if (S < 2) S = 2;
-    if (S > kMaxStages) S = kMaxStages;
-    auto bytes = [&](int32_t w, int32_t st) { return act + (int64_t)w * st * kStageBytes + 128; };
-    while (bytes(W, S) > smem_optin) {
+    const int32_t S0 = os > 0 ? (os < 2 ? 2 : os > kMaxStages ? kMaxStages : os) : 2;
+    // Row groups per warp unit: two for Q4_K with two or more vectors, unless
+    // the instantiation's full warp count would then not fit in shared memory
+    // (fewer warps cost more than the halved activation loads save: measured
+    // on the 4096 x 14336 projection at batch 8).
+    int32_t M = (fmt == kQ4K && bl >= 2 && slots == 0) ? 2 : 1;
+    if (om > 0) M = (om >= 2 && M == 2) ? 2 : 1;
+    auto bytes = [&](int32_t w, int32_t st, int32_t m) {
+        return act + (int64_t)w * st * m * kStageBytes + 128;
+    };
+    if (M == 2 && om <= 0 && bytes(wmax, 2, 2) > smem_optin) M = 1;
+    const int64_t units = (groups + M - 1) / M;
+    const int32_t grid = (int32_t)(units < sm_count ? units : sm_count);
+    const int64_t per_cta = (units + grid - 1) / grid;
+    int32_t W = (int32_t)(per_cta < wmax ? per_cta : wmax);
+    if (ow > 0) W = ow < wmax ? ow : wmax;
+    int32_t S = S0;
+    while (bytes(W, S, M) > smem_optin) {
         if (S > 2)
             --S;
         else if (W > 1)
@@ -264,11 +275,11 @@ xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
         else
             break;
     }
-    if (bytes(W, S) > smem_optin)
+    if (bytes(W, S, M) > smem_optin)
         return fail(XQ_ESHAPE, "plan needs %lld bytes of shared memory, device allows %lld",
-                    (long long)bytes(W, S), (long long)smem_optin);
+                    (long long)bytes(W, S, M), (long long)smem_optin);
     const int64_t tw = (int64_t)grid * W;
-    if (((groups + tw - 1) / tw) * spr > 0x7FFFFFFFLL)
+    if (((units + tw - 1) / tw) * spr > 0x7FFFFFFFLL)
         return fail(XQ_ESHAPE, "too many boxes per warp");
     p->warps = W;
     p->stages = S;
@@ -279,7 +290,8 @@ xq_status make_plan(int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
     p->groups = groups;
     p->batch_per_launch = bl;
     p->launches = (int32_t)((batch + bl - 1) / bl);
-    p->smem_bytes = bytes(W, S);
+    p->smem_bytes = bytes(W, S, M);
+    p->row_block = M;
     return XQ_OK;
 }
 
@@ -334,7 +346,7 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     DeviceState *dev = nullptr;
     if (xq_status s = device_state(&dev)) return s;
     xq_plan plan;
-    if (xq_status s = make_plan(rows, cols, batch, dev->sm_count, dev->smem_optin, &plan))
+    if (xq_status s = make_plan(op.fmt, rows, cols, batch, dev->sm_count, dev->smem_optin, &plan))
         return s;
     MatvecArgs a;
     memset(&a, 0, sizeof a);
@@ -345,6 +357,7 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     a.rows_per_group = plan.rows_per_group;
     a.segments = plan.segments;
     a.stages = plan.stages;
+    a.row_block = plan.row_block;
     if (cb4) pack_table(table, a.kv);
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -393,7 +406,7 @@ xq_status run_matvec_id(int fmt, const void *W, const int8_t *table, const int32
     DeviceState *dev = nullptr;
     if (xq_status s = device_state(&dev)) return s;
     xq_plan plan;
-    if (xq_status s = make_plan(rpe, cols, nvec, dev->sm_count, dev->smem_optin, &plan, used))
+    if (xq_status s = make_plan(fmt, rpe, cols, nvec, dev->sm_count, dev->smem_optin, &plan, used))
         return s;
     MatvecArgs a;
     memset(&a, 0, sizeof a);
@@ -406,6 +419,7 @@ xq_status run_matvec_id(int fmt, const void *W, const int8_t *table, const int32
     a.rows_per_group = plan.rows_per_group;
     a.segments = plan.segments;
     a.stages = plan.stages;
+    a.row_block = plan.row_block;
     a.sel = sel;
     a.rows_per_expert = rpe;
     a.n_experts = (int32_t)n_experts;
@@ -616,12 +630,17 @@ xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t bat
         return fail(XQ_EINVAL, "format must be XQ_FORMAT_Q4K, XQ_FORMAT_CB4 or XQ_FORMAT_CB4R");
     if (xq_status s = check_shape(rows, cols, batch, true)) return s;
     if (sm_count < 1) return fail(XQ_EINVAL, "sm_count must be positive");
-    return make_plan(rows, cols, batch, sm_count, smem_optin_bytes, plan);
+    return make_plan(format == XQ_FORMAT_Q4K ? kQ4K : format == XQ_FORMAT_CB4 ? kCB4 : kCB4R, rows,
+                     cols, batch, sm_count, smem_optin_bytes, plan);
 }
 
 void xq_set_plan_override(int32_t warps, int32_t stages) {
     g_override_warps.store(warps < 0 ? 0 : warps);
     g_override_stages.store(stages < 0 ? 0 : stages);
+}
+
+void xq_set_row_block_override(int32_t row_block) {
+    g_override_row_block.store(row_block < 0 ? 0 : row_block);
 }
 
 xq_status xq_last_plan(xq_plan *plan) {

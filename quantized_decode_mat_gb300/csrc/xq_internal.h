@@ -55,6 +55,7 @@ struct MatvecArgs {
     int32_t rows_per_group; // 32/nb if nb is a power of two below 32, else 1
     int32_t segments;       // boxes per group: 1, or ceil(nb/32) when rows_per_group == 1
     int32_t stages;         // shared-memory stages per warp (2..8)
+    int32_t row_block;      // row groups a warp works on at once (1, or 2 for Q4_K at batch >= 2)
     uint32_t kv[4];         // codebook bytes kv[0..15], little-endian words
     // grouped-expert form
     const int32_t *sel;     // [used] expert ids (device)
@@ -79,6 +80,9 @@ cudaError_t launch_matvec_cb4(const MatvecArgs &a, int batch, int kind, dim3 gri
 // Raise the dynamic shared memory limit of every instantiation of a format.
 cudaError_t configure_matvec_q4k(int smem_optin);
 cudaError_t configure_matvec_cb4(int smem_optin);
+cudaError_t launch_matvec_q4k_rb2(const MatvecArgs &a, int batch, int kind, dim3 grid,
+                                  dim3 block, size_t smem, cudaStream_t s);
+cudaError_t configure_matvec_q4k_rb2(int smem_optin);
 cudaError_t launch_matvec_cb4r(const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,
                                size_t smem, cudaStream_t s);
 cudaError_t configure_matvec_cb4r(int smem_optin);

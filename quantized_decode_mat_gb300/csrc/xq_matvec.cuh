@@ -143,6 +143,92 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w, const A
     }
 }
 
+// ---- Q4_K, M row groups at once --------------------------------------------------------
+// The same arithmetic as q4k_chunk for M chunks that share one column (lane
+// l's chunk in each of M row groups): every activation load from shared
+// memory is used against M chunks instead of one.  The loop runs over the four
+// 64-value groups, then the vectors, then the chunks; each 8-term dot is two
+// independent 4-term chains.  S1 is an exact integer and each (chunk, vector)
+// epilogue is the single-chunk one, so y is bit-for-bit that of the one-chunk
+// form.  ok[m] false: chunk m is not accumulated and its dots are not stored
+// (its shared-memory bytes may be stale).
+template <int B, int M, bool DOTS, class Act>
+__device__ __forceinline__ void q4k_chunks(const uint8_t *const (&w)[M], const bool (&ok)[M],
+                                           const Act &act, float (&hi)[M][B], float (&lo)[M][B],
+                                           int32_t *const (&dots)[M], int64_t dots_bstride) {
+    float d[M], dmin[M];
+    uint32_t sc_lo[M], sc_hi[M], m_lo[M], m_hi[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const uint4 h = *reinterpret_cast<const uint4 *>(w[m]);
+        d[m] = f16_bits_to_f32(h.x);
+        dmin[m] = f16_bits_to_f32(h.x >> 16);
+        sc_lo[m] = h.y & 0x3F3F3F3Fu;
+        m_lo[m] = h.z & 0x3F3F3F3Fu;
+        sc_hi[m] = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+        m_hi[m] = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+    }
+    int S1[M][B];
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int b = 0; b < B; ++b) S1[m][b] = 0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        // sub-block 2g: low nibbles of group g; sub-block 2g+1: its high nibbles
+        uint32_t ql[M][8], qh[M][8];
+        int s0[M], s1[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const uint4 v0 = *reinterpret_cast<const uint4 *>(w[m] + 16 + 32 * g);
+            const uint4 v1 = *reinterpret_cast<const uint4 *>(w[m] + 32 + 32 * g);
+            const uint32_t q[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                ql[m][k] = q[k] & 0x0F0F0F0Fu;
+                qh[m][k] = q[k] & 0xF0F0F0F0u;
+            }
+            const uint32_t scw = g < 2 ? sc_lo[m] : sc_hi[m];
+            s0[m] = byte_of(scw, 2 * (g & 1));
+            s1[m] = byte_of(scw, 2 * (g & 1) + 1);
+        }
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const uint4 a0 = act.q16(b, 4 * g + 0), a1 = act.q16(b, 4 * g + 1);
+            const uint4 a2 = act.q16(b, 4 * g + 2), a3 = act.q16(b, 4 * g + 3);
+            const uint32_t alo[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t ahi[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                int l0 = 0, l1 = 0, h0 = 0, h1 = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    l0 = dp4a(ql[m][k], alo[k], l0);
+                    l1 = dp4a(ql[m][k + 4], alo[k + 4], l1);
+                    h0 = dp4a_us(qh[m][k], ahi[k], h0);
+                    h1 = dp4a_us(qh[m][k + 4], ahi[k + 4], h1);
+                }
+                const int d0 = l0 + l1;
+                const int d1 = (h0 + h1) >> 4;  // high nibbles were used in place (x16)
+                S1[m][b] += s0[m] * d0 + s1[m] * d1;
+                if (DOTS && ok[m])
+                    *reinterpret_cast<int2 *>(dots[m] + b * dots_bstride + 2 * g) = make_int2(d0, d1);
+            }
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+        const uint4 sp = act.split(b);  // sum_j m_j * bsum_j as four byte dots
+        const float xs = act.xs(b);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const int S2 = dp4a_uu(m_hi[m], sp.y, dp4a_uu(m_lo[m], sp.x, 0)) +
+                           256 * dp4a_us(m_hi[m], sp.w, dp4a_us(m_lo[m], sp.z, 0));
+            if (ok[m]) q4k_epilogue(xs, d[m], dmin[m], S1[m][b], S2, hi[m][b], lo[m][b]);
+        }
+    }
+}
+
 // ---- codebook chunk -----------------------------------------------------------------
 // Eight nibbles of a payload word -> two words of int8 codebook values, LO for
 // the low nibbles (bytes in order) and HI for the high nibbles.  The table is
@@ -245,32 +331,82 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const A
 
 // ---- resident codebook rows: the staged slot map ------------------------------------
 // A box of resident rows is staged so that slot l (the chunk lane l takes)
-// has its 16 scale bytes at 16l and its eight 16-byte payloads at
-// 512 + 128l, payload i rotated to piece (i + l) & 7: eight lanes reading
-// their payload i then touch eight distinct 4-bank groups.
-__device__ __forceinline__ uint32_t cb4r_scale_slot(int slot) { return 16u * (uint32_t)slot; }
+// is 144 bytes at 144l: its 16 scale bytes, then its eight 16-byte payloads.
+// The 144-byte slot stride puts the slots that eight lanes read at once on
+// distinct 4-bank groups, and every read is a fixed offset from the slot.
+__device__ __forceinline__ uint32_t cb4r_scale_slot(int slot) { return 144u * (uint32_t)slot; }
 __device__ __forceinline__ uint32_t cb4r_payload_slot(int slot, int i) {
-    return 512u + 128u * (uint32_t)slot + 16u * (uint32_t)((i + slot) & 7);
+    return 144u * (uint32_t)slot + 16u + 16u * (uint32_t)i;
 }
 
 template <int B, bool DOTS, class Act>
-__device__ __forceinline__ void cb4r_chunk(const uint8_t *__restrict__ st, int slot,
-                                           const Act &act, const uint32_t (&T)[4], float (&hi)[B],
+__device__ __forceinline__ void cb4r_chunk(const uint8_t *__restrict__ w, const Act &act,
+                                           const uint32_t (&T)[4], float (&hi)[B],
                                            float (&lo)[B], int32_t *dots, int64_t dots_bstride) {
-    const uint4 sc = *reinterpret_cast<const uint4 *>(st + cb4r_scale_slot(slot));
+    const uint4 sc = *reinterpret_cast<const uint4 *>(w);
     const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
     float dk[8];
     uint32_t P[8][4];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         dk[k] = f16_bits_to_f32(sw[k >> 1] >> (16 * (k & 1)));
-        const uint4 t = *reinterpret_cast<const uint4 *>(st + cb4r_payload_slot(slot, k));
+        const uint4 t = *reinterpret_cast<const uint4 *>(w + 16 + 16 * k);
         P[k][0] = t.x;
         P[k][1] = t.y;
         P[k][2] = t.z;
         P[k][3] = t.w;
     }
     cb4_blocks<B, DOTS>(dk, P, act, T, hi, lo, dots, dots_bstride);
+}
+
+// ---- reduction of a row's partial sums -------------------------------------------------
+// Recursive halving over the aligned group of `width` lanes that share a row
+// (width a power of two): at offset o, a lane keeps the lower or upper half of
+// its batch values (by its lane bit o), sends the other half to lane ^ o and
+// adds the received half, compensated (acc_add).  log2(P) such steps leave
+// one value a lane, summed over 2^steps lanes; the remaining offsets are a
+// plain xor butterfly on that value.  With batch 1 this is the butterfly
+// alone.  Compared with a butterfly of every value, it moves and adds
+// B/2 + B/4 + ... values a lane instead of B*log2(width).  On return,
+// h[i], l[i] (i < nlive) hold vector base + i of the row, complete in the
+// lanes whose bits below `keep` are zero.
+template <int B>
+struct Pow2Ceil {
+    static constexpr int v = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8;
+};
+
+template <int P>
+__device__ __forceinline__ void halving_reduce(float (&h)[P], float (&l)[P], int width, int lane,
+                                               int &base, int &nlive, int &keep) {
+    base = 0;
+    nlive = P;
+    int off = width >> 1;
+#pragma unroll
+    for (int s = 0; (P >> s) >= 2; ++s) {
+        if (off == 0) break;
+        const int n = P >> s;
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float kh = up ? h[n / 2 + i] : h[i], kl = up ? l[n / 2 + i] : l[i];
+            const float sh = up ? h[i] : h[n / 2 + i], sl = up ? l[i] : l[n / 2 + i];
+            const float rh = __shfl_xor_sync(0xffffffffu, sh, off);
+            const float rl = __shfl_xor_sync(0xffffffffu, sl, off);
+            float a = kh, c = kl;
+            acc_add(a, c, rh, rl);
+            h[i] = a;
+            l[i] = c;
+        }
+        if (up) base += n / 2;
+        nlive = n / 2;
+        off >>= 1;
+    }
+    keep = off ? 2 * off - 1 : 0;
+    for (; off > 0; off >>= 1) {  // nlive == 1 here
+        const float oh = __shfl_xor_sync(0xffffffffu, h[0], off);
+        const float ol = __shfl_xor_sync(0xffffffffu, l[0], off);
+        acc_add(h[0], l[0], oh, ol);
+    }
 }
 
 // ---- work-unit descriptor ---------------------------------------------------------------
@@ -331,9 +467,13 @@ __device__ __forceinline__ GroupInfo group_info(const MatvecArgs &a, int64_t g, 
 template <int B>
 constexpr int max_threads() { return warps_limit(B) * 32; }
 
-template <int FMT, int B, bool DOTS, int FUSE, bool ID>
+// M: row groups a warp works on at once (a work unit).  Two for Q4_K with
+// several activation vectors, where the activation loads from shared memory
+// are the limit; one otherwise.
+template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M>
 __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const MatvecArgs a) {
     static_assert(!ID || (B == 1 && !DOTS && FUSE == 0), "the grouped form is batch 1 on q8 input");
+    static_assert(M == 1 || (M == 2 && FMT == kQ4K && !ID), "row blocking is a Q4_K form");
     static_assert(FUSE >= 0 && FUSE <= 2, "FUSE: 0 q8 input, 1 quantise x, 2 RMSNorm then quantise");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
@@ -350,21 +490,24 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
     const int64_t act_bstride = (int64_t)nb * kActStride;
     const int nvec = ID ? a.act_vectors : B;  // staged activation vectors
     const int act_bytes = (int)((nvec * act_bstride + 127) & ~(int64_t)127);
+    const uint32_t unit_bytes = (uint32_t)M * kStageBytes;  // one stage: M boxes
     uint8_t *act = smem;
-    uint8_t *stage0 = smem + act_bytes + (size_t)warp * S * kStageBytes;
+    uint8_t *stage0 = smem + act_bytes + (size_t)warp * S * unit_bytes;
     const uint32_t stage0_u32 = smem_u32(stage0);
 
     uint32_t T[4] = {a.kv[0], a.kv[1], a.kv[2], a.kv[3]};
 
-    // 1. this warp's row groups and their boxes; the first S-1 boxes are
-    //    requested before the activation is staged, so the two overlap
+    // 1. this warp's work units (M consecutive row groups) and their boxes;
+    //    the first S-1 stages are requested before the activation is staged,
+    //    so the two overlap
     const int G = gridDim.x;
     const int64_t gw = (int64_t)warp * G + blockIdx.x;
     const int64_t TW = (int64_t)G * W;
-    const int64_t my_groups = gw < ngroups ? (ngroups - 1 - gw) / TW + 1 : 0;
-    const int nitems = (int)(my_groups * spr);
+    const int64_t nunits = (ngroups + M - 1) / M;
+    const int64_t my_units = gw < nunits ? (nunits - 1 - gw) / TW + 1 : 0;
+    const int nitems = (int)(my_units * spr);
 
-    int64_t pg = gw;  // producer cursor: group, segment, stage
+    int64_t pu = gw;  // producer cursor: unit, segment, stage
     int ps = 0, p_stage = 0, issued = 0;
     // Resident rows: where each of this lane's nine 16-byte copies of a box
     // lands in the stage (the same for every box of the launch).  With whole
@@ -387,9 +530,9 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
             }
         }
     }
-    auto issue_next = [&]() {
+    // one box: row group pg, segment ps, into the stage bytes at dst_stage
+    auto issue_box = [&](int64_t pg, uint32_t dst_stage) {
         const GroupInfo gi = group_info<ID>(a, pg, R);
-        const uint32_t dst_stage = stage0_u32 + (uint32_t)p_stage * kStageBytes;
         if (FMT == kCB4R) {
             const uint8_t *rowp = a.W + gi.row0 * row_bytes;
             if (gi.bad) {
@@ -434,9 +577,16 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
                     if (16 * (lane + 32 * k) < valid) cp_async_16(dst + 512u * k, src + 512 * k);
             }
         }
+    };
+    auto issue_next = [&]() {
+        const uint32_t dst_stage = stage0_u32 + (uint32_t)p_stage * unit_bytes;
+#pragma unroll
+        for (int m = 0; m < M; ++m)
+            if (pu * M + m < ngroups)
+                issue_box(pu * M + m, dst_stage + (uint32_t)m * kStageBytes);
         if (++ps == spr) {
             ps = 0;
-            pg += TW;
+            pu += TW;
         }
         if (++p_stage == S) p_stage = 0;
         ++issued;
@@ -519,120 +669,163 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
     const int64_t dots_row = (int64_t)nb * 8;
     const int64_t dots_bstride = rows * dots_row;
     const int width = R > 1 ? nb : 32;  // lanes that share a row
+    const int rig = R > 1 ? lane / nb : 0;  // this lane's row within a group
     int c_stage = 0;
-    for (int64_t g = gw; g < ngroups; g += TW) {
-        const GroupInfo gi = group_info<ID>(a, g, R);
-        const int rig = R > 1 ? lane / nb : 0;  // this lane's row within the group
-        const int64_t row = gi.row0 + rig;      // its row in W (for the dots)
-        float hi[B], lo[B];
+    for (int64_t u = gw; u < nunits; u += TW) {
+        GroupInfo gi[M];
 #pragma unroll
-        for (int b = 0; b < B; ++b) hi[b] = lo[b] = 0.0f;
+        for (int m = 0; m < M; ++m) {
+            if (u * M + m < ngroups) {
+                gi[m] = group_info<ID>(a, u * M + m, R);
+            } else {
+                gi[m].row0 = gi[m].out0 = 0;
+                gi[m].valid = 0;
+                gi[m].vec = 0;
+                gi[m].bad = false;
+            }
+        }
+        float hi[M][B], lo[M][B];
+#pragma unroll
+        for (int m = 0; m < M; ++m)
+#pragma unroll
+            for (int b = 0; b < B; ++b) hi[m][b] = lo[m][b] = 0.0f;
         for (int s = 0; s < spr; ++s) {
             if (issued < nitems) issue_next();
             cp_async_commit();
-            cp_async_wait_pending(S - 1);  // this lane's copies of the box landed
+            cp_async_wait_pending(S - 1);  // this lane's copies of the stage landed
             __syncwarp();                  // ... and every other lane's
             const int c = R > 1 ? (lane & (nb - 1)) : s * 32 + lane;
-            const bool ok = rig < gi.valid && c < nb && !gi.bad;
-            if (ok) {
-                const uint8_t *st = stage0 + c_stage * kStageBytes;
-                const uint8_t *w = st + lane * kChunkBytes;
-                int32_t *dp = DOTS ? a.dots + row * dots_row + c * 8 : nullptr;
-                const ActSmem as{act + gi.vec * act_bstride + c * kActStride, act_bstride};
-                if (FMT == kQ4K)
-                    q4k_chunk<B, DOTS>(w, as, hi, lo, dp, dots_bstride);
-                else if (FMT == kCB4)
-                    cb4_chunk<B, DOTS>(w, as, T, hi, lo, dp, dots_bstride);
-                else
-                    cb4r_chunk<B, DOTS>(st, lane, as, T, hi, lo, dp, dots_bstride);
+            const uint8_t *st = stage0 + c_stage * unit_bytes + lane * kChunkBytes;
+            const ActSmem as{act + gi[0].vec * act_bstride + c * kActStride, act_bstride};
+            if (M > 1) {
+                const uint8_t *w[M];
+                bool ok[M];
+                int32_t *dp[M];
+                bool any = false;
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    w[m] = st + m * kStageBytes;
+                    ok[m] = rig < gi[m].valid && c < nb;
+                    any |= ok[m];
+                    dp[m] = DOTS && ok[m] ? a.dots + (gi[m].row0 + rig) * dots_row + c * 8 : nullptr;
+                }
+                if (any) q4k_chunks<B, M, DOTS>(w, ok, as, hi, lo, dp, dots_bstride);
+            } else {
+                const bool ok = rig < gi[0].valid && c < nb && !gi[0].bad;
+                if (ok) {
+                    int32_t *dp = DOTS ? a.dots + (gi[0].row0 + rig) * dots_row + c * 8 : nullptr;
+                    if (FMT == kQ4K)
+                        q4k_chunk<B, DOTS>(st, as, hi[0], lo[0], dp, dots_bstride);
+                    else if (FMT == kCB4)
+                        cb4_chunk<B, DOTS>(st, as, T, hi[0], lo[0], dp, dots_bstride);
+                    else
+                        cb4r_chunk<B, DOTS>(st, as, T, hi[0], lo[0], dp, dots_bstride);
+                }
             }
             __syncwarp();
             if (++c_stage == S) c_stage = 0;
         }
         if (!DOTS) {
-            // compensated butterfly over the row's lanes (aligned groups of `width`)
-            for (int off = width >> 1; off > 0; off >>= 1) {
+            constexpr int P = Pow2Ceil<B>::v;
 #pragma unroll
-                for (int b = 0; b < B; ++b) {
-                    const float oh = __shfl_xor_sync(0xffffffffu, hi[b], off);
-                    const float ol = __shfl_xor_sync(0xffffffffu, lo[b], off);
-                    acc_add(hi[b], lo[b], oh, ol);
+            for (int m = 0; m < M; ++m) {
+                float h[P], l[P];
+#pragma unroll
+                for (int b = 0; b < P; ++b) {
+                    h[b] = b < B ? hi[m][b] : 0.0f;
+                    l[b] = b < B ? lo[m][b] : 0.0f;
                 }
-            }
-            if ((lane & (width - 1)) == 0 && rig < gi.valid) {
-                const int64_t orow = gi.out0 + rig;
-                const float nan = __int_as_float(0x7FC00000);
+                int base, nlive, keep;
+                halving_reduce<P>(h, l, width, lane, base, nlive, keep);
+                if ((lane & keep) == 0 && rig < gi[m].valid) {
+                    const int64_t orow = gi[m].out0 + rig;
+                    const float nan = __int_as_float(0x7FC00000);
 #pragma unroll
-                for (int b = 0; b < B; ++b)
-                    a.y[(int64_t)b * rows + orow] = gi.bad ? nan : __fadd_rn(hi[b], lo[b]);
-                if (ID && gi.bad && rig == 0) atomicOr(a.status, kStatusBadExpertId);
+                    for (int i = 0; i < P; ++i)
+                        if (i < nlive && base + i < B)
+                            a.y[(int64_t)(base + i) * rows + orow] =
+                                gi[m].bad ? nan : __fadd_rn(h[i], l[i]);
+                    if (ID && gi[m].bad && rig == 0 && (lane & (width - 1)) == 0)
+                        atomicOr(a.status, kStatusBadExpertId);
+                }
             }
         }
     }
     cp_async_wait_all();  // only empty groups can remain; keeps the exit clean
 }
 
-template <int FMT, int B, bool DOTS, int FUSE, bool ID = false>
+template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>
 inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, size_t smem,
                                    cudaStream_t s) {
-    xq_matvec_kernel<FMT, B, DOTS, FUSE, ID><<<grid, block, smem, s>>>(a);
+    xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M><<<grid, block, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-template <int FMT, int B, bool DOTS, int FUSE, bool ID = false>
+template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>
 inline cudaError_t configure_t(int smem_optin) {
-    return cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID>,
+    return cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
 }
 
 // kind: 0 = mat-vec on q8 blocks, 1 = the same with the exact dots,
 // 2 = fused quantise + mat-vec, 3 = grouped experts (batch 1, q8 input),
-// 4 = fused RMSNorm + quantise + mat-vec.
-template <int FMT>
+// 4 = fused RMSNorm + quantise + mat-vec.  M: row groups per work unit
+// (batch 1 always takes M = 1).
+template <int FMT, int M>
 inline cudaError_t launch_matvec_fmt(const MatvecArgs &a, int batch, int kind, dim3 grid,
                                      dim3 block, size_t smem, cudaStream_t s) {
-    if (kind == 3)
-        return batch == 1 ? launch_matvec_t<FMT, 1, false, 0, true>(a, grid, block, smem, s)
-                          : cudaErrorInvalidValue;
-#define XQ_CASE(BB)                                                                    \
-    case BB:                                                                           \
-        return kind == 1   ? launch_matvec_t<FMT, BB, true, 0>(a, grid, block, smem, s)  \
-               : kind == 2 ? launch_matvec_t<FMT, BB, false, 1>(a, grid, block, smem, s) \
-               : kind == 4 ? launch_matvec_t<FMT, BB, false, 2>(a, grid, block, smem, s) \
-                           : launch_matvec_t<FMT, BB, false, 0>(a, grid, block, smem, s);
+    if constexpr (M == 1) {
+        if (kind == 3)
+            return batch == 1 ? launch_matvec_t<FMT, 1, false, 0, true>(a, grid, block, smem, s)
+                              : cudaErrorInvalidValue;
+        if (batch == 1)
+            return kind == 1   ? launch_matvec_t<FMT, 1, true, 0>(a, grid, block, smem, s)
+                   : kind == 2 ? launch_matvec_t<FMT, 1, false, 1>(a, grid, block, smem, s)
+                   : kind == 4 ? launch_matvec_t<FMT, 1, false, 2>(a, grid, block, smem, s)
+                               : launch_matvec_t<FMT, 1, false, 0>(a, grid, block, smem, s);
+    } else {
+        if (kind == 3 || batch == 1) return cudaErrorInvalidValue;
+    }
+#define XQ_CASE(BB, MM)                                                                         \
+    case BB:                                                                                    \
+        return kind == 1   ? launch_matvec_t<FMT, BB, true, 0, false, MM>(a, grid, block, smem, s)  \
+               : kind == 2 ? launch_matvec_t<FMT, BB, false, 1, false, MM>(a, grid, block, smem, s) \
+               : kind == 4 ? launch_matvec_t<FMT, BB, false, 2, false, MM>(a, grid, block, smem, s) \
+                           : launch_matvec_t<FMT, BB, false, 0, false, MM>(a, grid, block, smem, s);
     switch (batch) {
-        XQ_CASE(1)
-        XQ_CASE(2)
-        XQ_CASE(3)
-        XQ_CASE(4)
-        XQ_CASE(5)
-        XQ_CASE(6)
-        XQ_CASE(7)
-        XQ_CASE(8)
+        XQ_CASE(2, M)
+        XQ_CASE(3, M)
+        XQ_CASE(4, M)
+        XQ_CASE(5, M)
+        XQ_CASE(6, M)
+        XQ_CASE(7, M)
+        XQ_CASE(8, M)
         default:
             return cudaErrorInvalidValue;
     }
 #undef XQ_CASE
 }
 
-template <int FMT>
+template <int FMT, int M>
 inline cudaError_t configure_fmt(int smem_optin) {
     cudaError_t e = cudaSuccess;
-#define XQ_CFG(BB)                                                             \
-    if (e == cudaSuccess) e = configure_t<FMT, BB, false, 0>(smem_optin); \
-    if (e == cudaSuccess) e = configure_t<FMT, BB, true, 0>(smem_optin);  \
-    if (e == cudaSuccess) e = configure_t<FMT, BB, false, 1>(smem_optin); \
-    if (e == cudaSuccess) e = configure_t<FMT, BB, false, 2>(smem_optin);
-    XQ_CFG(1)
-    XQ_CFG(2)
-    XQ_CFG(3)
-    XQ_CFG(4)
-    XQ_CFG(5)
-    XQ_CFG(6)
-    XQ_CFG(7)
-    XQ_CFG(8)
+#define XQ_CFG(BB, MM)                                                                  \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, false, 0, false, MM>(smem_optin); \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, true, 0, false, MM>(smem_optin);  \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, false, 1, false, MM>(smem_optin); \
+    if (e == cudaSuccess) e = configure_t<FMT, BB, false, 2, false, MM>(smem_optin);
+    if constexpr (M == 1) {
+        XQ_CFG(1, 1)
+        if (e == cudaSuccess) e = configure_t<FMT, 1, false, 0, true>(smem_optin);
+    }
+    XQ_CFG(2, M)
+    XQ_CFG(3, M)
+    XQ_CFG(4, M)
+    XQ_CFG(5, M)
+    XQ_CFG(6, M)
+    XQ_CFG(7, M)
+    XQ_CFG(8, M)
 #undef XQ_CFG
-    if (e == cudaSuccess) e = configure_t<FMT, 1, false, 0, true>(smem_optin);
     return e;
 }
 

@@ -8,9 +8,9 @@ namespace xq {
 
 cudaError_t launch_matvec_cb4r(const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,
                                size_t smem, cudaStream_t s) {
-    return launch_matvec_fmt<kCB4R>(a, batch, kind, grid, block, smem, s);
+    return launch_matvec_fmt<kCB4R, 1>(a, batch, kind, grid, block, smem, s);
 }
 
-cudaError_t configure_matvec_cb4r(int smem_optin) { return configure_fmt<kCB4R>(smem_optin); }
+cudaError_t configure_matvec_cb4r(int smem_optin) { return configure_fmt<kCB4R, 1>(smem_optin); }
 
 }  // namespace xq

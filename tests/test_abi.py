@@ -155,28 +155,44 @@ def test_status_strings(raw):
     assert raw.xq_version() == 1
 
 
-@pytest.mark.parametrize("fmt,rows,cols,batch,warps,grid,R,spr,launches", [
-    ("q4k", 128256, 4096, 1, 16, 152, 2, 1, 1), ("q4k", 128256, 4096, 8, 8, 152, 2, 1, 1),
-    ("q4k", 4096, 4096, 1, 14, 152, 2, 1, 1), ("q4k", 14336, 4096, 4, 8, 152, 2, 1, 1),
-    ("q4k", 4096, 14336, 1, 16, 152, 1, 2, 1), ("q4k", 4096, 14336, 8, 8, 152, 1, 2, 1),
-    ("q4k", 256, 1024, 1, 1, 32, 8, 1, 1), ("cb4", 11008, 4096, 1, 16, 152, 2, 1, 1),
-    ("cb4", 4096, 4096, 1, 14, 152, 2, 1, 1), ("q4k", 33, 256, 2, 1, 2, 32, 1, 1),
-    ("q4k", 1, 512, 1, 1, 1, 16, 1, 1), ("q4k", 100, 2304, 1, 1, 100, 1, 1, 1),
-    ("q4k", 1000, 65536, 8, 6, 152, 1, 8, 4)])
-def test_plan(lib, fmt, rows, cols, batch, warps, grid, R, spr, launches):
+@pytest.mark.parametrize("fmt,rows,cols,batch,warps,grid,R,spr,launches,M", [
+    ("q4k", 128256, 4096, 1, 16, 152, 2, 1, 1, 1), ("q4k", 128256, 4096, 8, 8, 152, 2, 1, 1, 2),
+    ("q4k", 4096, 4096, 1, 14, 152, 2, 1, 1, 1), ("q4k", 14336, 4096, 4, 8, 152, 2, 1, 1, 2),
+    ("q4k", 4096, 14336, 1, 16, 152, 1, 2, 1, 1), ("q4k", 4096, 14336, 8, 8, 152, 1, 2, 1, 1),
+    ("q4k", 4096, 14336, 4, 8, 152, 1, 2, 1, 2),
+    ("q4k", 256, 1024, 1, 1, 32, 8, 1, 1, 1), ("cb4", 11008, 4096, 1, 16, 152, 2, 1, 1, 1),
+    ("cb4", 4096, 4096, 1, 14, 152, 2, 1, 1, 1), ("q4k", 33, 256, 2, 1, 1, 32, 1, 1, 2),
+    ("q4k", 1, 512, 1, 1, 1, 16, 1, 1, 1), ("q4k", 100, 2304, 1, 1, 100, 1, 1, 1, 1),
+    ("q4k", 1000, 65536, 8, 6, 152, 1, 8, 4, 1), ("cb4", 14336, 4096, 8, 8, 152, 2, 1, 1, 1),
+    ("cb4r", 300, 2304, 2, 2, 152, 1, 1, 1, 1)])
+def test_plan(lib, fmt, rows, cols, batch, warps, grid, R, spr, launches, M):
     p = lib.plan_matvec(rows, cols, batch, fmt=fmt, sm_count=152, smem_optin=232448)
-    assert (p["warps"], p["grid"], p["rows_per_group"], p["segments"], p["launches"]) == \
-        (warps, grid, R, spr, launches), p
+    assert (p["warps"], p["grid"], p["rows_per_group"], p["segments"], p["launches"],
+            p["row_block"]) == (warps, grid, R, spr, launches, M), p
     nb = cols // 256
     assert p["chunks_per_row"] == nb
     assert p["groups"] == -(-rows // R)
+    assert p["grid"] == min(-(-p["groups"] // M), 152)
     # a work unit is whole rows in one 4608-byte box, or one row in 32-chunk boxes
     assert (R > 1 and R * nb == 32 and spr == 1) or (R == 1 and spr == -(-nb // 32))
     assert p["stages"] == 2
     act = -(-p["batch_per_launch"] * nb * 336 // 128) * 128
-    assert p["smem_bytes"] == act + p["warps"] * p["stages"] * 4608 + 128
+    assert p["smem_bytes"] == act + p["warps"] * p["stages"] * M * 4608 + 128
     assert p["smem_bytes"] <= 232448
     assert p["batch_per_launch"] * (p["launches"] - 1) < batch <= p["batch_per_launch"] * p["launches"]
+
+
+def test_row_block_override(lib):
+    try:
+        lib.set_row_block_override(1)
+        p = lib.plan_matvec(128256, 4096, 8)
+        assert p["row_block"] == 1 and p["warps"] == 8 and p["grid"] == 152
+        lib.set_row_block_override(2)
+        assert lib.plan_matvec(128256, 4096, 1)["row_block"] == 1  # batch 1 has one
+        assert lib.plan_matvec(4096, 4096, 2, fmt="cb4")["row_block"] == 1
+    finally:
+        lib.set_row_block_override(0)
+    assert lib.plan_matvec(128256, 4096, 8)["row_block"] == 2
 
 
 def test_plan_override_is_clamped(lib):

@@ -199,7 +199,9 @@ def test_config5_sampled(xq, orc, name):
     assert np.array_equal(xq_dev.cpu().numpy(), xq_ref)
     y = run_matvec(xq, "q4k", W, None, xq_dev, c.rows, c.cols, c.batch)
     plan = xq.last_plan()
-    assert plan["grid"] == min(plan["groups"], torch.cuda.get_device_properties(0).multi_processor_count)
+    units = -(-plan["groups"] // plan["row_block"])
+    assert plan["grid"] == min(units, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["row_block"] == (2 if c.batch >= 2 else 1)
     rng = np.random.Generator(np.random.PCG64(5))
     sample = np.unique(np.concatenate([np.arange(64), np.arange(c.rows - 70, c.rows),
                                        rng.choice(c.rows, 1500, replace=False)]))
@@ -291,12 +293,14 @@ def test_plan_overrides_agree(xq, orc, warps, stages):
     xq_ref = orc.quantize_q8(x)
     try:
         xq.set_plan_override(warps, stages)
+        xq.set_row_block_override(1)  # one row group per unit: every split fits
         dots = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch, dots=True)
         y = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch)
         p = xq.last_plan()
         assert p["warps"] == warps and p["stages"] == stages
     finally:
         xq.set_plan_override(0, 0)
+        xq.set_row_block_override(0)
     assert np.array_equal(dots, orc.subdots_q4k(W, xq_ref, rows, cols, batch))
     check_y(y, orc.matvec_q4k(W, xq_ref, rows, cols, batch), f"override {warps}x{stages}")
 
@@ -542,3 +546,41 @@ def test_side_stream_and_graph_replay(xq, orc):
 
 def test_device_status_clean(xq):
     assert xq.device_status(clear=False) == 0
+
+
+# ---------------------------------------------------------------- row blocking
+@pytest.mark.parametrize("rows,cols,batch", [(33, 256, 2), (31, 1024, 3), (77, 4096, 8),
+                                             (101, 4096, 2), (9, 14336, 4), (64, 14336, 8),
+                                             (64, 14336, 4),
+                                             (5, 2304, 5), (3, 32768, 2)])
+def test_row_block_is_bit_identical(xq, orc, rows, cols, batch):
+    """Two row groups per warp unit (the automatic plan for Q4_K at batch >= 2)
+    and one give the same dots and the same y bits, fused or not: only which
+    warp handles a chunk differs.  Odd group counts leave a half unit."""
+    W = synthetic.q4k_weights(rows, cols, 3 * rows + cols)
+    x = synthetic.activations(batch, cols, rows + 5, outlier_frac=0.001)
+    xq_dev = run_quantize(xq, x)
+    Wd, xd = dev(W), dev(x)
+    out = {}
+    try:
+        for rb in (1, 0):
+            xq.set_row_block_override(rb)
+            dots = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch, dots=True)
+            y = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch)
+            p = xq.last_plan()
+            y_lin = xq.linear_q4k(xd, Wd, rows, cols).cpu().numpy()
+            y_nl = xq.norm_linear_q4k(xd, Wd, rows, cols).cpu().numpy()
+            out[rb] = (p["row_block"], dots, y, y_lin, y_nl)
+    finally:
+        xq.set_row_block_override(0)
+    props = torch.cuda.get_device_properties(0)
+    auto = xq.plan_matvec(rows, cols, batch, sm_count=props.multi_processor_count,
+                          smem_optin=props.shared_memory_per_block_optin)["row_block"]
+    assert out[1][0] == 1 and out[0][0] == auto
+    # eight warps of two row groups do not fit beside the activations of these two
+    assert auto == (1 if (rows, cols, batch) in ((64, 14336, 8), (3, 32768, 2)) else 2)
+    for a, b in zip(out[1][1:], out[0][1:]):
+        assert np.array_equal(a, b)
+    xq_ref = orc.quantize_q8(x)
+    assert np.array_equal(out[0][1], orc.subdots_q4k(W, xq_ref, rows, cols, batch))
+    check_y(out[0][2], orc.matvec_q4k(W, xq_ref, rows, cols, batch), "row block")
