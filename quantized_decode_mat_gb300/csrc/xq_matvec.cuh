@@ -53,9 +53,11 @@ __device__ __forceinline__ uint4 split_sums(uint4 s0, uint4 s1) {
 
 // ---- shared epilogue --------------------------------------------------------
 // Adds xs*(d*S1 - dmin*S2) to (hi, lo).  S1, S2 exact integers; |S2| < 2^24;
-// S1 is split into its f32 rounding and an exact residual.
+// S1 is split into its f32 rounding and an exact residual.  first: (hi, lo)
+// holds nothing yet, so the first compensated add (of t1 to zero, which
+// yields t1 and a zero error term exactly) is a plain assignment.
 __device__ __forceinline__ void q4k_epilogue(float xs, float d, float dmin, int S1, int S2,
-                                             float &hi, float &lo) {
+                                             float &hi, float &lo, bool first) {
     float ph, pl, qh, ql;
     two_prod(xs, d, ph, pl);        // xs*d    = ph + pl exactly
     two_prod(xs, dmin, qh, ql);     // xs*dmin = qh + ql exactly
@@ -68,7 +70,12 @@ __device__ __forceinline__ void q4k_epilogue(float xs, float d, float dmin, int 
     // second-order terms, each below 2^-23 of the main ones
     float small = __fmaf_rn(pl, f1, __fmaf_rn(ph, r1, __fadd_rn(e1, e2)));
     small = __fmaf_rn(-ql, f2, small);
-    acc_add(hi, lo, t1, 0.0f);
+    if (first) {
+        hi = t1;
+        lo = 0.0f;
+    } else {
+        acc_add(hi, lo, t1, 0.0f);
+    }
     acc_add(hi, lo, t2, small);
 }
 
@@ -81,7 +88,7 @@ __device__ __forceinline__ int byte_of(uint32_t x, int k) {
 template <int B, bool DOTS, class Act>
 __device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w, const Act &act,
                                           float (&hi)[B], float (&lo)[B], int32_t *dots,
-                                          int64_t dots_bstride) {
+                                          int64_t dots_bstride, bool first) {
     const uint4 h = *reinterpret_cast<const uint4 *>(w);
     uint32_t q[32];
 #pragma unroll
@@ -134,7 +141,7 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w, const A
         const uint4 sp = act.split(b);  // sum_j m_j * bsum_j as four byte dots
         const int S2 = dp4a_uu(m_hi, sp.y, dp4a_uu(m_lo, sp.x, 0)) +
                        256 * dp4a_us(m_hi, sp.w, dp4a_us(m_lo, sp.z, 0));
-        q4k_epilogue(act.xs(b), d, dmin, S1, S2, hi[b], lo[b]);
+        q4k_epilogue(act.xs(b), d, dmin, S1, S2, hi[b], lo[b], first);
         if (DOTS && dots != nullptr) {
             int4 *o = reinterpret_cast<int4 *>(dots + b * dots_bstride);
             o[0] = make_int4(dot[0], dot[1], dot[2], dot[3]);
@@ -147,15 +154,16 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w, const A
 // The same arithmetic as q4k_chunk for M chunks that share one column (lane
 // l's chunk in each of M row groups): every activation load from shared
 // memory is used against M chunks instead of one.  The loop runs over the four
-// 64-value groups, then the vectors, then the chunks; each 8-term dot is two
-// independent 4-term chains.  S1 is an exact integer and each (chunk, vector)
+// 64-value groups, then the vectors, then the chunks.  S1 is an exact
+// integer and each (chunk, vector)
 // epilogue is the single-chunk one, so y is bit-for-bit that of the one-chunk
 // form.  ok[m] false: chunk m is not accumulated and its dots are not stored
 // (its shared-memory bytes may be stale).
 template <int B, int M, bool DOTS, class Act>
 __device__ __forceinline__ void q4k_chunks(const uint8_t *const (&w)[M], const bool (&ok)[M],
                                            const Act &act, float (&hi)[M][B], float (&lo)[M][B],
-                                           int32_t *const (&dots)[M], int64_t dots_bstride) {
+                                           int32_t *const (&dots)[M], int64_t dots_bstride,
+                                           bool first) {
     float d[M], dmin[M];
     uint32_t sc_lo[M], sc_hi[M], m_lo[M], m_hi[M];
 #pragma unroll
@@ -200,16 +208,13 @@ __device__ __forceinline__ void q4k_chunks(const uint8_t *const (&w)[M], const b
             const uint32_t ahi[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-                int l0 = 0, l1 = 0, h0 = 0, h1 = 0;
+                int d0 = 0, d1 = 0;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    l0 = dp4a(ql[m][k], alo[k], l0);
-                    l1 = dp4a(ql[m][k + 4], alo[k + 4], l1);
-                    h0 = dp4a_us(qh[m][k], ahi[k], h0);
-                    h1 = dp4a_us(qh[m][k + 4], ahi[k + 4], h1);
+                for (int k = 0; k < 8; ++k) {
+                    d0 = dp4a(ql[m][k], alo[k], d0);
+                    d1 = dp4a_us(qh[m][k], ahi[k], d1);
                 }
-                const int d0 = l0 + l1;
-                const int d1 = (h0 + h1) >> 4;  // high nibbles were used in place (x16)
+                d1 >>= 4;  // high nibbles were used in place (x16)
                 S1[m][b] += s0[m] * d0 + s1[m] * d1;
                 if (DOTS && ok[m])
                     *reinterpret_cast<int2 *>(dots[m] + b * dots_bstride + 2 * g) = make_int2(d0, d1);
@@ -224,7 +229,7 @@ __device__ __forceinline__ void q4k_chunks(const uint8_t *const (&w)[M], const b
         for (int m = 0; m < M; ++m) {
             const int S2 = dp4a_uu(m_hi[m], sp.y, dp4a_uu(m_lo[m], sp.x, 0)) +
                            256 * dp4a_us(m_hi[m], sp.w, dp4a_us(m_lo[m], sp.z, 0));
-            if (ok[m]) q4k_epilogue(xs, d[m], dmin[m], S1[m][b], S2, hi[m][b], lo[m][b]);
+            if (ok[m]) q4k_epilogue(xs, d[m], dmin[m], S1[m][b], S2, hi[m][b], lo[m][b], first);
         }
     }
 }
@@ -709,13 +714,13 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
                     any |= ok[m];
                     dp[m] = DOTS && ok[m] ? a.dots + (gi[m].row0 + rig) * dots_row + c * 8 : nullptr;
                 }
-                if (any) q4k_chunks<B, M, DOTS>(w, ok, as, hi, lo, dp, dots_bstride);
+                if (any) q4k_chunks<B, M, DOTS>(w, ok, as, hi, lo, dp, dots_bstride, s == 0);
             } else {
                 const bool ok = rig < gi[0].valid && c < nb && !gi[0].bad;
                 if (ok) {
                     int32_t *dp = DOTS ? a.dots + (gi[0].row0 + rig) * dots_row + c * 8 : nullptr;
                     if (FMT == kQ4K)
-                        q4k_chunk<B, DOTS>(st, as, hi[0], lo[0], dp, dots_bstride);
+                        q4k_chunk<B, DOTS>(st, as, hi[0], lo[0], dp, dots_bstride, s == 0);
                     else if (FMT == kCB4)
                         cb4_chunk<B, DOTS>(st, as, T, hi[0], lo[0], dp, dots_bstride);
                     else
