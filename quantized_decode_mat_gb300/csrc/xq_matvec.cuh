@@ -235,68 +235,83 @@ __device__ __forceinline__ void q4k_chunks(const uint8_t *const (&w)[M], const b
 }
 
 // ---- codebook chunk -----------------------------------------------------------------
-// Eight nibbles of a payload word -> two words of int8 codebook values, LO for
-// the low nibbles (bytes in order) and HI for the high nibbles.  The table is
-// four registers; prmt looks up 8 entries at a time, so two lookups per half
-// table plus a byte select on nibble bit 3, then a byte shuffle that
-// separates low and high nibbles.  Exact by construction.
-__device__ __forceinline__ void cb4_decode(uint32_t q, const uint32_t (&T)[4], uint32_t &LO,
-                                           uint32_t &HI) {
-    const uint32_t s = q & 0x77777777u;     // entry index within a half table
+// The codebook kernels stage each 32-value sub-block of the activation
+// interleaved: word 2i holds values (4i, 4i+16, 4i+1, 4i+17) and word 2i+1
+// values (4i+2, 4i+18, 4i+3, 4i+19), i = 0..3 -- the order in which the
+// nibbles of payload word i sit (byte j: low nibble = element 4i+j, high
+// nibble = element 4i+j+16).  A decoded payload word then dots with two
+// activation words as it is.  (Sums are order-free, so the dots are those of
+// the natural order.)
+__device__ __forceinline__ uint32_t interleave_lo(uint32_t a, uint32_t b) {
+    return __byte_perm(a, b, 0x5140u);  // a.0 b.0 a.1 b.1
+}
+__device__ __forceinline__ uint32_t interleave_hi(uint32_t a, uint32_t b) {
+    return __byte_perm(a, b, 0x7362u);  // a.2 b.2 a.3 b.3
+}
+
+// Eight nibbles of a payload word -> two words of int8 codebook values in
+// nibble order: F0 = kv of nibbles 0..3 (L0, H0, L1, H1), F1 = of nibbles
+// 4..7.  The table is four registers.  prmt looks up 8 entries at a time,
+// so each nibble is looked up in both half tables with its low three bits,
+// and a byte mask made from its bit 3 (prmt's sign-replicate mode on the
+// byte whose top bit it is) selects the half.  Exact by construction.
+__device__ __forceinline__ void cb4_decode(uint32_t q, const uint32_t (&T)[4], uint32_t &F0,
+                                           uint32_t &F1) {
+    const uint32_t s = q & 0x77777777u;  // entry index within a half table
     const uint32_t sh = s >> 16;
-    const uint32_t a0 = __byte_perm(T[0], T[1], s);   // kv[0..7] at nibbles 0..3
-    const uint32_t a1 = __byte_perm(T[0], T[1], sh);  // kv[0..7] at nibbles 4..7
+    const uint32_t a0 = __byte_perm(T[0], T[1], s);   // kv[0..7] for nibbles 0..3
+    const uint32_t a1 = __byte_perm(T[0], T[1], sh);  // ... nibbles 4..7
     const uint32_t b0 = __byte_perm(T[2], T[3], s);   // kv[8..15]
     const uint32_t b1 = __byte_perm(T[2], T[3], sh);
-    // byte n of f0 = kv[nibble n of q] (n = 0..3: L0, H0, L1, H1)
-    const uint32_t f0 = __byte_perm(a0, b0, ((q >> 1) & 0x4444u) | 0x3210u);
-    const uint32_t f1 = __byte_perm(a1, b1, ((q >> 17) & 0x4444u) | 0x3210u);
-    LO = __byte_perm(f0, f1, 0x6420u);  // kv[L0], kv[L1], kv[L2], kv[L3]
-    HI = __byte_perm(f0, f1, 0x7531u);  // kv[H0], kv[H1], kv[H2], kv[H3]
+    // bit 3 of an even nibble is the top bit of its byte in q << 4, of an
+    // odd nibble the top bit of its byte in q; selector 8+j replicates it
+    const uint32_t q4 = q << 4;
+    const uint32_t m0 = prmt_sign(q4, q, 0xD9C8u);  // nibbles 0..3
+    const uint32_t m1 = prmt_sign(q4, q, 0xFBEAu);  // nibbles 4..7
+    F0 = (a0 & ~m0) | (b0 & m0);
+    F1 = (a1 & ~m1) | (b1 & m1);
 }
 
 // Eight codebook blocks of one chunk: scales dk[k] and payload words P[k][0..3]
-// (block k's 16 payload bytes, little-endian), against q8 block `act`.
+// (block k's 16 payload bytes, little-endian), against the interleaved q8
+// block `act`.  Block by block: decode, then its dot with every vector; per
+// vector the compensated sum over the blocks runs in block order.
 template <int B, bool DOTS, class Act>
 __device__ __forceinline__ void cb4_blocks(const float (&dk)[8], const uint32_t (&P)[8][4],
                                            const Act &act, const uint32_t (&T)[4], float (&hi)[B],
                                            float (&lo)[B], int32_t *dots, int64_t dots_bstride) {
-    uint32_t LO[8][4], HI[8][4];
+    float ch[B], cl[B];  // sum_k d_k * dot_k per vector, compensated
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
+    for (int b = 0; b < B; ++b) ch[b] = cl[b] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cb4_decode(P[k][i], T, LO[k][i], HI[k][i]);
+    for (int k = 0; k < 8; ++k) {
+        uint32_t F[8];
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-        float ch = 0.0f, cl = 0.0f;  // sum_k d_k * dot_k, compensated
-        int dts[8];
+        for (int i = 0; i < 4; ++i) cb4_decode(P[k][i], T, F[2 * i], F[2 * i + 1]);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            // block k: elements 0..15 against values 32k..32k+15, 16..31 against 32k+16..
+        for (int b = 0; b < B; ++b) {
             const uint4 a0 = act.q16(b, 2 * k), a1 = act.q16(b, 2 * k + 1);
             int dt = 0;
-            dt = dp4a(LO[k][0], a0.x, dt);
-            dt = dp4a(LO[k][1], a0.y, dt);
-            dt = dp4a(LO[k][2], a0.z, dt);
-            dt = dp4a(LO[k][3], a0.w, dt);
-            dt = dp4a(HI[k][0], a1.x, dt);
-            dt = dp4a(HI[k][1], a1.y, dt);
-            dt = dp4a(HI[k][2], a1.z, dt);
-            dt = dp4a(HI[k][3], a1.w, dt);
-            dts[k] = dt;
+            dt = dp4a(F[0], a0.x, dt);
+            dt = dp4a(F[1], a0.y, dt);
+            dt = dp4a(F[2], a0.z, dt);
+            dt = dp4a(F[3], a0.w, dt);
+            dt = dp4a(F[4], a1.x, dt);
+            dt = dp4a(F[5], a1.y, dt);
+            dt = dp4a(F[6], a1.z, dt);
+            dt = dp4a(F[7], a1.w, dt);
             float p, e;
             two_prod(dk[k], __int2float_rn(dt), p, e);  // |dt| < 2^20: exact in f32
-            acc_add(ch, cl, p, e);
+            acc_add(ch[b], cl[b], p, e);
+            if (DOTS && dots != nullptr) dots[b * dots_bstride + k] = dt;
         }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
         const float xs = act.xs(b);
         float t, te;
-        two_prod(ch, xs, t, te);
-        acc_add(hi[b], lo[b], t, __fmaf_rn(cl, xs, te));
-        if (DOTS && dots != nullptr) {
-            int4 *o = reinterpret_cast<int4 *>(dots + b * dots_bstride);
-            o[0] = make_int4(dts[0], dts[1], dts[2], dts[3]);
-            o[1] = make_int4(dts[4], dts[5], dts[6], dts[7]);
-        }
+        two_prod(ch[b], xs, t, te);
+        acc_add(hi[b], lo[b], t, __fmaf_rn(cl[b], xs, te));
     }
 }
 
@@ -647,7 +662,21 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
                 }
                 const Q8Lane r = q8_quantize_lane(vals);
                 uint8_t *dst = act + blk * kActStride;
-                *reinterpret_cast<uint2 *>(dst + lane * 8) = make_uint2(r.w0, r.w1);
+                if (FMT == kQ4K) {
+                    *reinterpret_cast<uint2 *>(dst + lane * 8) = make_uint2(r.w0, r.w1);
+                } else {
+                    // interleaved order: lane 4k+j writes words 2j, 2j+1 of
+                    // sub-block k, made of its words j and j+4 (lanes 4k + j/2
+                    // and 4k + 2 + j/2 hold them)
+                    const int j = lane & 3, src = (lane & ~3) + (j >> 1);
+                    const uint32_t v0 = __shfl_sync(0xffffffffu, r.w0, src);
+                    const uint32_t v1 = __shfl_sync(0xffffffffu, r.w1, src);
+                    const uint32_t u0 = __shfl_sync(0xffffffffu, r.w0, src + 2);
+                    const uint32_t u1 = __shfl_sync(0xffffffffu, r.w1, src + 2);
+                    const uint32_t wa = (j & 1) ? v1 : v0, wb = (j & 1) ? u1 : u0;
+                    *reinterpret_cast<uint2 *>(dst + lane * 8) =
+                        make_uint2(interleave_lo(wa, wb), interleave_hi(wa, wb));
+                }
                 if ((lane & 3) == 0) *reinterpret_cast<int *>(dst + kQ8SumAt + (lane >> 2) * 4) = r.sum;
                 uint32_t sums[8];
 #pragma unroll
@@ -660,13 +689,32 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
                 }
             }
         }
-    } else {
+    } else if (FMT == kQ4K) {
         // bytes 0..303 of every q8 block, then its split sums
         for (int i = threadIdx.x; i < nvec * nb * 20; i += blockDim.x) {
             const int blk = i / 20, piece = i - 20 * blk;
             const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
             *reinterpret_cast<uint4 *>(act + blk * kActStride + 16 * piece) =
                 piece < 19 ? __ldg(src + piece) : split_sums(__ldg(src + 16), __ldg(src + 17));
+        }
+    } else {
+        // the values of every q8 block in interleaved order (one 32-value
+        // sub-block an item), then bytes 256..303
+        for (int i = threadIdx.x; i < nvec * nb * 11; i += blockDim.x) {
+            const int blk = i / 11, part = i - 11 * blk;
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
+            uint4 *dst = reinterpret_cast<uint4 *>(act + blk * kActStride);
+            if (part < 8) {
+                const uint4 x0 = __ldg(src + 2 * part), x1 = __ldg(src + 2 * part + 1);
+                const uint32_t in[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                dst[2 * part] = make_uint4(interleave_lo(in[0], in[4]), interleave_hi(in[0], in[4]),
+                                           interleave_lo(in[1], in[5]), interleave_hi(in[1], in[5]));
+                dst[2 * part + 1] =
+                    make_uint4(interleave_lo(in[2], in[6]), interleave_hi(in[2], in[6]),
+                               interleave_lo(in[3], in[7]), interleave_hi(in[3], in[7]));
+            } else {
+                dst[8 + part] = __ldg(src + 8 + part);  // pieces 16..18
+            }
         }
     }
     __syncthreads();
