@@ -540,8 +540,9 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
 #pragma unroll
         for (int k = 0; k < 9; ++k) {
             if (R > 1) {
-                const int q = lane + 32 * k, rp = 9 * nb;  // pieces per resident row
-                const int rig = q / rp, r = q - rig * rp;
+                // pieces per resident row: 9 * nb, nb a power of two here
+                const int q = lane + 32 * k, rp = 9 * nb;
+                const int rig = (q >> (31 - __clz(nb))) / 9, r = q - rig * rp;
                 dmap[k] = r < nb ? cb4r_scale_slot(rig * nb + r)
                                  : cb4r_payload_slot(rig * nb + ((r - nb) >> 3), (r - nb) & 7);
             } else {
