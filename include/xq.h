@@ -119,6 +119,34 @@ xq_status xq_linear_q4k(const float *x, const void *W, float *y, int64_t rows, i
 xq_status xq_linear_cb4(const float *x, const void *W, const int8_t *table, float *y,
                         int64_t rows, int64_t cols, int64_t batch, void *stream);
 
+/* The decode step with a caller workspace.  It computes what xq_linear_q4k /
+ * _cb4 / _cb4r compute, bit for bit, and picks how by the shape
+ * (xq_plan.quantise_once):
+ *   - small activations: the one fused launch, where every CTA quantises the
+ *     activation into its own shared memory (the workspace is not touched);
+ *   - wide or batched activations (at least 32 q8 blocks a launch): the
+ *     activation is quantised once, by xq_quantize_q8's kernel, into the
+ *     workspace, and the mat-vec reads those q8 blocks.  Every CTA
+ *     re-quantising the whole activation costs more than the second launch
+ *     there (measured on GB300: 4096 x 14336 at batch 8, 58.4 us fused against
+ *     34.9 us).
+ * ws: DEVICE scratch of at least xq_linear_workspace_bytes(cols, batch) bytes
+ * (= xq_q8_bytes(cols, batch)), 16-byte aligned, not overlapping x, W or y;
+ * its contents on entry do not matter; on return it holds the q8 blocks of
+ * the last launch's vectors or is untouched.  Calls that share a workspace
+ * must not overlap on the GPU.  Source: "25 - Writing XPU Kernels" 25.2
+ * (quantise the activation once per call) and 25.5 (fuse where it removes
+ * work, not only launches). */
+size_t xq_linear_workspace_bytes(int64_t cols, int64_t batch);
+xq_status xq_linear_q4k_ws(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
+                           int64_t batch, void *ws, size_t ws_bytes, void *stream);
+xq_status xq_linear_cb4_ws(const float *x, const void *W, const int8_t *table, float *y,
+                           int64_t rows, int64_t cols, int64_t batch, void *ws, size_t ws_bytes,
+                           void *stream);
+xq_status xq_linear_cb4r_ws(const float *x, const void *Wr, const int8_t *table, float *y,
+                            int64_t rows, int64_t cols, int64_t batch, void *ws, size_t ws_bytes,
+                            void *stream);
+
 /* RMSNorm + q8 pack, the producer of the next layer's activation blocks:
  * for each of the batch vectors x_b ([batch][cols] f32, device),
  *   scale_b = 1 / sqrt(sum_i x_{b,i}^2 / cols + 1e-5),  y_b = x_b * scale_b,
@@ -231,7 +259,11 @@ enum { XQ_FORMAT_Q4K = 0, XQ_FORMAT_CB4 = 1, XQ_FORMAT_CB4R = 2 };
  * Each of the `warps` warps of the `grid` persistent CTAs keeps stages-1
  * stages in flight.  The batch's q8 blocks are staged in shared memory; if
  * they do not fit, each call makes `launches` launches of batch_per_launch
- * vectors (each re-reads W). */
+ * vectors (each re-reads W).  quantise_once: 1 if the decode step with a
+ * workspace (xq_linear_q4k_ws) quantises the activation once, in a launch of
+ * its own, 0 if every CTA of the fused launch quantises it for itself;
+ * xq_plan_matvec reports that step's choice, and the other entry points
+ * ignore the field. */
 typedef struct {
     int32_t warps;
     int32_t stages;
@@ -244,6 +276,7 @@ typedef struct {
     int32_t launches;
     int64_t smem_bytes;
     int32_t row_block;
+    int32_t quantise_once;
 } xq_plan;
 
 xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t batch,
@@ -256,6 +289,10 @@ void xq_set_plan_override(int32_t warps, int32_t stages);
  * automatic plan would use 2 (Q4_K at batch >= 2); 0 = automatic.
  * Process-wide, for sweeps and tests, like xq_set_plan_override. */
 void xq_set_row_block_override(int32_t row_block);
+/* Override the choice of the decode step with a workspace: 1 = every CTA
+ * quantises the activation, 2 = quantise once into the workspace, 0 =
+ * automatic.  Process-wide, for sweeps and tests. */
+void xq_set_quantise_once_override(int32_t mode);
 /* Plan used by the calling thread's last mat-vec or sub-dot launch. */
 xq_status xq_last_plan(xq_plan *plan);
 
@@ -279,7 +316,8 @@ enum {
     XQ_COUNT_LINEAR_CB4R = 15,
     XQ_COUNT_NORM_LINEAR_CB4R = 16,
     XQ_COUNT_MATVEC_ID_CB4R = 17,
-    XQ_COUNT_N = 18
+    XQ_COUNT_QUANTISE_ONCE = 18,
+    XQ_COUNT_N = 19
 };
 uint64_t xq_launch_count(int32_t which);
 

@@ -9,6 +9,7 @@ fallback: if the library is missing this package raises on import.
     y   = matvec_q4k(W, xq, rows, cols)        # W: uint8 Q4_K rows on cuda
     y   = matvec_cb4(W, table, xq, rows, cols) # W: uint8 codebook rows
     y   = linear_q4k(x, W, rows, cols)         # fused: quantise + mat-vec, one launch
+    y   = linear_ws("q4k", x, W, rows, cols, ws)  # the same, quantising once (workspace)
     xq  = rmsnorm_q8(x)                        # RMSNorm + q8 pack of the next input
     y   = norm_linear_q4k(x, W, rows, cols)    # fused: RMSNorm + quantise + mat-vec
     Wr  = repack_cb4(W, rows, cols)            # codebook rows -> resident rows
@@ -34,6 +35,7 @@ from ._native import (  # noqa: F401
     COUNT_LINEAR_CB4R,
     COUNT_NORM_LINEAR_CB4R,
     COUNT_MATVEC_ID_CB4R,
+    COUNT_QUANTISE_ONCE,
     COUNT_RMSNORM_Q8,
     COUNT_SUBDOTS_CB4,
     COUNT_SUBDOTS_Q4K,
@@ -51,6 +53,8 @@ from ._native import (  # noqa: F401
     lib_path,
     linear_cb4,
     linear_q4k,
+    linear_workspace_bytes,
+    linear_ws,
     matvec_cb4,
     matvec_id,
     matvec_q4k,
@@ -63,6 +67,7 @@ from ._native import (  # noqa: F401
     rmsnorm_q8,
     set_plan_override,
     set_row_block_override,
+    set_quantise_once_override,
     subdots_cb4,
     subdots_q4k,
 )

@@ -25,7 +25,8 @@ class _Plan(ctypes.Structure):
                 ("rows_per_group", ctypes.c_int32), ("segments", ctypes.c_int32),
                 ("chunks_per_row", ctypes.c_int32), ("groups", ctypes.c_int64),
                 ("batch_per_launch", ctypes.c_int32), ("launches", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int64), ("row_block", ctypes.c_int32)]
+                ("smem_bytes", ctypes.c_int64), ("row_block", ctypes.c_int32),
+                ("quantise_once", ctypes.c_int32)]
 
 
 def _sig(name, restype, argtypes):
@@ -60,6 +61,14 @@ _norm_linear_cb4r = _sig("xq_norm_linear_cb4r", ctypes.c_int,
 _matvec_cb4r_id = _sig("xq_matvec_cb4r_id", ctypes.c_int,
                        [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P])
 _subdots_cb4r = _sig("xq_subdots_cb4r", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
+_linear_ws_bytes = _sig("xq_linear_workspace_bytes", _SZ, [_I64, _I64])
+_linear_q4k_ws = _sig("xq_linear_q4k_ws", ctypes.c_int,
+                      [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P])
+_linear_cb4_ws = _sig("xq_linear_cb4_ws", ctypes.c_int,
+                      [_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P])
+_linear_cb4r_ws = _sig("xq_linear_cb4r_ws", ctypes.c_int,
+                       [_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P])
+_set_qonce = _sig("xq_set_quantise_once_override", None, [_I32])
 _subdots_q4k = _sig("xq_subdots_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
 _subdots_cb4 = _sig("xq_subdots_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
 _plan = _sig("xq_plan_matvec", ctypes.c_int, [_I32, _I64, _I64, _I64, _I32, _I64,
@@ -78,8 +87,8 @@ _version = _sig("xq_version", _I32, [])
  COUNT_LINEAR_Q4K, COUNT_LINEAR_CB4, COUNT_MATVEC_ID_Q4K, COUNT_MATVEC_ID_CB4,
  COUNT_RMSNORM_Q8, COUNT_NORM_LINEAR_Q4K, COUNT_NORM_LINEAR_CB4, COUNT_REPACK_CB4,
  COUNT_MATVEC_CB4R, COUNT_SUBDOTS_CB4R, COUNT_LINEAR_CB4R, COUNT_NORM_LINEAR_CB4R,
- COUNT_MATVEC_ID_CB4R) = range(18)
-COUNT_N = 18
+ COUNT_MATVEC_ID_CB4R, COUNT_QUANTISE_ONCE) = range(19)
+COUNT_N = 19
 
 
 class XQError(RuntimeError):
@@ -210,6 +219,42 @@ def linear_cb4(x: torch.Tensor, W: torch.Tensor, table, rows: int, cols: int,
                        ctypes.cast(_table(table), _P), _dev(out, "y", torch.float32), rows,
                        cols, batch, _stream(stream)))
     return out
+
+
+def linear_workspace_bytes(cols: int, batch: int = 1) -> int:
+    return int(_linear_ws_bytes(cols, batch))
+
+
+def linear_ws(fmt: str, x: torch.Tensor, W: torch.Tensor, rows: int, cols: int,
+              ws: torch.Tensor, table=None, out: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """The fused decode step with a caller workspace ``ws`` (uint8, CUDA, at
+    least linear_workspace_bytes(cols, batch) bytes): the same y as
+    linear_q4k / linear_cb4 / linear_cb4r, with the activation quantised once
+    across the grid when the plan says so.  fmt: "q4k", "cb4" or "cb4r"."""
+    x = _x2d(x)
+    batch = x.shape[0]
+    if x.shape[1] != cols:
+        raise ValueError("x has the wrong number of columns")
+    if out is None:
+        out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    xp, Wp, yp = _dev(x, "x", torch.float32), _dev(W, "W", torch.uint8), _dev(out, "y", torch.float32)
+    wp, nbytes = _dev(ws, "ws", torch.uint8), ws.numel()
+    if fmt == "q4k":
+        st = _linear_q4k_ws(xp, Wp, yp, rows, cols, batch, wp, nbytes, _stream(stream))
+    elif fmt in ("cb4", "cb4r"):
+        fn = _linear_cb4_ws if fmt == "cb4" else _linear_cb4r_ws
+        st = fn(xp, Wp, ctypes.cast(_table(table), _P), yp, rows, cols, batch, wp, nbytes,
+                _stream(stream))
+    else:
+        raise ValueError(f"unknown format {fmt!r}")
+    _check(st)
+    return out
+
+
+def set_quantise_once_override(mode: int = 0) -> None:
+    """1: every CTA quantises; 2: quantise once across the grid; 0: automatic."""
+    _set_qonce(mode)
 
 
 def rmsnorm_q8(x: torch.Tensor, out: torch.Tensor | None = None, y: torch.Tensor | None = None,

@@ -139,6 +139,12 @@ std::atomic<uint64_t> g_counts[XQ_COUNT_N];
 std::atomic<int32_t> g_override_warps{0};
 std::atomic<int32_t> g_override_stages{0};
 std::atomic<int32_t> g_override_row_block{0};
+std::atomic<int32_t> g_override_quantise_once{0};
+// The decode step with a workspace quantises the activation once, in a
+// launch of its own, when a launch's batch has at least this many q8 blocks;
+// below that every CTA of the one fused launch quantises it for itself
+// (measured crossover on GB300).
+constexpr int64_t kQuantOnceMinBlocks = 32;
 
 xq_status fail(xq_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 xq_status fail(xq_status s, const char *fmt, ...) {
@@ -231,7 +237,7 @@ int64_t align128(int64_t v) { return (v + 127) & ~(int64_t)127; }
 // form: `rows` rows per expert, `slots` selected experts, each group inside
 // one slot, and `batch` staged activation vectors (1 shared, or one per slot).
 xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
-                    int64_t smem_optin, xq_plan *p, int64_t slots = 0) {
+                    int64_t smem_optin, xq_plan *p, int64_t slots = 0, bool have_ws = false) {
     const int32_t nb = (int32_t)(cols / 256);
     const int32_t R = (nb < 32 && 32 % nb == 0) ? 32 / nb : 1;
     const int32_t spr = R > 1 ? 1 : (nb + 31) / 32;
@@ -292,6 +298,8 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     p->launches = (int32_t)((batch + bl - 1) / bl);
     p->smem_bytes = bytes(W, S, M);
     p->row_block = M;
+    const int32_t oq = g_override_quantise_once.load();
+    p->quantise_once = have_ws && (oq == 2 || (oq == 0 && (int64_t)bl * nb >= kQuantOnceMinBlocks));
     return XQ_OK;
 }
 
@@ -319,8 +327,15 @@ void pack_table(const int8_t *table, uint32_t (&kv)[4]) {
 }
 
 // in: q8 blocks (mat-vec and sub-dots) or f32 x (the fused linear ops).
+// ws (the fused linear ops only): a workspace of linear_ws_bytes(cols,
+// batch) bytes for the quantise-once form (the q8 blocks), or null.
+size_t linear_ws_bytes(int64_t cols, int64_t batch) {
+    return (size_t)batch * (cols / 256) * kQ8Bytes;
+}
+
 xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *in, void *out,
-                     int64_t rows, int64_t cols, int64_t batch, void *stream) {
+                     int64_t rows, int64_t cols, int64_t batch, void *stream,
+                     void *ws = nullptr, size_t ws_bytes = 0, bool want_ws = false) {
     const bool cb4 = op.fmt != kQ4K;
     const bool dots = op.kind == Kind::kDots;
     const bool norm = op.kind == Kind::kNormLinear;
@@ -342,11 +357,22 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     const size_t o_bytes = (size_t)batch * rows * (dots ? nb * 8 * 4 : 4);
     if (overlap(out, o_bytes, W, w_bytes) || overlap(out, o_bytes, in, in_bytes))
         return fail(XQ_EINVAL, "output overlaps an input");
+    if (want_ws) {
+        const size_t need = linear_ws_bytes(cols, batch);
+        if (!ws) return fail(XQ_EINVAL, "null workspace");
+        if (!aligned(ws, 16)) return fail(XQ_EALIGN, "workspace must be 16-byte aligned");
+        if (ws_bytes < need)
+            return fail(XQ_EINVAL, "workspace of %zu bytes is too small: %zu needed", ws_bytes, need);
+        if (overlap(ws, need, W, w_bytes) || overlap(ws, need, in, in_bytes) ||
+            overlap(ws, need, out, o_bytes))
+            return fail(XQ_EINVAL, "workspace overlaps x, W or y");
+    }
 
     DeviceState *dev = nullptr;
     if (xq_status s = device_state(&dev)) return s;
     xq_plan plan;
-    if (xq_status s = make_plan(op.fmt, rows, cols, batch, dev->sm_count, dev->smem_optin, &plan))
+    if (xq_status s = make_plan(op.fmt, rows, cols, batch, dev->sm_count, dev->smem_optin, &plan,
+                                0, want_ws && op.kind == Kind::kLinear))
         return s;
     MatvecArgs a;
     memset(&a, 0, sizeof a);
@@ -361,19 +387,30 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     if (cb4) pack_table(table, a.kv);
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int kind = dots ? 1 : norm ? 4 : fused ? 2 : 0;
+    // quantise once: q8 blocks into the workspace, then the mat-vec on them
+    const bool once = plan.quantise_once != 0;
+    const int kind = dots ? 1 : norm ? 4 : (fused && !once) ? 2 : 0;
     for (int64_t b0 = 0; b0 < batch; b0 += plan.batch_per_launch) {
         const int64_t bc = batch - b0 < plan.batch_per_launch ? batch - b0 : plan.batch_per_launch;
-        if (fused)
+        if (once) {
+            const int64_t nblk = bc * nb;
+            q8_quantize_kernel<<<(unsigned)((nblk + 7) / 8), 256, 0, s>>>(
+                static_cast<const float *>(in) + b0 * cols, static_cast<uint8_t *>(ws), nblk);
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
+            a.xq = static_cast<const uint8_t *>(ws);
+        } else if (fused) {
             a.x = static_cast<const float *>(in) + b0 * cols;
-        else
+        } else {
             a.xq = static_cast<const uint8_t *>(in) + b0 * nb * kQ8Bytes;
+        }
         a.y = dots ? nullptr : static_cast<float *>(out) + b0 * rows;
         a.dots = dots ? static_cast<int32_t *>(out) + b0 * rows * nb * 8 : nullptr;
         cudaError_t e = launch_fmt(op.fmt, a, (int)bc, kind, grid, block,
                                    (size_t)plan.smem_bytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "mat-vec launch");
         g_counts[op.count].fetch_add(1, std::memory_order_relaxed);
+        if (once) g_counts[XQ_COUNT_QUANTISE_ONCE].fetch_add(1, std::memory_order_relaxed);
     }
     t_last_plan = plan;
     t_have_plan = true;
@@ -526,6 +563,31 @@ xq_status xq_linear_cb4(const float *x, const void *W, const int8_t *table, floa
     return run_matvec({kCB4, Kind::kLinear, XQ_COUNT_LINEAR_CB4}, W, table, x, y, rows, cols, batch, stream);
 }
 
+size_t xq_linear_workspace_bytes(int64_t cols, int64_t batch) {
+    if (cols <= 0 || cols % 256 || batch < 1 || batch > 8) return 0;
+    return linear_ws_bytes(cols, batch);
+}
+
+xq_status xq_linear_q4k_ws(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
+                           int64_t batch, void *ws, size_t ws_bytes, void *stream) {
+    return run_matvec({kQ4K, Kind::kLinear, XQ_COUNT_LINEAR_Q4K}, W, nullptr, x, y, rows, cols,
+                      batch, stream, ws, ws_bytes, true);
+}
+
+xq_status xq_linear_cb4_ws(const float *x, const void *W, const int8_t *table, float *y,
+                           int64_t rows, int64_t cols, int64_t batch, void *ws, size_t ws_bytes,
+                           void *stream) {
+    return run_matvec({kCB4, Kind::kLinear, XQ_COUNT_LINEAR_CB4}, W, table, x, y, rows, cols,
+                      batch, stream, ws, ws_bytes, true);
+}
+
+xq_status xq_linear_cb4r_ws(const float *x, const void *Wr, const int8_t *table, float *y,
+                            int64_t rows, int64_t cols, int64_t batch, void *ws, size_t ws_bytes,
+                            void *stream) {
+    return run_matvec({kCB4R, Kind::kLinear, XQ_COUNT_LINEAR_CB4R}, Wr, table, x, y, rows, cols,
+                      batch, stream, ws, ws_bytes, true);
+}
+
 xq_status xq_norm_linear_q4k(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
                              int64_t batch, void *stream) {
     return run_matvec({kQ4K, Kind::kNormLinear, XQ_COUNT_NORM_LINEAR_Q4K}, W, nullptr, x, y, rows, cols, batch, stream);
@@ -631,7 +693,7 @@ xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t bat
     if (xq_status s = check_shape(rows, cols, batch, true)) return s;
     if (sm_count < 1) return fail(XQ_EINVAL, "sm_count must be positive");
     return make_plan(format == XQ_FORMAT_Q4K ? kQ4K : format == XQ_FORMAT_CB4 ? kCB4 : kCB4R, rows,
-                     cols, batch, sm_count, smem_optin_bytes, plan);
+                     cols, batch, sm_count, smem_optin_bytes, plan, 0, true);
 }
 
 void xq_set_plan_override(int32_t warps, int32_t stages) {
@@ -641,6 +703,10 @@ void xq_set_plan_override(int32_t warps, int32_t stages) {
 
 void xq_set_row_block_override(int32_t row_block) {
     g_override_row_block.store(row_block < 0 ? 0 : row_block);
+}
+
+void xq_set_quantise_once_override(int32_t mode) {
+    g_override_quantise_once.store(mode < 0 || mode > 2 ? 0 : mode);
 }
 
 xq_status xq_last_plan(xq_plan *plan) {

@@ -29,7 +29,7 @@ constexpr int kActStride = 336;
 constexpr int kActSplitAt = 304;
 constexpr int kActNormAt = 320;
 // q8 blocks whose activation values one warp loads at once in the fused
-// kernels (one L2 round trip per group).
+// kernels at batch 1 (one L2 round trip per group; twice as many above).
 constexpr int kQuantGroup = 4;
 constexpr int kMaxWarps = 8;
 constexpr int kMaxStages = 8;

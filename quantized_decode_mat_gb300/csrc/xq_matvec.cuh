@@ -619,16 +619,18 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
     }
 
     // 2. the activation (a different region of shared memory than the stages)
-    if (FUSE != 0) {
+    auto ld16 = [](const uint4 *p) { return __ldg(p); };  // q8 blocks: a kernel input
+    if (FUSE == 1 || FUSE == 2) {
         // quantise x (FUSE == 2: y = x * scale) here: warp w takes blocks w,
         // w+W, ... (vector-major) with the standalone producers' arithmetic,
-        // so the same bytes.  The values of kQuantGroup blocks are loaded
-        // before any of them is processed: one L2 round trip per group.
+        // so the same bytes.  The values of QG blocks are loaded before any
+        // of them is processed: one L2 round trip per group.
         const int nblk = B * nb;
-        float4 u[kQuantGroup], v[kQuantGroup];
+        constexpr int QG = B >= 2 ? 2 * kQuantGroup : kQuantGroup;
+        float4 u[QG], v[QG];
         auto load_group = [&](int k0) {
 #pragma unroll
-            for (int j = 0; j < kQuantGroup; ++j) {
+            for (int j = 0; j < QG; ++j) {
                 const int blk = k0 + j * W;
                 if (blk < nblk) {
                     const float4 *src = reinterpret_cast<const float4 *>(a.x + (int64_t)blk * 256 + lane * 8);
@@ -648,10 +650,10 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
             }
             __syncthreads();
         }
-        for (int k0 = warp; k0 < nblk; k0 += kQuantGroup * W) {
+        for (int k0 = warp; k0 < nblk; k0 += QG * W) {
             if (k0 != warp) load_group(k0);
 #pragma unroll
-            for (int j = 0; j < kQuantGroup; ++j) {
+            for (int j = 0; j < QG; ++j) {
                 const int blk = k0 + j * W;
                 if (blk >= nblk) break;  // warp-uniform
                 float vals[8] = {u[j].x, u[j].y, u[j].z, u[j].w, v[j].x, v[j].y, v[j].z, v[j].w};
@@ -696,7 +698,7 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
             const int blk = i / 20, piece = i - 20 * blk;
             const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
             *reinterpret_cast<uint4 *>(act + blk * kActStride + 16 * piece) =
-                piece < 19 ? __ldg(src + piece) : split_sums(__ldg(src + 16), __ldg(src + 17));
+                piece < 19 ? ld16(src + piece) : split_sums(ld16(src + 16), ld16(src + 17));
         }
     } else {
         // the values of every q8 block in interleaved order (one 32-value
@@ -706,7 +708,7 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
             const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
             uint4 *dst = reinterpret_cast<uint4 *>(act + blk * kActStride);
             if (part < 8) {
-                const uint4 x0 = __ldg(src + 2 * part), x1 = __ldg(src + 2 * part + 1);
+                const uint4 x0 = ld16(src + 2 * part), x1 = ld16(src + 2 * part + 1);
                 const uint32_t in[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
                 dst[2 * part] = make_uint4(interleave_lo(in[0], in[4]), interleave_hi(in[0], in[4]),
                                            interleave_lo(in[1], in[5]), interleave_hi(in[1], in[5]));
@@ -714,7 +716,7 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
                     make_uint4(interleave_lo(in[2], in[6]), interleave_hi(in[2], in[6]),
                                interleave_lo(in[3], in[7]), interleave_hi(in[3], in[7]));
             } else {
-                dst[8 + part] = __ldg(src + 8 + part);  // pieces 16..18
+                dst[8 + part] = ld16(src + 8 + part);  // pieces 16..18
             }
         }
     }

@@ -290,3 +290,35 @@ def test_resident_sizes(lib):
             lib.cb4_bytes(rows, cols)
     p = lib.plan_matvec(11008, 4096, 1, fmt="cb4r")
     assert p == lib.plan_matvec(11008, 4096, 1, fmt="cb4")
+
+
+def test_linear_ws_argument_checks(raw, lib):
+    SZ = ctypes.c_size_t
+    need = lib.linear_workspace_bytes(256, 1)
+    assert need == 320 and lib.linear_workspace_bytes(4096, 8) == 40960 == lib.q8_bytes(4096, 8)
+    assert lib.linear_workspace_bytes(300, 1) == 0 and lib.linear_workspace_bytes(256, 9) == 0
+    args = lambda ws, n: (V(P), V(P * 4), V(P * 8), I64(32), I64(256), I64(1), V(ws), SZ(n), V(0))
+    assert _call(raw, "xq_linear_q4k_ws", *args(0, need)) == 1            # null workspace
+    assert _call(raw, "xq_linear_q4k_ws", *args(P * 16, need - 1)) == 1   # too small
+    assert _call(raw, "xq_linear_q4k_ws", *args(P * 16 + 8, need)) == 2   # misaligned
+    assert _call(raw, "xq_linear_q4k_ws", *args(P * 8, need)) == 1        # overlaps y
+    tbl = (ctypes.c_int8 * 16)()
+    assert _call(raw, "xq_linear_cb4_ws", V(P), V(P * 4), V(0), V(P * 8), I64(32), I64(256),
+                 I64(1), V(P * 16), SZ(need), V(0)) == 1                   # null table
+    assert _call(raw, "xq_linear_cb4r_ws", V(P), V(P * 4), tbl, V(P * 8), I64(32), I64(300),
+                 I64(1), V(P * 16), SZ(need), V(0)) == 3                   # cols % 256
+
+
+def test_plan_reports_the_workspace_choice(lib):
+    assert lib.plan_matvec(128256, 4096, 1)["quantise_once"] == 0   # 16 blocks: per CTA
+    assert lib.plan_matvec(4096, 14336, 1)["quantise_once"] == 1    # 56 blocks: once
+    assert lib.plan_matvec(14336, 4096, 2)["quantise_once"] == 1    # 32 blocks: once
+    assert lib.plan_matvec(4096, 7936, 1)["quantise_once"] == 0     # 31 blocks: per CTA
+    assert lib.plan_matvec(14336, 4096, 8)["quantise_once"] == 1    # 128 blocks
+    try:
+        lib.set_quantise_once_override(2)
+        assert lib.plan_matvec(128256, 4096, 1)["quantise_once"] == 1
+        lib.set_quantise_once_override(1)
+        assert lib.plan_matvec(4096, 14336, 8)["quantise_once"] == 0
+    finally:
+        lib.set_quantise_once_override(0)
