@@ -147,6 +147,26 @@ xq_status xq_linear_cb4r_ws(const float *x, const void *Wr, const int8_t *table,
                             int64_t rows, int64_t cols, int64_t batch, void *ws, size_t ws_bytes,
                             void *stream);
 
+/* xq_linear_q4k_ws without a caller workspace, for callers that cannot
+ * allocate device memory where they run the decode step (a framework that
+ * owns all device memory and allows no allocation outside its pool, or a
+ * serving loop that may not call cudaMalloc, which can synchronise the
+ * device).  The scratch is a fixed device array of 256 KiB inside the library
+ * (every GPU that loads the library holds it until the process exits), so a
+ * call may need at most 819 q8 blocks (xq_linear_workspace_bytes(cols, batch)
+ * <= 262144, i.e. batch * cols <= 209664); larger shapes return XQ_ESHAPE and
+ * launch nothing.  The call
+ * allocates nothing.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) once for that device, so make that first
+ * call before any stream capture.  Nothing in the array needs clearing: the
+ * q8 blocks are written before they are read.  Every call shares the one
+ * array, which keeps the last call's contents, so calls that may overlap on
+ * the GPU (other streams, other threads) race; order them on one stream.
+ * Arguments, results and other errors as xq_linear_q4k_ws.  The pages have no
+ * counterpart to this entry point. */
+xq_status xq_linear_q4k_static(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
+                               int64_t batch, void *stream);
+
 /* RMSNorm + q8 pack, the producer of the next layer's activation blocks:
  * for each of the batch vectors x_b ([batch][cols] f32, device),
  *   scale_b = 1 / sqrt(sum_i x_{b,i}^2 / cols + 1e-5),  y_b = x_b * scale_b,

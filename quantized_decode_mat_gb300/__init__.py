@@ -53,6 +53,7 @@ from ._native import (  # noqa: F401
     lib_path,
     linear_cb4,
     linear_q4k,
+    linear_q4k_static,
     linear_workspace_bytes,
     linear_ws,
     matvec_cb4,

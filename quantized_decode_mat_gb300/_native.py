@@ -69,6 +69,8 @@ _linear_cb4_ws = _sig("xq_linear_cb4_ws", ctypes.c_int,
 _linear_cb4r_ws = _sig("xq_linear_cb4r_ws", ctypes.c_int,
                        [_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P])
 _set_qonce = _sig("xq_set_quantise_once_override", None, [_I32])
+_linear_q4k_static = _sig("xq_linear_q4k_static", ctypes.c_int,
+                          [_P, _P, _P, _I64, _I64, _I64, _P])
 _subdots_q4k = _sig("xq_subdots_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
 _subdots_cb4 = _sig("xq_subdots_cb4", ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P])
 _plan = _sig("xq_plan_matvec", ctypes.c_int, [_I32, _I64, _I64, _I64, _I32, _I64,
@@ -249,6 +251,22 @@ def linear_ws(fmt: str, x: torch.Tensor, W: torch.Tensor, rows: int, cols: int,
     else:
         raise ValueError(f"unknown format {fmt!r}")
     _check(st)
+    return out
+
+
+def linear_q4k_static(x: torch.Tensor, W: torch.Tensor, rows: int, cols: int,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """linear_ws("q4k", ...) with the library's fixed scratch instead of a
+    caller workspace (for callers that may not allocate; batch * cols <=
+    209664).  ``out`` must be given by a caller that may not allocate."""
+    x = _x2d(x)
+    batch = x.shape[0]
+    if x.shape[1] != cols:
+        raise ValueError("x has the wrong number of columns")
+    if out is None:
+        out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    _check(_linear_q4k_static(_dev(x, "x", torch.float32), _dev(W, "W", torch.uint8),
+                              _dev(out, "y", torch.float32), rows, cols, batch, _stream(stream)))
     return out
 
 

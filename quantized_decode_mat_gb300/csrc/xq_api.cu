@@ -477,6 +477,47 @@ xq_status run_matvec_id(int fmt, const void *W, const int8_t *table, const int32
     return XQ_OK;
 }
 
+// ---- fixed scratch for callers that cannot allocate ---------------------------------------
+// Scratch of xq_linear_q4k_static: the q8 blocks of the activation, when the
+// plan quantises it once.  A file-scope device array: every GPU that loads the
+// library holds it until the process exits.  Host code may use its name only
+// to look up its device address (cudaGetSymbolAddress), never as a pointer.
+constexpr size_t kStaticScratchBytes = 256 * 1024;
+
+struct StaticScratch {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    void *ptr = nullptr;
+};
+StaticScratch g_static_scratch_state[kMaxDevices];
+
+}  // namespace
+}  // namespace xq
+
+static __device__ __align__(256) uint8_t g_static_scratch[xq::kStaticScratchBytes];
+
+namespace xq {
+namespace {
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (the first call on a device, which should come before any stream
+// capture).
+xq_status static_scratch(void **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(XQ_ELAUNCH, "device %d out of range", dev);
+    StaticScratch &st = g_static_scratch_state[dev];
+    std::call_once(st.once, [&st]() {
+        void *p = nullptr;
+        st.err = cudaGetSymbolAddress(&p, g_static_scratch);
+        st.ptr = st.err == cudaSuccess ? p : nullptr;
+    });
+    if (st.err != cudaSuccess) return cuda_fail(st.err, "cudaGetSymbolAddress(static scratch)");
+    *out = st.ptr;
+    return XQ_OK;
+}
+
 }  // namespace
 }  // namespace xq
 
@@ -572,6 +613,28 @@ xq_status xq_linear_q4k_ws(const float *x, const void *W, float *y, int64_t rows
                            int64_t batch, void *ws, size_t ws_bytes, void *stream) {
     return run_matvec({kQ4K, Kind::kLinear, XQ_COUNT_LINEAR_Q4K}, W, nullptr, x, y, rows, cols,
                       batch, stream, ws, ws_bytes, true);
+}
+
+// Some callers cannot allocate device memory where they run the decode
+// step: a host framework that owns all device memory through its own pool and
+// allows no allocation outside it, or a latency-bound serving loop that may
+// not call cudaMalloc (which can synchronise the device).  This variant of
+// xq_linear_q4k_ws takes its workspace from the library's fixed device array
+// instead of from the caller, and allocates nothing.
+xq_status xq_linear_q4k_static(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
+                               int64_t batch, void *stream) {
+    t_error.clear();
+    const size_t need = xq_linear_workspace_bytes(cols, batch);
+    if (need > kStaticScratchBytes)
+        return fail(XQ_ESHAPE,
+                    "batch %lld x cols %lld needs %zu bytes of scratch; the fixed scratch holds %zu "
+                    "(batch * cols <= %zu)",
+                    (long long)batch, (long long)cols, need, kStaticScratchBytes,
+                    kStaticScratchBytes / kQ8Bytes * 256);
+    void *ws = nullptr;
+    if (xq_status st = static_scratch(&ws)) return st;
+    return run_matvec({kQ4K, Kind::kLinear, XQ_COUNT_LINEAR_Q4K}, W, nullptr, x, y, rows, cols,
+                      batch, stream, ws, kStaticScratchBytes, true);
 }
 
 xq_status xq_linear_cb4_ws(const float *x, const void *W, const int8_t *table, float *y,
