@@ -24,7 +24,7 @@
  *        work is one rounding per operation with nothing contracted into an
  *        FMA; float16 rounds to nearest even; integers are exact.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - q8 scale rule: amax = max|x|, iscale = 127/amax (f32), q = clamp(
  *     rint(x*iscale), -127, 127) with round-half-even, d = amax/127 (f32);
  *     an all-zero block has d = 0 and q = 0; a NaN product gives q = 0.
