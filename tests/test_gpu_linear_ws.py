@@ -131,3 +131,35 @@ def test_linear_ws_rejects_a_small_workspace(xq):
     with pytest.raises(xq.XQError) as e:
         xq.linear_ws("q4k", x, Wd, rows, cols, ws)
     assert e.value.status == 1 and "too small" in e.value.detail
+
+
+@pytest.mark.parametrize("name", sorted(synthetic.CASES))
+def test_step_at_full_size(xq, orc, name):
+    """Every configuration at full size through the step the bench times
+    (xq_linear_*_ws, planned as the bench plans it): every output against the
+    oracle, or for the vocabulary projection the first and last tiles and
+    1500 random rows."""
+    c = synthetic.CASES[name]
+    W, x = c.weights(), c.x()
+    kv = synthetic.cb4_table()
+    Wd = dev(W)
+    if c.fmt == "cb4r":
+        Wd = xq.repack_cb4(Wd, c.rows, c.cols)
+    ws = torch.full((xq.linear_workspace_bytes(c.cols, c.batch),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    out = Guarded((c.batch, c.rows), torch.float32)
+    xq.linear_ws(c.fmt, dev(x), Wd, c.rows, c.cols, ws, table=kv, out=out.t)
+    torch.cuda.synchronize()
+    out.check_guard()
+    y = out.t.cpu().numpy()
+    xq_ref = orc.quantize_q8(x)
+    if c.rows > 20000:
+        rng = np.random.Generator(np.random.PCG64(11))
+        rows = np.unique(np.concatenate([np.arange(64), np.arange(c.rows - 70, c.rows),
+                                         rng.choice(c.rows, 1500, replace=False)]))
+    else:
+        rows = np.arange(c.rows)
+    Ws = np.ascontiguousarray(W[rows])
+    y_ref = (orc.matvec_q4k(Ws, xq_ref, len(rows), c.cols, c.batch) if c.fmt == "q4k"
+             else orc.matvec_cb4(Ws, kv, xq_ref, len(rows), c.cols, c.batch))
+    check_y(y[:, rows], y_ref, f"step {name}")
