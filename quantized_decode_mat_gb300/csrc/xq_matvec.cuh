@@ -259,15 +259,15 @@ __device__ __forceinline__ void cb4_decode(uint32_t q, const uint32_t (&T)[4], u
                                            uint32_t &F1) {
     const uint32_t s = q & 0x77777777u;  // entry index within a half table
     const uint32_t sh = s >> 16;
-    const uint32_t a0 = __byte_perm(T[0], T[1], s);   // kv[0..7] for nibbles 0..3
-    const uint32_t a1 = __byte_perm(T[0], T[1], sh);  // ... nibbles 4..7
-    const uint32_t b0 = __byte_perm(T[2], T[3], s);   // kv[8..15]
-    const uint32_t b1 = __byte_perm(T[2], T[3], sh);
+    const uint32_t a0 = prmt(T[0], T[1], s);   // kv[0..7] for nibbles 0..3
+    const uint32_t a1 = prmt(T[0], T[1], sh);  // ... nibbles 4..7
+    const uint32_t b0 = prmt(T[2], T[3], s);   // kv[8..15]
+    const uint32_t b1 = prmt(T[2], T[3], sh);
     // bit 3 of an even nibble is the top bit of its byte in q << 4, of an
     // odd nibble the top bit of its byte in q; selector 8+j replicates it
     const uint32_t q4 = q << 4;
-    const uint32_t m0 = prmt_sign(q4, q, 0xD9C8u);  // nibbles 0..3
-    const uint32_t m1 = prmt_sign(q4, q, 0xFBEAu);  // nibbles 4..7
+    const uint32_t m0 = prmt(q4, q, 0xD9C8u);  // nibbles 0..3
+    const uint32_t m1 = prmt(q4, q, 0xFBEAu);  // nibbles 4..7
     F0 = (a0 & ~m0) | (b0 & m0);
     F1 = (a1 & ~m1) | (b1 & m1);
 }

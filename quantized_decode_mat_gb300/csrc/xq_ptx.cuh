@@ -70,10 +70,12 @@ __device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
     return (int)d;
 }
 
-// Byte permute in prmt's generic mode, where bit 3 of a selector nibble
-// replicates the sign (top) bit of the selected byte over the target byte.
-// (__byte_perm uses only the low three bits of each selector nibble.)
-__device__ __forceinline__ uint32_t prmt_sign(uint32_t a, uint32_t b, uint32_t sel) {
+// Byte permute in prmt's generic mode: the low three bits of selector nibble
+// i pick byte i of the result from the eight bytes of (a, b); bit 3 set
+// replicates the sign (top) bit of that byte over the whole result byte.
+// (__byte_perm keeps only the low three bits of each nibble, which costs a
+// masking operation per call when the selector is not a constant.)
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
