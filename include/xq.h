@@ -38,6 +38,9 @@
  *     [batch][cols/256][320 B], y is [batch][rows] f32, fully overwritten.
  *   - Preconditions, all checked on the host before any CUDA call:
  *     cols > 0 and cols % 256 == 0; 1 <= rows <= 2^31-1; 1 <= batch <= 8;
+ *     the mat-vec kernels also need one q8 vector to fit in shared memory
+ *     beside two weight stages: cols <= 169984 on GB300 (232448 bytes of
+ *     shared memory a CTA), else XQ_ESHAPE;
  *     W, xq, x and dots 16-byte aligned; y 4-byte aligned; outputs must not
  *     overlap inputs.  A violation returns XQ_EINVAL / XQ_EALIGN / XQ_ESHAPE
  *     and launches nothing.

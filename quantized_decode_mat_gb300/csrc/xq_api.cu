@@ -303,6 +303,22 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     return XQ_OK;
 }
 
+// When every CTA quantises the activation itself, its warps share that work
+// one q8 block each; a plan with fewer warps than blocks (few rows a CTA) gets
+// more warps, which find no row group of their own and only quantise.
+void widen_for_quantise(xq_plan *p, int64_t nb, int64_t smem_optin) {
+    const int64_t nblk = (int64_t)p->batch_per_launch * nb;
+    const int32_t wmax = warps_limit(p->batch_per_launch);
+    int32_t W = p->warps;
+    const int64_t want = nblk < wmax ? nblk : wmax;
+    if (W >= want) return;
+    const int64_t act = align128((int64_t)p->batch_per_launch * nb * kActStride);
+    const int64_t per_warp = (int64_t)p->stages * p->row_block * kStageBytes;
+    while (W < want && act + (int64_t)(W + 1) * per_warp + 128 <= smem_optin) ++W;
+    p->warps = W;
+    p->smem_bytes = act + (int64_t)W * per_warp + 128;
+}
+
 enum class Kind { kMatvec, kDots, kLinear, kNormLinear };
 
 struct OpInfo {
@@ -385,10 +401,12 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     a.stages = plan.stages;
     a.row_block = plan.row_block;
     if (cb4) pack_table(table, a.kv);
-    const dim3 grid(plan.grid), block(plan.warps * 32);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     // quantise once: q8 blocks into the workspace, then the mat-vec on them
     const bool once = plan.quantise_once != 0;
+    if (fused && !once && g_override_warps.load() == 0)  // an override is kept as given
+        widen_for_quantise(&plan, nb, dev->smem_optin);
+    const dim3 grid(plan.grid), block(plan.warps * 32);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int kind = dots ? 1 : norm ? 4 : (fused && !once) ? 2 : 0;
     for (int64_t b0 = 0; b0 < batch; b0 += plan.batch_per_launch) {
         const int64_t bc = batch - b0 < plan.batch_per_launch ? batch - b0 : plan.batch_per_launch;

@@ -322,3 +322,14 @@ def test_plan_reports_the_workspace_choice(lib):
         assert lib.plan_matvec(4096, 14336, 8)["quantise_once"] == 0
     finally:
         lib.set_quantise_once_override(0)
+
+
+def test_widest_rows_that_fit(lib):
+    """One q8 vector (cols/256 blocks at 336 bytes of shared memory each) must
+    fit beside two 4608-byte stages: cols 169984 is the widest on GB300."""
+    p = lib.plan_matvec(7, 169984, 2, sm_count=152, smem_optin=232448)
+    assert p["batch_per_launch"] == 1 and p["launches"] == 2 and p["segments"] == 21
+    assert p["smem_bytes"] <= 232448
+    with pytest.raises(lib.XQError) as e:
+        lib.plan_matvec(7, 169984 + 256, 1, sm_count=152, smem_optin=232448)
+    assert e.value.status == 3 and "shared memory" in e.value.detail
