@@ -6,7 +6,10 @@
 One step = one pass of the whole hot path over one batch: the decode step
 xq_linear_q4k_ws (quantise the f32 activation to q8 blocks and the Q4_K
 mat-vec; one fused launch for small activations, a quantise launch into the
-workspace and the mat-vec for wide or batched ones), inputs resident in HBM.
+workspace and the mat-vec for wide or batched ones), inputs resident in HBM,
+with overlapped launches (--overlap on, the default: the weights are constant,
+so a step may start streaming them while the previous step finishes; the step
+without overlap is timed beside it).
 The one-launch fused form, the two-call path (xq_quantize_q8 + xq_matvec_q4k)
 and the mat-vec alone on q8 input are timed beside it for the breakdown.  Default workload: the L2-exceeding vocabulary
 projection, Q4_K 128256 x 4096, batch 1 (W = 295.5 MB, larger than the 129 MB
@@ -394,18 +397,24 @@ def run_ours(args, c):
                 fn()
         return g
 
+    # Overlapped launches (xq_set_overlap_launches) for the step: the weights
+    # are constant, so a launch may start streaming them while the previous
+    # step finishes.  The other arms are captured without it; the step
+    # without it is timed beside it.
+    overlap = args.overlap == "on"
     per_graph = max(1, min(args.steps, 100))
     rem = args.steps % per_graph
     ncount = xq.COUNT_N
     counts0 = [xq.launch_count(i) for i in range(ncount)]
     graphs = {}
-    for name, fn in (("step", do_step), ("fused", do_fused), ("matvec", do_matvec),
+    xq.set_overlap_launches(overlap)
+    graphs["step"] = (capture(do_step, per_graph), capture(do_step, rem) if rem else None)
+    launches_per_step = sum(xq.launch_count(i) - counts0[i] for i in range(ncount)) / per_graph
+    xq.set_overlap_launches(False)
+    for name, fn in (("step_plain", do_step), ("fused", do_fused), ("matvec", do_matvec),
                      ("two_call", do_two_call),
                      ("norm_linear", do_norm_linear), ("norm_two_call", do_norm_two_call)):
         graphs[name] = (capture(fn, per_graph), capture(fn, rem) if rem else None)
-        if name == "step":
-            launches_per_step = sum(xq.launch_count(i) - counts0[i]
-                                    for i in range(ncount)) / per_graph
 
     def timed(name, k):
         g, g_r = graphs[name]
@@ -438,6 +447,7 @@ def run_ours(args, c):
     # the same kernels outside the step, for the breakdown
     mv_ms = timed("matvec", args.steps)
     fused_ms = timed("fused", args.steps)
+    plain_ms = timed("step_plain", args.steps)
     two_ms = timed("two_call", args.steps)
     nl_ms = timed("norm_linear", args.steps)
     n2_ms = timed("norm_two_call", args.steps)
@@ -482,9 +492,11 @@ def run_ours(args, c):
         ev1.synchronize()
         return ev0.elapsed_time(ev1) / n
 
+    xq.set_overlap_launches(overlap)
     e2e_run(4, True)
     e2e_serial_ms = max_over_ranks(e2e_run(e2e_steps, False), dist)
     e2e_ms = max_over_ranks(e2e_run(e2e_steps, True), dist)
+    xq.set_overlap_launches(False)
     status = xq.device_status(stream=stream)
 
     if rank != 0:
@@ -509,7 +521,10 @@ def run_ours(args, c):
         "us_per_matvec": step_ms * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8 dp4a (int32 sums) + f32 epilogue",
         "data": "synthetic (seeded, shapes and distributions of the decode workloads)",
-        "config": workload_config(c),
+        "config": {**workload_config(c),
+                   "launch": ("overlapped launches (programmatic stream serialization: a step may "
+                              "start streaming W while the previous one finishes)" if overlap
+                              else "plain stream order")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy (burst)",
                      "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
@@ -522,6 +537,8 @@ def run_ours(args, c):
         "plan": {k: step_plan[k] for k in ("warps", "stages", "grid", "rows_per_group",
                                             "segments", "row_block", "quantise_once")},
         "breakdown": {
+            "step_without_overlap": {"us": plain_ms * 1e3,
+                                     "GBs": nbytes["linear"] / (plain_ms * 1e-3) / 1e9},
             "fused_one_launch": {"us": fused_ms * 1e3,
                                  "GBs": nbytes["linear"] / (fused_ms * 1e-3) / 1e9},
             "matvec_on_q8_input": {"us": mv_ms * 1e3,
@@ -560,6 +577,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--case", default=DEFAULT_CASE, choices=sorted(synthetic.CASES))
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
+    ap.add_argument("--overlap", choices=["on", "off"], default="on",
+                    help="overlapped launches for the timed step (the weights are constant)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -319,6 +319,21 @@ void xq_set_quantise_once_override(int32_t mode);
 /* Plan used by the calling thread's last mat-vec or sub-dot launch. */
 xq_status xq_last_plan(xq_plan *plan);
 
+/* Overlapped launches (process-wide; default off).  When on, the mat-vec,
+ * quantise and RMSNorm entry points launch their kernels with programmatic
+ * stream serialization: a launch may start while the kernel before it on the
+ * stream is still finishing.  Such a kernel first requests its first weight
+ * boxes (it reads W and nothing else), then waits until the earlier kernel has
+ * completed and its writes are visible before it reads x, q8 blocks or expert
+ * ids and before it writes anything.  So the kernel just before a mat-vec on
+ * the stream must not write that mat-vec's W (for instance xq_repack_cb4 into
+ * the rows it then reads): separate the two with an event or a stream
+ * synchronisation, or keep overlap off.  Constant weights, the decode case,
+ * are safe.  With overlap on, consecutive launches hide each other's start-up
+ * and tail. */
+void xq_set_overlap_launches(int32_t enable);
+int32_t xq_overlap_launches(void);
+
 /* Launch counters (process-wide, monotonic) per kernel family. */
 enum {
     XQ_COUNT_QUANTIZE = 0,

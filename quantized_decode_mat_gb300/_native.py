@@ -69,6 +69,8 @@ _linear_cb4_ws = _sig("xq_linear_cb4_ws", ctypes.c_int,
 _linear_cb4r_ws = _sig("xq_linear_cb4r_ws", ctypes.c_int,
                        [_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P])
 _set_qonce = _sig("xq_set_quantise_once_override", None, [_I32])
+_set_overlap = _sig("xq_set_overlap_launches", None, [_I32])
+_get_overlap = _sig("xq_overlap_launches", _I32, [])
 _linear_q4k_static = _sig("xq_linear_q4k_static", ctypes.c_int,
                           [_P, _P, _P, _I64, _I64, _I64, _P])
 _subdots_q4k = _sig("xq_subdots_q4k", ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P])
@@ -268,6 +270,17 @@ def linear_q4k_static(x: torch.Tensor, W: torch.Tensor, rows: int, cols: int,
     _check(_linear_q4k_static(_dev(x, "x", torch.float32), _dev(W, "W", torch.uint8),
                               _dev(out, "y", torch.float32), rows, cols, batch, _stream(stream)))
     return out
+
+
+def set_overlap_launches(enable: bool) -> None:
+    """Overlapped launches (see xq_set_overlap_launches in include/xq.h): a
+    launch may start streaming W while the kernel before it on the stream
+    finishes.  Only when that kernel does not write the W being read."""
+    _set_overlap(1 if enable else 0)
+
+
+def overlap_launches() -> bool:
+    return bool(_get_overlap())
 
 
 def set_quantise_once_override(mode: int = 0) -> None:

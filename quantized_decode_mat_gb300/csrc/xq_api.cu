@@ -8,6 +8,7 @@
 #include <string>
 
 #include "xq_internal.h"
+#include "xq_ptx.cuh"
 #include "xq_norm.cuh"
 #include "xq_q8.cuh"
 
@@ -25,6 +26,8 @@ __device__ uint32_t g_status_word;
 __global__ void __launch_bounds__(256) q8_quantize_kernel(const float *__restrict__ x,
                                                           uint8_t *__restrict__ xq,
                                                           int64_t nblocks) {
+    grid_dependency_wait();  // x may come from the kernel before on the stream
+    grid_dependency_trigger();
     const int64_t blk = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (blk >= nblocks) return;  // whole warps leave together
@@ -51,6 +54,8 @@ __global__ void __launch_bounds__(256) rmsnorm_q8_kernel(const float *__restrict
                                                          uint8_t *__restrict__ xq,
                                                          float *__restrict__ y, int64_t cols) {
     __shared__ float s_scale;
+    grid_dependency_wait();  // x may come from the kernel before on the stream
+    grid_dependency_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nb = cols / 256;
     const int64_t k = (int64_t)blockIdx.x * 8 + warp;  // this warp's q8 block
@@ -140,6 +145,7 @@ std::atomic<int32_t> g_override_warps{0};
 std::atomic<int32_t> g_override_stages{0};
 std::atomic<int32_t> g_override_row_block{0};
 std::atomic<int32_t> g_override_quantise_once{0};
+std::atomic<int32_t> g_overlap{0};
 // The decode step with a workspace quantises the activation once, in a
 // launch of its own, when a launch's batch has at least this many q8 blocks;
 // below that every CTA of the one fused launch quantises it for itself
@@ -400,6 +406,7 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     a.segments = plan.segments;
     a.stages = plan.stages;
     a.row_block = plan.row_block;
+    a.overlap = g_overlap.load();
     if (cb4) pack_table(table, a.kv);
     // quantise once: q8 blocks into the workspace, then the mat-vec on them
     const bool once = plan.quantise_once != 0;
@@ -412,9 +419,9 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
         const int64_t bc = batch - b0 < plan.batch_per_launch ? batch - b0 : plan.batch_per_launch;
         if (once) {
             const int64_t nblk = bc * nb;
-            q8_quantize_kernel<<<(unsigned)((nblk + 7) / 8), 256, 0, s>>>(
+            const cudaError_t e = launch_kernel(
+                q8_quantize_kernel, dim3((unsigned)((nblk + 7) / 8)), dim3(256), 0, s, a.overlap != 0,
                 static_cast<const float *>(in) + b0 * cols, static_cast<uint8_t *>(ws), nblk);
-            const cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
             a.xq = static_cast<const uint8_t *>(ws);
         } else if (fused) {
@@ -475,6 +482,7 @@ xq_status run_matvec_id(int fmt, const void *W, const int8_t *table, const int32
     a.segments = plan.segments;
     a.stages = plan.stages;
     a.row_block = plan.row_block;
+    a.overlap = g_overlap.load();
     a.sel = sel;
     a.rows_per_expert = rpe;
     a.n_experts = (int32_t)n_experts;
@@ -570,9 +578,9 @@ xq_status xq_quantize_q8(const float *x, void *xq_out, int64_t cols, int64_t bat
     DeviceState *dev = nullptr;
     if (xq_status s = device_state(&dev)) return s;
     const unsigned grid = (unsigned)((nblocks + 7) / 8);
-    q8_quantize_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        x, static_cast<uint8_t *>(xq_out), nblocks);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e =
+        launch_kernel(q8_quantize_kernel, dim3(grid), dim3(256), 0, static_cast<cudaStream_t>(stream),
+                      g_overlap.load() != 0, x, static_cast<uint8_t *>(xq_out), nblocks);
     if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
     g_counts[XQ_COUNT_QUANTIZE].fetch_add(1, std::memory_order_relaxed);
     return XQ_OK;
@@ -594,9 +602,9 @@ xq_status xq_rmsnorm_q8(const float *x, void *xq_out, float *y, int64_t cols, in
     DeviceState *dev = nullptr;
     if (xq_status s = device_state(&dev)) return s;
     const dim3 grid((unsigned)((cols / 256 + 7) / 8), (unsigned)batch);
-    rmsnorm_q8_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        x, static_cast<uint8_t *>(xq_out), y, cols);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e =
+        launch_kernel(rmsnorm_q8_kernel, grid, dim3(256), 0, static_cast<cudaStream_t>(stream),
+                      g_overlap.load() != 0, x, static_cast<uint8_t *>(xq_out), y, cols);
     if (e != cudaSuccess) return cuda_fail(e, "RMSNorm launch");
     g_counts[XQ_COUNT_RMSNORM_Q8].fetch_add(1, std::memory_order_relaxed);
     return XQ_OK;
@@ -785,6 +793,10 @@ void xq_set_plan_override(int32_t warps, int32_t stages) {
 void xq_set_row_block_override(int32_t row_block) {
     g_override_row_block.store(row_block < 0 ? 0 : row_block);
 }
+
+void xq_set_overlap_launches(int32_t enable) { g_overlap.store(enable ? 1 : 0); }
+
+int32_t xq_overlap_launches(void) { return g_overlap.load(); }
 
 void xq_set_quantise_once_override(int32_t mode) {
     g_override_quantise_once.store(mode < 0 || mode > 2 ? 0 : mode);

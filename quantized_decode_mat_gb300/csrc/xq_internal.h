@@ -64,7 +64,31 @@ struct MatvecArgs {
     int32_t groups_per_slot;
     int32_t act_vectors;    // 1: every slot reads vector 0; used: slot kk reads vector kk
     uint32_t *status;       // device status word
+    int32_t overlap;        // host side: launch with programmatic stream serialization
 };
+
+// Launch a kernel, with programmatic stream serialization when `overlap`: the
+// grid may start while the one before it on the stream finishes (its kernels
+// call grid_dependency_wait before touching anything but the weights).
+template <class... P, class... A>
+inline cudaError_t launch_kernel(void (*kern)(P...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, bool overlap, A... args) {
+    if (!overlap) {
+        kern<<<grid, block, smem, s>>>(args...);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // Status word bits (see xq_device_status).
 constexpr uint32_t kStatusBadExpertId = 2u;

@@ -613,10 +613,16 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
         ++issued;
     };
 
+    // The weights are the one input no earlier kernel on the stream writes, so
+    // their first boxes are requested before waiting for that kernel (under
+    // an overlapped launch); the expert ids of the grouped form are not.
+    if (ID) grid_dependency_wait();
     for (int j = 0; j < S - 1; ++j) {  // prologue: S-1 boxes in flight
         if (issued < nitems) issue_next();
         cp_async_commit();
     }
+    grid_dependency_wait();     // x, q8 blocks and y belong to the stream's order
+    grid_dependency_trigger();  // the next launch may start its own prologue
 
     // 2. the activation (a different region of shared memory than the stages)
     auto ld16 = [](const uint4 *p) { return __ldg(p); };  // q8 blocks: a kernel input
@@ -813,8 +819,8 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
 template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>
 inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, size_t smem,
                                    cudaStream_t s) {
-    xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M><<<grid, block, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M>, grid, block, smem, s,
+                         a.overlap != 0, a);
 }
 
 template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>

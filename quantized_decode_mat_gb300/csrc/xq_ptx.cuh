@@ -81,6 +81,19 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
+// ---- programmatic dependent launch (sm_90+) ------------------------------------------
+// Wait until the grid launched before this one on the stream has completed and
+// its memory writes are visible; returns at once when this grid was launched
+// without the programmatic-serialization attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the next grid on the stream (if launched with that attribute) start its
+// prologue; it still waits for this grid's completion before it reads inputs.
+__device__ __forceinline__ void grid_dependency_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float f16_bits_to_f32(uint32_t bits16) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
 }

@@ -1,0 +1,70 @@
+"""Overlapped launches (xq_set_overlap_launches): a launch may start while the
+kernel before it on the stream finishes, touching only the weights before it
+waits for that kernel.  A chain in which every kernel reads what the one
+before it wrote must give the same bits as with overlap off, eagerly and
+replayed from a CUDA graph."""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def xq():
+    import quantized_decode_mat_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    return m
+
+
+def _chain(xq, W1, W2, Wc, kv, sel_src, slab, x, ws):
+    """Each step's input is the previous step's output (square 4096 x 4096
+    layers, and a wide-activation step that takes the quantise-once path)."""
+    n = 4096
+    y1 = xq.matvec_q4k(W1, xq.rmsnorm_q8(x), n, n)              # rmsnorm -> mat-vec
+    y2 = xq.matvec_q4k(W2, xq.quantize_q8(y1), n, n)            # quantise reads y1
+    y3 = xq.linear_ws("q4k", y2, W1, n, n, ws)                  # fused step on y2
+    y4 = xq.norm_linear_cb4(y3, Wc, kv, n, n)                   # codebook on y3
+    y5 = xq.linear_ws("q4k", torch.cat([y4, y3, y2, y1]), W2, n, n, ws)  # 64 blocks: once
+    sel = (sel_src + y5[:1, :3].abs().argmin(dim=1, keepdim=True).int() * 0).reshape(-1)
+    y6 = xq.matvec_id("q4k", slab, sel, xq.quantize_q8(y5[:1].contiguous()), 512, n, 3)
+    return [y1, y2, y3, y4, y5, y6]
+
+
+def test_overlapped_chain_is_bit_identical(xq):
+    n = 4096
+    W1 = torch.from_numpy(synthetic.q4k_weights(n, n, 1)).cuda()
+    W2 = torch.from_numpy(synthetic.q4k_weights(n, n, 2)).cuda()
+    Wc = torch.from_numpy(synthetic.cb4_weights(n, n, 3)).cuda()
+    slab = torch.from_numpy(synthetic.q4k_weights(3 * 512, n, 4)).cuda()
+    kv = synthetic.cb4_table()
+    x = torch.from_numpy(synthetic.activations(1, n, 5)).cuda()
+    sel_src = torch.tensor([[2], [0], [1]], dtype=torch.int32, device="cuda")
+    ws = torch.empty(xq.linear_workspace_bytes(n, 4), dtype=torch.uint8, device="cuda")
+    runs = {}
+    try:
+        for ov in (False, True):
+            xq.set_overlap_launches(ov)
+            assert xq.overlap_launches() == ov
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                eager = [t.clone() for t in _chain(xq, W1, W2, Wc, kv, sel_src, slab, x, ws)]
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                outs = _chain(xq, W1, W2, Wc, kv, sel_src, slab, x, ws)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            runs[ov] = ([t.cpu().numpy() for t in eager], [t.cpu().numpy() for t in outs])
+    finally:
+        xq.set_overlap_launches(False)
+    for k, (a, b) in enumerate(zip(runs[False][0], runs[True][0])):
+        assert np.array_equal(a, b), f"eager step {k + 1}"
+    for k, (a, b) in enumerate(zip(runs[False][0], runs[True][1])):
+        assert np.array_equal(a, b), f"graph step {k + 1}"
+    assert all(np.isfinite(a).all() for a in runs[False][0])
+    assert xq.device_status() == 0
