@@ -379,6 +379,23 @@ def run_ours(args, c):
         xq.rmsnorm_q8(x, out=xq_buf)
         do_matvec()
 
+    # grouped experts: the matrix as a slab of 8 experts of rows/8 rows, two
+    # of them selected (device ids), on q8 vector 0
+    n_exp, rpe = 8, c.rows // 8
+    sel = torch.tensor([3, 6], dtype=torch.int32, device=dev)
+    y_id = torch.empty((2, rpe), dtype=torch.float32, device=dev)
+    has_id = c.rows % 8 == 0
+
+    def do_experts():
+        xq.matvec_id(c.fmt, W, sel, xq_buf[:1], rpe, c.cols, n_exp, table=kv, out=y_id)
+
+    # resident rows: the bind-time repack of the whole matrix, raw -> resident
+    W_raw = torch.from_numpy(c.weights()).to(dev) if c.fmt == "cb4r" else None
+    W_rep = torch.empty_like(W) if c.fmt == "cb4r" else None
+
+    def do_repack():
+        xq.repack_cb4(W_raw, c.rows, c.cols, out=W_rep)
+
     # eager warm-up: the first call per device configures the kernels (before capture)
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -411,8 +428,10 @@ def run_ours(args, c):
     graphs["step"] = (capture(do_step, per_graph), capture(do_step, rem) if rem else None)
     launches_per_step = sum(xq.launch_count(i) - counts0[i] for i in range(ncount)) / per_graph
     xq.set_overlap_launches(False)
+    extra = ((("experts", do_experts),) if has_id else ()) + \
+        ((("repack", do_repack),) if c.fmt == "cb4r" else ())
     for name, fn in (("step_plain", do_step), ("fused", do_fused), ("matvec", do_matvec),
-                     ("two_call", do_two_call),
+                     ("two_call", do_two_call), *extra,
                      ("norm_linear", do_norm_linear), ("norm_two_call", do_norm_two_call)):
         graphs[name] = (capture(fn, per_graph), capture(fn, rem) if rem else None)
 
@@ -451,6 +470,8 @@ def run_ours(args, c):
     two_ms = timed("two_call", args.steps)
     nl_ms = timed("norm_linear", args.steps)
     n2_ms = timed("norm_two_call", args.steps)
+    id_ms = timed("experts", args.steps) if has_id else None
+    rp_ms = timed("repack", min(args.steps, 1000)) if c.fmt == "cb4r" else None
     time.sleep(0.2)
     sampler.stop()
     clocks = sampler.summary(t_wall0, time.time())
@@ -548,7 +569,14 @@ def run_ours(args, c):
             "rmsnorm_quantise_matvec_fused": {"us": nl_ms * 1e3,
                                               "GBs": nbytes["linear"] / (nl_ms * 1e-3) / 1e9},
             "rmsnorm_q8_then_matvec": {"us": n2_ms * 1e3,
-                                       "GBs": nbytes["two_call"] / (n2_ms * 1e-3) / 1e9}},
+                                       "GBs": nbytes["two_call"] / (n2_ms * 1e-3) / 1e9},
+            **({"grouped_experts_2_of_8": {
+                "us": id_ms * 1e3, "rows_per_expert": rpe,
+                "GBs": (2 * c.w_bytes // 8 + (c.cols // 256) * 320 + 2 * rpe * 4)
+                       / (id_ms * 1e-3) / 1e9}} if has_id else {}),
+            **({"repack_whole_matrix": {
+                "us": rp_ms * 1e3, "GBs": 2 * c.w_bytes / (rp_ms * 1e-3) / 1e9,
+                "bytes": "raw blocks read + resident rows written"}} if rp_ms else {})},
         "cpu_baseline": cpu,
         "e2e": {"value": world * nbytes["linear"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
