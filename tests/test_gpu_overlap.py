@@ -20,7 +20,7 @@ def xq():
     return m
 
 
-def _chain(xq, W1, W2, Wc, kv, sel_src, slab, x, ws):
+def _chain(xq, W1, W2, Wc, kv, sel_src, slab, x, ws, Ww, wsw):
     """Each step's input is the previous step's output (square 4096 x 4096
     layers, and a wide-activation step that takes the quantise-once path)."""
     n = 4096
@@ -31,7 +31,11 @@ def _chain(xq, W1, W2, Wc, kv, sel_src, slab, x, ws):
     y5 = xq.linear_ws("q4k", torch.cat([y4, y3, y2, y1]), W2, n, n, ws)  # 64 blocks: once
     sel = (sel_src + y5[:1, :3].abs().argmin(dim=1, keepdim=True).int() * 0).reshape(-1)
     y6 = xq.matvec_id("q4k", slab, sel, xq.quantize_q8(y5[:1].contiguous()), 512, n, 3)
-    return [y1, y2, y3, y4, y5, y6]
+    # 8 vectors of 65536: the batch is split over launches, each a quantise
+    # launch into the shared workspace and a mat-vec
+    xw = y5.reshape(-1).repeat(32).reshape(8, 65536)
+    y7 = xq.linear_ws("q4k", xw, Ww, 64, 65536, wsw)
+    return [y1, y2, y3, y4, y5, y6, y7]
 
 
 def test_overlapped_chain_is_bit_identical(xq):
@@ -44,6 +48,8 @@ def test_overlapped_chain_is_bit_identical(xq):
     x = torch.from_numpy(synthetic.activations(1, n, 5)).cuda()
     sel_src = torch.tensor([[2], [0], [1]], dtype=torch.int32, device="cuda")
     ws = torch.empty(xq.linear_workspace_bytes(n, 4), dtype=torch.uint8, device="cuda")
+    Ww = torch.from_numpy(synthetic.q4k_weights(64, 65536, 6)).cuda()
+    wsw = torch.empty(xq.linear_workspace_bytes(65536, 8), dtype=torch.uint8, device="cuda")
     runs = {}
     try:
         for ov in (False, True):
@@ -51,11 +57,14 @@ def test_overlapped_chain_is_bit_identical(xq):
             assert xq.overlap_launches() == ov
             s = torch.cuda.Stream()
             with torch.cuda.stream(s):
-                eager = [t.clone() for t in _chain(xq, W1, W2, Wc, kv, sel_src, slab, x, ws)]
+                eager = [t.clone() for t in _chain(xq, W1, W2, Wc, kv, sel_src, slab, x, ws, Ww,
+                                                   wsw)]
+                p = xq.last_plan()
+                assert p["launches"] > 1 and p["quantise_once"] == 1
             s.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=s):
-                outs = _chain(xq, W1, W2, Wc, kv, sel_src, slab, x, ws)
+                outs = _chain(xq, W1, W2, Wc, kv, sel_src, slab, x, ws, Ww, wsw)
             for _ in range(3):
                 g.replay()
             torch.cuda.synchronize()
