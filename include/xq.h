@@ -280,7 +280,8 @@ enum { XQ_FORMAT_Q4K = 0, XQ_FORMAT_CB4 = 1, XQ_FORMAT_CB4R = 2 };
  * once (2 for Q4_K with two or more activation vectors: each activation load
  * then serves two chunks of one column), one stage holding row_block boxes.
  * Each of the `warps` warps of the `grid` persistent CTAs keeps stages-1
- * stages in flight.  The batch's q8 blocks are staged in shared memory; if
+ * stages in flight (with one stage, the warp waits for its own copies and the
+ * other warps' work covers them).  The batch's q8 blocks are staged in shared memory; if
  * they do not fit, each call makes `launches` launches of batch_per_launch
  * vectors (each re-reads W).  quantise_once: 1 if the decode step with a
  * workspace (xq_linear_q4k_ws) quantises the activation once, in a launch of
@@ -305,7 +306,7 @@ typedef struct {
 xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t batch,
                          int32_t sm_count, int64_t smem_optin_bytes, xq_plan *plan);
 /* Override the automatic plan for sweeps: warps (up to 16 at batch 1, 8
- * above) and stages (2..8), 0 = automatic.  Process-wide; not for concurrent
+ * above) and stages (1..8), 0 = automatic.  Process-wide; not for concurrent
  * use with launches. */
 void xq_set_plan_override(int32_t warps, int32_t stages);
 /* Override the row groups a warp works on at once: 1, or 2 where the

@@ -262,17 +262,20 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     const int32_t om = g_override_row_block.load();
     // Two stages (one box in flight per warp while the other is consumed) read
     // fastest on GB300: the warps of the GPU then stream one contiguous window.
-    const int32_t S0 = os > 0 ? (os < 2 ? 2 : os > kMaxStages ? kMaxStages : os) : 2;
-    // Row groups per warp unit: two for Q4_K with two or more vectors, unless
-    // the instantiation's full warp count would then not fit in shared memory
-    // (fewer warps cost more than the halved activation loads save: measured
-    // on the 4096 x 14336 projection at batch 8).
+    const int32_t S0 = os > 0 ? (os > kMaxStages ? kMaxStages : os) : 2;
+    // Row groups per warp unit: two for Q4_K with two or more vectors.  When
+    // the instantiation's full warp count of two-box stages does not fit in
+    // shared memory beside the activations, a single stage a warp (the warps
+    // overlap one another's copies) measured faster than fewer warps or one
+    // row group (4096 x 14336 at batch 8: 32.9 against 34.4 us); if even that
+    // does not fit, one row group.
     int32_t M = (fmt == kQ4K && bl >= 2 && slots == 0) ? 2 : 1;
     if (om > 0) M = (om >= 2 && M == 2) ? 2 : 1;
     auto bytes = [&](int32_t w, int32_t st, int32_t m) {
         return act + (int64_t)w * st * m * kStageBytes + 128;
     };
-    if (M == 2 && om <= 0 && bytes(wmax, 2, 2) > smem_optin) M = 1;
+    if (M == 2 && om <= 0 && bytes(wmax, 1, 2) > smem_optin) M = 1;
+    const int32_t Smin = M == 2 ? 1 : 2;  // the fewest stages the planner lowers to
     const int64_t units = (groups + M - 1) / M;
     const int32_t grid = (int32_t)(units < sm_count ? units : sm_count);
     const int64_t per_cta = (units + grid - 1) / grid;
@@ -280,7 +283,7 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     if (ow > 0) W = ow < wmax ? ow : wmax;
     int32_t S = S0;
     while (bytes(W, S, M) > smem_optin) {
-        if (S > 2)
+        if (S > Smin)
             --S;
         else if (W > 1)
             --W;

@@ -577,8 +577,7 @@ def test_row_block_is_bit_identical(xq, orc, rows, cols, batch):
     auto = xq.plan_matvec(rows, cols, batch, sm_count=props.multi_processor_count,
                           smem_optin=props.shared_memory_per_block_optin)["row_block"]
     assert out[1][0] == 1 and out[0][0] == auto
-    # eight warps of two row groups do not fit beside the activations of these two
-    assert auto == (1 if (rows, cols, batch) in ((64, 14336, 8), (3, 32768, 2)) else 2)
+    assert auto == 2
     for a, b in zip(out[1][1:], out[0][1:]):
         assert np.array_equal(a, b)
     xq_ref = orc.quantize_q8(x)
