@@ -369,7 +369,7 @@ xq_status xq_device_status(uint32_t *out, int32_t clear, void *stream);
 const char *xq_status_string(xq_status s);
 /* Detail text of the calling thread's last failed call ("" if none). */
 const char *xq_last_error(void);
-/* ABI version: 1. */
+/* ABI version: 2 (the plan struct gained row_block and quantise_once). */
 int32_t xq_version(void);
 
 #ifdef __cplusplus

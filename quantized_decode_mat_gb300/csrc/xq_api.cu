@@ -845,6 +845,6 @@ const char *xq_status_string(xq_status s) {
 
 const char *xq_last_error(void) { return t_error.c_str(); }
 
-int32_t xq_version(void) { return 1; }
+int32_t xq_version(void) { return 2; }
 
 }  // extern "C"

@@ -152,7 +152,7 @@ def test_status_strings(raw):
     fn.restype = ctypes.c_char_p
     for s in range(6):
         assert fn(s).startswith(b"XQ_")
-    assert raw.xq_version() == 1
+    assert raw.xq_version() == 2
 
 
 @pytest.mark.parametrize("fmt,rows,cols,batch,warps,grid,R,spr,launches,M", [
