@@ -71,11 +71,14 @@ def step_bytes(c) -> dict:
 
 
 def source_digest() -> str:
-    """Digest of the kernel sources (the CUDA files the kernels are compiled
-    from); a recorded ncu traffic figure holds only while it is unchanged."""
+    """Digest of the mat-vec kernel's sources (every CUDA file except the host
+    API, xq_api.cu); a recorded ncu traffic figure holds only while it is
+    unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_decode_mat_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if name == "xq_api.cu":
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
