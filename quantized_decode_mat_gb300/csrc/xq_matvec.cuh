@@ -470,20 +470,22 @@ __device__ __forceinline__ GroupInfo group_info(const MatvecArgs &a, int64_t g, 
 }
 
 // ---- the kernel ------------------------------------------------------------------------
-// Work unit: a row group of R rows.  When nb (256-weight chunks per row) is a
-// power of two below 32, R = 32/nb and the group is one contiguous 4608-byte
-// box; otherwise R = 1 and the row is streamed as ceil(nb/32) contiguous
-// segments of up to 32 chunks.  Lane l of the warp takes chunk l of the box
-// ("one wave per row, consecutive lanes read consecutive bytes", 25.2).
-// Global warp g (warp-major over CTAs) takes groups g, g + TW, ...
+// Row group: R rows.  When nb (256-weight chunks per row) is a power of two
+// below 32, R = 32/nb and the group is one contiguous 4608-byte box;
+// otherwise R = 1 and the row is streamed as ceil(nb/32) contiguous segments
+// of up to 32 chunks.  Lane l of the warp takes chunk l of the box ("one wave
+// per row, consecutive lanes read consecutive bytes", 25.2).  Work unit: M
+// consecutive row groups, processed together (lane l holds chunk l of each).
+// Global warp g (warp-major over CTAs) takes units g, g + TW, ...
 //
 // Shared memory: the batch's q8 blocks, staged once per CTA at kActStride
-// bytes per chunk | [W][S] box stages of 4608 bytes.  Each warp fills its
-// stages with coalesced 16-byte cp.async copies (copy p moves bytes
-// 16p..16p+15 of the box to shared offset 16p; lane l's chunk lands at
-// 144*l), keeping S-1 boxes in flight.  (Requesting all S boxes before the
-// activation is staged measured slower.)  The act stride puts the chunks
-// that one instruction reads on distinct bank groups.
+// bytes per chunk | [W][S] stages of M boxes of 4608 bytes.  Each warp fills
+// its stages with coalesced 16-byte cp.async copies (copy p moves bytes
+// 16p..16p+15 of a box to shared offset 16p; lane l's chunk lands at 144*l),
+// keeping S-1 stages in flight (none with S = 1: the warp waits for its own
+// copies and the CTA's other warps cover them).  (Requesting all S stages
+// before the activation is staged measured slower.)  The act stride puts the
+// chunks that one instruction reads on distinct bank groups.
 template <int B>
 constexpr int max_threads() { return warps_limit(B) * 32; }
 
