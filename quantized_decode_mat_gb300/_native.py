@@ -119,14 +119,36 @@ def _stream(stream) -> int:
     return stream.cuda_stream
 
 
-def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+def _dev(t: torch.Tensor, name: str, dtype=None, nbytes: int | None = None) -> int:
+    """Device address of t after checking it: CUDA, dtype, contiguous, and at
+    least nbytes long (the C ABI takes raw pointers and cannot check sizes, so
+    a short buffer would be read or written past its end)."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if nbytes is not None and t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, {nbytes} needed")
     return t.data_ptr()
+
+
+def _w_bytes(rows: int, cols: int) -> int:
+    """Bytes of a weight matrix: 144 per 256 weights in every format."""
+    return rows * max(cols // 256, 0) * 144
+
+
+def _wp(W: torch.Tensor, rows: int, cols: int, name: str = "W") -> int:
+    return _dev(W, name, torch.uint8, _w_bytes(rows, cols))
+
+
+def _yp(y: torch.Tensor, batch: int, rows: int) -> int:
+    return _dev(y, "y", torch.float32, 4 * batch * rows)
+
+
+def _dotsp(d: torch.Tensor, batch: int, rows: int, cols: int) -> int:
+    return _dev(d, "dots", torch.int32, 4 * batch * rows * (cols // 32))
 
 
 def _table(table) -> ctypes.Array:
@@ -156,7 +178,8 @@ def quantize_q8(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -
     batch, cols = x.shape
     if out is None:
         out = torch.empty((batch, max(cols // 256, 0), 320), dtype=torch.uint8, device=x.device)
-    _check(_quantize(_dev(x, "x", torch.float32), _dev(out, "xq", torch.uint8), cols, batch,
+    _check(_quantize(_dev(x, "x", torch.float32),
+                     _dev(out, "xq", torch.uint8, q8_bytes(cols, batch)), cols, batch,
                      _stream(stream)))
     return out
 
@@ -174,8 +197,8 @@ def matvec_q4k(W: torch.Tensor, xq: torch.Tensor, rows: int, cols: int,
     batch = _batch_of(xq, cols)
     if out is None:
         out = torch.empty((batch, rows), dtype=torch.float32, device=xq.device)
-    _check(_matvec_q4k(_dev(W, "W", torch.uint8), _dev(xq, "xq", torch.uint8),
-                       _dev(out, "y", torch.float32), rows, cols, batch, _stream(stream)))
+    _check(_matvec_q4k(_wp(W, rows, cols), _dev(xq, "xq", torch.uint8),
+                       _yp(out, batch, rows), rows, cols, batch, _stream(stream)))
     return out
 
 
@@ -185,8 +208,8 @@ def matvec_cb4(W: torch.Tensor, table, xq: torch.Tensor, rows: int, cols: int,
     batch = _batch_of(xq, cols)
     if out is None:
         out = torch.empty((batch, rows), dtype=torch.float32, device=xq.device)
-    _check(_matvec_cb4(_dev(W, "W", torch.uint8), ctypes.cast(_table(table), _P),
-                       _dev(xq, "xq", torch.uint8), _dev(out, "y", torch.float32), rows, cols,
+    _check(_matvec_cb4(_wp(W, rows, cols), ctypes.cast(_table(table), _P),
+                       _dev(xq, "xq", torch.uint8), _yp(out, batch, rows), rows, cols,
                        batch, _stream(stream)))
     return out
 
@@ -205,8 +228,8 @@ def linear_q4k(x: torch.Tensor, W: torch.Tensor, rows: int, cols: int,
         raise ValueError("x has the wrong number of columns")
     if out is None:
         out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
-    _check(_linear_q4k(_dev(x, "x", torch.float32), _dev(W, "W", torch.uint8),
-                       _dev(out, "y", torch.float32), rows, cols, batch, _stream(stream)))
+    _check(_linear_q4k(_dev(x, "x", torch.float32), _wp(W, rows, cols),
+                       _yp(out, batch, rows), rows, cols, batch, _stream(stream)))
     return out
 
 
@@ -219,8 +242,8 @@ def linear_cb4(x: torch.Tensor, W: torch.Tensor, table, rows: int, cols: int,
         raise ValueError("x has the wrong number of columns")
     if out is None:
         out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
-    _check(_linear_cb4(_dev(x, "x", torch.float32), _dev(W, "W", torch.uint8),
-                       ctypes.cast(_table(table), _P), _dev(out, "y", torch.float32), rows,
+    _check(_linear_cb4(_dev(x, "x", torch.float32), _wp(W, rows, cols),
+                       ctypes.cast(_table(table), _P), _yp(out, batch, rows), rows,
                        cols, batch, _stream(stream)))
     return out
 
@@ -242,7 +265,7 @@ def linear_ws(fmt: str, x: torch.Tensor, W: torch.Tensor, rows: int, cols: int,
         raise ValueError("x has the wrong number of columns")
     if out is None:
         out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
-    xp, Wp, yp = _dev(x, "x", torch.float32), _dev(W, "W", torch.uint8), _dev(out, "y", torch.float32)
+    xp, Wp, yp = _dev(x, "x", torch.float32), _wp(W, rows, cols), _yp(out, batch, rows)
     wp, nbytes = _dev(ws, "ws", torch.uint8), ws.numel()
     if fmt == "q4k":
         st = _linear_q4k_ws(xp, Wp, yp, rows, cols, batch, wp, nbytes, _stream(stream))
@@ -267,8 +290,8 @@ def linear_q4k_static(x: torch.Tensor, W: torch.Tensor, rows: int, cols: int,
         raise ValueError("x has the wrong number of columns")
     if out is None:
         out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
-    _check(_linear_q4k_static(_dev(x, "x", torch.float32), _dev(W, "W", torch.uint8),
-                              _dev(out, "y", torch.float32), rows, cols, batch, _stream(stream)))
+    _check(_linear_q4k_static(_dev(x, "x", torch.float32), _wp(W, rows, cols),
+                              _yp(out, batch, rows), rows, cols, batch, _stream(stream)))
     return out
 
 
@@ -297,8 +320,9 @@ def rmsnorm_q8(x: torch.Tensor, out: torch.Tensor | None = None, y: torch.Tensor
     batch, cols = x.shape
     if out is None:
         out = torch.empty((batch, max(cols // 256, 0), 320), dtype=torch.uint8, device=x.device)
-    yp = None if y is None else _dev(y, "y", torch.float32)
-    _check(_rmsnorm_q8(_dev(x, "x", torch.float32), _dev(out, "xq", torch.uint8), yp, cols,
+    yp = None if y is None else _dev(y, "y", torch.float32, 4 * batch * cols)
+    _check(_rmsnorm_q8(_dev(x, "x", torch.float32), _dev(out, "xq", torch.uint8,
+                                                         q8_bytes(cols, batch)), yp, cols,
                        batch, _stream(stream)))
     return out
 
@@ -310,10 +334,10 @@ def _norm_linear(fn, x, W, table, rows, cols, out, stream):
         raise ValueError("x has the wrong number of columns")
     if out is None:
         out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
-    args = [_dev(x, "x", torch.float32), _dev(W, "W", torch.uint8)]
+    args = [_dev(x, "x", torch.float32), _wp(W, rows, cols)]
     if table is not None:
         args.append(ctypes.cast(_table(table), _P))
-    _check(fn(*args, _dev(out, "y", torch.float32), rows, cols, batch, _stream(stream)))
+    _check(fn(*args, _yp(out, batch, rows), rows, cols, batch, _stream(stream)))
     return out
 
 
@@ -340,17 +364,18 @@ def matvec_id(fmt: str, W: torch.Tensor, sel: torch.Tensor, xq: torch.Tensor,
     if out is None:
         out = torch.empty((used, rows_per_expert), dtype=torch.float32, device=xq.device)
     s = _dev(sel, "sel", torch.int32)
+    Wp = _dev(W, "W", torch.uint8, n_experts * _w_bytes(rows_per_expert, cols))
+    xp = _dev(xq, "xq", torch.uint8, (used if x_per_slot else 1) * q8_bytes(cols, 1))
+    yp = _dev(out, "y", torch.float32, 4 * used * rows_per_expert)
     if fmt == "q4k":
-        _check(_matvec_q4k_id(_dev(W, "W", torch.uint8), s, _dev(xq, "xq", torch.uint8),
-                              _dev(out, "y", torch.float32), rows_per_expert, cols, n_experts,
-                              used, int(x_per_slot), _stream(stream)))
-    else:
+        _check(_matvec_q4k_id(Wp, s, xp, yp, rows_per_expert, cols, n_experts, used,
+                              int(x_per_slot), _stream(stream)))
+    elif fmt in ("cb4", "cb4r"):
         fn = _matvec_cb4_id if fmt == "cb4" else _matvec_cb4r_id
-        if fmt not in ("cb4", "cb4r"):
-            raise ValueError(f"unknown format {fmt!r}")
-        _check(fn(_dev(W, "W", torch.uint8), ctypes.cast(_table(table), _P), s,
-                  _dev(xq, "xq", torch.uint8), _dev(out, "y", torch.float32),
-                  rows_per_expert, cols, n_experts, used, int(x_per_slot), _stream(stream)))
+        _check(fn(Wp, ctypes.cast(_table(table), _P), s, xp, yp, rows_per_expert, cols, n_experts,
+                  used, int(x_per_slot), _stream(stream)))
+    else:
+        raise ValueError(f"unknown format {fmt!r}")
     return out
 
 
@@ -360,8 +385,8 @@ def subdots_q4k(W: torch.Tensor, xq: torch.Tensor, rows: int, cols: int,
     batch = _batch_of(xq, cols)
     if out is None:
         out = torch.empty((batch, rows, cols // 32), dtype=torch.int32, device=xq.device)
-    _check(_subdots_q4k(_dev(W, "W", torch.uint8), _dev(xq, "xq", torch.uint8),
-                        _dev(out, "dots", torch.int32), rows, cols, batch, _stream(stream)))
+    _check(_subdots_q4k(_wp(W, rows, cols), _dev(xq, "xq", torch.uint8),
+                        _dotsp(out, batch, rows, cols), rows, cols, batch, _stream(stream)))
     return out
 
 
@@ -370,8 +395,8 @@ def subdots_cb4(W: torch.Tensor, table, xq: torch.Tensor, rows: int, cols: int,
     batch = _batch_of(xq, cols)
     if out is None:
         out = torch.empty((batch, rows, cols // 32), dtype=torch.int32, device=xq.device)
-    _check(_subdots_cb4(_dev(W, "W", torch.uint8), ctypes.cast(_table(table), _P),
-                        _dev(xq, "xq", torch.uint8), _dev(out, "dots", torch.int32), rows, cols,
+    _check(_subdots_cb4(_wp(W, rows, cols), ctypes.cast(_table(table), _P),
+                        _dev(xq, "xq", torch.uint8), _dotsp(out, batch, rows, cols), rows, cols,
                         batch, _stream(stream)))
     return out
 
@@ -394,7 +419,8 @@ def repack_cb4(src: torch.Tensor, rows: int, cols: int, out: torch.Tensor | None
     base = _dev(src, "src", torch.uint8)
     if src_offset < 0 or src_offset + 18 * n_blocks > src.numel():
         raise ValueError("src is too small for the chunk")
-    _check(_repack_cb4(base + src_offset, _dev(out, "Wr", torch.uint8), block_base, n_blocks,
+    _check(_repack_cb4(base + src_offset, _dev(out, "Wr", torch.uint8, cb4r_bytes(rows, cols)),
+                       block_base, n_blocks,
                        rows, cols, _stream(stream)))
     return out
 
@@ -405,8 +431,8 @@ def matvec_cb4r(Wr: torch.Tensor, table, xq: torch.Tensor, rows: int, cols: int,
     batch = _batch_of(xq, cols)
     if out is None:
         out = torch.empty((batch, rows), dtype=torch.float32, device=xq.device)
-    _check(_matvec_cb4r(_dev(Wr, "Wr", torch.uint8), ctypes.cast(_table(table), _P),
-                        _dev(xq, "xq", torch.uint8), _dev(out, "y", torch.float32), rows, cols,
+    _check(_matvec_cb4r(_wp(Wr, rows, cols, "Wr"), ctypes.cast(_table(table), _P),
+                        _dev(xq, "xq", torch.uint8), _yp(out, batch, rows), rows, cols,
                         batch, _stream(stream)))
     return out
 
@@ -420,8 +446,8 @@ def linear_cb4r(x: torch.Tensor, Wr: torch.Tensor, table, rows: int, cols: int,
         raise ValueError("x has the wrong number of columns")
     if out is None:
         out = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
-    _check(_linear_cb4r(_dev(x, "x", torch.float32), _dev(Wr, "Wr", torch.uint8),
-                        ctypes.cast(_table(table), _P), _dev(out, "y", torch.float32), rows,
+    _check(_linear_cb4r(_dev(x, "x", torch.float32), _wp(Wr, rows, cols, "Wr"),
+                        ctypes.cast(_table(table), _P), _yp(out, batch, rows), rows,
                         cols, batch, _stream(stream)))
     return out
 
@@ -437,8 +463,8 @@ def subdots_cb4r(Wr: torch.Tensor, table, xq: torch.Tensor, rows: int, cols: int
     batch = _batch_of(xq, cols)
     if out is None:
         out = torch.empty((batch, rows, cols // 32), dtype=torch.int32, device=xq.device)
-    _check(_subdots_cb4r(_dev(Wr, "Wr", torch.uint8), ctypes.cast(_table(table), _P),
-                         _dev(xq, "xq", torch.uint8), _dev(out, "dots", torch.int32), rows,
+    _check(_subdots_cb4r(_wp(Wr, rows, cols, "Wr"), ctypes.cast(_table(table), _P),
+                         _dev(xq, "xq", torch.uint8), _dotsp(out, batch, rows, cols), rows,
                          cols, batch, _stream(stream)))
     return out
 

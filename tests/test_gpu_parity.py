@@ -583,3 +583,38 @@ def test_row_block_is_bit_identical(xq, orc, rows, cols, batch):
     xq_ref = orc.quantize_q8(x)
     assert np.array_equal(out[0][1], orc.subdots_q4k(W, xq_ref, rows, cols, batch))
     check_y(out[0][2], orc.matvec_q4k(W, xq_ref, rows, cols, batch), "row block")
+
+
+# ---------------------------------------------------------------- the binding's size checks
+def test_binding_rejects_short_buffers(xq):
+    """The C ABI takes raw pointers and cannot see allocation sizes; the
+    binding checks every buffer against the shape before it calls, so a short
+    W, y, dots or q8 buffer raises instead of being read or written past its
+    end, and nothing is launched."""
+    rows, cols, batch = 64, 1024, 2
+    W = dev(synthetic.q4k_weights(rows, cols, 1))
+    x = dev(synthetic.activations(batch, cols, 2))
+    q8 = xq.quantize_q8(x)
+    kv = synthetic.cb4_table()
+    ws = torch.empty(xq.linear_workspace_bytes(cols, batch), dtype=torch.uint8, device="cuda")
+    short_W = W.reshape(-1)[:-16].contiguous()
+    short_y = torch.empty((batch, rows - 1), dtype=torch.float32, device="cuda")
+    short_d = torch.empty((batch, rows, cols // 32 - 1), dtype=torch.int32, device="cuda")
+    counts = [xq.launch_count(i) for i in range(xq.COUNT_N)]
+    calls = [
+        lambda: xq.matvec_q4k(short_W, q8, rows, cols),
+        lambda: xq.matvec_q4k(W, q8, rows, cols, out=short_y),
+        lambda: xq.subdots_q4k(W, q8, rows, cols, out=short_d),
+        lambda: xq.linear_q4k(x, short_W, rows, cols),
+        lambda: xq.linear_ws("q4k", x, W, rows, cols, ws, out=short_y),
+        lambda: xq.matvec_cb4(short_W, kv, q8, rows, cols),
+        lambda: xq.quantize_q8(x, out=q8.reshape(-1)[:-1]),
+        lambda: xq.matvec_id("q4k", W, torch.tensor([0, 1], dtype=torch.int32, device="cuda"),
+                             q8, rows // 2, cols, 3),
+        lambda: xq.repack_cb4(W, rows, cols, out=short_W),
+    ]
+    for k, call in enumerate(calls):
+        with pytest.raises(ValueError):
+            call()
+    torch.cuda.synchronize()
+    assert [xq.launch_count(i) for i in range(xq.COUNT_N)] == counts
