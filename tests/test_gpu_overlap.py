@@ -77,3 +77,35 @@ def test_overlapped_chain_is_bit_identical(xq):
         assert np.array_equal(a, b), f"graph step {k + 1}"
     assert all(np.isfinite(a).all() for a in runs[False][0])
     assert xq.device_status() == 0
+
+
+def test_two_streams_with_own_buffers(xq):
+    """The end-to-end pattern: steps alternate between two streams, each with
+    its own x, y and workspace, copies to and from pinned host memory in line,
+    overlap on.  Every step's y equals the same step run alone."""
+    rows, cols, batch = 4096, 14336, 2   # 112 q8 blocks: the quantise-once plan
+    W = torch.from_numpy(synthetic.q4k_weights(rows, cols, 21)).cuda()
+    xs_host = [torch.from_numpy(synthetic.activations(batch, cols, 30 + i)).pin_memory()
+               for i in range(6)]
+    ref = []
+    ws0 = torch.empty(xq.linear_workspace_bytes(cols, batch), dtype=torch.uint8, device="cuda")
+    for xh in xs_host:
+        ref.append(xq.linear_ws("q4k", xh.cuda(), W, rows, cols, ws0).cpu().numpy())
+    lanes = [{"s": torch.cuda.Stream(), "x": torch.empty((batch, cols), device="cuda"),
+              "y": torch.empty((batch, rows), device="cuda"),
+              "ws": torch.empty_like(ws0)} for _ in range(2)]
+    outs = [torch.empty((batch, rows), dtype=torch.float32).pin_memory() for _ in xs_host]
+    try:
+        xq.set_overlap_launches(True)
+        torch.cuda.synchronize()
+        for i, xh in enumerate(xs_host):
+            ln = lanes[i % 2]
+            with torch.cuda.stream(ln["s"]):
+                ln["x"].copy_(xh, non_blocking=True)
+                xq.linear_ws("q4k", ln["x"], W, rows, cols, ln["ws"], out=ln["y"])
+                outs[i].copy_(ln["y"], non_blocking=True)
+        torch.cuda.synchronize()
+    finally:
+        xq.set_overlap_launches(False)
+    for i in range(len(xs_host)):
+        assert np.array_equal(outs[i].numpy(), ref[i]), f"step {i}"
