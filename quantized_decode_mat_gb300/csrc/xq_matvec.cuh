@@ -155,15 +155,20 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *__restrict__ w, const A
 // l's chunk in each of M row groups): every activation load from shared
 // memory is used against M chunks instead of one.  The loop runs over the four
 // 64-value groups, then the vectors, then the chunks.  S1 is an exact
-// integer and each (chunk, vector)
-// epilogue is the single-chunk one, so y is bit-for-bit that of the one-chunk
-// form.  ok[m] false: chunk m is not accumulated and its dots are not stored
-// (its shared-memory bytes may be stale).
-template <int B, int M, bool DOTS, class Act>
+// integer and each (chunk, vector) epilogue is the single-chunk one, so y is
+// bit-for-bit that of the one-chunk form.
+//
+// The high-nibble dots are used in place (x16), so the low sub-block's scale
+// is taken x16 and the sum is 16*S1, shifted once per chunk and vector
+// (|16*S1| <= 16 * 8 * 63 * 32 * 15 * 127 < 2^29).  Chunks of rows that do not
+// exist were zero-filled when staged (d = dmin = 0, no scales, mins or values)
+// and add exact zeros, so no lane branches around its epilogue; ok[m] gates
+// only the dots export.  FIRST: this is the row's first chunk of the lane (one
+// segment per row), so the epilogue assigns (hi, lo) instead of adding to it.
+template <int B, int M, bool DOTS, bool FIRST, class Act>
 __device__ __forceinline__ void q4k_chunks(const uint8_t *const (&w)[M], const bool (&ok)[M],
                                            const Act &act, float (&hi)[M][B], float (&lo)[M][B],
-                                           int32_t *const (&dots)[M], int64_t dots_bstride,
-                                           bool first) {
+                                           int32_t *const (&dots)[M], int64_t dots_bstride) {
     float d[M], dmin[M];
     uint32_t sc_lo[M], sc_hi[M], m_lo[M], m_hi[M];
 #pragma unroll
@@ -176,16 +181,16 @@ __device__ __forceinline__ void q4k_chunks(const uint8_t *const (&w)[M], const b
         sc_hi[m] = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
         m_hi[m] = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
     }
-    int S1[M][B];
+    int S16[M][B];  // 16 * S1
 #pragma unroll
     for (int m = 0; m < M; ++m)
 #pragma unroll
-        for (int b = 0; b < B; ++b) S1[m][b] = 0;
+        for (int b = 0; b < B; ++b) S16[m][b] = 0;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         // sub-block 2g: low nibbles of group g; sub-block 2g+1: its high nibbles
         uint32_t ql[M][8], qh[M][8];
-        int s0[M], s1[M];
+        int s0x16[M], s1[M];
 #pragma unroll
         for (int m = 0; m < M; ++m) {
             const uint4 v0 = *reinterpret_cast<const uint4 *>(w[m] + 16 + 32 * g);
@@ -197,7 +202,7 @@ __device__ __forceinline__ void q4k_chunks(const uint8_t *const (&w)[M], const b
                 qh[m][k] = q[k] & 0xF0F0F0F0u;
             }
             const uint32_t scw = g < 2 ? sc_lo[m] : sc_hi[m];
-            s0[m] = byte_of(scw, 2 * (g & 1));
+            s0x16[m] = byte_of(scw, 2 * (g & 1)) << 4;
             s1[m] = byte_of(scw, 2 * (g & 1) + 1);
         }
 #pragma unroll
@@ -208,16 +213,16 @@ __device__ __forceinline__ void q4k_chunks(const uint8_t *const (&w)[M], const b
             const uint32_t ahi[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-                int d0 = 0, d1 = 0;
+                int d0 = 0, d1 = 0;  // d1: 16 * the high sub-block's dot
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     d0 = dp4a(ql[m][k], alo[k], d0);
                     d1 = dp4a_us(qh[m][k], ahi[k], d1);
                 }
-                d1 >>= 4;  // high nibbles were used in place (x16)
-                S1[m][b] += s0[m] * d0 + s1[m] * d1;
+                S16[m][b] += s0x16[m] * d0 + s1[m] * d1;
                 if (DOTS && ok[m])
-                    *reinterpret_cast<int2 *>(dots[m] + b * dots_bstride + 2 * g) = make_int2(d0, d1);
+                    *reinterpret_cast<int2 *>(dots[m] + b * dots_bstride + 2 * g) =
+                        make_int2(d0, d1 >> 4);
             }
         }
     }
@@ -229,7 +234,7 @@ __device__ __forceinline__ void q4k_chunks(const uint8_t *const (&w)[M], const b
         for (int m = 0; m < M; ++m) {
             const int S2 = dp4a_uu(m_hi[m], sp.y, dp4a_uu(m_lo[m], sp.x, 0)) +
                            256 * dp4a_us(m_hi[m], sp.w, dp4a_us(m_lo[m], sp.z, 0));
-            if (ok[m]) q4k_epilogue(xs, d[m], dmin[m], S1[m][b], S2, hi[m][b], lo[m][b], first);
+            q4k_epilogue(xs, d[m], dmin[m], S16[m][b] >> 4, S2, hi[m][b], lo[m][b], FIRST);
         }
     }
 }
@@ -594,6 +599,14 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
             if (valid == kStageBytes) {
 #pragma unroll
                 for (int k = 0; k < 9; ++k) cp_async_16(dst + 512u * k, src + 512 * k);
+            } else if (M > 1) {
+                // bytes past the rows' end are zero-filled (no global read): the
+                // row-blocked arithmetic runs over them unconditionally
+#pragma unroll
+                for (int k = 0; k < 9; ++k) {
+                    const bool in = 16 * (lane + 32 * k) < valid;
+                    cp_async_16_zfill(dst + 512u * k, in ? src + 512 * k : a.W, in ? 16u : 0u);
+                }
             } else {
 #pragma unroll
                 for (int k = 0; k < 9; ++k)
@@ -604,9 +617,16 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
     auto issue_next = [&]() {
         const uint32_t dst_stage = stage0_u32 + (uint32_t)p_stage * unit_bytes;
 #pragma unroll
-        for (int m = 0; m < M; ++m)
-            if (pu * M + m < ngroups)
+        for (int m = 0; m < M; ++m) {
+            if (pu * M + m < ngroups) {
                 issue_box(pu * M + m, dst_stage + (uint32_t)m * kStageBytes);
+            } else if (M > 1) {  // the unit's missing last group: zeros
+#pragma unroll
+                for (int k = 0; k < 9; ++k)
+                    cp_async_16_zfill(dst_stage + (uint32_t)m * kStageBytes + 16u * lane + 512u * k,
+                                      a.W, 0u);
+            }
+        }
         if (++ps == spr) {
             ps = 0;
             pu += TW;
@@ -760,7 +780,10 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
             __syncwarp();                  // ... and every other lane's
             const int c = R > 1 ? (lane & (nb - 1)) : s * 32 + lane;
             const uint8_t *st = stage0 + c_stage * unit_bytes + lane * kChunkBytes;
-            const ActSmem as{act + gi[0].vec * act_bstride + c * kActStride, act_bstride};
+            // (M > 1 reads the activation of chunks past the row's end too, and
+            // multiplies it by zero-filled weights: a real block keeps it finite)
+            const int ca = M > 1 && c >= nb ? nb - 1 : c;
+            const ActSmem as{act + gi[0].vec * act_bstride + ca * kActStride, act_bstride};
             if (M > 1) {
                 const uint8_t *w[M];
                 bool ok[M];
@@ -773,7 +796,12 @@ __global__ void __launch_bounds__(max_threads<B>(), 1) xq_matvec_kernel(const Ma
                     any |= ok[m];
                     dp[m] = DOTS && ok[m] ? a.dots + (gi[m].row0 + rig) * dots_row + c * 8 : nullptr;
                 }
-                if (any) q4k_chunks<B, M, DOTS>(w, ok, as, hi, lo, dp, dots_bstride, s == 0);
+                if (any) {
+                    if (spr == 1)  // one segment a row: every chunk is its lane's first
+                        q4k_chunks<B, M, DOTS, true>(w, ok, as, hi, lo, dp, dots_bstride);
+                    else  // (hi, lo) start at zero, to which an exact add is an assignment
+                        q4k_chunks<B, M, DOTS, false>(w, ok, as, hi, lo, dp, dots_bstride);
+                }
             } else {
                 const bool ok = rig < gi[0].valid && c < nb && !gi[0].bad;
                 if (ok) {
