@@ -257,7 +257,7 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     const int64_t act = align128((int64_t)bl * nb * kActStride);
     if (slots > 0 && bl != batch)
         return fail(XQ_ESHAPE, "the per-slot activations do not fit in shared memory");
-    const int32_t wmax = warps_limit(slots > 0 ? 1 : bl);
+    const int32_t wmax = warps_limit(fmt, slots > 0 ? 1 : bl);
     const int32_t ow = g_override_warps.load(), os = g_override_stages.load();
     const int32_t om = g_override_row_block.load();
     // Two stages (one box in flight per warp while the other is consumed) read
@@ -281,6 +281,10 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     const int64_t per_cta = (units + grid - 1) / grid;
     int32_t W = (int32_t)(per_cta < wmax ? per_cta : wmax);
     if (ow > 0) W = ow < wmax ? ow : wmax;
+    // above 8 warps, whole warps a scheduler (12, 16) with two stages each;
+    // where those do not fit, the next such count down
+    if (ow <= 0)
+        while (W > kMaxWarps && bytes(W, S0, M) > smem_optin) W = (W - 1) / 4 * 4;
     int32_t S = S0;
     while (bytes(W, S, M) > smem_optin) {
         if (S > Smin)
@@ -315,9 +319,9 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
 // When every CTA quantises the activation itself, its warps share that work
 // one q8 block each; a plan with fewer warps than blocks (few rows a CTA) gets
 // more warps, which find no row group of their own and only quantise.
-void widen_for_quantise(xq_plan *p, int64_t nb, int64_t smem_optin) {
+void widen_for_quantise(xq_plan *p, int fmt, int64_t nb, int64_t smem_optin) {
     const int64_t nblk = (int64_t)p->batch_per_launch * nb;
-    const int32_t wmax = warps_limit(p->batch_per_launch);
+    const int32_t wmax = warps_limit(fmt, p->batch_per_launch);
     int32_t W = p->warps;
     const int64_t want = nblk < wmax ? nblk : wmax;
     if (W >= want) return;
@@ -414,7 +418,7 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     // quantise once: q8 blocks into the workspace, then the mat-vec on them
     const bool once = plan.quantise_once != 0;
     if (fused && !once && g_override_warps.load() == 0)  // an override is kept as given
-        widen_for_quantise(&plan, nb, dev->smem_optin);
+        widen_for_quantise(&plan, op.fmt, nb, dev->smem_optin);
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int kind = dots ? 1 : norm ? 4 : (fused && !once) ? 2 : 0;

@@ -39,9 +39,18 @@ constexpr int kMaxStages = 8;
 // 128 bytes of payloads, 144 bytes in all, as in the raw layout.
 enum Format { kQ4K = 0, kCB4 = 1, kCB4R = 2 };
 
-// Largest warps per CTA of an instantiation, which its register budget
-// allows no more: 16 at batch 1 (at most 128 registers a thread), 8 above.
-constexpr int warps_limit(int64_t batch) { return batch == 1 ? 2 * kMaxWarps : kMaxWarps; }
+// Largest warps per CTA of an instantiation (format, batch), which its
+// register budget allows no more.  Each of the SM's four schedulers has a
+// quarter of the register file, so the cap is set by the warps a scheduler
+// holds: 16 warps (4 a scheduler) allow 128 registers a thread, 12 allow 168,
+// 8 allow 255.  Q4_K: 16 at batch 1, 12 at batch 2, 8 above (its row-blocked
+// kernels need up to 211).  Codebook: 16 up to batch 4 (98-128 registers), 8
+// above (12 measured slower there).  Warp counts that split unevenly over the
+// schedulers measured slower.
+constexpr int warps_limit(int fmt, int64_t batch) {
+    return fmt == kQ4K ? (batch == 1 ? 16 : batch == 2 ? 12 : kMaxWarps)
+                       : (batch <= 4 ? 16 : kMaxWarps);
+}
 
 struct MatvecArgs {
     const uint8_t *W;       // [rows][nb][144]

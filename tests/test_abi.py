@@ -159,11 +159,12 @@ def test_status_strings(raw):
     ("q4k", 128256, 4096, 1, 16, 152, 2, 1, 1, 1), ("q4k", 128256, 4096, 8, 8, 152, 2, 1, 1, 2),
     ("q4k", 4096, 4096, 1, 14, 152, 2, 1, 1, 1), ("q4k", 14336, 4096, 4, 8, 152, 2, 1, 1, 2),
     ("q4k", 4096, 14336, 1, 16, 152, 1, 2, 1, 1), ("q4k", 4096, 14336, 8, 8, 152, 1, 2, 1, 2),
-    ("q4k", 4096, 14336, 4, 8, 152, 1, 2, 1, 2),
+    ("q4k", 4096, 14336, 4, 8, 152, 1, 2, 1, 2), ("q4k", 14336, 4096, 2, 12, 152, 2, 1, 1, 2),
+    ("q4k", 4096, 14336, 2, 8, 152, 1, 2, 1, 2),
     ("q4k", 256, 1024, 1, 1, 32, 8, 1, 1, 1), ("cb4", 11008, 4096, 1, 16, 152, 2, 1, 1, 1),
     ("cb4", 4096, 4096, 1, 14, 152, 2, 1, 1, 1), ("q4k", 33, 256, 2, 1, 1, 32, 1, 1, 2),
     ("q4k", 1, 512, 1, 1, 1, 16, 1, 1, 1), ("q4k", 100, 2304, 1, 1, 100, 1, 1, 1, 1),
-    ("q4k", 1000, 65536, 8, 6, 152, 1, 8, 4, 1), ("cb4", 14336, 4096, 8, 8, 152, 2, 1, 1, 1),
+    ("q4k", 1000, 65536, 8, 6, 152, 1, 8, 4, 1), ("cb4", 14336, 4096, 8, 8, 152, 2, 1, 1, 1), ("cb4", 11008, 4096, 4, 16, 152, 2, 1, 1, 1),
     ("cb4r", 300, 2304, 2, 2, 152, 1, 1, 1, 1)])
 def test_plan(lib, fmt, rows, cols, batch, warps, grid, R, spr, launches, M):
     p = lib.plan_matvec(rows, cols, batch, fmt=fmt, sm_count=152, smem_optin=232448)
@@ -203,6 +204,8 @@ def test_plan_override_is_clamped(lib):
         p = lib.plan_matvec(1000, 1024, 1)
         assert p["warps"] == 16 and p["stages"] <= 8 and p["smem_bytes"] <= 232448
         p = lib.plan_matvec(1000, 1024, 2)
+        assert p["warps"] == 12
+        p = lib.plan_matvec(1000, 1024, 3)
         assert p["warps"] == 8
         lib.set_plan_override(warps=2, stages=3)
         p = lib.plan_matvec(1000, 4096, 1)
