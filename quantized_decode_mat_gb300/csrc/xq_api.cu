@@ -243,7 +243,8 @@ int64_t align128(int64_t v) { return (v + 127) & ~(int64_t)127; }
 // form: `rows` rows per expert, `slots` selected experts, each group inside
 // one slot, and `batch` staged activation vectors (1 shared, or one per slot).
 xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
-                    int64_t smem_optin, xq_plan *p, int64_t slots = 0, bool have_ws = false) {
+                    int64_t smem_optin, xq_plan *p, int64_t slots = 0, bool have_ws = false,
+                    int fuse = 0) {
     const int32_t nb = (int32_t)(cols / 256);
     const int32_t R = (nb < 32 && 32 % nb == 0) ? 32 / nb : 1;
     const int32_t spr = R > 1 ? 1 : (nb + 31) / 32;
@@ -257,7 +258,7 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     const int64_t act = align128((int64_t)bl * nb * kActStride);
     if (slots > 0 && bl != batch)
         return fail(XQ_ESHAPE, "the per-slot activations do not fit in shared memory");
-    const int32_t wmax = warps_limit(fmt, slots > 0 ? 1 : bl);
+    const int32_t wmax = warps_limit(fmt, slots > 0 ? 1 : bl, fuse);
     const int32_t ow = g_override_warps.load(), os = g_override_stages.load();
     const int32_t om = g_override_row_block.load();
     // Two stages (one box in flight per warp while the other is consumed) read
@@ -279,7 +280,15 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     const int64_t units = (groups + M - 1) / M;
     const int32_t grid = (int32_t)(units < sm_count ? units : sm_count);
     const int64_t per_cta = (units + grid - 1) / grid;
-    int32_t W = (int32_t)(per_cta < wmax ? per_cta : wmax);
+    const int32_t oq = g_override_quantise_once.load();
+    const bool qonce = have_ws && (oq == 2 || (oq == 0 && (int64_t)bl * nb >= kQuantOnceMinBlocks));
+    // Batch 1: 16 warps, the fastest for Q4_K boxes of whole rows (20: 46.1
+    // against 44.6 us on 128256 x 4096) and for the fused forms; 20 for the
+    // mat-vec behind a quantise launch (4096 x 14336 step: 8.23 against 9.15
+    // us) and for raw codebook blocks (11008 x 4096 step: 7.42 against 7.63 us)
+    const bool wide1 = slots == 0 && (qonce || fmt == kCB4);
+    const int32_t wpref = bl == 1 && !wide1 && wmax > 16 ? 16 : wmax;
+    int32_t W = (int32_t)(per_cta < wpref ? per_cta : wpref);
     if (ow > 0) W = ow < wmax ? ow : wmax;
     // above 8 warps, whole warps a scheduler (12, 16) with two stages each;
     // where those do not fit, the next such count down
@@ -311,17 +320,16 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     p->launches = (int32_t)((batch + bl - 1) / bl);
     p->smem_bytes = bytes(W, S, M);
     p->row_block = M;
-    const int32_t oq = g_override_quantise_once.load();
-    p->quantise_once = have_ws && (oq == 2 || (oq == 0 && (int64_t)bl * nb >= kQuantOnceMinBlocks));
+    p->quantise_once = qonce;
     return XQ_OK;
 }
 
 // When every CTA quantises the activation itself, its warps share that work
 // one q8 block each; a plan with fewer warps than blocks (few rows a CTA) gets
 // more warps, which find no row group of their own and only quantise.
-void widen_for_quantise(xq_plan *p, int fmt, int64_t nb, int64_t smem_optin) {
+void widen_for_quantise(xq_plan *p, int fmt, int fuse, int64_t nb, int64_t smem_optin) {
     const int64_t nblk = (int64_t)p->batch_per_launch * nb;
-    const int32_t wmax = warps_limit(fmt, p->batch_per_launch);
+    const int32_t wmax = warps_limit(fmt, p->batch_per_launch, fuse);
     int32_t W = p->warps;
     const int64_t want = nblk < wmax ? nblk : wmax;
     if (W >= want) return;
@@ -401,7 +409,7 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     if (xq_status s = device_state(&dev)) return s;
     xq_plan plan;
     if (xq_status s = make_plan(op.fmt, rows, cols, batch, dev->sm_count, dev->smem_optin, &plan,
-                                0, want_ws && op.kind == Kind::kLinear))
+                                0, want_ws && op.kind == Kind::kLinear, norm ? 2 : 0))
         return s;
     MatvecArgs a;
     memset(&a, 0, sizeof a);
@@ -418,7 +426,7 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     // quantise once: q8 blocks into the workspace, then the mat-vec on them
     const bool once = plan.quantise_once != 0;
     if (fused && !once && g_override_warps.load() == 0)  // an override is kept as given
-        widen_for_quantise(&plan, op.fmt, nb, dev->smem_optin);
+        widen_for_quantise(&plan, op.fmt, norm ? 2 : 1, nb, dev->smem_optin);
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int kind = dots ? 1 : norm ? 4 : (fused && !once) ? 2 : 0;

@@ -42,14 +42,16 @@ enum Format { kQ4K = 0, kCB4 = 1, kCB4R = 2 };
 // Largest warps per CTA of an instantiation (format, batch), which its
 // register budget allows no more.  Each of the SM's four schedulers has a
 // quarter of the register file, so the cap is set by the warps a scheduler
-// holds: 16 warps (4 a scheduler) allow 128 registers a thread, 12 allow 168,
-// 8 allow 255.  Q4_K: 16 at batch 1, 12 at batch 2, 8 above (its row-blocked
-// kernels need up to 211).  Codebook: 16 up to batch 4 (98-128 registers), 8
-// above (12 measured slower there).  Warp counts that split unevenly over the
-// schedulers measured slower.
-constexpr int warps_limit(int fmt, int64_t batch) {
-    return fmt == kQ4K ? (batch == 1 ? 16 : batch == 2 ? 12 : kMaxWarps)
-                       : (batch <= 4 ? 16 : kMaxWarps);
+// holds: 20 warps (5 a scheduler) allow 96 registers a thread, 16 allow 128,
+// 12 allow 168, 8 allow 255.  Batch 1: 20 (72-95 registers), but 16 for
+// the fused RMSNorm form (fuse 2), whose one-warp norm pass ran slower in 96
+// registers.  Q4_K: 12 at batch 2, 8 above (its row-blocked kernels need up
+// to 211).  Codebook: 16 up to batch 4 (98-128 registers), 8 above (12
+// measured slower there).  Warp counts that split unevenly over the
+// schedulers measured slower.  The planner may use fewer (see make_plan).
+constexpr int warps_limit(int fmt, int64_t batch, int fuse = 0) {
+    return batch == 1 ? (fuse == 2 ? 16 : 20)
+                      : fmt == kQ4K ? (batch == 2 ? 12 : kMaxWarps) : (batch <= 4 ? 16 : kMaxWarps);
 }
 
 struct MatvecArgs {

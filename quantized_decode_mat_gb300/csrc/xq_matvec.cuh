@@ -491,14 +491,14 @@ __device__ __forceinline__ GroupInfo group_info(const MatvecArgs &a, int64_t g, 
 // copies and the CTA's other warps cover them).  (Requesting all S stages
 // before the activation is staged measured slower.)  The act stride puts the
 // chunks that one instruction reads on distinct bank groups.
-template <int FMT, int B>
-constexpr int max_threads() { return warps_limit(FMT, B) * 32; }
+template <int FMT, int B, int FUSE>
+constexpr int max_threads() { return warps_limit(FMT, B, FUSE) * 32; }
 
 // M: row groups a warp works on at once (a work unit).  Two for Q4_K with
 // several activation vectors, where the activation loads from shared memory
 // are the limit; one otherwise.
 template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M>
-__global__ void __launch_bounds__(max_threads<FMT, B>(), 1) xq_matvec_kernel(const MatvecArgs a) {
+__global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kernel(const MatvecArgs a) {
     static_assert(!ID || (B == 1 && !DOTS && FUSE == 0), "the grouped form is batch 1 on q8 input");
     static_assert(M == 1 || (M == 2 && FMT == kQ4K && !ID), "row blocking is a Q4_K form");
     static_assert(FUSE >= 0 && FUSE <= 2, "FUSE: 0 q8 input, 1 quantise x, 2 RMSNorm then quantise");
