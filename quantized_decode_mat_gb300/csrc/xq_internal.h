@@ -31,6 +31,14 @@ constexpr int kActNormAt = 320;
 // q8 blocks whose activation values one warp loads at once in the fused
 // kernels at batch 1 (one L2 round trip per group; twice as many above).
 constexpr int kQuantGroup = 4;
+// Staging of q8 blocks into shared memory: from kStageAsyncBlocks blocks up
+// (Q4_K), asynchronous copies all in flight at once (4096 x 14336 at batch 8:
+// 23.5 against 31.4 us for one load a thread at a time); below, and for the
+// codebook (whose reordering pass then runs after the copies and measured
+// slower), loads issued kStageItems items (16 or 32 bytes each) at a time
+// before any store (4 and 8 measured alike; 4 keeps the registers low).
+constexpr int kStageAsyncBlocks = 64;
+constexpr int kStageItems = 4;
 constexpr int kMaxWarps = 8;
 constexpr int kMaxStages = 8;
 

@@ -647,7 +647,6 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
     grid_dependency_trigger();  // the next launch may start its own prologue
 
     // 2. the activation (a different region of shared memory than the stages)
-    auto ld16 = [](const uint4 *p) { return __ldg(p); };  // q8 blocks: a kernel input
     if (FUSE == 1 || FUSE == 2) {
         // quantise x (FUSE == 2: y = x * scale) here: warp w takes blocks w,
         // w+W, ... (vector-major) with the standalone producers' arithmetic,
@@ -720,31 +719,93 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
                 }
             }
         }
+    } else if (FMT == kQ4K && nvec * nb >= kStageAsyncBlocks) {
+        // Many q8 blocks: bytes 0..303 of every block by asynchronous copies,
+        // all in flight at once (one commit group after the prologue's weight
+        // boxes, so waiting for it waits for those too), then each block's
+        // split sums from its staged int32 sums.
+        const int nblk = nvec * nb;
+        const uint32_t act_u32 = smem_u32(act);
+        for (int i = threadIdx.x; i < nblk * 19; i += blockDim.x) {
+            const int blk = i / 19, piece = i - 19 * blk;
+            cp_async_16(act_u32 + (uint32_t)(blk * kActStride + 16 * piece),
+                        a.xq + (int64_t)blk * kQ8Bytes + 16 * piece);
+        }
+        cp_async_commit();
+        cp_async_wait_pending(0);
+        __syncthreads();
+        for (int blk = threadIdx.x; blk < nblk; blk += blockDim.x) {
+            const uint4 *sums = reinterpret_cast<const uint4 *>(act + blk * kActStride + kQ8SumAt);
+            const uint4 sp = split_sums(sums[0], sums[1]);
+            *reinterpret_cast<uint4 *>(act + blk * kActStride + kActSplitAt) = sp;
+        }
     } else if (FMT == kQ4K) {
-        // bytes 0..303 of every q8 block, then its split sums
-        for (int i = threadIdx.x; i < nvec * nb * 20; i += blockDim.x) {
-            const int blk = i / 20, piece = i - 20 * blk;
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
-            *reinterpret_cast<uint4 *>(act + blk * kActStride + 16 * piece) =
-                piece < 19 ? ld16(src + piece) : split_sums(ld16(src + 16), ld16(src + 17));
+        // Few q8 blocks: bytes 0..303 of every block, then its split sums
+        // (item 19 of the block, from its int32 sums), by loads and stores:
+        // each thread issues the loads of kStageItems items before it stores
+        // any, one L2 round trip per group of items, and the weight boxes
+        // already in flight are not waited for here.
+        const int n = nvec * nb * 20;
+        for (int i0 = threadIdx.x; i0 < n; i0 += kStageItems * blockDim.x) {
+            uint4 u[kStageItems], v[kStageItems];
+#pragma unroll
+            for (int j = 0; j < kStageItems; ++j) {
+                const int i = i0 + j * blockDim.x;
+                v[j] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < n) {
+                    const int blk = i / 20, piece = i - 20 * blk;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
+                    u[j] = __ldg(src + (piece < 19 ? piece : 16));
+                    if (piece == 19) v[j] = __ldg(src + 17);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kStageItems; ++j) {
+                const int i = i0 + j * blockDim.x;
+                if (i < n) {
+                    const int blk = i / 20, piece = i - 20 * blk;
+                    *reinterpret_cast<uint4 *>(act + blk * kActStride + 16 * piece) =
+                        piece < 19 ? u[j] : split_sums(u[j], v[j]);
+                }
+            }
         }
     } else {
-        // the values of every q8 block in interleaved order (one 32-value
-        // sub-block an item), then bytes 256..303
-        for (int i = threadIdx.x; i < nvec * nb * 11; i += blockDim.x) {
-            const int blk = i / 11, part = i - 11 * blk;
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
-            uint4 *dst = reinterpret_cast<uint4 *>(act + blk * kActStride);
-            if (part < 8) {
-                const uint4 x0 = ld16(src + 2 * part), x1 = ld16(src + 2 * part + 1);
-                const uint32_t in[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                dst[2 * part] = make_uint4(interleave_lo(in[0], in[4]), interleave_hi(in[0], in[4]),
-                                           interleave_lo(in[1], in[5]), interleave_hi(in[1], in[5]));
-                dst[2 * part + 1] =
-                    make_uint4(interleave_lo(in[2], in[6]), interleave_hi(in[2], in[6]),
-                               interleave_lo(in[3], in[7]), interleave_hi(in[3], in[7]));
-            } else {
-                dst[8 + part] = ld16(src + 8 + part);  // pieces 16..18
+        // The values of every q8 block in interleaved order (one 32-value
+        // sub-block an item), then bytes 256..303 (three items of one piece),
+        // loads issued kStageItems items at a time as above.
+        const int n = nvec * nb * 11;
+        for (int i0 = threadIdx.x; i0 < n; i0 += kStageItems * blockDim.x) {
+            uint4 u[kStageItems], v[kStageItems];
+#pragma unroll
+            for (int j = 0; j < kStageItems; ++j) {
+                const int i = i0 + j * blockDim.x;
+                v[j] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < n) {
+                    const int blk = i / 11, part = i - 11 * blk;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(a.xq + (int64_t)blk * kQ8Bytes);
+                    u[j] = __ldg(src + (part < 8 ? 2 * part : 8 + part));
+                    if (part < 8) v[j] = __ldg(src + 2 * part + 1);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kStageItems; ++j) {
+                const int i = i0 + j * blockDim.x;
+                if (i < n) {
+                    const int blk = i / 11, part = i - 11 * blk;
+                    uint4 *dst = reinterpret_cast<uint4 *>(act + blk * kActStride);
+                    if (part < 8) {
+                        const uint32_t in[8] = {u[j].x, u[j].y, u[j].z, u[j].w,
+                                                v[j].x, v[j].y, v[j].z, v[j].w};
+                        dst[2 * part] =
+                            make_uint4(interleave_lo(in[0], in[4]), interleave_hi(in[0], in[4]),
+                                       interleave_lo(in[1], in[5]), interleave_hi(in[1], in[5]));
+                        dst[2 * part + 1] =
+                            make_uint4(interleave_lo(in[2], in[6]), interleave_hi(in[2], in[6]),
+                                       interleave_lo(in[3], in[7]), interleave_hi(in[3], in[7]));
+                    } else {
+                        dst[8 + part] = u[j];  // pieces 16..18
+                    }
+                }
             }
         }
     }
