@@ -268,7 +268,7 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     // the instantiation's full warp count of two-box stages does not fit in
     // shared memory beside the activations, a single stage a warp (the warps
     // overlap one another's copies) measured faster than fewer warps or one
-    // row group (4096 x 14336 at batch 8: 32.9 against 34.4 us); if even that
+    // row group (4096 x 14336 at batch 8: 23.5 against 26.5 us); if even that
     // does not fit, one row group.
     int32_t M = (fmt == kQ4K && bl >= 2 && slots == 0) ? 2 : 1;
     if (om > 0) M = (om >= 2 && M == 2) ? 2 : 1;
