@@ -46,14 +46,15 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float *__restric
 
 // ---- RMSNorm + q8 pack -------------------------------------------------------------
 // Grid (ceil(nb/8), batch), 256 threads: block (c, b) owns q8 blocks 8c ..
-// 8c+7 of vector b, one per warp.  Each warp loads its block's values, warp
-// 0 takes the scale in the fixed order (rms_scale_warp; every CTA of the
-// vector gets the same bits), then each warp writes y = x * scale (when y
-// is non-null) and its q8 block via q8_quantize_lane.
+// 8c+7 of vector b, one per warp.  Each warp loads its block's values, the
+// block's 256 threads take the scale in the fixed order (rms_scale_block,
+// the workgroup itself; every CTA of the vector gets the same bits), then
+// each warp writes y = x * scale (when y is non-null) and its q8 block via
+// q8_quantize_lane.
 __global__ void __launch_bounds__(256) rmsnorm_q8_kernel(const float *__restrict__ x,
                                                          uint8_t *__restrict__ xq,
                                                          float *__restrict__ y, int64_t cols) {
-    __shared__ float s_scale;
+    __shared__ float s_wave[8];
     grid_dependency_wait();  // x may come from the kernel before on the stream
     grid_dependency_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -66,13 +67,8 @@ __global__ void __launch_bounds__(256) rmsnorm_q8_kernel(const float *__restrict
         u = __ldg(src);
         v = __ldg(src + 1);
     }
-    if (warp == 0) {
-        const float sc = rms_scale_warp(xv, cols, lane);
-        if (lane == 0) s_scale = sc;
-    }
-    __syncthreads();
+    const float scale = rms_scale_block(xv, cols, s_wave);
     if (k >= nb) return;  // whole warps
-    const float scale = s_scale;
     float vals[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) vals[i] = __fmul_rn(vals[i], scale);

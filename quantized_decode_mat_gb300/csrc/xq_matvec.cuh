@@ -667,13 +667,26 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
             }
         };
         load_group(warp);  // in flight while the RMSNorm scale is taken
-        // FUSE == 2: warp w takes the RMSNorm scale of vectors w, w+W, ...
-        // and parks it in bytes 320..335 of the vector's first staged block
-        // (stride padding that nothing else reads or writes)
+        // FUSE == 2: the RMSNorm scale of each vector (warp w takes vectors
+        // w, w+W, ...; one vector with eight warps or more, warps 0..7
+        // together) is parked in bytes 320..335 of the vector's first staged
+        // block (stride padding that nothing else reads or writes)
         if (FUSE == 2) {
-            for (int b = warp; b < B; b += W) {
-                const float sc = rms_scale_warp(a.x + (int64_t)b * nb * 256, (int64_t)nb * 256, lane);
-                if (lane == 0) *reinterpret_cast<float *>(act + b * act_bstride + kActNormAt) = sc;
+            if (B == 1 && W >= 8) {
+                // one vector and eight warps or more: warps 0..7 are the
+                // workgroup (rms_scale_block: one L2 round trip per 32 rows
+                // instead of per 8); its wave partials meet in warp 0's last
+                // stage, to which no copy is issued before the main loop
+                if (warp < 8) {
+                    float *s_wave = reinterpret_cast<float *>(smem + act_bytes + (S - 1) * unit_bytes);
+                    const float sc = rms_scale_block(a.x, (int64_t)nb * 256, s_wave, true);
+                    if (threadIdx.x == 0) *reinterpret_cast<float *>(act + kActNormAt) = sc;
+                }
+            } else {
+                for (int b = warp; b < B; b += W) {
+                    const float sc = rms_scale_warp(a.x + (int64_t)b * nb * 256, (int64_t)nb * 256, lane);
+                    if (lane == 0) *reinterpret_cast<float *>(act + b * act_bstride + kActNormAt) = sc;
+                }
             }
             __syncthreads();
         }

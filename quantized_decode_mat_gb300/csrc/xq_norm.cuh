@@ -55,4 +55,45 @@ __device__ __forceinline__ float rms_scale_warp(const float *__restrict__ x, int
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, 1e-5f)));
 }
 
+// The same scale evaluated by the workgroup itself: 256 threads, thread t is
+// item t (t = threadIdx.x), the wave butterfly is a shuffle butterfly and the
+// eight wave partials meet in s_wave (8 floats of shared memory).  Each thread
+// loads 32 of its rows before adding any, so a vector of n values takes
+// ceil(n / 8192) L2 round trips (one warp alone needs one per 8 rows); a row
+// past the end adds an exact zero (the partial sums are never negative).
+// Every thread of the block must call (with named: threads 0..255 only, which
+// then meet at barrier 1 instead of the block barrier); every calling thread
+// returns the scale.
+__device__ __forceinline__ float rms_scale_block(const float *__restrict__ x, int64_t n,
+                                                 float *s_wave, bool named = false) {
+    const int t = threadIdx.x;
+    const int64_t rows = n / 256;
+    float s = 0.0f;
+    for (int64_t k = 0; k < rows; k += 32) {
+        const float *p = x + k * 256 + t;
+        float v[32];
+        if (k + 32 <= rows) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __ldg(p + j * 256);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = k + j < rows ? __ldg(p + j * 256) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s = __fadd_rn(s, __fmul_rn(v[j], v[j]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
+    if ((t & 31) == 0) s_wave[t >> 5] = s;
+    if (named)
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+    else
+        __syncthreads();
+    float total = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) total = __fadd_rn(total, s_wave[w]);
+    const float mean = __fdiv_rn(total, (float)n);
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, 1e-5f)));
+}
+
 }  // namespace xq

@@ -434,8 +434,10 @@ def test_norm_linear_is_rmsnorm_then_matvec(xq, orc, fmt, rows, cols, batch):
 
 
 def test_norm_linear_with_few_and_many_warps(xq, orc):
-    """Plans of 1, 3 and 16 warps: one warp takes all eight waves of the
-    reduction, three take them round robin, sixteen leave eight idle."""
+    """Plans of 1, 3, 7, 8 and 16 warps and 1 to 3 stages: below eight warps
+    one warp walks each vector for its scale; from eight up warps 0..7 are
+    the workgroup, their partials meeting in warp 0's last stage.  The same
+    bits every way."""
     rows, cols = 2048, 4096
     W = _weights("q4k", rows, cols, 91)
     x = synthetic.activations(1, cols, 92)
@@ -443,11 +445,12 @@ def test_norm_linear_with_few_and_many_warps(xq, orc):
     y_ref = orc.matvec_q4k(W, xq_ref, rows, cols, 1)
     ys = []
     try:
-        for w in (1, 3, 16):
-            xq.set_plan_override(w, 0)
+        for w, st in ((1, 0), (3, 0), (7, 0), (8, 0), (8, 1), (16, 0), (16, 1), (16, 3)):
+            xq.set_plan_override(w, st)
             y = xq.norm_linear_q4k(dev(x), dev(W), rows, cols)
             torch.cuda.synchronize()
             assert xq.last_plan()["warps"] == w
+            assert st == 0 or xq.last_plan()["stages"] == st
             ys.append(y.cpu().numpy())
     finally:
         xq.set_plan_override(0, 0)
