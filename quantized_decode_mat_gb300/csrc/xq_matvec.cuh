@@ -904,13 +904,16 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
                 int base, nlive, keep;
                 halving_reduce<P>(h, l, width, lane, base, nlive, keep);
                 if ((lane & keep) == 0 && rig < gi[m].valid) {
-                    const int64_t orow = gi[m].out0 + rig;
+                    float *yb = a.y + (int64_t)base * rows + gi[m].out0 + rig;
                     const float nan = __int_as_float(0x7FC00000);
+                    if (P == 1 || nlive == 1) {  // rows of P lanes or more: one value a lane
+                        if (base < B) yb[0] = gi[m].bad ? nan : __fadd_rn(h[0], l[0]);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < P; ++i)
-                        if (i < nlive && base + i < B)
-                            a.y[(int64_t)(base + i) * rows + orow] =
-                                gi[m].bad ? nan : __fadd_rn(h[i], l[i]);
+                        for (int i = 0; i < P; ++i)
+                            if (i < nlive && base + i < B)
+                                yb[(int64_t)i * rows] = gi[m].bad ? nan : __fadd_rn(h[i], l[i]);
+                    }
                     if (ID && gi[m].bad && rig == 0 && (lane & (width - 1)) == 0)
                         atomicOr(a.status, kStatusBadExpertId);
                 }
