@@ -621,3 +621,23 @@ def test_binding_rejects_short_buffers(xq):
             call()
     torch.cuda.synchronize()
     assert [xq.launch_count(i) for i in range(xq.COUNT_N)] == counts
+
+
+@pytest.mark.parametrize("fmt", ["q4k", "cb4"])
+@pytest.mark.parametrize("rows,cols,batch", [(300, 8192, 2), (257, 7936, 3), (64, 16384, 4), (100, 4096, 8)])
+def test_batch_vectors_are_independent(xq, orc, fmt, rows, cols, batch):
+    """Each vector of a batch gets the bits it gets alone: the staging of the
+    q8 blocks (asynchronous copies from 64 Q4_K blocks a launch, grouped
+    loads below; the shapes straddle that threshold), the row blocking and
+    the reduction never mix vectors."""
+    kv = synthetic.cb4_table()
+    W = _weights(fmt, rows, cols, 17)
+    x = synthetic.activations(batch, cols, 18)
+    xq_dev = run_quantize(xq, x)
+    y = run_matvec(xq, fmt, W, kv, xq_dev, rows, cols, batch)
+    for b in range(batch):
+        yb = run_matvec(xq, fmt, W, kv, xq_dev[b:b + 1].contiguous(), rows, cols, 1)
+        assert np.array_equal(y[b], yb[0]), f"vector {b}"
+    check_y(y, (orc.matvec_q4k if fmt == "q4k" else
+                (lambda W_, q, r, c, n: orc.matvec_cb4(W_, kv, q, r, c, n)))(
+        W, orc.quantize_q8(x), rows, cols, batch), f"{fmt} batch {batch}")
