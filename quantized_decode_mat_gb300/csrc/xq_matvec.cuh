@@ -281,7 +281,7 @@ __device__ __forceinline__ void cb4_decode(uint32_t q, const uint32_t (&T)[4], u
 // (block k's 16 payload bytes, little-endian), against the interleaved q8
 // block `act`.  Block by block: decode, then its dot with every vector; per
 // vector the compensated sum over the blocks runs in block order.
-template <int B, bool DOTS, class Act>
+template <int B, bool DOTS, bool FIRST, class Act>
 __device__ __forceinline__ void cb4_blocks(const float (&dk)[8], const uint32_t (&P)[8][4],
                                            const Act &act, const uint32_t (&T)[4], float (&hi)[B],
                                            float (&lo)[B], int32_t *dots, int64_t dots_bstride) {
@@ -307,7 +307,12 @@ __device__ __forceinline__ void cb4_blocks(const float (&dk)[8], const uint32_t 
             dt = dp4a(F[7], a1.w, dt);
             float p, e;
             two_prod(dk[k], __int2float_rn(dt), p, e);  // |dt| < 2^20: exact in f32
-            acc_add(ch[b], cl[b], p, e);
+            if (k == 0) {  // an exact add to zero is an assignment
+                ch[b] = p;
+                cl[b] = e;
+            } else {
+                acc_add(ch[b], cl[b], p, e);
+            }
             if (DOTS && dots != nullptr) dots[b * dots_bstride + k] = dt;
         }
     }
@@ -316,13 +321,18 @@ __device__ __forceinline__ void cb4_blocks(const float (&dk)[8], const uint32_t 
         const float xs = act.xs(b);
         float t, te;
         two_prod(ch[b], xs, t, te);
-        acc_add(hi[b], lo[b], t, __fmaf_rn(cl[b], xs, te));
+        if (FIRST) {  // the lane's first chunk of the row: (hi, lo) holds nothing yet
+            hi[b] = t;
+            lo[b] = __fmaf_rn(cl[b], xs, te);
+        } else {
+            acc_add(hi[b], lo[b], t, __fmaf_rn(cl[b], xs, te));
+        }
     }
 }
 
 // Raw layout: w is this lane's 144-byte chunk (eight 18-byte blocks) in
 // shared memory.
-template <int B, bool DOTS, class Act>
+template <int B, bool DOTS, bool FIRST, class Act>
 __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const Act &act,
                                           const uint32_t (&T)[4], float (&hi)[B], float (&lo)[B],
                                           int32_t *dots, int64_t dots_bstride) {
@@ -351,7 +361,7 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const A
             P[2 * p + 1][i] = v[9 * p + 5 + i];
         }
     }
-    cb4_blocks<B, DOTS>(dk, P, act, T, hi, lo, dots, dots_bstride);
+    cb4_blocks<B, DOTS, FIRST>(dk, P, act, T, hi, lo, dots, dots_bstride);
 }
 
 // ---- resident codebook rows: the staged slot map ------------------------------------
@@ -364,7 +374,7 @@ __device__ __forceinline__ uint32_t cb4r_payload_slot(int slot, int i) {
     return 144u * (uint32_t)slot + 16u + 16u * (uint32_t)i;
 }
 
-template <int B, bool DOTS, class Act>
+template <int B, bool DOTS, bool FIRST, class Act>
 __device__ __forceinline__ void cb4r_chunk(const uint8_t *__restrict__ w, const Act &act,
                                            const uint32_t (&T)[4], float (&hi)[B],
                                            float (&lo)[B], int32_t *dots, int64_t dots_bstride) {
@@ -381,7 +391,7 @@ __device__ __forceinline__ void cb4r_chunk(const uint8_t *__restrict__ w, const 
         P[k][2] = t.z;
         P[k][3] = t.w;
     }
-    cb4_blocks<B, DOTS>(dk, P, act, T, hi, lo, dots, dots_bstride);
+    cb4_blocks<B, DOTS, FIRST>(dk, P, act, T, hi, lo, dots, dots_bstride);
 }
 
 // ---- reduction of a row's partial sums -------------------------------------------------
@@ -882,10 +892,14 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
                     int32_t *dp = DOTS ? a.dots + (gi[0].row0 + rig) * dots_row + c * 8 : nullptr;
                     if (FMT == kQ4K)
                         q4k_chunk<B, DOTS>(st, as, hi[0], lo[0], dp, dots_bstride, s == 0);
+                    else if (FMT == kCB4 && spr == 1)  // one segment a row: the lane's first chunk
+                        cb4_chunk<B, DOTS, true>(st, as, T, hi[0], lo[0], dp, dots_bstride);
                     else if (FMT == kCB4)
-                        cb4_chunk<B, DOTS>(st, as, T, hi[0], lo[0], dp, dots_bstride);
+                        cb4_chunk<B, DOTS, false>(st, as, T, hi[0], lo[0], dp, dots_bstride);
+                    else if (spr == 1)
+                        cb4r_chunk<B, DOTS, true>(st, as, T, hi[0], lo[0], dp, dots_bstride);
                     else
-                        cb4r_chunk<B, DOTS>(st, as, T, hi[0], lo[0], dp, dots_bstride);
+                        cb4r_chunk<B, DOTS, false>(st, as, T, hi[0], lo[0], dp, dots_bstride);
                 }
             }
             __syncwarp();
