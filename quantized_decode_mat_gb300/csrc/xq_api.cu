@@ -286,7 +286,7 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     const int32_t wpref = bl == 1 && !wide1 && wmax > 16 ? 16 : wmax;
     int32_t W = (int32_t)(per_cta < wpref ? per_cta : wpref);
     if (ow > 0) W = ow < wmax ? ow : wmax;
-    // above 8 warps, whole warps a scheduler (12, 16) with two stages each;
+    // above 8 warps, whole warps a scheduler (12, 16, 20) with two stages each;
     // where those do not fit, the next such count down
     if (ow <= 0)
         while (W > kMaxWarps && bytes(W, S0, M) > smem_optin) W = (W - 1) / 4 * 4;
