@@ -306,8 +306,9 @@ typedef struct {
 xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t batch,
                          int32_t sm_count, int64_t smem_optin_bytes, xq_plan *plan);
 /* Override the automatic plan for sweeps: warps (up to the kernel's limit:
- * 20 at batch 1; Q4_K 12 at batch 2, 8 above; codebook 16 up to batch 4, 8
- * above) and stages (1..8), 0 = automatic.  Process-wide; not for concurrent
+ * 20 at batch 1, 16 for the fused RMSNorm form there; Q4_K 12 at batch 2, 8
+ * above; codebook 16 up to batch 4, 8 above) and stages (1..8), 0 =
+ * automatic.  Process-wide; not for concurrent
  * use with launches. */
 void xq_set_plan_override(int32_t warps, int32_t stages);
 /* Override the row groups a warp works on at once: 1, or 2 where the

@@ -491,6 +491,11 @@ def last_plan() -> dict:
 
 
 def set_plan_override(warps: int = 0, stages: int = 0) -> None:
+    """Force the warps a CTA (clamped to the kernel's limit: 20 at batch 1,
+    16 for the fused RMSNorm form there; Q4_K 12 at batch 2, 8 above;
+    codebook 16 up to batch 4, 8 above) and the stages a warp (1..8, lowered
+    until shared memory fits); 0 restores the automatic plan.  For sweeps
+    and tests: process-wide, not for use beside concurrent launches."""
     _set_override(warps, stages)
 
 
