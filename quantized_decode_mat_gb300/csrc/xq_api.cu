@@ -279,10 +279,11 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     const int32_t oq = g_override_quantise_once.load();
     const bool qonce = have_ws && (oq == 2 || (oq == 0 && (int64_t)bl * nb >= kQuantOnceMinBlocks));
     // Batch 1: 16 warps, the fastest for Q4_K boxes of whole rows (20: 46.1
-    // against 44.6 us on 128256 x 4096) and for the fused forms; 20 for the
-    // mat-vec behind a quantise launch (4096 x 14336 step: 8.23 against 9.15
-    // us) and for raw codebook blocks (11008 x 4096 step: 7.42 against 7.63 us)
-    const bool wide1 = slots == 0 && (qonce || fmt == kCB4);
+    // against 44.6 us on 128256 x 4096) and for the fused RMSNorm form; 20 for
+    // the mat-vec behind a quantise launch (4096 x 14336 step: 8.23 against
+    // 9.15 us) and for the codebook (11008 x 4096 step: 7.42 against 7.63 us,
+    // resident rows 8.88 against 9.08 us)
+    const bool wide1 = slots == 0 && (qonce || fmt != kQ4K);
     const int32_t wpref = bl == 1 && !wide1 && wmax > 16 ? 16 : wmax;
     int32_t W = (int32_t)(per_cta < wpref ? per_cta : wpref);
     if (ow > 0) W = ow < wmax ? ow : wmax;

@@ -1,4 +1,4 @@
-"""The wide plans: 20 warps a CTA at batch 1 (raw codebook blocks, and the
+"""The wide plans: 20 warps a CTA at batch 1 (codebook blocks, and the
 Q4_K mat-vec behind a quantise launch), 16 for the codebook at batch 2..4,
 12 for Q4_K at batch 2 and where 16 warps of two stages do not fit, and 16
 for the fused RMSNorm form.  Each shape is large enough that the planner
@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 # (format, rows, cols, batch, warps the step's plan takes)
 STEPS = [
     ("cb4", 6000, 4096, 1, 20),
-    ("cb4r", 6000, 4096, 1, 16),
+    ("cb4r", 6000, 4096, 1, 20),
     ("q4k", 4096, 14336, 1, 20),
     ("cb4", 5000, 4096, 2, 16),
     ("cb4", 5000, 4096, 3, 16),
