@@ -81,3 +81,54 @@ def test_random_shape(xq, orc, i):
              else orc.matvec_cb4(W, kv, xq_ref, rows, cols, batch))
     check_y(y, y_ref, f"random {i}: {fmt} {rows}x{cols} b{batch} overlap {overlap}")
     assert xq.device_status() == 0
+
+
+N_LARGE = 12
+
+
+def _draw_large(i):
+    rng = np.random.Generator(np.random.PCG64(5000 + i))
+    fmt = ("q4k", "cb4", "cb4r")[i % 3]
+    nb = int(rng.choice([4, 8, 16, 24, 31, 32, 40, 56, 64, 80]))
+    rows = int(rng.integers(2000, 20000))
+    batch = int(rng.integers(1, 9))
+    return fmt, rows, 256 * nb, batch, bool(i % 2), rng
+
+
+@pytest.mark.parametrize("i", range(N_LARGE))
+def test_random_large_shape(xq, orc, i):
+    """Seeded large shapes (2000..20000 rows), so the plans with many warps a
+    CTA, both q8 staging paths and the row blocking are drawn at random too:
+    the workspace step agrees bit for bit with the mat-vec on q8 blocks, and
+    with the oracle on a sample of rows."""
+    fmt, rows, cols, batch, overlap, rng = _draw_large(i)
+    seed = 31 * i + rows
+    kv = synthetic.cb4_table()
+    x = synthetic.activations(batch, cols, seed + 1, outlier_frac=0.001)
+    W = (synthetic.q4k_weights(rows, cols, seed) if fmt == "q4k"
+         else synthetic.cb4_weights(rows, cols, seed))
+    Wd = dev(W)
+    if fmt == "cb4r":
+        Wd = xq.repack_cb4(Wd, rows, cols)
+    xd = dev(x)
+    ws = torch.full((xq.linear_workspace_bytes(cols, batch),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    try:
+        xq.set_overlap_launches(overlap)
+        y = xq.linear_ws(fmt, xd, Wd, rows, cols, ws, table=kv)
+        q8 = xq.quantize_q8(xd)
+        y_mv = (xq.matvec_q4k(Wd, q8, rows, cols) if fmt == "q4k"
+                else xq.matvec_cb4(Wd, kv, q8, rows, cols) if fmt == "cb4"
+                else xq.matvec_cb4r(Wd, kv, q8, rows, cols))
+        torch.cuda.synchronize()
+    finally:
+        xq.set_overlap_launches(False)
+    y = y.cpu().numpy()
+    assert np.array_equal(y, y_mv.cpu().numpy())
+    sample = np.unique(rng.choice(rows, min(rows, 500), replace=False))
+    Ws = np.ascontiguousarray(W[sample])
+    xq_ref = orc.quantize_q8(x)
+    y_ref = (orc.matvec_q4k(Ws, xq_ref, len(sample), cols, batch) if fmt == "q4k"
+             else orc.matvec_cb4(Ws, kv, xq_ref, len(sample), cols, batch))
+    check_y(y[:, sample], y_ref, f"{fmt} {rows}x{cols} b{batch}")
+    assert xq.device_status() == 0
