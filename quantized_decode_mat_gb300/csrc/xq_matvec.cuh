@@ -506,8 +506,10 @@ constexpr int max_threads() { return warps_limit(FMT, B, FUSE) * 32; }
 
 // M: row groups a warp works on at once (a work unit).  Two for Q4_K with
 // several activation vectors, where the activation loads from shared memory
-// are the limit; one otherwise.
-template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M>
+// are the limit; one otherwise.  WR: a build for boxes of whole rows only
+// (R > 1), where the segment bookkeeping folds away at compile time; the
+// row-blocked launches take it when the plan's rows per group exceed one.
+template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M, bool WR = false>
 __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kernel(const MatvecArgs a) {
     static_assert(!ID || (B == 1 && !DOTS && FUSE == 0), "the grouped form is batch 1 on q8 input");
     static_assert(M == 1 || (M == 2 && FMT == kQ4K && !ID), "row blocking is a Q4_K form");
@@ -520,7 +522,8 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
     const int S = a.stages;
     const int nb = a.nb;
     const int R = a.rows_per_group;
-    const int spr = a.segments;
+    const bool whole = WR || R > 1;  // whole rows in a box (WR: known at compile time)
+    const int spr = WR ? 1 : a.segments;
     const int64_t rows = a.rows;
     const int64_t ngroups = a.groups;
     const int64_t row_bytes = (int64_t)nb * kChunkBytes;
@@ -556,7 +559,7 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
     if (FMT == kCB4R) {
 #pragma unroll
         for (int k = 0; k < 9; ++k) {
-            if (R > 1) {
+            if (whole) {
                 // pieces per resident row: 9 * nb, nb a power of two here
                 const int q = lane + 32 * k, rp = 9 * nb;
                 const int rig = (q >> (31 - __clz(nb))) / 9, r = q - rig * rp;
@@ -575,7 +578,7 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
             const uint8_t *rowp = a.W + gi.row0 * row_bytes;
             if (gi.bad) {
                 // an invalid expert id reads nothing
-            } else if (R > 1) {
+            } else if (whole) {
                 const int valid = gi.valid * (int)row_bytes;
 #pragma unroll
                 for (int k = 0; k < 9; ++k)
@@ -595,7 +598,7 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
         } else {
             const uint8_t *src0;
             int valid;  // bytes of the box that exist in W
-            if (R > 1) {
+            if (whole) {
                 src0 = a.W + gi.row0 * row_bytes;
                 valid = gi.valid * (int)row_bytes;
             } else {
@@ -836,8 +839,8 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
 
     const int64_t dots_row = (int64_t)nb * 8;
     const int64_t dots_bstride = rows * dots_row;
-    const int width = R > 1 ? nb : 32;  // lanes that share a row
-    const int rig = R > 1 ? lane / nb : 0;  // this lane's row within a group
+    const int width = whole ? nb : 32;  // lanes that share a row
+    const int rig = whole ? lane / nb : 0;  // this lane's row within a group
     int c_stage = 0;
     for (int64_t u = gw; u < nunits; u += TW) {
         GroupInfo gi[M];
@@ -862,7 +865,7 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
             cp_async_commit();
             cp_async_wait_pending(S - 1);  // this lane's copies of the stage landed
             __syncwarp();                  // ... and every other lane's
-            const int c = R > 1 ? (lane & (nb - 1)) : s * 32 + lane;
+            const int c = whole ? (lane & (nb - 1)) : s * 32 + lane;
             const uint8_t *st = stage0 + c_stage * unit_bytes + lane * kChunkBytes;
             // (M > 1 reads the activation of chunks past the row's end too, and
             // multiplies it by zero-filled weights: a real block keeps it finite)
@@ -940,12 +943,23 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
 template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>
 inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, size_t smem,
                                    cudaStream_t s) {
+    if constexpr (M == 2) {  // row blocking: a build for whole-row boxes
+        if (a.rows_per_group > 1)
+            return launch_kernel(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, true>, grid, block,
+                                 smem, s, a.overlap != 0, a);
+    }
     return launch_kernel(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M>, grid, block, smem, s,
                          a.overlap != 0, a);
 }
 
 template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>
 inline cudaError_t configure_t(int smem_optin) {
+    if constexpr (M == 2) {
+        const cudaError_t e = cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, true>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   smem_optin);
+        if (e != cudaSuccess) return e;
+    }
     return cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
 }
