@@ -1,33 +1,45 @@
 """Benchmark of the 4-bit decode mat-vec on the integer route.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--case NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--rounds R]
+                    [--impl ours|reference] [--case NAME]
 
 One step = one pass of the whole hot path over one batch: the decode step
-xq_linear_q4k_ws (quantise the f32 activation to q8 blocks and the Q4_K
-mat-vec; one fused launch for small activations, a quantise launch into the
-workspace and the mat-vec for wide or batched ones), inputs resident in HBM,
-with overlapped launches (--overlap on, the default: the weights are constant,
-so a step may start streaming them while the previous step finishes; the step
-without overlap is timed beside it).
-The one-launch fused form, the two-call path (xq_quantize_q8 + xq_matvec_q4k)
-and the mat-vec alone on q8 input are timed beside it for the breakdown.  Default workload: the L2-exceeding vocabulary
-projection, Q4_K 128256 x 4096, batch 1 (W = 295.5 MB, larger than the 129 MB
-L2, so no flush is needed between steps).  Steps are replayed from CUDA graphs
-and timed with CUDA events on the launching stream.
+xq_linear_*_ws (quantise the f32 activation to q8 blocks and the mat-vec; one
+fused launch for small activations, a quantise launch into the workspace and
+the mat-vec for wide or batched ones), inputs resident in HBM, with
+overlapped launches (--overlap on, the default: the weights are constant, so
+a step may start streaming them while the previous step finishes; the step
+without overlap is timed beside it).  Default workload: the L2-exceeding
+vocabulary projection, Q4_K 128256 x 4096, batch 1 (W = 295.5 MB, larger than
+the 129 MB L2).  A W larger than the L2 is held twice and the steps alternate
+between the two copies, so no step can find its weights in L2 (the step on
+one copy is timed beside it).
+
+Timing: K steps are replayed from CUDA graphs and timed with CUDA events on
+the launching stream, bracketed by a barrier and a device synchronisation;
+this is done R times (rounds), interleaved with the mat-vec alone in ABBA
+order (step, mat-vec | mat-vec, step | ...), and ms_per_step is the median
+round.  The fused one-launch form, the two-call path (xq_quantize_q8 +
+mat-vec), the RMSNorm forms and, where they apply, the grouped-experts and
+repack arms are timed once each for the breakdown.
+
+Bytes: the metric's algorithmic bytes of one mat-vec are the weights once and
+the activation as q8 blocks, W + batch * q8; the y write is reported beside
+them, not in them.
 
 Prints ONE JSON line (rank 0): value = achieved GB/s of algorithmic bytes per
-step (all ranks), ms_per_step, a roofline object for the mat-vec kernel timed
-alone, the end-to-end figure through the public API with host buffers, the CPU
-oracle baseline, the SM clocks sampled during the timed region.
+step (all ranks), ms_per_step, the rounds, a roofline object for the step's
+dominant kernel, the end-to-end figure through the public API with host
+buffers, the CPU oracle baseline (all cores and one thread), the SM clocks
+sampled during the timed region.
 
 --impl reference times the CPU oracle (the plain C reference implementation
 of the same method) on the host cores on a bounded row sample of the same
 workload; it is a deliberately slow baseline.
 
 Multi-GPU: replicas only (every rank runs the same single-GPU workload, no
-collective on the data path); under torchrun the timed region is bracketed by
-barriers and the slowest rank's time is used.
+collective on the data path); under torchrun every timed region is bracketed
+by barriers and the slowest rank's time is used.
 """
 from __future__ import annotations
 
@@ -35,6 +47,7 @@ import argparse
 import hashlib
 import json
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -56,19 +69,17 @@ NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "matvec_q4k_traffic.json")
 E2E_TRIALS = 3  # runs of each end-to-end form; the fastest is reported
+BYTES_FORMULA = "W + batch*q8: every weight byte once, the activation as q8 blocks; y not included"
 
 
 # ---------------------------------------------------------------- helpers
 def step_bytes(c) -> dict:
-    """Algorithmic bytes per call: every weight byte once, y written once, and
-    the activation as each path moves it.  linear: the fused step reads f32 x
-    (its q8 blocks never leave the SM); matvec: the mat-vec on q8 input reads
-    the q8 blocks; two_call: quantise (x in, q8 out) then the mat-vec."""
+    """Bytes of one mat-vec.  'algorithmic' is the metric's count: every weight
+    byte once and the activation as q8 blocks (W + batch*q8).  The f32
+    activation and the y write are listed beside it, not counted in it."""
     q8 = c.batch * (c.cols // 256) * 320
-    x = 4 * c.batch * c.cols
-    y = 4 * c.batch * c.rows
-    return {"weights": c.w_bytes, "linear": c.w_bytes + x + y,
-            "matvec": c.w_bytes + q8 + y, "two_call": c.w_bytes + x + 2 * q8 + y}
+    return {"weights": c.w_bytes, "q8": q8, "x": 4 * c.batch * c.cols,
+            "y": 4 * c.batch * c.rows, "algorithmic": c.w_bytes + q8}
 
 
 def source_digest() -> str:
@@ -167,6 +178,33 @@ class ClockSampler:
                 "samples": len(window), "scope": scope}
 
 
+def host_cores() -> int:
+    """Host cores this process may run on (its affinity mask)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
 def dist_env() -> tuple[int, int, int]:
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -237,11 +275,10 @@ class OracleRunner:
             f.result()
 
     def bytes_per_step(self) -> int:
-        """Algorithmic bytes of the sample, counted as for the fused step:
-        the weights once, x read once, y written once."""
+        """Algorithmic bytes of the sample, counted as for the GPU: the
+        sample's weights once and the activation as q8 blocks."""
         c = self.c
-        w = self.rows * (c.cols // 256) * 144
-        return w + 4 * c.batch * c.cols + 4 * c.batch * self.rows
+        return self.rows * (c.cols // 256) * 144 + c.batch * (c.cols // 256) * 320
 
     def close(self):
         self.pool.shutdown()
@@ -276,8 +313,23 @@ def oracle_rate(c, wall_budget_s: float, threads: int) -> dict:
     out = {"value": r.bytes_per_step() / sec / 1e9, "unit": "GB/s", "cores": r.threads,
            "kind": "oracle", "sec_per_pass": sec,
            "sample": f"{r.rows} of {c.rows} rows x {c.cols} cols, batch {c.batch} (quantise + "
-                     f"mat-vec), {r.threads} host threads, {n} passes, {el:.1f} s wall"}
+                     f"mat-vec), {r.threads} host thread{'s' if r.threads > 1 else ''}, {n} "
+                     f"passes, {el:.1f} s wall"}
     r.close()
+    return out
+
+
+def cpu_baseline(c, wall_budget_s: float) -> dict:
+    """The oracle on every core of the affinity mask, with the same on one
+    thread beside it, and the host it ran on."""
+    cores = host_cores()
+    out = oracle_rate(c, wall_budget_s, cores)
+    out["single_thread"] = {k: v for k, v in oracle_rate(c, wall_budget_s, 1).items()
+                            if k in ("value", "unit", "sec_per_pass", "sample")}
+    out["affinity_cores"] = cores
+    out["cpu_model"] = cpu_model()
+    out["hostname"] = socket.gethostname()
+    out["bytes"] = BYTES_FORMULA
     return out
 
 
@@ -286,7 +338,7 @@ def run_reference(args, c):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    threads = os.cpu_count() or 1
+    threads = host_cores()
     budget = 90.0  # seconds for warm-up + timed steps together
     rows = calibrated_rows(c, threads, budget / (args.steps + args.warmup))
     r = OracleRunner(c, rows, threads)
@@ -306,7 +358,9 @@ def run_reference(args, c):
             "vs_baseline": None, "dtype": "int64 dots + f64 scaling", "data": "synthetic",
             "config": workload_config(c),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": r.threads,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "affinity_cores": threads,
+                             "cpu_model": cpu_model(), "hostname": socket.gethostname(),
+                             "bytes": BYTES_FORMULA},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -339,6 +393,11 @@ def run_ours(args, c):
     W = torch.from_numpy(c.weights()).to(dev)
     if c.fmt == "cb4r":  # resident rows, repacked once at bind time (not timed)
         W = xq.repack_cb4(W, c.rows, c.cols)
+    # A W larger than the L2 is held twice and consecutive steps alternate
+    # between the copies: a step's weights were last read two steps earlier,
+    # with a whole other W read in between, so none of it can still be in L2.
+    large = c.w_bytes > L2_BYTES
+    Ws = [W, W.clone()] if large else [W]
     x_np = c.x()
     x = torch.from_numpy(x_np).to(dev)
     kv = synthetic.cb4_table()
@@ -348,40 +407,46 @@ def run_ours(args, c):
     y = torch.empty((c.batch, c.rows), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def do_step():  # the whole hot path, one library call: quantise x, mat-vec
+    def do_step(i):  # the whole hot path, one library call: quantise x, mat-vec
+        xq.linear_ws(c.fmt, x, Ws[i % len(Ws)], c.rows, c.cols, ws, table=kv, out=y)
+
+    def do_step_one_buffer(i):
         xq.linear_ws(c.fmt, x, W, c.rows, c.cols, ws, table=kv, out=y)
 
-    def do_fused():  # the one-launch fused form: every CTA quantises x
+    def do_fused(i):  # the one-launch fused form: every CTA quantises x
+        Wi = Ws[i % len(Ws)]
         if c.fmt == "q4k":
-            xq.linear_q4k(x, W, c.rows, c.cols, out=y)
+            xq.linear_q4k(x, Wi, c.rows, c.cols, out=y)
         elif c.fmt == "cb4":
-            xq.linear_cb4(x, W, kv, c.rows, c.cols, out=y)
+            xq.linear_cb4(x, Wi, kv, c.rows, c.cols, out=y)
         else:
-            xq.linear_cb4r(x, W, kv, c.rows, c.cols, out=y)
+            xq.linear_cb4r(x, Wi, kv, c.rows, c.cols, out=y)
 
-    def do_matvec():  # the mat-vec alone on q8 input
+    def do_matvec(i):  # the mat-vec alone on q8 input
+        Wi = Ws[i % len(Ws)]
         if c.fmt == "q4k":
-            xq.matvec_q4k(W, xq_buf, c.rows, c.cols, out=y)
+            xq.matvec_q4k(Wi, xq_buf, c.rows, c.cols, out=y)
         elif c.fmt == "cb4":
-            xq.matvec_cb4(W, kv, xq_buf, c.rows, c.cols, out=y)
+            xq.matvec_cb4(Wi, kv, xq_buf, c.rows, c.cols, out=y)
         else:
-            xq.matvec_cb4r(W, kv, xq_buf, c.rows, c.cols, out=y)
+            xq.matvec_cb4r(Wi, kv, xq_buf, c.rows, c.cols, out=y)
 
-    def do_two_call():  # xq_quantize_q8, then the mat-vec
+    def do_two_call(i):  # xq_quantize_q8, then the mat-vec
         xq.quantize_q8(x, out=xq_buf)
-        do_matvec()
+        do_matvec(i)
 
-    def do_norm_linear():  # RMSNorm, quantise and mat-vec in one launch
+    def do_norm_linear(i):  # RMSNorm, quantise and mat-vec in one launch
+        Wi = Ws[i % len(Ws)]
         if c.fmt == "q4k":
-            xq.norm_linear_q4k(x, W, c.rows, c.cols, out=y)
+            xq.norm_linear_q4k(x, Wi, c.rows, c.cols, out=y)
         elif c.fmt == "cb4":
-            xq.norm_linear_cb4(x, W, kv, c.rows, c.cols, out=y)
+            xq.norm_linear_cb4(x, Wi, kv, c.rows, c.cols, out=y)
         else:
-            xq.norm_linear_cb4r(x, W, kv, c.rows, c.cols, out=y)
+            xq.norm_linear_cb4r(x, Wi, kv, c.rows, c.cols, out=y)
 
-    def do_norm_two_call():  # xq_rmsnorm_q8, then the mat-vec
+    def do_norm_two_call(i):  # xq_rmsnorm_q8, then the mat-vec
         xq.rmsnorm_q8(x, out=xq_buf)
-        do_matvec()
+        do_matvec(i)
 
     # grouped experts: the matrix as a slab of 8 experts of rows/8 rows, two
     # of them selected (device ids), on q8 vector 0
@@ -390,40 +455,43 @@ def run_ours(args, c):
     y_id = torch.empty((2, rpe), dtype=torch.float32, device=dev)
     has_id = c.rows % 8 == 0
 
-    def do_experts():
-        xq.matvec_id(c.fmt, W, sel, xq_buf[:1], rpe, c.cols, n_exp, table=kv, out=y_id)
+    def do_experts(i):
+        xq.matvec_id(c.fmt, Ws[i % len(Ws)], sel, xq_buf[:1], rpe, c.cols, n_exp, table=kv,
+                     out=y_id)
 
     # resident rows: the bind-time repack of the whole matrix, raw -> resident
     W_raw = torch.from_numpy(c.weights()).to(dev) if c.fmt == "cb4r" else None
     W_rep = torch.empty_like(W) if c.fmt == "cb4r" else None
 
-    def do_repack():
+    def do_repack(i):
         xq.repack_cb4(W_raw, c.rows, c.cols, out=W_rep)
 
     # eager warm-up: the first call per device configures the kernels (before capture)
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            do_two_call()
-            do_norm_two_call()
-            do_norm_linear()
-            do_fused()
-            do_step()
+        for i in range(3):
+            do_two_call(i)
+            do_norm_two_call(i)
+            do_norm_linear(i)
+            do_fused(i)
+            do_step(i)
     stream.synchronize()
     step_plan = xq.last_plan()
 
     def capture(fn, n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for _ in range(n):
-                fn()
+            for i in range(n):
+                fn(i)
         return g
 
     # Overlapped launches (xq_set_overlap_launches) for the step: the weights
     # are constant, so a launch may start streaming them while the previous
-    # step finishes.  The other arms are captured without it; the step
-    # without it is timed beside it.
+    # step finishes.  The mat-vec arm of the rounds is captured the same way;
+    # the other arms without it, and the step without it is timed beside it.
+    # A graph holds an even number of steps, so the copies of W alternate
+    # across replays too.
     overlap = args.overlap == "on"
-    per_graph = max(1, min(args.steps, 100))
+    per_graph = max(2, min(args.steps, 100) // 2 * 2)
     rem = args.steps % per_graph
     ncount = xq.COUNT_N
     counts0 = [xq.launch_count(i) for i in range(ncount)]
@@ -431,12 +499,16 @@ def run_ours(args, c):
     xq.set_overlap_launches(overlap)
     graphs["step"] = (capture(do_step, per_graph), capture(do_step, rem) if rem else None)
     launches_per_step = sum(xq.launch_count(i) - counts0[i] for i in range(ncount)) / per_graph
+    graphs["matvec"] = (capture(do_matvec, per_graph), capture(do_matvec, rem) if rem else None)
+    if large:
+        graphs["step_one_buffer"] = (capture(do_step_one_buffer, per_graph),
+                                     capture(do_step_one_buffer, rem) if rem else None)
     xq.set_overlap_launches(False)
     extra = ((("experts", do_experts),) if has_id else ()) + \
         ((("repack", do_repack),) if c.fmt == "cb4r" else ())
-    for name, fn in (("step_plain", do_step), ("fused", do_fused), ("matvec", do_matvec),
-                     ("two_call", do_two_call), *extra,
-                     ("norm_linear", do_norm_linear), ("norm_two_call", do_norm_two_call)):
+    for name, fn in (("step_plain", do_step), ("fused", do_fused), ("two_call", do_two_call),
+                     *extra, ("norm_linear", do_norm_linear),
+                     ("norm_two_call", do_norm_two_call)):
         graphs[name] = (capture(fn, per_graph), capture(fn, rem) if rem else None)
 
     def timed(name, k):
@@ -452,23 +524,32 @@ def run_ours(args, c):
         ev1.synchronize()
         return ev0.elapsed_time(ev1) / k
 
-    # warm-up steps (untimed), then the timed region: exactly K steps
+    # warm-up steps (untimed), then R rounds, each exactly K steps of the step
+    # and K of the mat-vec alone, in ABBA order, each region bracketed by a
+    # barrier and a device synchronisation
     with torch.cuda.stream(stream):
         for _ in range(max(1, -(-args.warmup // per_graph))):
             graphs["step"][0].replay()
+            graphs["matvec"][0].replay()
     stream.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    barrier(dist)
-    torch.cuda.synchronize()
+    rounds = {"step": [], "matvec": []}
     t_wall0 = time.time()
-    step_ms = timed("step", args.steps)
-    torch.cuda.synchronize()
-    barrier(dist)
+    for r in range(args.rounds):
+        for name in (("step", "matvec") if r % 2 == 0 else ("matvec", "step")):
+            barrier(dist)
+            torch.cuda.synchronize()
+            rounds[name].append(timed(name, args.steps))
+            torch.cuda.synchronize()
+            barrier(dist)
+    t_wall1 = time.time()
+    step_ms = statistics.median(rounds["step"])
+    mv_ms = statistics.median(rounds["matvec"])
     step_ms_max = max_over_ranks(step_ms, dist)
-    # the same kernels outside the step, for the breakdown
-    mv_ms = timed("matvec", args.steps)
+    # the other forms, for the breakdown
+    one_ms = timed("step_one_buffer", args.steps) if large else None
     fused_ms = timed("fused", args.steps)
     plain_ms = timed("step_plain", args.steps)
     two_ms = timed("two_call", args.steps)
@@ -485,15 +566,15 @@ def run_ours(args, c):
     if 4 * 1024 * 1024 <= c.w_bytes < L2_BYTES:
         ncopy = -(-2 * L2_BYTES // c.w_bytes)
         copies = [W.clone() for _ in range(ncopy)]
-        rounds = max(1, 100 // ncopy)
+        nrounds = max(1, 100 // ncopy)
 
-        def do_cycle():
-            for k in range(ncopy * rounds):
+        def do_cycle(_):
+            for k in range(ncopy * nrounds):
                 xq.linear_ws(c.fmt, x, copies[k % ncopy], c.rows, c.cols, ws, table=kv, out=y)
         xq.set_overlap_launches(overlap)
         g_cold = capture(do_cycle, 1)
         xq.set_overlap_launches(False)
-        reps = max(1, args.steps // (ncopy * rounds))
+        reps = max(1, args.steps // (ncopy * nrounds))
         with torch.cuda.stream(stream):
             g_cold.replay()
             ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -502,12 +583,11 @@ def run_ours(args, c):
                 g_cold.replay()
             ev1.record(stream)
         ev1.synchronize()
-        cold_ms = ev0.elapsed_time(ev1) / (reps * ncopy * rounds)
+        cold_ms = ev0.elapsed_time(ev1) / (reps * ncopy * nrounds)
         cold_copies = ncopy
         del copies, g_cold
-    time.sleep(0.2)
     sampler.stop()
-    clocks = sampler.summary(t_wall0, time.time())
+    clocks = sampler.summary(t_wall0, t_wall1)
 
     # end to end through the public API with pinned host buffers: every step
     # copies its x from pinned host memory to the device, runs the step and
@@ -525,10 +605,11 @@ def run_ours(args, c):
                       "x": torch.empty_like(x), "y": torch.empty_like(y),
                       "ws": torch.empty_like(ws)})
 
-    def e2e_step(ln):
+    def e2e_step(ln, i):
         with torch.cuda.stream(ln["s"]):
             ln["x"].copy_(ln["x_host"], non_blocking=True)
-            xq.linear_ws(c.fmt, ln["x"], W, c.rows, c.cols, ln["ws"], table=kv, out=ln["y"])
+            xq.linear_ws(c.fmt, ln["x"], Ws[i % len(Ws)], c.rows, c.cols, ln["ws"], table=kv,
+                         out=ln["y"])
             ln["y_host"].copy_(ln["y"], non_blocking=True)
 
     def e2e_run(n, pipelined):
@@ -538,7 +619,7 @@ def run_ours(args, c):
         ev0.record(s0)
         lanes[1]["s"].wait_event(ev0)
         for i in range(n):
-            e2e_step(lanes[i % 2] if pipelined else lanes[0])
+            e2e_step(lanes[i % 2] if pipelined else lanes[0], i)
         end1 = torch.cuda.Event()
         end1.record(lanes[1]["s"])
         s0.wait_event(end1)
@@ -562,29 +643,45 @@ def run_ours(args, c):
     if rank != 0:
         return
     nbytes = step_bytes(c)
-    value = world * nbytes["linear"] / (step_ms_max * 1e-3) / 1e9
-    # the dominant kernel: the fused launch itself, or (quantise-once plan)
-    # the mat-vec on the q8 blocks, timed alone over the same K launches
+    B = nbytes["algorithmic"]
+
+    def gbs(ms):
+        return B / (ms * 1e-3) / 1e9
+
+    value = world * gbs(step_ms_max)
+    # the dominant kernel: the fused launch itself (the step is that one
+    # launch), or with the quantise-once plan the mat-vec on the q8 blocks;
+    # either way the median of its rounds, timed on its launching stream
     once = bool(step_plan["quantise_once"])
-    if once:
-        achieved = nbytes["matvec"] / (mv_ms * 1e-3) / 1e9
-        kernel_bytes, kernel_us = nbytes["matvec"], mv_ms * 1e3
-    else:
-        achieved = nbytes["linear"] / (step_ms * 1e-3) / 1e9
-        kernel_bytes, kernel_us = nbytes["linear"], step_ms * 1e3
+    kernel_ms = mv_ms if once else step_ms
+    achieved = gbs(kernel_ms)
     peak, peak_kind = measured_peak()
-    cpu = oracle_rate(c, wall_budget_s=args.cpu_seconds, threads=os.cpu_count() or 1)
+    cpu = cpu_baseline(c, args.cpu_seconds)
     fmt = FORMAT_NAMES[c.fmt]
+    us = [round(v * 1e3, 4) for v in rounds["step"]]
+    mv_us = [round(v * 1e3, 4) for v in rounds["matvec"]]
+    config = workload_config(c)
+    config["launch"] = ("overlapped launches (programmatic stream serialization: a step may "
+                        "start streaming W while the previous one finishes)" if overlap
+                        else "plain stream order")
+    if large:
+        config["l2"] = (f"inputs larger than L2: W {c.w_bytes / 1e6:.1f} MB > 129 MB, held "
+                        "twice, consecutive steps alternate between the copies; no flush")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
         "us_per_matvec": step_ms * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8 dp4a (int32 sums) + f32 epilogue",
         "data": "synthetic (seeded, shapes and distributions of the decode workloads)",
-        "config": {**workload_config(c),
-                   "launch": ("overlapped launches (programmatic stream serialization: a step may "
-                              "start streaming W while the previous one finishes)" if overlap
-                              else "plain stream order")},
+        "config": config,
+        "bytes": {"formula": BYTES_FORMULA, "per_step": B, "weights": nbytes["weights"],
+                  "q8": nbytes["q8"], "y_written": nbytes["y"], "x_f32": nbytes["x"]},
+        "rounds": {"n": args.rounds, "steps_each": args.steps,
+                   "order": "ABBA: rounds alternate (step, mat-vec) and (mat-vec, step)",
+                   "step_us": us, "median_us": statistics.median(us), "min_us": min(us),
+                   "max_us": max(us), "matvec_us": mv_us,
+                   "matvec_median_us": statistics.median(mv_us), "matvec_min_us": min(mv_us),
+                   "matvec_max_us": max(mv_us)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy (burst)",
                      "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
@@ -592,37 +689,35 @@ def run_ours(args, c):
                      "kernel": (f"xq_matvec_kernel<{fmt}, batch {c.batch}> on q8 blocks (after "
                                 f"the quantise launch)" if once else
                                 f"xq_matvec_kernel<{fmt}, batch {c.batch}, fused quantise>"),
-                     "kernel_us": kernel_us,
-                     "algorithmic_bytes_per_launch": kernel_bytes},
+                     "kernel_us": kernel_ms * 1e3,
+                     "algorithmic_bytes_per_launch": B,
+                     "timing": "median of the rounds, CUDA events on the launching stream"},
         "plan": {k: step_plan[k] for k in ("warps", "stages", "grid", "rows_per_group",
                                             "segments", "row_block", "quantise_once")},
         "breakdown": {
-            "step_without_overlap": {"us": plain_ms * 1e3,
-                                     "GBs": nbytes["linear"] / (plain_ms * 1e-3) / 1e9},
-            **({"step_cold_l2": {"us": cold_ms * 1e3,
-                                 "GBs": nbytes["linear"] / (cold_ms * 1e-3) / 1e9,
+            **({"step_one_buffer": {"us": one_ms * 1e3, "GBs": gbs(one_ms),
+                                    "how": "every step on the same copy of W"}}
+               if one_ms else {}),
+            "step_without_overlap": {"us": plain_ms * 1e3, "GBs": gbs(plain_ms)},
+            **({"step_cold_l2": {"us": cold_ms * 1e3, "GBs": gbs(cold_ms),
                                  "how": f"the step cycled over {cold_copies} copies of W (more "
                                         "than twice the L2), graph-replayed, overlapped launches"}}
                if cold_ms else {}),
-            "fused_one_launch": {"us": fused_ms * 1e3,
-                                 "GBs": nbytes["linear"] / (fused_ms * 1e-3) / 1e9},
-            "matvec_on_q8_input": {"us": mv_ms * 1e3,
-                                   "GBs": nbytes["matvec"] / (mv_ms * 1e-3) / 1e9},
-            "quantise_then_matvec": {"us": two_ms * 1e3,
-                                     "GBs": nbytes["two_call"] / (two_ms * 1e-3) / 1e9},
-            "rmsnorm_quantise_matvec_fused": {"us": nl_ms * 1e3,
-                                              "GBs": nbytes["linear"] / (nl_ms * 1e-3) / 1e9},
-            "rmsnorm_q8_then_matvec": {"us": n2_ms * 1e3,
-                                       "GBs": nbytes["two_call"] / (n2_ms * 1e-3) / 1e9},
+            "fused_one_launch": {"us": fused_ms * 1e3, "GBs": gbs(fused_ms)},
+            "matvec_on_q8_input": {"us": mv_ms * 1e3, "GBs": gbs(mv_ms),
+                                   "how": "median of the rounds"},
+            "quantise_then_matvec": {"us": two_ms * 1e3, "GBs": gbs(two_ms)},
+            "rmsnorm_quantise_matvec_fused": {"us": nl_ms * 1e3, "GBs": gbs(nl_ms)},
+            "rmsnorm_q8_then_matvec": {"us": n2_ms * 1e3, "GBs": gbs(n2_ms)},
             **({"grouped_experts_2_of_8": {
                 "us": id_ms * 1e3, "rows_per_expert": rpe,
-                "GBs": (2 * c.w_bytes // 8 + (c.cols // 256) * 320 + 2 * rpe * 4)
-                       / (id_ms * 1e-3) / 1e9}} if has_id else {}),
+                "GBs": (2 * c.w_bytes // 8 + (c.cols // 256) * 320) / (id_ms * 1e-3) / 1e9}}
+               if has_id else {}),
             **({"repack_whole_matrix": {
                 "us": rp_ms * 1e3, "GBs": 2 * c.w_bytes / (rp_ms * 1e-3) / 1e9,
                 "bytes": "raw blocks read + resident rows written"}} if rp_ms else {})},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * nbytes["linear"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": world * gbs(e2e_ms), "unit": "GB/s",
                 "ms_per_step": e2e_ms, "steps": e2e_steps, "trials": E2E_TRIALS,
                 "median_ms_per_step": e2e_median_ms,
                 "h2d_bytes_per_step": 4 * c.batch * c.cols,
@@ -631,7 +726,7 @@ def run_ours(args, c):
                         "cudaMemcpyAsync -> pinned y, eager calls through the Python binding; "
                         "two streams with their own buffers, so one step's copies overlap the "
                         "other's kernel (and one kernel's tail the next one's start)",
-                "serial": {"value": world * nbytes["linear"] / (e2e_serial_ms * 1e-3) / 1e9,
+                "serial": {"value": world * gbs(e2e_serial_ms),
                            "ms_per_step": e2e_serial_ms,
                            "path": "the same on one stream, copies in line with the kernel"}},
         "gpu_launches": int(round(launches_per_step * args.steps)),
@@ -647,6 +742,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--rounds", type=int, default=5,
+                    help="timed rounds of K steps (ABBA with the mat-vec alone); the median is reported")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--case", default=DEFAULT_CASE, choices=sorted(synthetic.CASES))
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
@@ -655,6 +752,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.rounds < 1:
+        ap.error("--rounds must be at least 1")
     c = synthetic.CASES[args.case]
     if args.impl == "reference":
         run_reference(args, c)

@@ -159,9 +159,11 @@ xq_status xq_linear_cb4r_ws(const float *x, const void *Wr, const int8_t *table,
  * call may need at most 819 q8 blocks (xq_linear_workspace_bytes(cols, batch)
  * <= 262144, i.e. batch * cols <= 209664); larger shapes return XQ_ESHAPE and
  * launch nothing.  The call
- * allocates nothing.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) once for that device, so make that first
- * call before any stream capture.  Nothing in the array needs clearing: the
+ * allocates nothing.  Null pointers and bad shapes are refused before any
+ * CUDA call.  The first call on a device that passes those checks looks up
+ * the array's device address (cudaGetSymbolAddress) for that device and keeps
+ * it (a failed lookup is not kept: the next call tries again), so make that
+ * first call before any stream capture.  Nothing in the array needs clearing: the
  * q8 blocks are written before they are read.  Every call shares the one
  * array, which keeps the last call's contents, so calls that may overlap on
  * the GPU (other streams, other threads) race; order them on one stream.

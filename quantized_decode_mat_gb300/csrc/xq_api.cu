@@ -522,12 +522,10 @@ xq_status run_matvec_id(int fmt, const void *W, const int8_t *table, const int32
 // to look up its device address (cudaGetSymbolAddress), never as a pointer.
 constexpr size_t kStaticScratchBytes = 256 * 1024;
 
-struct StaticScratch {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
-    void *ptr = nullptr;
-};
-StaticScratch g_static_scratch_state[kMaxDevices];
+// The scratch's device address per device, kept once a lookup has succeeded;
+// a failed lookup is not kept, so the next call tries again.
+std::mutex g_static_scratch_mutex;
+void *g_static_scratch_ptr[kMaxDevices];
 
 }  // namespace
 }  // namespace xq
@@ -537,22 +535,22 @@ static __device__ __align__(256) uint8_t g_static_scratch[xq::kStaticScratchByte
 namespace xq {
 namespace {
 
-// Device address of g_static_scratch on the current device, looked up once per
-// device (the first call on a device, which should come before any stream
-// capture).
+// Device address of g_static_scratch on the current device, looked up on the
+// first call with that device current that gets this far (that call should
+// come before any stream capture) and kept from then on.
 xq_status static_scratch(void **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(XQ_ELAUNCH, "device %d out of range", dev);
-    StaticScratch &st = g_static_scratch_state[dev];
-    std::call_once(st.once, [&st]() {
+    std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
+    if (!g_static_scratch_ptr[dev]) {
         void *p = nullptr;
-        st.err = cudaGetSymbolAddress(&p, g_static_scratch);
-        st.ptr = st.err == cudaSuccess ? p : nullptr;
-    });
-    if (st.err != cudaSuccess) return cuda_fail(st.err, "cudaGetSymbolAddress(static scratch)");
-    *out = st.ptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        g_static_scratch_ptr[dev] = p;
+    }
+    *out = g_static_scratch_ptr[dev];
     return XQ_OK;
 }
 
@@ -662,6 +660,9 @@ xq_status xq_linear_q4k_ws(const float *x, const void *W, float *y, int64_t rows
 xq_status xq_linear_q4k_static(const float *x, const void *W, float *y, int64_t rows, int64_t cols,
                                int64_t batch, void *stream) {
     t_error.clear();
+    // the caller's arguments first: a bad call makes no CUDA call at all
+    if (!x || !W || !y) return fail(XQ_EINVAL, "null device pointer (x, W or y)");
+    if (xq_status s = check_shape(rows, cols, batch, true)) return s;
     const size_t need = xq_linear_workspace_bytes(cols, batch);
     if (need > kStaticScratchBytes)
         return fail(XQ_ESHAPE,

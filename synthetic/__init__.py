@@ -14,6 +14,9 @@ Workloads (sizes, distributions) follow the five decode configurations:
   3. Q4_K FFN pair 14336x4096 (up) and 4096x14336 (down), batch 1/2/4/8
   4. codebook 4096x4096 and 11008x4096, batch 1
   5. Q4_K 128256x4096 (L2-exceeding vocabulary projection), batch 1 and 8
+and one measurement case beside them: the codebook format at the vocabulary
+projection's shape, 128256x4096 batch 1 (raw and resident rows), so that the
+codebook kernel also has a matrix larger than the L2 cache.
 PRNG: numpy PCG64 (``np.random.Generator``); normals are numpy's standard
 normal in float64, cast to float32.
 """
@@ -147,4 +150,9 @@ CASES = {
                                           sub=1),
     "c5_q4k_128256x4096_b1": MatvecCase("c5_q4k_128256x4096_b1", "q4k", 128256, 4096, 1, 5),
     "c5_q4k_128256x4096_b8": MatvecCase("c5_q4k_128256x4096_b8", "q4k", 128256, 4096, 8, 5),
+    # the codebook format with W larger than the L2 cache (295.5 MB), raw blocks
+    # and the same matrix in resident rows
+    "hbm_cb4_128256x4096_b1": MatvecCase("hbm_cb4_128256x4096_b1", "cb4", 128256, 4096, 1, 6),
+    "hbm_cb4r_128256x4096_b1": MatvecCase("hbm_cb4r_128256x4096_b1", "cb4r", 128256, 4096, 1,
+                                          6),
 }

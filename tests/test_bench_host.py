@@ -82,20 +82,35 @@ def test_reference_arm_line(monkeypatch):
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    for k in ("affinity_cores", "cpu_model", "hostname"):
+        assert k in d["cpu_baseline"], k
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["steps"] == 2 and d["warmup"] == 3 and d["higher_is_better"] is True
 
 
 def test_algorithmic_bytes():
+    """The metric's bytes of one mat-vec: the weights once and the activation
+    as q8 blocks; the y write and the f32 activation are listed, not counted."""
     sys.path.insert(0, ROOT)
     import bench
     import synthetic
     c = synthetic.CASES["c5_q4k_128256x4096_b1"]
     b = bench.step_bytes(c)
-    assert b["weights"] == 295_501_824
-    assert b["matvec"] == 295_501_824 + 16 * 320 + 4 * 128256
-    assert b["linear"] == 295_501_824 + 4 * 4096 + 4 * 128256
-    assert b["two_call"] == b["matvec"] + 4 * 4096 + 16 * 320
+    assert b["weights"] == 128256 * 16 * 144 == 295_501_824
+    assert b["q8"] == 16 * 320
+    assert b["algorithmic"] == 295_501_824 + 16 * 320
+    assert b["y"] == 4 * 128256 and b["x"] == 4 * 4096
+    c8 = synthetic.CASES["c5_q4k_128256x4096_b8"]
+    assert bench.step_bytes(c8)["algorithmic"] == 295_501_824 + 8 * 16 * 320
+    cb = synthetic.CASES["hbm_cb4_128256x4096_b1"]
+    assert bench.step_bytes(cb)["weights"] == 128256 * 128 * 18 == 295_501_824
+
+
+def test_host_context():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert 1 <= bench.host_cores() <= (os.cpu_count() or 1)
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
 
 
 def test_warmup_floor():

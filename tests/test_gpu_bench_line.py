@@ -24,7 +24,7 @@ def _run(*args):
 
 def test_bench_line_contract():
     d = _run("--case", "c2_q4k_4096x4096_b1", "--steps", "200", "--warmup", "5",
-             "--cpu-seconds", "0.2")
+             "--rounds", "4", "--cpu-seconds", "0.2")
     for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
               "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
               "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
@@ -40,8 +40,17 @@ def test_bench_line_contract():
     assert e["h2d_bytes_per_step"] == 4 * 4096 and e["d2h_bytes_per_step"] == 4 * 4096
     assert e["ms_per_step"] <= e["median_ms_per_step"]
     assert d["gpu_launches"] >= d["steps"]
+    rd = d["rounds"]
+    assert rd["n"] == 4 and len(rd["step_us"]) == 4 and len(rd["matvec_us"]) == 4
+    assert rd["min_us"] <= rd["median_us"] <= rd["max_us"]
+    assert abs(rd["median_us"] - d["ms_per_step"] * 1e3) < 1e-3
+    b = d["bytes"]
+    assert b["per_step"] == b["weights"] + b["q8"] == 9437184 + 16 * 320
+    assert abs(d["value"] - b["per_step"] / (d["ms_per_step"] * 1e-3) / 1e9) < 1e-6 * d["value"]
     c = d["cpu_baseline"]
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0
+    assert c["cores"] == c["affinity_cores"] and c["cpu_model"] and c["hostname"]
+    assert c["single_thread"]["value"] > 0
     assert d["clocks"]["sm_mhz"] > 0
     assert d["device_status"] == 0
 

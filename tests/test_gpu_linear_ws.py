@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle_rows
 import synthetic
 from test_gpu_parity import Guarded, check_y, dev, run_quantize
 
@@ -136,9 +137,8 @@ def test_linear_ws_rejects_a_small_workspace(xq):
 @pytest.mark.parametrize("name", sorted(synthetic.CASES))
 def test_step_at_full_size(xq, orc, name):
     """Every configuration at full size through the step the bench times
-    (xq_linear_*_ws, planned as the bench plans it): every output against the
-    oracle, or for the vocabulary projection the first and last tiles and
-    1500 random rows."""
+    (xq_linear_*_ws, planned as the bench plans it): every output of every
+    row against the oracle."""
     c = synthetic.CASES[name]
     W, x = c.weights(), c.x()
     kv = synthetic.cb4_table()
@@ -153,13 +153,6 @@ def test_step_at_full_size(xq, orc, name):
     out.check_guard()
     y = out.t.cpu().numpy()
     xq_ref = orc.quantize_q8(x)
-    if c.rows > 20000:
-        rng = np.random.Generator(np.random.PCG64(11))
-        rows = np.unique(np.concatenate([np.arange(64), np.arange(c.rows - 70, c.rows),
-                                         rng.choice(c.rows, 1500, replace=False)]))
-    else:
-        rows = np.arange(c.rows)
-    Ws = np.ascontiguousarray(W[rows])
-    y_ref = (orc.matvec_q4k(Ws, xq_ref, len(rows), c.cols, c.batch) if c.fmt == "q4k"
-             else orc.matvec_cb4(Ws, kv, xq_ref, len(rows), c.cols, c.batch))
-    check_y(y[:, rows], y_ref, f"step {name}")
+    y_ref = oracle_rows.matvec(orc, "q4k" if c.fmt == "q4k" else "cb4", W, kv, xq_ref, c.rows,
+                               c.cols, c.batch)
+    check_y(y, y_ref, f"step {name}")

@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle_rows
 import synthetic
 
 pytestmark = pytest.mark.gpu
@@ -167,8 +168,11 @@ def test_matvec_within_tolerance(xq, orc, fmt, rows, cols, batch):
 
 
 # ---------------------------------------------------------------- the configurations
+L2_BYTES = 129 * 1024 * 1024
 SMALL_CASES = [k for k, c in synthetic.CASES.items()
-               if not k.startswith("c5_") and c.fmt != "cb4r"]  # resident: test_gpu_resident
+               if c.w_bytes < L2_BYTES and c.fmt != "cb4r"]  # resident: test_gpu_resident
+LARGE_CASES = [k for k, c in synthetic.CASES.items()
+               if c.w_bytes >= L2_BYTES and c.fmt != "cb4r"]
 
 
 @pytest.mark.parametrize("name", SMALL_CASES)
@@ -186,32 +190,31 @@ def test_config_full(xq, orc, name):
     check_y(y, y_ref, name)
 
 
-@pytest.mark.parametrize("name", ["c5_q4k_128256x4096_b1", "c5_q4k_128256x4096_b8"])
-def test_config5_sampled(xq, orc, name):
-    """The L2-exceeding vocabulary projection at full size, in the launch
-    configuration the bench times; the oracle recomputes sampled rows (the
-    first and last tiles, including the ragged end, and 1500 random rows) and
-    every sub-block dot of 64 sampled rows."""
+@pytest.mark.parametrize("name", LARGE_CASES)
+def test_large_config_every_row(xq, orc, name):
+    """The L2-exceeding vocabulary projection at full size (configuration 5,
+    and the codebook format at the same shape), in the launch configuration
+    the bench times: every output of every row against the oracle (so an
+    unwritten row anywhere shows as NaN poison), and every exact sub-block
+    dot of every row bit for bit."""
     c = synthetic.CASES[name]
     W, x = c.weights(), c.x()
+    kv = synthetic.cb4_table()
     xq_dev = run_quantize(xq, x)
     xq_ref = orc.quantize_q8(x)
     assert np.array_equal(xq_dev.cpu().numpy(), xq_ref)
-    y = run_matvec(xq, "q4k", W, None, xq_dev, c.rows, c.cols, c.batch)
+    y = run_matvec(xq, c.fmt, W, kv, xq_dev, c.rows, c.cols, c.batch)
     plan = xq.last_plan()
     units = -(-plan["groups"] // plan["row_block"])
     assert plan["grid"] == min(units, torch.cuda.get_device_properties(0).multi_processor_count)
-    assert plan["row_block"] == (2 if c.batch >= 2 else 1)
-    rng = np.random.Generator(np.random.PCG64(5))
-    sample = np.unique(np.concatenate([np.arange(64), np.arange(c.rows - 70, c.rows),
-                                       rng.choice(c.rows, 1500, replace=False)]))
-    Ws = np.ascontiguousarray(W[sample])
-    y_ref = orc.matvec_q4k(Ws, xq_ref, len(sample), c.cols, c.batch)
-    check_y(y[:, sample], y_ref, name)
-    dots = run_matvec(xq, "q4k", W, None, xq_dev, c.rows, c.cols, c.batch, dots=True)
-    s2 = sample[:: max(1, len(sample) // 64)]
-    ref_d = orc.subdots_q4k(np.ascontiguousarray(W[s2]), xq_ref, len(s2), c.cols, c.batch)
-    assert np.array_equal(dots[:, s2], ref_d)
+    assert plan["row_block"] == (2 if c.batch >= 2 and c.fmt == "q4k" else 1)
+    assert y.shape == (c.batch, c.rows)
+    y_ref = oracle_rows.matvec(orc, c.fmt, W, kv, xq_ref, c.rows, c.cols, c.batch)
+    check_y(y, y_ref, name)
+    dots = run_matvec(xq, c.fmt, W, kv, xq_dev, c.rows, c.cols, c.batch, dots=True)
+    ref_d = oracle_rows.subdots(orc, c.fmt, W, kv, xq_ref, c.rows, c.cols, c.batch)
+    diff = np.argwhere(dots != ref_d)
+    assert diff.size == 0, f"{len(diff)} dots differ, first at {diff[:4].tolist()}"
 
 
 # ---------------------------------------------------------------- degenerate cases
