@@ -78,7 +78,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 
 def ptxas_report() -> dict[str, dict[str, int]]:
-    """Registers and spill bytes per kernel, parsed from the ptxas logs."""
+    """Registers, spill bytes and stack-frame bytes (local arrays) per kernel,
+    parsed from the ptxas logs."""
     out: dict[str, dict[str, int]] = {}
     for log in glob.glob(os.path.join(BUILD, "*.ptxas.log")):
         current = None
@@ -86,11 +87,14 @@ def ptxas_report() -> dict[str, dict[str, int]]:
             for line in f:
                 if "Compiling entry function" in line:
                     current = line.split("'")[1]
-                    out[current] = {"registers": -1, "spill_stores": 0, "spill_loads": 0}
+                    out[current] = {"registers": -1, "spill_stores": 0, "spill_loads": 0,
+                                    "stack_frame": 0}
                 elif current and "spill stores" in line:
                     parts = line.replace(",", "").split()
                     out[current]["spill_stores"] = int(parts[parts.index("spill") - 2])
                     out[current]["spill_loads"] = int(parts[parts.index("loads") - 3])
+                    if "stack" in parts:
+                        out[current]["stack_frame"] = int(parts[parts.index("stack") - 2])
                 elif current and "Used" in line and "registers" in line:
                     parts = line.replace(",", " ").split()
                     out[current]["registers"] = int(parts[parts.index("registers") - 1])

@@ -52,31 +52,33 @@ __device__ __forceinline__ uint4 split_sums(uint4 s0, uint4 s1) {
 }
 
 // ---- shared epilogue --------------------------------------------------------
-// Adds xs*(d*S1 - dmin*S2) to (hi, lo).  S1, S2 exact integers; |S2| < 2^24;
-// S1 is split into its f32 rounding and an exact residual.  first: (hi, lo)
-// holds nothing yet, so the first compensated add (of t1 to zero, which
-// yields t1 and a zero error term exactly) is a plain assignment.
+// Adds xs*(d*S1 - dmin*S2) to (hi, lo).  S1, S2 exact integers, |S1| < 2^25,
+// |S2| < 2^24.  The inner difference is formed first as an unevaluated pair
+// D + Dl (TwoProduct of each scale with its exact integer, then TwoSum of
+// the two products), then scaled by xs (one TwoProduct), so the term reaches
+// (hi, lo) with an error of the order of 2^-44 of its magnitude.  S1 is split
+// into its f32 rounding and an exact residual (0 unless |S1| > 2^24).
+// first: (hi, lo) holds nothing yet, so the term is assigned to it.
 __device__ __forceinline__ void q4k_epilogue(float xs, float d, float dmin, int S1, int S2,
                                              float &hi, float &lo, bool first) {
-    float ph, pl, qh, ql;
-    two_prod(xs, d, ph, pl);        // xs*d    = ph + pl exactly
-    two_prod(xs, dmin, qh, ql);     // xs*dmin = qh + ql exactly
     const float f1 = __int2float_rn(S1);
-    const float r1 = __int2float_rn(S1 - __float2int_rn(f1));  // exact, 0 if |S1| <= 2^24
+    const float r1 = __int2float_rn(S1 - __float2int_rn(f1));  // exact, |r1| <= 1
     const float f2 = __int2float_rn(S2);                       // exact
-    float t1, e1, t2, e2;
-    two_prod(ph, f1, t1, e1);
-    two_prod(-qh, f2, t2, e2);
-    // second-order terms, each below 2^-23 of the main ones
-    float small = __fmaf_rn(pl, f1, __fmaf_rn(ph, r1, __fadd_rn(e1, e2)));
-    small = __fmaf_rn(-ql, f2, small);
+    float a, ae, b, be, D, De;
+    two_prod(d, f1, a, ae);          // d*f1 = a + ae exactly
+    ae = __fmaf_rn(d, r1, ae);       // + d*r1 (second order)
+    two_prod(dmin, f2, b, be);       // dmin*S2 = b + be exactly
+    two_sum(a, -b, D, De);           // a - b = D + De exactly
+    const float Dl = __fadd_rn(__fsub_rn(ae, be), De);
+    float t, te;
+    two_prod(xs, D, t, te);          // xs*D = t + te exactly
+    const float tl = __fmaf_rn(xs, Dl, te);
     if (first) {
-        hi = t1;
-        lo = 0.0f;
+        hi = t;
+        lo = tl;
     } else {
-        acc_add(hi, lo, t1, 0.0f);
+        acc_add(hi, lo, t, tl);
     }
-    acc_add(hi, lo, t2, small);
 }
 
 __device__ __forceinline__ int byte_of(uint32_t x, int k) {
@@ -484,6 +486,61 @@ __device__ __forceinline__ GroupInfo group_info(const MatvecArgs &a, int64_t g, 
     return gi;
 }
 
+// ---- transposed reduction for rows of 16 chunks ----------------------------------------
+// Whole rows of 16 chunks in a box (4096 columns): lane l holds chunk l % 16 of
+// row l / 16 of each of the unit's M row groups, for B vectors.  The lanes
+// write their partial sums (M * P pairs, P = B rounded up to a power of two)
+// to a warp-private scratch -- the stage the unit was just read from -- and
+// read them back transposed: lane t then holds the 16 chunks of one (row
+// group, row, vector) and adds them with the pairing tree of the shuffle
+// reductions (chunks 8 apart, then 4, 2, 1).  acc_add is symmetric, so the
+// bits are those of every other reduction form, at a fraction of the
+// instructions and none of the shuffle latency.  The row stride of
+// (M * P + 1) * 8 bytes puts the writes of 16 lanes, and the reads of one
+// scratch row, on distinct banks.
+template <int M, int B>
+__device__ __forceinline__ void reduce_rows16_store(const float (&hi)[M][B], const float (&lo)[M][B],
+                                                    uint8_t *scratch, int lane,
+                                                    const GroupInfo (&gi)[M], float *y,
+                                                    int64_t rows) {
+    constexpr int P = Pow2Ceil<B>::v;
+    constexpr int kStride = (M * P + 1) * 8;
+    static_assert(M * 2 * P <= 32, "one output a lane at most");
+    static_assert(M == 1 || M == 2, "row groups are picked by a select");
+    float2 *mine = reinterpret_cast<float2 *>(scratch + lane * kStride);
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int b = 0; b < B; ++b) mine[m * P + b] = make_float2(hi[m][b], lo[m][b]);
+    __syncwarp();
+    const int b = lane % P, m = (lane / P) % M, rig = lane / (P * M);
+    if (lane < M * 2 * P && b < B) {
+        float h[16], l[16];
+        const uint8_t *src = scratch + rig * 16 * kStride + (m * P + b) * 8;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const float2 v = *reinterpret_cast<const float2 *>(src + c * kStride);
+            h[c] = v.x;
+            l[c] = v.y;
+        }
+        // levels with pairs 8, 4, 2, 1 apart (constant trip counts, so the
+        // arrays stay in registers)
+#pragma unroll
+        for (int lvl = 0; lvl < 4; ++lvl) {
+            const int off = 8 >> lvl;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < off) acc_add(h[i], l[i], h[i + off], l[i + off]);
+        }
+        // this lane's row group by selects, not an index into gi (a run-time
+        // index would put gi in local memory)
+        const int valid = m == 0 ? gi[0].valid : gi[M - 1].valid;
+        const int64_t out0 = m == 0 ? gi[0].out0 : gi[M - 1].out0;
+        if (rig < valid) y[(int64_t)b * rows + out0 + rig] = __fadd_rn(h[0], l[0]);
+    }
+    __syncwarp();  // the scratch is read before the stage is refilled
+}
+
 // ---- the kernel ------------------------------------------------------------------------
 // Row group: R rows.  When nb (256-weight chunks per row) is a power of two
 // below 32, R = 32/nb and the group is one contiguous 4608-byte box;
@@ -504,13 +561,24 @@ __device__ __forceinline__ GroupInfo group_info(const MatvecArgs &a, int64_t g, 
 template <int FMT, int B, int FUSE>
 constexpr int max_threads() { return warps_limit(FMT, B, FUSE) * 32; }
 
+// The launch bound a build is compiled for.  The row-blocked whole-row builds
+// are compiled for 12 warps (at most 168 registers a thread) although the plan
+// runs them with 8 beside the batch's activation: the tighter register budget
+// schedules faster (128256 x 4096 batch 8: 107.3 -> 106.0 us, 14336 x 4096
+// batch 8: 15.69 -> 15.59 us) and still spills nothing.
+template <int FMT, int B, int FUSE, int M, bool WR>
+constexpr int bound_threads() {
+    return (M == 2 && WR && max_threads<FMT, B, FUSE>() < 384) ? 384 : max_threads<FMT, B, FUSE>();
+}
+
 // M: row groups a warp works on at once (a work unit).  Two for Q4_K with
 // several activation vectors, where the activation loads from shared memory
 // are the limit; one otherwise.  WR: a build for boxes of whole rows only
 // (R > 1), where the segment bookkeeping folds away at compile time; the
-// row-blocked launches take it when the plan's rows per group exceed one.
+// row-blocked launches and the batch-1 codebook launches take it when the
+// plan's rows per group exceed one (has_whole_row_build).
 template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M, bool WR = false>
-__global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kernel(const MatvecArgs a) {
+__global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR>(), 1) xq_matvec_kernel(const MatvecArgs a) {
     static_assert(!ID || (B == 1 && !DOTS && FUSE == 0), "the grouped form is batch 1 on q8 input");
     static_assert(M == 1 || (M == 2 && FMT == kQ4K && !ID), "row blocking is a Q4_K form");
     static_assert(FUSE >= 0 && FUSE <= 2, "FUSE: 0 q8 input, 1 quantise x, 2 RMSNorm then quantise");
@@ -908,7 +976,19 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
             __syncwarp();
             if (++c_stage == S) c_stage = 0;
         }
-        if (!DOTS) {
+        bool stored = false;
+        // rows of 16 chunks, three vectors or more: the transposed reduction
+        // (with one or two vectors it leaves most lanes without an output, and
+        // the shuffle reduction is faster: 14336 x 4096 batch 2, 8.64 against
+        // 8.37 us)
+        if constexpr (M == 2 && WR && !DOTS && B >= 3) {
+            if (nb == 16) {
+                const int used = c_stage == 0 ? S - 1 : c_stage - 1;  // the stage just read
+                reduce_rows16_store<M, B>(hi, lo, stage0 + used * unit_bytes, lane, gi, a.y, rows);
+                stored = true;
+            }
+        }
+        if (!DOTS && !stored) {
             constexpr int P = Pow2Ceil<B>::v;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
@@ -940,10 +1020,18 @@ __global__ void __launch_bounds__(max_threads<FMT, B, FUSE>(), 1) xq_matvec_kern
     cp_async_wait_all();  // only empty groups can remain; keeps the exit clean
 }
 
+// Builds for boxes of whole rows (WR): the row-blocked Q4_K kernels, and the
+// batch-1 codebook kernels (raw or resident rows; 128256 x 4096: 56.7 ->
+// 55.4 us).  The batch-1 Q4_K kernel is HBM-bound and measured no faster.
+template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M>
+constexpr bool has_whole_row_build() {
+    return M == 2 || (M == 1 && FMT != kQ4K && B == 1 && !DOTS && !ID);
+}
+
 template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>
 inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, size_t smem,
                                    cudaStream_t s) {
-    if constexpr (M == 2) {  // row blocking: a build for whole-row boxes
+    if constexpr (has_whole_row_build<FMT, B, DOTS, FUSE, ID, M>()) {
         if (a.rows_per_group > 1)
             return launch_kernel(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, true>, grid, block,
                                  smem, s, a.overlap != 0, a);
@@ -954,7 +1042,7 @@ inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, s
 
 template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>
 inline cudaError_t configure_t(int smem_optin) {
-    if constexpr (M == 2) {
+    if constexpr (has_whole_row_build<FMT, B, DOTS, FUSE, ID, M>()) {
         const cudaError_t e = cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, true>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    smem_optin);

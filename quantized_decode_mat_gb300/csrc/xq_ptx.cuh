@@ -112,12 +112,17 @@ __device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
     e = __fmaf_rn(a, b, -p);
 }
 
-// acc (hi, lo) += v (a value with its own small correction term v_lo).
+// acc (hi, lo) += v (a value with its own small correction term v_lo).  The
+// result is symmetric in its two operands: TwoSum's sum and error term are,
+// and the correction terms are added to each other before the error term, so
+// a sum over a fixed pairing tree has the same bits whichever side of each
+// pair holds the accumulator (a lane's own value or one received from
+// another lane).
 __device__ __forceinline__ void acc_add(float &hi, float &lo, float v, float v_lo) {
     float s, e;
     two_sum(hi, v, s, e);
     hi = s;
-    lo = __fadd_rn(lo, __fadd_rn(e, v_lo));
+    lo = __fadd_rn(__fadd_rn(lo, v_lo), e);
 }
 
 }  // namespace xq

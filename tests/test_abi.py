@@ -222,7 +222,8 @@ def test_python_binding_rejects_host_tensors(lib):
 
 def test_no_kernel_spills(lib):
     """Spill is invisible to timing ("25 - Writing XPU Kernels" 25.5, the
-    manifest before the wall clock): no kernel of the library spills -- every
+    manifest before the wall clock): no kernel of the library spills or keeps
+    a per-thread array in local memory (a stack frame) -- every
     mat-vec build (each format, batch 1..8, with or without the dots, every
     fused form, the grouped form, one or two row groups a unit, the
     whole-row builds) and the quantise, RMSNorm and repack kernels."""
@@ -232,13 +233,15 @@ def test_no_kernel_spills(lib):
     matvec = [n for n in rep if "xq_matvec_kernel" in n]
     # format x batch x (dots, fused quantise, fused RMSNorm, plain) + the grouped
     # form (3 formats, batch 1) + the Q4_K row-blocked builds (7 batches x 4
-    # kinds x 2 box shapes)
-    assert len(matvec) == 3 * 8 * 4 + 3 + 7 * 4 * 2, len(matvec)
+    # kinds x 2 box shapes) + the whole-row batch-1 codebook builds (2 formats x
+    # plain, fused quantise, fused RMSNorm)
+    assert len(matvec) == 3 * 8 * 4 + 3 + 7 * 4 * 2 + 2 * 3, len(matvec)
     for helper in ("q8_quantize_kernel", "rmsnorm_q8_kernel", "repack_cb4_kernel"):
         assert any(helper in n for n in rep), helper
     for name, r in rep.items():
         assert r["registers"] > 0, (name, r)
         assert r["spill_stores"] == 0 and r["spill_loads"] == 0, (name, r)
+        assert r["stack_frame"] == 0, (name, r)  # no per-thread array in local memory
 
 
 def test_oracle_and_product_share_no_code():
