@@ -566,18 +566,19 @@ constexpr int max_threads() { return warps_limit(FMT, B, FUSE) * 32; }
 // runs them with 8 beside the batch's activation: the tighter register budget
 // schedules faster (128256 x 4096 batch 8: 107.3 -> 106.0 us, 14336 x 4096
 // batch 8: 15.69 -> 15.59 us) and still spills nothing.
-template <int FMT, int B, int FUSE, int M, bool WR>
+template <int FMT, int B, int FUSE, int M, int WR>
 constexpr int bound_threads() {
     return (M == 2 && WR && max_threads<FMT, B, FUSE>() < 384) ? 384 : max_threads<FMT, B, FUSE>();
 }
 
 // M: row groups a warp works on at once (a work unit).  Two for Q4_K with
 // several activation vectors, where the activation loads from shared memory
-// are the limit; one otherwise.  WR: a build for boxes of whole rows only
-// (R > 1), where the segment bookkeeping folds away at compile time; the
-// row-blocked launches and the batch-1 codebook launches take it when the
-// plan's rows per group exceed one (has_whole_row_build).
-template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M, bool WR = false>
+// are the limit; one otherwise.  WR: 0 for the general build; 16 for a build
+// for rows of exactly 16 chunks (4096 columns: two whole rows a box), where
+// the row width, the rows a box and the segment bookkeeping are known at
+// compile time; the row-blocked launches and the batch-1 codebook launches
+// take it for such rows (has_whole_row_build).
+template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M, int WR = 0>
 __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR>(), 1) xq_matvec_kernel(const MatvecArgs a) {
     static_assert(!ID || (B == 1 && !DOTS && FUSE == 0), "the grouped form is batch 1 on q8 input");
     static_assert(M == 1 || (M == 2 && FMT == kQ4K && !ID), "row blocking is a Q4_K form");
@@ -588,8 +589,9 @@ __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR>(), 1) xq_ma
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = a.stages;
-    const int nb = a.nb;
-    const int R = a.rows_per_group;
+    static_assert(WR == 0 || WR == 16, "the whole-row build is for rows of 16 chunks");
+    const int nb = WR ? WR : a.nb;
+    const int R = WR ? kTileRows / WR : a.rows_per_group;
     const bool whole = WR || R > 1;  // whole rows in a box (WR: known at compile time)
     const int spr = WR ? 1 : a.segments;
     const int64_t rows = a.rows;
@@ -981,12 +983,10 @@ __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR>(), 1) xq_ma
         // (with one or two vectors it leaves most lanes without an output, and
         // the shuffle reduction is faster: 14336 x 4096 batch 2, 8.64 against
         // 8.37 us)
-        if constexpr (M == 2 && WR && !DOTS && B >= 3) {
-            if (nb == 16) {
-                const int used = c_stage == 0 ? S - 1 : c_stage - 1;  // the stage just read
-                reduce_rows16_store<M, B>(hi, lo, stage0 + used * unit_bytes, lane, gi, a.y, rows);
-                stored = true;
-            }
+        if constexpr (M == 2 && WR == 16 && !DOTS && B >= 3) {
+            const int used = c_stage == 0 ? S - 1 : c_stage - 1;  // the stage just read
+            reduce_rows16_store<M, B>(hi, lo, stage0 + used * unit_bytes, lane, gi, a.y, rows);
+            stored = true;
         }
         if (!DOTS && !stored) {
             constexpr int P = Pow2Ceil<B>::v;
@@ -1020,9 +1020,10 @@ __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR>(), 1) xq_ma
     cp_async_wait_all();  // only empty groups can remain; keeps the exit clean
 }
 
-// Builds for boxes of whole rows (WR): the row-blocked Q4_K kernels, and the
-// batch-1 codebook kernels (raw or resident rows; 128256 x 4096: 56.7 ->
-// 55.4 us).  The batch-1 Q4_K kernel is HBM-bound and measured no faster.
+// Builds for rows of 16 chunks (WR = 16): the row-blocked Q4_K kernels, and
+// the batch-1 codebook kernels (raw or resident rows; 128256 x 4096: 56.7 ->
+// 51.8 us, 11008 x 4096: 7.33 -> 6.80 us).  The batch-1 Q4_K kernel is
+// HBM-bound and measured no faster with a whole-row build.
 template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M>
 constexpr bool has_whole_row_build() {
     return M == 2 || (M == 1 && FMT != kQ4K && B == 1 && !DOTS && !ID);
@@ -1032,8 +1033,8 @@ template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>
 inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, size_t smem,
                                    cudaStream_t s) {
     if constexpr (has_whole_row_build<FMT, B, DOTS, FUSE, ID, M>()) {
-        if (a.rows_per_group > 1)
-            return launch_kernel(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, true>, grid, block,
+        if (a.nb == 16)
+            return launch_kernel(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, 16>, grid, block,
                                  smem, s, a.overlap != 0, a);
     }
     return launch_kernel(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M>, grid, block, smem, s,
@@ -1043,7 +1044,7 @@ inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, s
 template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>
 inline cudaError_t configure_t(int smem_optin) {
     if constexpr (has_whole_row_build<FMT, B, DOTS, FUSE, ID, M>()) {
-        const cudaError_t e = cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, true>,
+        const cudaError_t e = cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, 16>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    smem_optin);
         if (e != cudaSuccess) return e;
