@@ -240,7 +240,7 @@ int64_t align128(int64_t v) { return (v + 127) & ~(int64_t)127; }
 // one slot, and `batch` staged activation vectors (1 shared, or one per slot).
 xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
                     int64_t smem_optin, xq_plan *p, int64_t slots = 0, bool have_ws = false,
-                    int fuse = 0) {
+                    int fuse = 0, bool dots = false) {
     const int32_t nb = (int32_t)(cols / 256);
     const int32_t R = (nb < 32 && 32 % nb == 0) ? 32 / nb : 1;
     const int32_t spr = R > 1 ? 1 : (nb + 31) / 32;
@@ -254,7 +254,7 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     const int64_t act = align128((int64_t)bl * nb * kActStride);
     if (slots > 0 && bl != batch)
         return fail(XQ_ESHAPE, "the per-slot activations do not fit in shared memory");
-    const int32_t wmax = warps_limit(fmt, slots > 0 ? 1 : bl, fuse);
+    const int32_t wmax = warps_limit(fmt, slots > 0 ? 1 : bl, fuse, dots);
     const int32_t ow = g_override_warps.load(), os = g_override_stages.load();
     const int32_t om = g_override_row_block.load();
     // Two stages (one box in flight per warp while the other is consumed) read
@@ -406,7 +406,7 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     if (xq_status s = device_state(&dev)) return s;
     xq_plan plan;
     if (xq_status s = make_plan(op.fmt, rows, cols, batch, dev->sm_count, dev->smem_optin, &plan,
-                                0, want_ws && op.kind == Kind::kLinear, norm ? 2 : 0))
+                                0, want_ws && op.kind == Kind::kLinear, norm ? 2 : 0, dots))
         return s;
     MatvecArgs a;
     memset(&a, 0, sizeof a);

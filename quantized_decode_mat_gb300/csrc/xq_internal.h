@@ -56,10 +56,13 @@ enum Format { kQ4K = 0, kCB4 = 1, kCB4R = 2 };
 // registers.  Q4_K: 12 at batch 2, 8 above (its row-blocked kernels need up
 // to 211).  Codebook: 16 up to batch 4 (98-128 registers), 8 above (12
 // measured slower there).  Warp counts that split unevenly over the
-// schedulers measured slower.  The planner may use fewer (see make_plan).
-constexpr int warps_limit(int fmt, int64_t batch, int fuse = 0) {
+// schedulers measured slower.  The exact-dots builds (a test export) of two
+// vectors or more take 8, so that writing the dots never spills.  The planner
+// may use fewer (see make_plan).
+constexpr int warps_limit(int fmt, int64_t batch, int fuse = 0, bool dots = false) {
     return batch == 1 ? (fuse == 2 ? 16 : 20)
-                      : fmt == kQ4K ? (batch == 2 ? 12 : kMaxWarps) : (batch <= 4 ? 16 : kMaxWarps);
+           : dots     ? kMaxWarps
+           : fmt == kQ4K ? (batch == 2 ? 12 : kMaxWarps) : (batch <= 4 ? 16 : kMaxWarps);
 }
 
 struct MatvecArgs {

@@ -366,28 +366,40 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const A
     cb4_blocks<B, DOTS, FIRST>(dk, P, act, T, hi, lo, dots, dots_bstride);
 }
 
-// ---- resident codebook rows: the staged slot map ------------------------------------
-// A box of resident rows is staged so that slot l (the chunk lane l takes)
-// is 144 bytes at 144l: its 16 scale bytes, then its eight 16-byte payloads.
-// The 144-byte slot stride puts the slots that eight lanes read at once on
-// distinct 4-bank groups, and every read is a fixed offset from the slot.
-__device__ __forceinline__ uint32_t cb4r_scale_slot(int slot) { return 144u * (uint32_t)slot; }
+// ---- resident codebook rows: the staged layout ----------------------------------------
+// A box of resident rows (32 chunks, 4608 bytes) is staged as 32 payload
+// slots of 128 bytes -- slot l holds the eight 16-byte payloads of the chunk
+// lane l takes, payload i at 16-byte position i ^ (l & 7) -- followed by 32
+// scale slots of 16 bytes at 4096 + 16 l.  A warp's copy instruction moves 32
+// consecutive 16-byte pieces of a row, which land in four whole 128-byte
+// payload slots (or in the contiguous scale slots), so each copy is written
+// as four shared-memory wavefronts; the position swizzle puts the payloads
+// that eight lanes read at once on distinct 4-bank groups.  (A slot of the
+// chunk's scales followed by its payloads, 144 bytes, left every 128-byte run
+// unaligned: 12.9 wavefronts a copy instruction, and each line fetched from
+// L2 about 1.55 times.)
+__device__ __forceinline__ uint32_t cb4r_scale_slot(int slot) {
+    return 4096u + 16u * (uint32_t)slot;
+}
 __device__ __forceinline__ uint32_t cb4r_payload_slot(int slot, int i) {
-    return 144u * (uint32_t)slot + 16u + 16u * (uint32_t)i;
+    return 128u * (uint32_t)slot + 16u * (uint32_t)(i ^ (slot & 7));
 }
 
+// stage: the staged box; slot: the chunk this lane takes.
 template <int B, bool DOTS, bool FIRST, class Act>
-__device__ __forceinline__ void cb4r_chunk(const uint8_t *__restrict__ w, const Act &act,
-                                           const uint32_t (&T)[4], float (&hi)[B],
+__device__ __forceinline__ void cb4r_chunk(const uint8_t *__restrict__ stage, int slot,
+                                           const Act &act, const uint32_t (&T)[4], float (&hi)[B],
                                            float (&lo)[B], int32_t *dots, int64_t dots_bstride) {
-    const uint4 sc = *reinterpret_cast<const uint4 *>(w);
+    const uint4 sc = *reinterpret_cast<const uint4 *>(stage + cb4r_scale_slot(slot));
     const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
+    const uint8_t *pay = stage + 128 * slot;
+    const int key = slot & 7;
     float dk[8];
     uint32_t P[8][4];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         dk[k] = f16_bits_to_f32(sw[k >> 1] >> (16 * (k & 1)));
-        const uint4 t = *reinterpret_cast<const uint4 *>(w + 16 + 16 * k);
+        const uint4 t = *reinterpret_cast<const uint4 *>(pay + 16 * (k ^ key));
         P[k][0] = t.x;
         P[k][1] = t.y;
         P[k][2] = t.z;
@@ -558,17 +570,19 @@ __device__ __forceinline__ void reduce_rows16_store(const float (&hi)[M][B], con
 // copies and the CTA's other warps cover them).  (Requesting all S stages
 // before the activation is staged measured slower.)  The act stride puts the
 // chunks that one instruction reads on distinct bank groups.
-template <int FMT, int B, int FUSE>
-constexpr int max_threads() { return warps_limit(FMT, B, FUSE) * 32; }
+template <int FMT, int B, int FUSE, bool DOTS = false>
+constexpr int max_threads() { return warps_limit(FMT, B, FUSE, DOTS) * 32; }
 
 // The launch bound a build is compiled for.  The row-blocked whole-row builds
 // are compiled for 12 warps (at most 168 registers a thread) although the plan
 // runs them with 8 beside the batch's activation: the tighter register budget
 // schedules faster (128256 x 4096 batch 8: 107.3 -> 106.0 us, 14336 x 4096
 // batch 8: 15.69 -> 15.59 us) and still spills nothing.
-template <int FMT, int B, int FUSE, int M, int WR>
+template <int FMT, int B, int FUSE, int M, int WR, bool DOTS>
 constexpr int bound_threads() {
-    return (M == 2 && WR && max_threads<FMT, B, FUSE>() < 384) ? 384 : max_threads<FMT, B, FUSE>();
+    return (M == 2 && WR && max_threads<FMT, B, FUSE, DOTS>() < 384)
+               ? 384
+               : max_threads<FMT, B, FUSE, DOTS>();
 }
 
 // M: row groups a warp works on at once (a work unit).  Two for Q4_K with
@@ -579,7 +593,7 @@ constexpr int bound_threads() {
 // compile time; the row-blocked launches and the batch-1 codebook launches
 // take it for such rows (has_whole_row_build).
 template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M, int WR = 0>
-__global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR>(), 1) xq_matvec_kernel(const MatvecArgs a) {
+__global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR, DOTS>(), 1) xq_matvec_kernel(const MatvecArgs a) {
     static_assert(!ID || (B == 1 && !DOTS && FUSE == 0), "the grouped form is batch 1 on q8 input");
     static_assert(M == 1 || (M == 2 && FMT == kQ4K && !ID), "row blocking is a Q4_K form");
     static_assert(FUSE >= 0 && FUSE <= 2, "FUSE: 0 q8 input, 1 quantise x, 2 RMSNorm then quantise");
@@ -650,10 +664,16 @@ __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR>(), 1) xq_ma
                 // an invalid expert id reads nothing
             } else if (whole) {
                 const int valid = gi.valid * (int)row_bytes;
+                if (valid == kStageBytes) {  // a full box: no per-copy test
 #pragma unroll
-                for (int k = 0; k < 9; ++k)
-                    if (16 * (lane + 32 * k) < valid)
+                    for (int k = 0; k < 9; ++k)
                         cp_async_16(dst_stage + dmap[k], rowp + 16 * (lane + 32 * k));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 9; ++k)
+                        if (16 * (lane + 32 * k) < valid)
+                            cp_async_16(dst_stage + dmap[k], rowp + 16 * (lane + 32 * k));
+                }
             } else {
                 const int c0 = ps * 32;
                 const int n = nb - c0 < 32 ? nb - c0 : 32;  // chunks of this segment
@@ -970,9 +990,11 @@ __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR>(), 1) xq_ma
                     else if (FMT == kCB4)
                         cb4_chunk<B, DOTS, false>(st, as, T, hi[0], lo[0], dp, dots_bstride);
                     else if (spr == 1)
-                        cb4r_chunk<B, DOTS, true>(st, as, T, hi[0], lo[0], dp, dots_bstride);
+                        cb4r_chunk<B, DOTS, true>(st - lane * kChunkBytes, lane, as, T, hi[0],
+                                                  lo[0], dp, dots_bstride);
                     else
-                        cb4r_chunk<B, DOTS, false>(st, as, T, hi[0], lo[0], dp, dots_bstride);
+                        cb4r_chunk<B, DOTS, false>(st - lane * kChunkBytes, lane, as, T, hi[0],
+                                                   lo[0], dp, dots_bstride);
                 }
             }
             __syncwarp();
