@@ -17,9 +17,9 @@ one copy is timed beside it).
 
 Timing: K steps are replayed from CUDA graphs and timed with CUDA events on
 the launching stream, bracketed by a barrier and a device synchronisation;
-this is done R times (rounds), interleaved with the mat-vec alone in ABBA
-order (step, mat-vec | mat-vec, step | ...), and ms_per_step is the median
-round.  The fused one-launch form, the two-call path (xq_quantize_q8 +
+this is done R times (rounds, 15 by default), interleaved with the mat-vec
+alone in ABBA order (step, mat-vec | mat-vec, step | ...), and ms_per_step is
+the median round.  The fused one-launch form, the two-call path (xq_quantize_q8 +
 mat-vec), the RMSNorm forms and, where they apply, the grouped-experts and
 repack arms are timed once each for the breakdown.
 
@@ -730,6 +730,8 @@ def run_ours(args, c):
                            "ms_per_step": e2e_serial_ms,
                            "path": "the same on one stream, copies in line with the kernel"}},
         "gpu_launches": int(round(launches_per_step * args.steps)),
+        "gpu_launches_note": "this library's kernels in one timed round of K steps (every "
+                             "round launches the same)",
         "launches_per_step": launches_per_step,
         "clocks": clocks,
         "device_status": status,
@@ -742,8 +744,9 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
-    ap.add_argument("--rounds", type=int, default=5,
-                    help="timed rounds of K steps (ABBA with the mat-vec alone); the median is reported")
+    ap.add_argument("--rounds", type=int, default=15,
+                    help="timed rounds of K steps (ABBA with the mat-vec alone); the median is "
+                         "reported (fifteen interleaved rounds, as in the pages' timing protocol)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--case", default=DEFAULT_CASE, choices=sorted(synthetic.CASES))
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
