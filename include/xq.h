@@ -289,7 +289,12 @@ enum { XQ_FORMAT_Q4K = 0, XQ_FORMAT_CB4 = 1, XQ_FORMAT_CB4R = 2 };
  * workspace (xq_linear_q4k_ws) quantises the activation once, in a launch of
  * its own, 0 if every CTA of the fused launch quantises it for itself;
  * xq_plan_matvec reports that step's choice, and the other entry points
- * ignore the field. */
+ * ignore the field.  vector_pairs: 1 if each unit of work (two row groups)
+ * and its stages are shared by a pair of warps that compute half of the
+ * vectors each (the Q4_K mat-vec on q8 blocks with rows of 16 chunks at 8
+ * vectors, on matrices large enough to give each pair many units; then
+ * warps = 12 by default, stages counts the stages of a pair, and smem_bytes
+ * includes each warp's reduction scratch). */
 typedef struct {
     int32_t warps;
     int32_t stages;
@@ -303,6 +308,7 @@ typedef struct {
     int64_t smem_bytes;
     int32_t row_block;
     int32_t quantise_once;
+    int32_t vector_pairs;
 } xq_plan;
 
 xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t batch,
@@ -321,6 +327,23 @@ void xq_set_row_block_override(int32_t row_block);
  * quantises the activation, 2 = quantise once into the workspace, 0 =
  * automatic.  Process-wide, for sweeps and tests. */
 void xq_set_quantise_once_override(int32_t mode);
+/* Override the use of warp pairs (xq_plan.vector_pairs): 1 = never, 2 =
+ * wherever they apply (the Q4_K mat-vec on q8 blocks, rows of 16 chunks, 8
+ * vectors, any matrix size), 0 = automatic (not beside a warp or stage
+ * override).  When forced, a warp override (rounded down to even, 2..12) and
+ * a stage override (2..8) size the pairs if they fit in shared memory.
+ * Process-wide, for sweeps and tests; the results are bit-identical either
+ * way. */
+void xq_set_vector_pairs_override(int32_t mode);
+/* The codebook table as the one-vector launches use it, when it splits: four
+ * words, bytes L[0..7] then H[0..7], with kv[n] = L[n] + rep(H[n]) and
+ * kv[n + 8] = rep(L[n]) + H[n] for n = 0..7 (signed bytes; rep(v) = -1 if
+ * v < 0, else 0), which a byte permute in its sign-replicating mode reads as
+ * two lookups whose sum is kv.  Returns 1 and writes out[0..3], or 0 when no
+ * such split exists (an entry of 127 next to one that needs a larger
+ * partner), in which case those launches decode with the sixteen-byte table.
+ * Host only; for tests. */
+int32_t xq_codebook_split_table(const int8_t *table, uint32_t *out);
 /* Plan used by the calling thread's last mat-vec or sub-dot launch. */
 xq_status xq_last_plan(xq_plan *plan);
 

@@ -26,7 +26,7 @@ class _Plan(ctypes.Structure):
                 ("chunks_per_row", ctypes.c_int32), ("groups", ctypes.c_int64),
                 ("batch_per_launch", ctypes.c_int32), ("launches", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int64), ("row_block", ctypes.c_int32),
-                ("quantise_once", ctypes.c_int32)]
+                ("quantise_once", ctypes.c_int32), ("vector_pairs", ctypes.c_int32)]
 
 
 def _sig(name, restype, argtypes):
@@ -79,6 +79,7 @@ _plan = _sig("xq_plan_matvec", ctypes.c_int, [_I32, _I64, _I64, _I64, _I32, _I64
                                              ctypes.POINTER(_Plan)])
 _set_override = _sig("xq_set_plan_override", None, [_I32, _I32])
 _set_row_block = _sig("xq_set_row_block_override", None, [_I32])
+_set_vector_pairs = _sig("xq_set_vector_pairs_override", None, [_I32])
 _last_plan = _sig("xq_last_plan", ctypes.c_int, [ctypes.POINTER(_Plan)])
 _launch_count = _sig("xq_launch_count", ctypes.c_uint64, [_I32])
 _device_status = _sig("xq_device_status", ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32),
@@ -502,6 +503,13 @@ def set_plan_override(warps: int = 0, stages: int = 0) -> None:
 def set_row_block_override(row_block: int = 0) -> None:
     """1 forces one row group per warp unit; 0 restores the automatic plan."""
     _set_row_block(row_block)
+
+
+def set_vector_pairs_override(mode: int = 0) -> None:
+    """Warp pairs sharing each unit (xq_plan.vector_pairs): 1 never, 2 wherever
+    they apply (then set_plan_override's warps and stages, if set, size the
+    pairs), 0 automatic.  The results are bit-identical either way."""
+    _set_vector_pairs(mode)
 
 
 def launch_count(which: int) -> int:

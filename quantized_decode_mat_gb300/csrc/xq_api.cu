@@ -141,12 +141,17 @@ std::atomic<int32_t> g_override_warps{0};
 std::atomic<int32_t> g_override_stages{0};
 std::atomic<int32_t> g_override_row_block{0};
 std::atomic<int32_t> g_override_quantise_once{0};
+std::atomic<int32_t> g_override_vector_pairs{0};
 std::atomic<int32_t> g_overlap{0};
 // The decode step with a workspace quantises the activation once, in a
 // launch of its own, when a launch's batch has at least this many q8 blocks;
 // below that every CTA of the one fused launch quantises it for itself
 // (measured crossover on GB300).
 constexpr int64_t kQuantOnceMinBlocks = 32;
+// Whether the planner picks warp pairs by itself (the override can force
+// them either way).
+constexpr bool kVectorPairsAuto = true;
+constexpr int64_t kVpMinUnits = 16;
 
 xq_status fail(xq_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 xq_status fail(xq_status s, const char *fmt, ...) {
@@ -220,6 +225,7 @@ xq_status device_state(DeviceState **out) {
         if (st.err == cudaSuccess) step(configure_matvec_cb4(st.smem_optin), "configure codebook kernels");
         if (st.err == cudaSuccess)
             step(configure_matvec_cb4r(st.smem_optin), "configure resident codebook kernels");
+
     });
     if (st.err != cudaSuccess) return cuda_fail(st.err, st.what);
     *out = &st;
@@ -238,9 +244,11 @@ int64_t align128(int64_t v) { return (v + 127) & ~(int64_t)127; }
 // fewer warps if even that does not fit.  slots > 0 plans the grouped-expert
 // form: `rows` rows per expert, `slots` selected experts, each group inside
 // one slot, and `batch` staged activation vectors (1 shared, or one per slot).
+// fused: the launch is the fused decode step (xq_linear_*), whose kernel
+// quantises x itself unless the plan quantises once into a workspace.
 xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t sm_count,
                     int64_t smem_optin, xq_plan *p, int64_t slots = 0, bool have_ws = false,
-                    int fuse = 0, bool dots = false) {
+                    int fuse = 0, bool dots = false, bool fused = false) {
     const int32_t nb = (int32_t)(cols / 256);
     const int32_t R = (nb < 32 && 32 % nb == 0) ? 32 / nb : 1;
     const int32_t spr = R > 1 ? 1 : (nb + 31) / 32;
@@ -318,6 +326,33 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     p->smem_bytes = bytes(W, S, M);
     p->row_block = M;
     p->quantise_once = qonce;
+    p->vector_pairs = 0;
+    // Warp pairs: the row-blocked mat-vec on q8 blocks (the plain mat-vec, or
+    // the decode step when it quantises once) for rows of 16 chunks at 8
+    // vectors, on matrices that give every pair at least kVpMinUnits units,
+    // when no warp or stage override is set: 12 warps (six pairs, three warps
+    // a scheduler) share two stages of two boxes a pair (128256 x 4096: 105.9
+    // against 100.2 us; slower on 14336 x 4096, 15.5 against 17.7 us, and at
+    // 6 vectors, 79.6 against 86.2 us).  Only those kernels have a warp-pair
+    // build.  Forced on (override 2), the warp and stage overrides size it.
+    const int32_t ovp = g_override_vector_pairs.load();
+    const bool q8_input = fuse == 0 && !dots && (!fused || qonce);
+    if (fmt == kQ4K && M == 2 && nb == 16 && bl == 8 && slots == 0 && q8_input && ovp != 1) {
+        int32_t vw = kVpWarps, vs = kVpStages;
+        if (ovp == 2 && ow > 0) vw = ow & ~1;
+        if (ovp == 2 && os > 0) vs = os;
+        const bool want = ovp == 2 || (kVectorPairsAuto && ow <= 0 && os <= 0 &&
+                                       units >= (int64_t)kVpMinUnits * grid * (vw / 2));
+        const int64_t vp_bytes = act + (int64_t)(vw / 2) * vs * M * kStageBytes +
+                                 (int64_t)vw * kVpScratchBytes + 128;
+        if (want && vw >= 2 && vw <= kVpWarps && vs >= 2 && vs <= kMaxStages &&
+            vp_bytes <= smem_optin) {
+            p->warps = vw;
+            p->stages = vs;
+            p->smem_bytes = vp_bytes;
+            p->vector_pairs = 1;
+        }
+    }
     return XQ_OK;
 }
 
@@ -358,6 +393,40 @@ void pack_table(const int8_t *table, uint32_t (&kv)[4]) {
         for (int j = 0; j < 4; ++j) w |= (uint32_t)(uint8_t)table[4 * i + j] << (8 * j);
         kv[i] = w;
     }
+}
+
+// The two lookup tables of the one-vector codebook dot (cb4_dot_split): bytes
+// L[0..7] in kv[0..1] and H[0..7] in kv[2..3] with, for i = 0..7,
+//   kv[i]     = L[i] + rep(H[i])      (rep: 0 for a byte >= 0, -1 below 0)
+//   kv[i + 8] = rep(L[i]) + H[i]
+// since prmt returns byte n of a table for an index n < 8 and rep of byte
+// n - 8 for n >= 8.  Per i the signs s = rep(H[i]), t = rep(L[i]) must agree
+// with the bytes they produce; one of the two choices of s works unless an
+// entry is 127 where its partner needs one more (then false: the select
+// decode is used).
+bool split_table(const int8_t *table, uint32_t (&kv)[4]) {
+    uint8_t L[8], H[8];
+    for (int i = 0; i < 8; ++i) {
+        bool found = false;
+        for (int s = 0; s <= 1 && !found; ++s) {  // s = 1: H[i] < 0, so rep(H[i]) = -1
+            const int l = table[i] + s;
+            const int t = l < 0 ? 1 : 0;
+            const int h = table[i + 8] + t;
+            if (l > 127 || h > 127 || h < -128 || (h < 0 ? 1 : 0) != s) continue;
+            L[i] = (uint8_t)(int8_t)l;
+            H[i] = (uint8_t)(int8_t)h;
+            found = true;
+        }
+        if (!found) return false;
+    }
+    for (int w = 0; w < 2; ++w) {
+        kv[w] = kv[w + 2] = 0;
+        for (int j = 0; j < 4; ++j) {
+            kv[w] |= (uint32_t)L[4 * w + j] << (8 * j);
+            kv[w + 2] |= (uint32_t)H[4 * w + j] << (8 * j);
+        }
+    }
+    return true;
 }
 
 // in: q8 blocks (mat-vec and sub-dots) or f32 x (the fused linear ops).
@@ -406,7 +475,7 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     if (xq_status s = device_state(&dev)) return s;
     xq_plan plan;
     if (xq_status s = make_plan(op.fmt, rows, cols, batch, dev->sm_count, dev->smem_optin, &plan,
-                                0, want_ws && op.kind == Kind::kLinear, norm ? 2 : 0, dots))
+                                0, want_ws && op.kind == Kind::kLinear, norm ? 2 : 0, dots, fused))
         return s;
     MatvecArgs a;
     memset(&a, 0, sizeof a);
@@ -418,8 +487,12 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     a.segments = plan.segments;
     a.stages = plan.stages;
     a.row_block = plan.row_block;
+    a.vector_pairs = plan.vector_pairs;
     a.overlap = g_overlap.load();
-    if (cb4) pack_table(table, a.kv);
+    if (cb4) {
+        a.kv_split = plan.batch_per_launch == 1 && split_table(table, a.kv);
+        if (!a.kv_split) pack_table(table, a.kv);
+    }
     // quantise once: q8 blocks into the workspace, then the mat-vec on them
     const bool once = plan.quantise_once != 0;
     if (fused && !once && g_override_warps.load() == 0)  // an override is kept as given
@@ -427,6 +500,12 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int kind = dots ? 1 : norm ? 4 : (fused && !once) ? 2 : 0;
+    // only the row-blocked Q4_K mat-vec on q8 blocks has a warp-pair build
+    if (plan.vector_pairs && !(kind == 0 && op.fmt == kQ4K && plan.row_block == 2 && nb == 16 &&
+                               plan.launches == 1 && plan.warps % 2 == 0 &&
+                               plan.warps <= kVpWarps && plan.stages >= 2 &&
+                               plan.batch_per_launch == 8))
+        return fail(XQ_ELAUNCH, "internal: a warp-pair plan for a kernel without that build");
     for (int64_t b0 = 0; b0 < batch; b0 += plan.batch_per_launch) {
         const int64_t bc = batch - b0 < plan.batch_per_launch ? batch - b0 : plan.batch_per_launch;
         if (once) {
@@ -501,7 +580,10 @@ xq_status run_matvec_id(int fmt, const void *W, const int8_t *table, const int32
     a.groups_per_slot = (int32_t)(plan.groups / used);
     a.act_vectors = (int32_t)nvec;
     a.status = dev->status;
-    if (cb4) pack_table(table, a.kv);
+    if (cb4) {  // one vector a slot
+        a.kv_split = split_table(table, a.kv);
+        if (!a.kv_split) pack_table(table, a.kv);
+    }
     const dim3 grid(plan.grid), block(plan.warps * 32);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_fmt(fmt, a, 1, 3, grid, block, (size_t)plan.smem_bytes, s);
@@ -795,7 +877,7 @@ xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t bat
     if (xq_status s = check_shape(rows, cols, batch, true)) return s;
     if (sm_count < 1) return fail(XQ_EINVAL, "sm_count must be positive");
     return make_plan(format == XQ_FORMAT_Q4K ? kQ4K : format == XQ_FORMAT_CB4 ? kCB4 : kCB4R, rows,
-                     cols, batch, sm_count, smem_optin_bytes, plan, 0, true);
+                     cols, batch, sm_count, smem_optin_bytes, plan, 0, true, 0, false, true);
 }
 
 void xq_set_plan_override(int32_t warps, int32_t stages) {
@@ -813,6 +895,18 @@ int32_t xq_overlap_launches(void) { return g_overlap.load(); }
 
 void xq_set_quantise_once_override(int32_t mode) {
     g_override_quantise_once.store(mode < 0 || mode > 2 ? 0 : mode);
+}
+
+int32_t xq_codebook_split_table(const int8_t *table, uint32_t *out) {
+    if (!table || !out) return 0;
+    uint32_t kv[4];
+    if (!split_table(table, kv)) return 0;
+    for (int i = 0; i < 4; ++i) out[i] = kv[i];
+    return 1;
+}
+
+void xq_set_vector_pairs_override(int32_t mode) {
+    g_override_vector_pairs.store(mode < 0 || mode > 2 ? 0 : mode);
 }
 
 xq_status xq_last_plan(xq_plan *plan) {
@@ -855,6 +949,6 @@ const char *xq_status_string(xq_status s) {
 
 const char *xq_last_error(void) { return t_error.c_str(); }
 
-int32_t xq_version(void) { return 2; }
+int32_t xq_version(void) { return 3; }
 
 }  // extern "C"

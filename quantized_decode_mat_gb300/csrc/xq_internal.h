@@ -40,6 +40,13 @@ constexpr int kQuantGroup = 4;
 constexpr int kStageAsyncBlocks = 64;
 constexpr int kStageItems = 4;
 constexpr int kMaxWarps = 8;
+// Warp pairs (the row-blocked Q4_K form for rows of 16 chunks, 8 vectors): each unit of two row groups and its stages are shared by two
+// warps, each computing half of the vectors; 12 warps a CTA (6 pairs), and
+// each warp's reduction scratch (32 lanes x (2 x 4 + 1) pairs of floats) after
+// the stages.
+constexpr int kVpWarps = 12;
+constexpr int kVpStages = 2;
+constexpr int kVpScratchBytes = (2 * 4 + 1) * 8 * 32;
 constexpr int kMaxStages = 8;
 
 // kCB4R: codebook blocks in resident rows (scale prefix, then 16-byte
@@ -78,7 +85,10 @@ struct MatvecArgs {
     int32_t segments;       // boxes per group: 1, or ceil(nb/32) when rows_per_group == 1
     int32_t stages;         // shared-memory stages per warp (2..8)
     int32_t row_block;      // row groups a warp works on at once (1, or 2 for Q4_K at batch >= 2)
-    uint32_t kv[4];         // codebook bytes kv[0..15], little-endian words
+    int32_t vector_pairs;   // 1: warp pairs share each unit, half of the vectors each
+    uint32_t kv[4];         // codebook bytes kv[0..15], little-endian words (or, with
+                            // kv_split, the two lookup tables whose sum is kv)
+    int32_t kv_split;       // 1: kv holds the split tables (one-vector launches)
     // grouped-expert form
     const int32_t *sel;     // [used] expert ids (device)
     int64_t rows_per_expert;

@@ -279,34 +279,68 @@ __device__ __forceinline__ void cb4_decode(uint32_t q, const uint32_t (&T)[4], u
     F1 = (a1 & ~m1) | (b1 & m1);
 }
 
+// The dot of a payload word q (eight nibbles) with the two activation words
+// in its nibble order, from a table split in two: kv[n] = L[n] + H[n] (signed
+// bytes), where one lookup of the whole nibble in (S[0], S[1]) gives L -- an
+// entry for n < 8, and for n >= 8 prmt's sign replication of byte n - 8,
+// 0 or -1 -- and one lookup of n ^ 8 in (S[2], S[3]) gives H the other way
+// round (the host finds the bytes; split_table in the API).  Four lookups
+// and four dp4a, no select: seven operations of decode a word against the
+// eleven of cb4_decode, for one vector (with more vectors the select form
+// does fewer operations, as its decoded words are shared).
+__device__ __forceinline__ int cb4_dot_split(uint32_t q, const uint32_t (&S)[4], uint32_t a0,
+                                             uint32_t a1, int acc) {
+    const uint32_t qx = q ^ 0x88888888u;
+    const uint32_t l0 = prmt(S[0], S[1], q);          // nibbles 0..3
+    const uint32_t h0 = prmt(S[2], S[3], qx);
+    const uint32_t l1 = prmt(S[0], S[1], q >> 16);    // nibbles 4..7
+    const uint32_t h1 = prmt(S[2], S[3], qx >> 16);
+    acc = dp4a(l0, a0, acc);
+    acc = dp4a(h0, a0, acc);
+    acc = dp4a(l1, a1, acc);
+    return dp4a(h1, a1, acc);
+}
+
 // Eight codebook blocks of one chunk: scales dk[k] and payload words P[k][0..3]
 // (block k's 16 payload bytes, little-endian), against the interleaved q8
 // block `act`.  Block by block: decode, then its dot with every vector; per
-// vector the compensated sum over the blocks runs in block order.
-template <int B, bool DOTS, bool FIRST, class Act>
+// vector the compensated sum over the blocks runs in block order.  T: the
+// table as sixteen bytes, or with SPLIT (one vector only) as the two lookup
+// tables of cb4_dot_split; either gives the same integer dots.
+template <int B, bool DOTS, bool FIRST, bool SPLIT, class Act>
 __device__ __forceinline__ void cb4_blocks(const float (&dk)[8], const uint32_t (&P)[8][4],
                                            const Act &act, const uint32_t (&T)[4], float (&hi)[B],
                                            float (&lo)[B], int32_t *dots, int64_t dots_bstride) {
+    static_assert(!SPLIT || B == 1, "the split table serves one vector");
     float ch[B], cl[B];  // sum_k d_k * dot_k per vector, compensated
 #pragma unroll
     for (int b = 0; b < B; ++b) ch[b] = cl[b] = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         uint32_t F[8];
+        if constexpr (!SPLIT) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cb4_decode(P[k][i], T, F[2 * i], F[2 * i + 1]);
+            for (int i = 0; i < 4; ++i) cb4_decode(P[k][i], T, F[2 * i], F[2 * i + 1]);
+        }
 #pragma unroll
         for (int b = 0; b < B; ++b) {
             const uint4 a0 = act.q16(b, 2 * k), a1 = act.q16(b, 2 * k + 1);
             int dt = 0;
-            dt = dp4a(F[0], a0.x, dt);
-            dt = dp4a(F[1], a0.y, dt);
-            dt = dp4a(F[2], a0.z, dt);
-            dt = dp4a(F[3], a0.w, dt);
-            dt = dp4a(F[4], a1.x, dt);
-            dt = dp4a(F[5], a1.y, dt);
-            dt = dp4a(F[6], a1.z, dt);
-            dt = dp4a(F[7], a1.w, dt);
+            if constexpr (SPLIT) {
+                dt = cb4_dot_split(P[k][0], T, a0.x, a0.y, dt);
+                dt = cb4_dot_split(P[k][1], T, a0.z, a0.w, dt);
+                dt = cb4_dot_split(P[k][2], T, a1.x, a1.y, dt);
+                dt = cb4_dot_split(P[k][3], T, a1.z, a1.w, dt);
+            } else {
+                dt = dp4a(F[0], a0.x, dt);
+                dt = dp4a(F[1], a0.y, dt);
+                dt = dp4a(F[2], a0.z, dt);
+                dt = dp4a(F[3], a0.w, dt);
+                dt = dp4a(F[4], a1.x, dt);
+                dt = dp4a(F[5], a1.y, dt);
+                dt = dp4a(F[6], a1.z, dt);
+                dt = dp4a(F[7], a1.w, dt);
+            }
             float p, e;
             two_prod(dk[k], __int2float_rn(dt), p, e);  // |dt| < 2^20: exact in f32
             if (k == 0) {  // an exact add to zero is an assignment
@@ -334,7 +368,7 @@ __device__ __forceinline__ void cb4_blocks(const float (&dk)[8], const uint32_t 
 
 // Raw layout: w is this lane's 144-byte chunk (eight 18-byte blocks) in
 // shared memory.
-template <int B, bool DOTS, bool FIRST, class Act>
+template <int B, bool DOTS, bool FIRST, bool SPLIT, class Act>
 __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const Act &act,
                                           const uint32_t (&T)[4], float (&hi)[B], float (&lo)[B],
                                           int32_t *dots, int64_t dots_bstride) {
@@ -363,7 +397,7 @@ __device__ __forceinline__ void cb4_chunk(const uint8_t *__restrict__ w, const A
             P[2 * p + 1][i] = v[9 * p + 5 + i];
         }
     }
-    cb4_blocks<B, DOTS, FIRST>(dk, P, act, T, hi, lo, dots, dots_bstride);
+    cb4_blocks<B, DOTS, FIRST, SPLIT>(dk, P, act, T, hi, lo, dots, dots_bstride);
 }
 
 // ---- resident codebook rows: the staged layout ----------------------------------------
@@ -386,7 +420,7 @@ __device__ __forceinline__ uint32_t cb4r_payload_slot(int slot, int i) {
 }
 
 // stage: the staged box; slot: the chunk this lane takes.
-template <int B, bool DOTS, bool FIRST, class Act>
+template <int B, bool DOTS, bool FIRST, bool SPLIT, class Act>
 __device__ __forceinline__ void cb4r_chunk(const uint8_t *__restrict__ stage, int slot,
                                            const Act &act, const uint32_t (&T)[4], float (&hi)[B],
                                            float (&lo)[B], int32_t *dots, int64_t dots_bstride) {
@@ -405,7 +439,7 @@ __device__ __forceinline__ void cb4r_chunk(const uint8_t *__restrict__ stage, in
         P[k][2] = t.z;
         P[k][3] = t.w;
     }
-    cb4_blocks<B, DOTS, FIRST>(dk, P, act, T, hi, lo, dots, dots_bstride);
+    cb4_blocks<B, DOTS, FIRST, SPLIT>(dk, P, act, T, hi, lo, dots, dots_bstride);
 }
 
 // ---- reduction of a row's partial sums -------------------------------------------------
@@ -592,9 +626,18 @@ constexpr int bound_threads() {
 // the row width, the rows a box and the segment bookkeeping are known at
 // compile time; the row-blocked launches and the batch-1 codebook launches
 // take it for such rows (has_whole_row_build).
-template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M, int WR = 0>
-__global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR, DOTS>(), 1) xq_matvec_kernel(const MatvecArgs a) {
+template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M, int WR = 0, bool VP = false,
+          bool KS = false>
+__global__ void __launch_bounds__(VP ? kVpWarps * 32 : bound_threads<FMT, B, FUSE, M, WR, DOTS>(), 1)
+    xq_matvec_kernel(const MatvecArgs a) {
+    static_assert(!KS || (FMT != kQ4K && B == 1), "KS: the codebook table split, one vector");
     static_assert(!ID || (B == 1 && !DOTS && FUSE == 0), "the grouped form is batch 1 on q8 input");
+    static_assert(!VP || (FMT == kQ4K && M == 2 && WR == 16 && !DOTS && !ID && FUSE == 0 &&
+                          B == 8),
+                  "warp pairs: the row-blocked Q4_K form for rows of 16 chunks, on q8 input");
+    // BW: the vectors this warp computes (VP: a warp pair shares each unit and
+    // its stages, each warp taking half of the vectors)
+    constexpr int BW = VP ? B / 2 : B;
     static_assert(M == 1 || (M == 2 && FMT == kQ4K && !ID), "row blocking is a Q4_K form");
     static_assert(FUSE >= 0 && FUSE <= 2, "FUSE: 0 q8 input, 1 quantise x, 2 RMSNorm then quantise");
     extern __shared__ uint8_t smem_raw[];
@@ -602,6 +645,9 @@ __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR, DOTS>(), 1)
     const int W = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int half = VP ? (warp & 1) : 0;        // which half of the vectors
+    const int uwarp = VP ? (warp >> 1) : warp;   // the unit stream (a pair in VP)
+    const int WU = VP ? (W >> 1) : W;
     const int S = a.stages;
     static_assert(WR == 0 || WR == 16, "the whole-row build is for rows of 16 chunks");
     const int nb = WR ? WR : a.nb;
@@ -616,17 +662,18 @@ __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR, DOTS>(), 1)
     const int act_bytes = (int)((nvec * act_bstride + 127) & ~(int64_t)127);
     const uint32_t unit_bytes = (uint32_t)M * kStageBytes;  // one stage: M boxes
     uint8_t *act = smem;
-    uint8_t *stage0 = smem + act_bytes + (size_t)warp * S * unit_bytes;
+    uint8_t *stage0 = smem + act_bytes + (size_t)uwarp * S * unit_bytes;
     const uint32_t stage0_u32 = smem_u32(stage0);
 
+    // the codebook table (KS: its two split lookup tables)
     uint32_t T[4] = {a.kv[0], a.kv[1], a.kv[2], a.kv[3]};
 
     // 1. this warp's work units (M consecutive row groups) and their boxes;
     //    the first S-1 stages are requested before the activation is staged,
     //    so the two overlap
     const int G = gridDim.x;
-    const int64_t gw = (int64_t)warp * G + blockIdx.x;
-    const int64_t TW = (int64_t)G * W;
+    const int64_t gw = (int64_t)uwarp * G + blockIdx.x;
+    const int64_t TW = (int64_t)G * WU;
     const int64_t nunits = (ngroups + M - 1) / M;
     const int64_t my_units = gw < nunits ? (nunits - 1 - gw) / TW + 1 : 0;
     const int nitems = (int)(my_units * spr);
@@ -721,6 +768,7 @@ __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR, DOTS>(), 1)
         const uint32_t dst_stage = stage0_u32 + (uint32_t)p_stage * unit_bytes;
 #pragma unroll
         for (int m = 0; m < M; ++m) {
+            if (VP && m != half) continue;  // the partner warp copies the other box
             if (pu * M + m < ngroups) {
                 issue_box(pu * M + m, dst_stage + (uint32_t)m * kStageBytes);
             } else if (M > 1) {  // the unit's missing last group: zeros
@@ -945,22 +993,35 @@ __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR, DOTS>(), 1)
                 gi[m].bad = false;
             }
         }
-        float hi[M][B], lo[M][B];
+        float hi[M][BW], lo[M][BW];
 #pragma unroll
         for (int m = 0; m < M; ++m)
 #pragma unroll
-            for (int b = 0; b < B; ++b) hi[m][b] = lo[m][b] = 0.0f;
+            for (int b = 0; b < BW; ++b) hi[m][b] = lo[m][b] = 0.0f;
         for (int s = 0; s < spr; ++s) {
-            if (issued < nitems) issue_next();
-            cp_async_commit();
-            cp_async_wait_pending(S - 1);  // this lane's copies of the stage landed
-            __syncwarp();                  // ... and every other lane's
+            if constexpr (VP) {
+                // the unit's copies were issued one unit ahead, half by each warp
+                // of the pair: wait for this warp's, then meet the partner, after
+                // which both have landed and both warps are done with the stage
+                // read in the previous unit, which is refilled next (S >= 2)
+                cp_async_wait_pending(S - 2);
+                __syncwarp();
+                pair_barrier(uwarp);
+                if (issued < nitems) issue_next();
+                cp_async_commit();
+            } else {
+                if (issued < nitems) issue_next();
+                cp_async_commit();
+                cp_async_wait_pending(S - 1);  // this lane's copies of the stage landed
+                __syncwarp();                  // ... and every other lane's
+            }
             const int c = whole ? (lane & (nb - 1)) : s * 32 + lane;
             const uint8_t *st = stage0 + c_stage * unit_bytes + lane * kChunkBytes;
             // (M > 1 reads the activation of chunks past the row's end too, and
             // multiplies it by zero-filled weights: a real block keeps it finite)
             const int ca = M > 1 && c >= nb ? nb - 1 : c;
-            const ActSmem as{act + gi[0].vec * act_bstride + ca * kActStride, act_bstride};
+            const ActSmem as{act + (gi[0].vec + half * BW) * act_bstride + ca * kActStride,
+                             act_bstride};
             if (M > 1) {
                 const uint8_t *w[M];
                 bool ok[M];
@@ -975,26 +1036,26 @@ __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR, DOTS>(), 1)
                 }
                 if (any) {
                     if (spr == 1)  // one segment a row: every chunk is its lane's first
-                        q4k_chunks<B, M, DOTS, true>(w, ok, as, hi, lo, dp, dots_bstride);
+                        q4k_chunks<BW, M, DOTS, true>(w, ok, as, hi, lo, dp, dots_bstride);
                     else  // (hi, lo) start at zero, to which an exact add is an assignment
-                        q4k_chunks<B, M, DOTS, false>(w, ok, as, hi, lo, dp, dots_bstride);
+                        q4k_chunks<BW, M, DOTS, false>(w, ok, as, hi, lo, dp, dots_bstride);
                 }
             } else {
                 const bool ok = rig < gi[0].valid && c < nb && !gi[0].bad;
                 if (ok) {
                     int32_t *dp = DOTS ? a.dots + (gi[0].row0 + rig) * dots_row + c * 8 : nullptr;
                     if (FMT == kQ4K)
-                        q4k_chunk<B, DOTS>(st, as, hi[0], lo[0], dp, dots_bstride, s == 0);
+                        q4k_chunk<BW, DOTS>(st, as, hi[0], lo[0], dp, dots_bstride, s == 0);
                     else if (FMT == kCB4 && spr == 1)  // one segment a row: the lane's first chunk
-                        cb4_chunk<B, DOTS, true>(st, as, T, hi[0], lo[0], dp, dots_bstride);
+                        cb4_chunk<BW, DOTS, true, KS>(st, as, T, hi[0], lo[0], dp, dots_bstride);
                     else if (FMT == kCB4)
-                        cb4_chunk<B, DOTS, false>(st, as, T, hi[0], lo[0], dp, dots_bstride);
+                        cb4_chunk<BW, DOTS, false, KS>(st, as, T, hi[0], lo[0], dp, dots_bstride);
                     else if (spr == 1)
-                        cb4r_chunk<B, DOTS, true>(st - lane * kChunkBytes, lane, as, T, hi[0],
-                                                  lo[0], dp, dots_bstride);
+                        cb4r_chunk<BW, DOTS, true, KS>(st - lane * kChunkBytes, lane, as, T,
+                                                       hi[0], lo[0], dp, dots_bstride);
                     else
-                        cb4r_chunk<B, DOTS, false>(st - lane * kChunkBytes, lane, as, T, hi[0],
-                                                   lo[0], dp, dots_bstride);
+                        cb4r_chunk<BW, DOTS, false, KS>(st - lane * kChunkBytes, lane, as, T,
+                                                        hi[0], lo[0], dp, dots_bstride);
                 }
             }
             __syncwarp();
@@ -1005,32 +1066,38 @@ __global__ void __launch_bounds__(bound_threads<FMT, B, FUSE, M, WR, DOTS>(), 1)
         // (with one or two vectors it leaves most lanes without an output, and
         // the shuffle reduction is faster: 14336 x 4096 batch 2, 8.64 against
         // 8.37 us)
-        if constexpr (M == 2 && WR == 16 && !DOTS && B >= 3) {
-            const int used = c_stage == 0 ? S - 1 : c_stage - 1;  // the stage just read
-            reduce_rows16_store<M, B>(hi, lo, stage0 + used * unit_bytes, lane, gi, a.y, rows);
+        if constexpr (M == 2 && WR == 16 && !DOTS && BW >= 3) {
+            // scratch: the stage just read, or with warp pairs (whose stages are
+            // shared) this warp's own region after all the stages
+            const int used = c_stage == 0 ? S - 1 : c_stage - 1;
+            uint8_t *scratch = VP ? smem + act_bytes + (size_t)WU * S * unit_bytes +
+                                        (size_t)warp * kVpScratchBytes
+                                  : stage0 + used * unit_bytes;
+            reduce_rows16_store<M, BW>(hi, lo, scratch, lane, gi, a.y + (int64_t)half * BW * rows,
+                                       rows);
             stored = true;
         }
         if (!DOTS && !stored) {
-            constexpr int P = Pow2Ceil<B>::v;
+            constexpr int P = Pow2Ceil<BW>::v;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 float h[P], l[P];
 #pragma unroll
                 for (int b = 0; b < P; ++b) {
-                    h[b] = b < B ? hi[m][b] : 0.0f;
-                    l[b] = b < B ? lo[m][b] : 0.0f;
+                    h[b] = b < BW ? hi[m][b] : 0.0f;
+                    l[b] = b < BW ? lo[m][b] : 0.0f;
                 }
                 int base, nlive, keep;
                 halving_reduce<P>(h, l, width, lane, base, nlive, keep);
                 if ((lane & keep) == 0 && rig < gi[m].valid) {
-                    float *yb = a.y + (int64_t)base * rows + gi[m].out0 + rig;
+                    float *yb = a.y + (int64_t)(half * BW + base) * rows + gi[m].out0 + rig;
                     const float nan = __int_as_float(0x7FC00000);
                     if (P == 1 || nlive == 1) {  // rows of P lanes or more: one value a lane
-                        if (base < B) yb[0] = gi[m].bad ? nan : __fadd_rn(h[0], l[0]);
+                        if (base < BW) yb[0] = gi[m].bad ? nan : __fadd_rn(h[0], l[0]);
                     } else {
 #pragma unroll
                         for (int i = 0; i < P; ++i)
-                            if (i < nlive && base + i < B)
+                            if (i < nlive && base + i < BW)
                                 yb[(int64_t)i * rows] = gi[m].bad ? nan : __fadd_rn(h[i], l[i]);
                     }
                     if (ID && gi[m].bad && rig == 0 && (lane & (width - 1)) == 0)
@@ -1051,9 +1118,32 @@ constexpr bool has_whole_row_build() {
     return M == 2 || (M == 1 && FMT != kQ4K && B == 1 && !DOTS && !ID);
 }
 
+// Builds for warp pairs (VP): the row-blocked Q4_K mat-vec on q8 blocks for
+// rows of 16 chunks at 8 vectors, launched when the plan asks for them.
+template <int FMT, int B, bool DOTS, int FUSE, bool ID, int M>
+constexpr bool has_vector_pair_build() {
+    return FMT == kQ4K && M == 2 && !DOTS && !ID && FUSE == 0 && B == 8;
+}
+
 template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>
 inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, size_t smem,
                                    cudaStream_t s) {
+    if constexpr (FMT != kQ4K && B == 1) {  // one vector: the split codebook table, if it splits
+        if (a.kv_split) {
+            if constexpr (has_whole_row_build<FMT, B, DOTS, FUSE, ID, M>()) {
+                if (a.nb == 16)
+                    return launch_kernel(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, 16, false, true>,
+                                         grid, block, smem, s, a.overlap != 0, a);
+            }
+            return launch_kernel(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, 0, false, true>, grid,
+                                 block, smem, s, a.overlap != 0, a);
+        }
+    }
+    if constexpr (has_vector_pair_build<FMT, B, DOTS, FUSE, ID, M>()) {
+        if (a.vector_pairs && a.nb == 16)
+            return launch_kernel(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, 16, true>, grid, block,
+                                 smem, s, a.overlap != 0, a);
+    }
     if constexpr (has_whole_row_build<FMT, B, DOTS, FUSE, ID, M>()) {
         if (a.nb == 16)
             return launch_kernel(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, 16>, grid, block,
@@ -1065,6 +1155,24 @@ inline cudaError_t launch_matvec_t(const MatvecArgs &a, dim3 grid, dim3 block, s
 
 template <int FMT, int B, bool DOTS, int FUSE, bool ID = false, int M = 1>
 inline cudaError_t configure_t(int smem_optin) {
+    if constexpr (FMT != kQ4K && B == 1) {
+        if constexpr (has_whole_row_build<FMT, B, DOTS, FUSE, ID, M>()) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, 16, false, true>,
+                cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+            if (e != cudaSuccess) return e;
+        }
+        const cudaError_t e = cudaFuncSetAttribute(
+            xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, 0, false, true>,
+            cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+        if (e != cudaSuccess) return e;
+    }
+    if constexpr (has_vector_pair_build<FMT, B, DOTS, FUSE, ID, M>()) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, 16, true>,
+            cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+        if (e != cudaSuccess) return e;
+    }
     if constexpr (has_whole_row_build<FMT, B, DOTS, FUSE, ID, M>()) {
         const cudaError_t e = cudaFuncSetAttribute(xq_matvec_kernel<FMT, B, DOTS, FUSE, ID, M, 16>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,

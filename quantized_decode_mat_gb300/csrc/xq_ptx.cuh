@@ -94,6 +94,12 @@ __device__ __forceinline__ void grid_dependency_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Named barrier of the two warps of warp pair `pair` (barrier ids 2..;
+// 0 is __syncthreads and 1 the RMSNorm workgroup's).
+__device__ __forceinline__ void pair_barrier(int pair) {
+    asm volatile("bar.sync %0, 64;" ::"r"(2 + pair) : "memory");
+}
+
 __device__ __forceinline__ float f16_bits_to_f32(uint32_t bits16) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
 }

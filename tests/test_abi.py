@@ -9,6 +9,8 @@ import re
 import numpy as np
 import pytest
 
+import synthetic
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "xq.h")
 
@@ -152,11 +154,11 @@ def test_status_strings(raw):
     fn.restype = ctypes.c_char_p
     for s in range(6):
         assert fn(s).startswith(b"XQ_")
-    assert raw.xq_version() == 2
+    assert raw.xq_version() == 3
 
 
 @pytest.mark.parametrize("fmt,rows,cols,batch,warps,grid,R,spr,launches,M", [
-    ("q4k", 128256, 4096, 1, 16, 152, 2, 1, 1, 1), ("q4k", 128256, 4096, 8, 8, 152, 2, 1, 1, 2),
+    ("q4k", 128256, 4096, 1, 16, 152, 2, 1, 1, 1), ("q4k", 128256, 4096, 8, 12, 152, 2, 1, 1, 2),
     ("q4k", 4096, 4096, 1, 14, 152, 2, 1, 1, 1), ("q4k", 14336, 4096, 4, 8, 152, 2, 1, 1, 2),
     ("q4k", 4096, 14336, 1, 20, 152, 1, 2, 1, 1), ("q4k", 4096, 14336, 8, 8, 152, 1, 2, 1, 2),
     ("q4k", 4096, 14336, 4, 8, 152, 1, 2, 1, 2), ("q4k", 14336, 4096, 2, 12, 152, 2, 1, 1, 2),
@@ -176,11 +178,18 @@ def test_plan(lib, fmt, rows, cols, batch, warps, grid, R, spr, launches, M):
     assert p["grid"] == min(-(-p["groups"] // M), 152)
     # a work unit is whole rows in one 4608-byte box, or one row in 32-chunk boxes
     assert (R > 1 and R * nb == 32 and spr == 1) or (R == 1 and spr == -(-nb // 32))
-    # two stages, or one where two-box stages for every warp do not fit
     act = -(-p["batch_per_launch"] * nb * 336 // 128) * 128
-    two = act + p["warps"] * 2 * M * 4608 + 128
-    assert p["stages"] == (2 if two <= 232448 or M == 1 else 1)
-    assert p["smem_bytes"] == act + p["warps"] * p["stages"] * M * 4608 + 128
+    if p["vector_pairs"]:
+        # warp pairs: 12 warps, two stages a pair, a 2304-byte reduction
+        # scratch a warp
+        assert fmt == "q4k" and M == 2 and nb == 16 and batch == 8
+        assert p["warps"] == 12 and p["stages"] == 2
+        assert p["smem_bytes"] == act + 6 * 2 * M * 4608 + 12 * 2304 + 128
+    else:
+        # two stages, or one where two-box stages for every warp do not fit
+        two = act + p["warps"] * 2 * M * 4608 + 128
+        assert p["stages"] == (2 if two <= 232448 or M == 1 else 1)
+        assert p["smem_bytes"] == act + p["warps"] * p["stages"] * M * 4608 + 128
     assert p["smem_bytes"] <= 232448
     assert p["batch_per_launch"] * (p["launches"] - 1) < batch <= p["batch_per_launch"] * p["launches"]
 
@@ -196,6 +205,91 @@ def test_row_block_override(lib):
     finally:
         lib.set_row_block_override(0)
     assert lib.plan_matvec(128256, 4096, 8)["row_block"] == 2
+
+
+def test_vector_pairs_plan(lib):
+    """Warp pairs only for the Q4_K mat-vec on q8 blocks with rows of 16
+    chunks at 8 vectors; the override turns them off or on."""
+    assert lib.plan_matvec(128256, 4096, 8)["vector_pairs"] == 1
+    assert lib.plan_matvec(128256, 4096, 6)["vector_pairs"] == 0
+    # at least 16 units (four rows each) for each of the 152 x 6 pairs
+    assert lib.plan_matvec(4 * 16 * 152 * 6, 4096, 8)["vector_pairs"] == 1
+    assert lib.plan_matvec(4 * 16 * 152 * 6 - 4, 4096, 8)["vector_pairs"] == 0
+    for rows, cols, batch, fmt in ((14336, 4096, 4, "q4k"), (128256, 4096, 1, "q4k"),
+                                   (14336, 4096, 8, "q4k"), (14336, 4096, 6, "q4k"),
+                                   (4096, 14336, 8, "q4k"), (11008, 4096, 8, "cb4"),
+                                   (1000, 2048, 8, "q4k"), (14336, 4096, 7, "q4k")):
+        assert lib.plan_matvec(rows, cols, batch, fmt=fmt)["vector_pairs"] == 0
+    try:
+        lib.set_vector_pairs_override(1)
+        p = lib.plan_matvec(128256, 4096, 8)
+        assert p["vector_pairs"] == 0 and p["warps"] == 8
+        lib.set_vector_pairs_override(2)  # forced: any size
+        p = lib.plan_matvec(100, 4096, 8)
+        assert p["vector_pairs"] == 1 and (p["warps"], p["stages"]) == (12, 2)
+        assert lib.plan_matvec(100, 4096, 6)["vector_pairs"] == 0
+        lib.set_plan_override(warps=11, stages=3)  # forced: the overrides size the pairs
+        p = lib.plan_matvec(14336, 4096, 8)
+        act = 8 * 16 * 336
+        assert p["vector_pairs"] == 1 and (p["warps"], p["stages"]) == (10, 3)
+        assert p["smem_bytes"] == act + 5 * 3 * 2 * 4608 + 10 * 2304 + 128
+        lib.set_plan_override(warps=12, stages=4)  # does not fit: no pairs
+        assert lib.plan_matvec(14336, 4096, 8)["vector_pairs"] == 0
+        lib.set_vector_pairs_override(0)
+        lib.set_plan_override(warps=8, stages=2)  # a warp or stage override turns them off
+        assert lib.plan_matvec(128256, 4096, 8)["vector_pairs"] == 0
+    finally:
+        lib.set_vector_pairs_override(0)
+        lib.set_plan_override(0, 0)
+
+
+def _prmt_lookup(words, sel_nibble):
+    """One byte of a byte permute in its generic mode: the nibble's low three
+    bits pick a byte of the two words, bit 3 replicates that byte's sign."""
+    b = ((words[0] | (words[1] << 32)) >> (8 * (sel_nibble & 7))) & 0xFF
+    v = b - 256 if b >= 128 else b
+    return (-1 if v < 0 else 0) if sel_nibble & 8 else v
+
+
+def _split_exists(a, b):
+    """Brute force: some signed bytes l, h with a = l + rep(h), b = rep(l) + h."""
+    for l in range(-128, 128):
+        for sh in (0, -1):
+            h = b - (-1 if l < 0 else 0)
+            if -128 <= h <= 127 and (-1 if h < 0 else 0) == sh and l + sh == a:
+                return True
+    return False
+
+
+def test_codebook_split_table(raw):
+    """The one-vector codebook decode's table split: the two lookups of every
+    nibble (n in one table, n ^ 8 in the other) sum to the table entry, for
+    the seeded table, random tables and edge tables; no split is reported
+    exactly when none exists."""
+    fn = raw.xq_codebook_split_table
+    fn.restype = ctypes.c_int32
+    rng = np.random.default_rng(5)
+    tables = [synthetic.cb4_table(), np.arange(-8, 8, dtype=np.int8),
+              np.full(16, -128, np.int8), np.full(16, 127, np.int8), np.zeros(16, np.int8),
+              np.array([-127] * 8 + [127] * 8, np.int8), np.array([127] * 8 + [-1] * 8, np.int8),
+              np.array([-1] * 8 + [-1] * 8, np.int8), np.array([0] * 8 + [-128] * 8, np.int8)]
+    tables += [rng.integers(-128, 128, 16).astype(np.int8) for _ in range(300)]
+    splits = 0
+    for t in tables:
+        t = np.ascontiguousarray(t, np.int8)
+        out = (ctypes.c_uint32 * 4)()
+        ok = fn(t.ctypes.data_as(ctypes.c_void_p), out)
+        exists = all(_split_exists(int(t[i]), int(t[i + 8])) for i in range(8))
+        assert bool(ok) == exists, t
+        if ok:
+            splits += 1
+            L, H = (out[0], out[1]), (out[2], out[3])
+            for n in range(16):
+                assert _prmt_lookup(L, n) + _prmt_lookup(H, n ^ 8) == t[n], (t, n)
+    assert splits > 250
+    ok = fn(np.ascontiguousarray(synthetic.cb4_table()).ctypes.data_as(ctypes.c_void_p),
+            (ctypes.c_uint32 * 4)())
+    assert ok == 1  # the seeded workload's table takes the split decode
 
 
 def test_plan_override_is_clamped(lib):
@@ -234,8 +328,10 @@ def test_no_kernel_spills(lib):
     # format x batch x (dots, fused quantise, fused RMSNorm, plain) + the grouped
     # form (3 formats, batch 1) + the Q4_K row-blocked builds (7 batches x 4
     # kinds x 2 box shapes) + the whole-row batch-1 codebook builds (2 formats x
-    # plain, fused quantise, fused RMSNorm)
-    assert len(matvec) == 3 * 8 * 4 + 3 + 7 * 4 * 2 + 2 * 3, len(matvec)
+    # plain, fused quantise, fused RMSNorm) + the warp-pair build (batch 8) +
+    # the split-table batch-1 codebook builds (2 formats x (plain, dots, fused
+    # quantise, fused RMSNorm, grouped, and the 3 whole-row forms))
+    assert len(matvec) == 3 * 8 * 4 + 3 + 7 * 4 * 2 + 2 * 3 + 1 + 2 * 8, len(matvec)
     for helper in ("q8_quantize_kernel", "rmsnorm_q8_kernel", "repack_cb4_kernel"):
         assert any(helper in n for n in rep), helper
     for name, r in rep.items():

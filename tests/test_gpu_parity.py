@@ -591,6 +591,82 @@ def test_row_block_is_bit_identical(xq, orc, rows, cols, batch):
     check_y(out[0][2], orc.matvec_q4k(W, xq_ref, rows, cols, batch), "row block")
 
 
+# ---------------------------------------------------------------- warp pairs
+@pytest.mark.parametrize("rows,batch", [(1, 8), (3, 8), (5, 8), (77, 8), (1000, 8), (4099, 8),
+                                        (14338, 8)])
+def test_vector_pairs_are_bit_identical(xq, orc, rows, batch):
+    """Warp pairs (two warps share each unit and its stages, each computing
+    half of the vectors) give the y bits of the one-warp unit, with any pair
+    count and stage depth, on the mat-vec and on the decode step; pairs with
+    no unit, half units and ragged tails included."""
+    cols = 4096
+    W = synthetic.q4k_weights(rows, cols, 7 * rows + batch)
+    x = synthetic.activations(batch, cols, rows + 11, outlier_frac=0.001)
+    xq_dev = run_quantize(xq, x)
+    Wd, xd = dev(W), dev(x)
+    ws = torch.empty(xq.linear_workspace_bytes(cols, batch), dtype=torch.uint8, device="cuda")
+    out = []
+    try:
+        for vp, warps, stages in ((1, 0, 0), (2, 12, 2), (2, 10, 3), (2, 2, 2), (2, 4, 4)):
+            xq.set_vector_pairs_override(vp)
+            xq.set_plan_override(warps, stages)
+            y = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch)
+            p = xq.last_plan()
+            assert p["vector_pairs"] == (vp == 2)
+            if vp == 2:
+                assert (p["warps"], p["stages"]) == (warps, stages)
+            y_ws = xq.linear_ws("q4k", xd, Wd, rows, cols, ws).cpu().numpy()
+            assert xq.last_plan()["vector_pairs"] == (vp == 2)
+            out.append((y, y_ws))
+    finally:
+        xq.set_vector_pairs_override(0)
+        xq.set_plan_override(0, 0)
+    for y, y_ws in out:
+        assert np.array_equal(y, out[0][0]) and np.array_equal(y_ws, out[0][0])
+    check_y(out[0][0], orc.matvec_q4k(W, orc.quantize_q8(x), rows, cols, batch), "warp pairs")
+
+
+# ---------------------------------------------------------------- codebook table forms
+@pytest.mark.parametrize("fmt", ["cb4", "cb4r"])
+@pytest.mark.parametrize("table", ["seeded", "unsplit", "random0", "random1", "extremes"])
+def test_codebook_table_forms_agree(xq, orc, fmt, table):
+    """One-vector launches decode with the table split into two lookups (when
+    it splits) and batched ones with the select decode; both give the exact
+    dots, so a vector's y has the same bits either way, for tables that split
+    and for one that does not (an entry 127 beside a negative partner)."""
+    import ctypes
+    rows, cols, batch = 300, 4096, 2
+    if table == "seeded":
+        kv = synthetic.cb4_table()
+    elif table == "unsplit":
+        kv = np.array([-1] * 8 + [127] * 8, np.int8)
+    elif table == "extremes":
+        kv = np.array([-128, 127, -127, 126, 0, -1, 1, 64, -64, 100, -100, 2, -2, 50, -50, 127],
+                      np.int8)
+    else:
+        kv = np.random.default_rng(int(table[-1])).integers(-128, 128, 16).astype(np.int8)
+    lib = ctypes.CDLL(xq.lib_path())
+    lib.xq_codebook_split_table.restype = ctypes.c_int32
+    splits = lib.xq_codebook_split_table(np.ascontiguousarray(kv).ctypes.data_as(ctypes.c_void_p),
+                                         (ctypes.c_uint32 * 4)())
+    if table in ("seeded", "unsplit"):
+        assert splits == (table == "seeded")
+    W = synthetic.cb4_weights(rows, cols, 21)
+    x = synthetic.activations(batch, cols, 22, outlier_frac=0.001)
+    xq_dev = run_quantize(xq, x)
+    Wd = dev(W)
+    if fmt == "cb4r":
+        Wd = xq.repack_cb4(Wd, rows, cols)
+    y2 = getattr(xq, "matvec_" + fmt)(Wd, kv, xq_dev, rows, cols).cpu().numpy()
+    for b in range(batch):
+        y1 = getattr(xq, "matvec_" + fmt)(Wd, kv, xq_dev[b:b + 1].contiguous(), rows, cols)
+        assert np.array_equal(y1.cpu().numpy()[0], y2[b]), b
+    d1 = xq.subdots_cb4(dev(W), kv, xq_dev[:1].contiguous(), rows, cols).cpu().numpy()
+    xq_ref = orc.quantize_q8(x)
+    assert np.array_equal(d1, orc.subdots_cb4(W, kv, xq_ref[:1], rows, cols, 1))
+    check_y(y2, orc.matvec_cb4(W, kv, xq_ref, rows, cols, batch), f"{fmt} table {table}")
+
+
 # ---------------------------------------------------------------- the binding's size checks
 def test_binding_rejects_short_buffers(xq):
     """The C ABI takes raw pointers and cannot see allocation sizes; the
