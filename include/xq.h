@@ -293,7 +293,7 @@ enum { XQ_FORMAT_Q4K = 0, XQ_FORMAT_CB4 = 1, XQ_FORMAT_CB4R = 2 };
  * and its stages are shared by a pair of warps that compute half of the
  * vectors each (the Q4_K mat-vec on q8 blocks with rows of 16 chunks at 8
  * vectors, on matrices large enough to give each pair many units; then
- * warps = 12 by default, stages counts the stages of a pair, and smem_bytes
+ * warps = 16 by default, stages counts the stages of a pair, and smem_bytes
  * includes each warp's reduction scratch). */
 typedef struct {
     int32_t warps;
@@ -330,7 +330,7 @@ void xq_set_quantise_once_override(int32_t mode);
 /* Override the use of warp pairs (xq_plan.vector_pairs): 1 = never, 2 =
  * wherever they apply (the Q4_K mat-vec on q8 blocks, rows of 16 chunks, 8
  * vectors, any matrix size), 0 = automatic (not beside a warp or stage
- * override).  When forced, a warp override (rounded down to even, 2..12) and
+ * override).  When forced, a warp override (rounded down to even, 2..16) and
  * a stage override (2..8) size the pairs if they fit in shared memory.
  * Process-wide, for sweeps and tests; the results are bit-identical either
  * way. */

@@ -330,11 +330,12 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     // Warp pairs: the row-blocked mat-vec on q8 blocks (the plain mat-vec, or
     // the decode step when it quantises once) for rows of 16 chunks at 8
     // vectors, on matrices that give every pair at least kVpMinUnits units,
-    // when no warp or stage override is set: 12 warps (six pairs, three warps
-    // a scheduler) share two stages of two boxes a pair (128256 x 4096: 105.9
-    // against 100.2 us; slower on 14336 x 4096, 15.5 against 17.7 us, and at
-    // 6 vectors, 79.6 against 86.2 us).  Only those kernels have a warp-pair
-    // build.  Forced on (override 2), the warp and stage overrides size it.
+    // when no warp or stage override is set: 16 warps (eight pairs, four warps
+    // a scheduler) share two stages of two boxes a pair (128256 x 4096: 106.3
+    // against 99.1 us, 99.8 with 12 warps; slower on 14336 x 4096, 15.7
+    // against 18.0 us, and at 6 vectors, 79.6 against 86.2 us with 12 warps).
+    // Only those kernels have a warp-pair build.  Forced on (override 2), the
+    // warp and stage overrides size it.
     const int32_t ovp = g_override_vector_pairs.load();
     const bool q8_input = fuse == 0 && !dots && (!fused || qonce);
     if (fmt == kQ4K && M == 2 && nb == 16 && bl == 8 && slots == 0 && q8_input && ovp != 1) {

@@ -40,11 +40,12 @@ constexpr int kQuantGroup = 4;
 constexpr int kStageAsyncBlocks = 64;
 constexpr int kStageItems = 4;
 constexpr int kMaxWarps = 8;
-// Warp pairs (the row-blocked Q4_K form for rows of 16 chunks, 8 vectors): each unit of two row groups and its stages are shared by two
-// warps, each computing half of the vectors; 12 warps a CTA (6 pairs), and
-// each warp's reduction scratch (32 lanes x (2 x 4 + 1) pairs of floats) after
-// the stages.
-constexpr int kVpWarps = 12;
+// Warp pairs (the row-blocked Q4_K form for rows of 16 chunks, 8 vectors):
+// each unit of two row groups and its stages are shared by two warps, each
+// computing half of the vectors; 16 warps a CTA (8 pairs, 128 registers a
+// thread), and each warp's reduction scratch (32 lanes x (2 x 4 + 1) pairs of
+// floats) after the stages.
+constexpr int kVpWarps = 16;
 constexpr int kVpStages = 2;
 constexpr int kVpScratchBytes = (2 * 4 + 1) * 8 * 32;
 constexpr int kMaxStages = 8;

@@ -158,7 +158,7 @@ def test_status_strings(raw):
 
 
 @pytest.mark.parametrize("fmt,rows,cols,batch,warps,grid,R,spr,launches,M", [
-    ("q4k", 128256, 4096, 1, 16, 152, 2, 1, 1, 1), ("q4k", 128256, 4096, 8, 12, 152, 2, 1, 1, 2),
+    ("q4k", 128256, 4096, 1, 16, 152, 2, 1, 1, 1), ("q4k", 128256, 4096, 8, 16, 152, 2, 1, 1, 2),
     ("q4k", 4096, 4096, 1, 14, 152, 2, 1, 1, 1), ("q4k", 14336, 4096, 4, 8, 152, 2, 1, 1, 2),
     ("q4k", 4096, 14336, 1, 20, 152, 1, 2, 1, 1), ("q4k", 4096, 14336, 8, 8, 152, 1, 2, 1, 2),
     ("q4k", 4096, 14336, 4, 8, 152, 1, 2, 1, 2), ("q4k", 14336, 4096, 2, 12, 152, 2, 1, 1, 2),
@@ -180,11 +180,11 @@ def test_plan(lib, fmt, rows, cols, batch, warps, grid, R, spr, launches, M):
     assert (R > 1 and R * nb == 32 and spr == 1) or (R == 1 and spr == -(-nb // 32))
     act = -(-p["batch_per_launch"] * nb * 336 // 128) * 128
     if p["vector_pairs"]:
-        # warp pairs: 12 warps, two stages a pair, a 2304-byte reduction
+        # warp pairs: 16 warps, two stages a pair, a 2304-byte reduction
         # scratch a warp
         assert fmt == "q4k" and M == 2 and nb == 16 and batch == 8
-        assert p["warps"] == 12 and p["stages"] == 2
-        assert p["smem_bytes"] == act + 6 * 2 * M * 4608 + 12 * 2304 + 128
+        assert p["warps"] == 16 and p["stages"] == 2
+        assert p["smem_bytes"] == act + 8 * 2 * M * 4608 + 16 * 2304 + 128
     else:
         # two stages, or one where two-box stages for every warp do not fit
         two = act + p["warps"] * 2 * M * 4608 + 128
@@ -212,9 +212,9 @@ def test_vector_pairs_plan(lib):
     chunks at 8 vectors; the override turns them off or on."""
     assert lib.plan_matvec(128256, 4096, 8)["vector_pairs"] == 1
     assert lib.plan_matvec(128256, 4096, 6)["vector_pairs"] == 0
-    # at least 16 units (four rows each) for each of the 152 x 6 pairs
-    assert lib.plan_matvec(4 * 16 * 152 * 6, 4096, 8)["vector_pairs"] == 1
-    assert lib.plan_matvec(4 * 16 * 152 * 6 - 4, 4096, 8)["vector_pairs"] == 0
+    # at least 16 units (four rows each) for each of the 152 x 8 pairs
+    assert lib.plan_matvec(4 * 16 * 152 * 8, 4096, 8)["vector_pairs"] == 1
+    assert lib.plan_matvec(4 * 16 * 152 * 8 - 4, 4096, 8)["vector_pairs"] == 0
     for rows, cols, batch, fmt in ((14336, 4096, 4, "q4k"), (128256, 4096, 1, "q4k"),
                                    (14336, 4096, 8, "q4k"), (14336, 4096, 6, "q4k"),
                                    (4096, 14336, 8, "q4k"), (11008, 4096, 8, "cb4"),
@@ -226,14 +226,14 @@ def test_vector_pairs_plan(lib):
         assert p["vector_pairs"] == 0 and p["warps"] == 8
         lib.set_vector_pairs_override(2)  # forced: any size
         p = lib.plan_matvec(100, 4096, 8)
-        assert p["vector_pairs"] == 1 and (p["warps"], p["stages"]) == (12, 2)
+        assert p["vector_pairs"] == 1 and (p["warps"], p["stages"]) == (16, 2)
         assert lib.plan_matvec(100, 4096, 6)["vector_pairs"] == 0
         lib.set_plan_override(warps=11, stages=3)  # forced: the overrides size the pairs
         p = lib.plan_matvec(14336, 4096, 8)
         act = 8 * 16 * 336
         assert p["vector_pairs"] == 1 and (p["warps"], p["stages"]) == (10, 3)
         assert p["smem_bytes"] == act + 5 * 3 * 2 * 4608 + 10 * 2304 + 128
-        lib.set_plan_override(warps=12, stages=4)  # does not fit: no pairs
+        lib.set_plan_override(warps=16, stages=3)  # does not fit: no pairs
         assert lib.plan_matvec(14336, 4096, 8)["vector_pairs"] == 0
         lib.set_vector_pairs_override(0)
         lib.set_plan_override(warps=8, stages=2)  # a warp or stage override turns them off
