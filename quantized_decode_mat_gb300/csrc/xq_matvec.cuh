@@ -559,6 +559,36 @@ __device__ __forceinline__ void reduce_rows16_store(const float (&hi)[M][B], con
 #pragma unroll
         for (int b = 0; b < B; ++b) mine[m * P + b] = make_float2(hi[m][b], lo[m][b]);
     __syncwarp();
+    if constexpr (M * 2 * P == 16) {
+        // sixteen outputs: two lanes an output, lane half h taking the chunks
+        // of parity h (the tree's first three levels pair chunks of equal
+        // parity), then one exchange for the last level
+        const int o = lane & 15, h = lane >> 4;
+        const int b = o % P, m = (o / P) % M, rig = o / (P * M);
+        float hh[8], ll[8];
+        const uint8_t *src = scratch + rig * 16 * kStride + (m * P + b) * 8 + h * kStride;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {  // chunk 2j + h
+            const float2 v = *reinterpret_cast<const float2 *>(src + 2 * j * kStride);
+            hh[j] = v.x;
+            ll[j] = v.y;
+        }
+#pragma unroll
+        for (int lvl = 0; lvl < 3; ++lvl) {
+            const int off = 4 >> lvl;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < off) acc_add(hh[j], ll[j], hh[j + off], ll[j + off]);
+        }
+        const float ph = __shfl_xor_sync(0xffffffffu, hh[0], 16);
+        const float pl = __shfl_xor_sync(0xffffffffu, ll[0], 16);
+        acc_add(hh[0], ll[0], ph, pl);
+        const int valid = m == 0 ? gi[0].valid : gi[M - 1].valid;
+        const int64_t out0 = m == 0 ? gi[0].out0 : gi[M - 1].out0;
+        if (h == 0 && b < B && rig < valid) y[(int64_t)b * rows + out0 + rig] = __fadd_rn(hh[0], ll[0]);
+        __syncwarp();  // the scratch is read before the stage is refilled
+        return;
+    }
     const int b = lane % P, m = (lane / P) % M, rig = lane / (P * M);
     if (lane < M * 2 * P && b < B) {
         float h[16], l[16];
