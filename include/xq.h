@@ -47,7 +47,9 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *     compute entry point is asynchronous on it: the return code covers
  *     argument checks and the launch only.  Nothing here synchronises except
- *     xq_device_status.  No kernel traps, asserts or spins.
+ *     xq_device_status.  No kernel traps or asserts; the one wait in a kernel
+ *     on its own tensor-core operations is bounded and, if it runs out,
+ *     sets bit 2 of the device status word.
  *   - The first call on a device configures the kernels for that device;
  *     make one call per device before capturing a stream into a CUDA graph.
  */
@@ -294,7 +296,12 @@ enum { XQ_FORMAT_Q4K = 0, XQ_FORMAT_CB4 = 1, XQ_FORMAT_CB4R = 2 };
  * vectors each (the Q4_K mat-vec on q8 blocks with rows of 16 chunks at 8
  * vectors, on matrices large enough to give each pair many units; then
  * warps = 16 by default, stages counts the stages of a pair, and smem_bytes
- * includes each warp's reduction scratch). */
+ * includes each warp's reduction scratch).  tensor: 1 if the dots are
+ * taken on the tensor cores (tcgen05; the Q4_K mat-vec on q8 blocks with
+ * rows of 16 chunks at 5..8 vectors): one CTA of thirteen warps an SM then
+ * owns tiles of 128 rows (groups = tiles, rows_per_group = 128, segments =
+ * 16 chunks a tile), and smem_bytes includes the activation staged as
+ * f16. */
 typedef struct {
     int32_t warps;
     int32_t stages;
@@ -309,6 +316,7 @@ typedef struct {
     int32_t row_block;
     int32_t quantise_once;
     int32_t vector_pairs;
+    int32_t tensor;
 } xq_plan;
 
 xq_status xq_plan_matvec(int32_t format, int64_t rows, int64_t cols, int64_t batch,
@@ -335,6 +343,12 @@ void xq_set_quantise_once_override(int32_t mode);
  * Process-wide, for sweeps and tests; the results are bit-identical either
  * way. */
 void xq_set_vector_pairs_override(int32_t mode);
+/* Override the use of the tensor cores (xq_plan.tensor): 1 = never, 2 =
+ * wherever they apply (the Q4_K mat-vec on q8 blocks, rows of 16 chunks, 5..8
+ * vectors), 0 = automatic.  When forced, a stage override (2..8) sizes the
+ * plan if it fits in shared memory.  Process-wide, for sweeps and tests; the
+ * results are bit-identical either way. */
+void xq_set_tensor_override(int32_t mode);
 /* The codebook table as the one-vector launches use it, when it splits: four
  * words, bytes L[0..7] then H[0..7], with kv[n] = L[n] + rep(H[n]) and
  * kv[n + 8] = rep(L[n]) + H[n] for n = 0..7 (signed bytes; rep(v) = -1 if
@@ -389,7 +403,9 @@ uint64_t xq_launch_count(int32_t which);
 
 /* Read (and optionally clear) the current device's status word, where
  * kernels report errors without trapping: bit 1 = a grouped mat-vec met an
- * expert id outside [0, n_experts).  Returns XQ_EDEVICE when it is non-zero.
+ * expert id outside [0, n_experts); bit 2 = a tensor-core mat-vec gave up
+ * waiting for its own products (its outputs are then not written).  Returns
+ * XQ_EDEVICE when it is non-zero.
  * SYNCHRONISES `stream` (device-to-host copy of 4 bytes, and a clear). */
 xq_status xq_device_status(uint32_t *out, int32_t clear, void *stream);
 

@@ -69,6 +69,7 @@ from ._native import (  # noqa: F401
     set_plan_override,
     set_row_block_override,
     set_vector_pairs_override,
+    set_tensor_override,
     set_overlap_launches,
     overlap_launches,
     set_quantise_once_override,

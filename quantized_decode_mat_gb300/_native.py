@@ -26,7 +26,8 @@ class _Plan(ctypes.Structure):
                 ("chunks_per_row", ctypes.c_int32), ("groups", ctypes.c_int64),
                 ("batch_per_launch", ctypes.c_int32), ("launches", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int64), ("row_block", ctypes.c_int32),
-                ("quantise_once", ctypes.c_int32), ("vector_pairs", ctypes.c_int32)]
+                ("quantise_once", ctypes.c_int32), ("vector_pairs", ctypes.c_int32),
+                ("tensor", ctypes.c_int32)]
 
 
 def _sig(name, restype, argtypes):
@@ -80,6 +81,7 @@ _plan = _sig("xq_plan_matvec", ctypes.c_int, [_I32, _I64, _I64, _I64, _I32, _I64
 _set_override = _sig("xq_set_plan_override", None, [_I32, _I32])
 _set_row_block = _sig("xq_set_row_block_override", None, [_I32])
 _set_vector_pairs = _sig("xq_set_vector_pairs_override", None, [_I32])
+_set_tensor = _sig("xq_set_tensor_override", None, [_I32])
 _last_plan = _sig("xq_last_plan", ctypes.c_int, [ctypes.POINTER(_Plan)])
 _launch_count = _sig("xq_launch_count", ctypes.c_uint64, [_I32])
 _device_status = _sig("xq_device_status", ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32),
@@ -510,6 +512,13 @@ def set_vector_pairs_override(mode: int = 0) -> None:
     they apply (then set_plan_override's warps and stages, if set, size the
     pairs), 0 automatic.  The results are bit-identical either way."""
     _set_vector_pairs(mode)
+
+
+def set_tensor_override(mode: int = 0) -> None:
+    """Dots on the tensor cores (xq_plan.tensor): 1 never, 2 wherever they
+    apply (then set_plan_override's stages, if set, size the plan), 0
+    automatic.  The results are bit-identical either way."""
+    _set_tensor(mode)
 
 
 def launch_count(which: int) -> int:

@@ -18,8 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libxq.so")
-SOURCES = ["xq_api.cu", "xq_matvec_q4k.cu", "xq_matvec_q4k_rb2.cu", "xq_matvec_cb4.cu",
-           "xq_matvec_cb4r.cu"]
+SOURCES = ["xq_api.cu", "xq_matvec_q4k.cu", "xq_matvec_q4k_rb2.cu", "xq_matvec_q4k_tc.cu",
+           "xq_matvec_cb4.cu", "xq_matvec_cb4r.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               f"-I{INCLUDE}"]

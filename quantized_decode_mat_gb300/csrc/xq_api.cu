@@ -142,6 +142,7 @@ std::atomic<int32_t> g_override_stages{0};
 std::atomic<int32_t> g_override_row_block{0};
 std::atomic<int32_t> g_override_quantise_once{0};
 std::atomic<int32_t> g_override_vector_pairs{0};
+std::atomic<int32_t> g_override_tensor{0};
 std::atomic<int32_t> g_overlap{0};
 // The decode step with a workspace quantises the activation once, in a
 // launch of its own, when a launch's batch has at least this many q8 blocks;
@@ -152,6 +153,8 @@ constexpr int64_t kQuantOnceMinBlocks = 32;
 // them either way).
 constexpr bool kVectorPairsAuto = true;
 constexpr int64_t kVpMinUnits = 16;
+// Whether the planner picks the tensor-core kernel by itself.
+constexpr bool kTensorAuto = false;
 
 xq_status fail(xq_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 xq_status fail(xq_status s, const char *fmt, ...) {
@@ -225,6 +228,8 @@ xq_status device_state(DeviceState **out) {
         if (st.err == cudaSuccess) step(configure_matvec_cb4(st.smem_optin), "configure codebook kernels");
         if (st.err == cudaSuccess)
             step(configure_matvec_cb4r(st.smem_optin), "configure resident codebook kernels");
+        if (st.err == cudaSuccess)
+            step(configure_matvec_q4k_tc(st.smem_optin), "configure tensor-core Q4_K kernels");
 
     });
     if (st.err != cudaSuccess) return cuda_fail(st.err, st.what);
@@ -327,6 +332,7 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
     p->row_block = M;
     p->quantise_once = qonce;
     p->vector_pairs = 0;
+    p->tensor = 0;
     // Warp pairs: the row-blocked mat-vec on q8 blocks (the plain mat-vec, or
     // the decode step when it quantises once) for rows of 16 chunks at 8
     // vectors, on matrices that give every pair at least kVpMinUnits units,
@@ -352,6 +358,29 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
             p->stages = vs;
             p->smem_bytes = vp_bytes;
             p->vector_pairs = 1;
+        }
+    }
+    // The tensor-core kernel: the Q4_K mat-vec on q8 blocks for rows of 16
+    // chunks at 5..8 vectors; one CTA of thirteen warps an SM on tiles of 128
+    // rows (it holds all 512 columns of tensor memory), three stages.  Forced
+    // on (override 2), a stage override (two or more) sizes it.
+    const int32_t otc = g_override_tensor.load();
+    if (fmt == kQ4K && nb == kTcChunks && bl >= 5 && bl <= 8 && slots == 0 && q8_input &&
+        otc != 1 && (otc == 2 || (kTensorAuto && ow <= 0 && os <= 0))) {
+        const int32_t ts = otc == 2 && os >= 2 ? os : kTcStages;
+        const int64_t tiles = (rows + kTcRows - 1) / kTcRows;
+        const int64_t t_bytes = tc_smem_bytes(ts);
+        if (ts <= kMaxStages && t_bytes <= smem_optin) {
+            p->warps = kTcThreads / 32;
+            p->stages = ts;
+            p->grid = (int32_t)(tiles < sm_count ? tiles : sm_count);
+            p->rows_per_group = kTcRows;
+            p->segments = kTcChunks;
+            p->groups = tiles;
+            p->row_block = 1;
+            p->smem_bytes = t_bytes;
+            p->vector_pairs = 0;
+            p->tensor = 1;
         }
     }
     return XQ_OK;
@@ -489,6 +518,8 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
     a.stages = plan.stages;
     a.row_block = plan.row_block;
     a.vector_pairs = plan.vector_pairs;
+    a.tensor = plan.tensor;
+    a.status = dev->status;
     a.overlap = g_overlap.load();
     if (cb4) {
         a.kv_split = plan.batch_per_launch == 1 && split_table(table, a.kv);
@@ -507,6 +538,11 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
                                plan.warps <= kVpWarps && plan.stages >= 2 &&
                                plan.batch_per_launch == 8))
         return fail(XQ_ELAUNCH, "internal: a warp-pair plan for a kernel without that build");
+    if (plan.tensor && !(kind == 0 && op.fmt == kQ4K && nb == kTcChunks && plan.launches == 1 &&
+                         plan.batch_per_launch >= 5 && plan.batch_per_launch <= 8 &&
+                         plan.warps * 32 == kTcThreads && plan.stages >= 2 &&
+                         plan.smem_bytes == tc_smem_bytes(plan.stages)))
+        return fail(XQ_ELAUNCH, "internal: a tensor-core plan for a kernel without that build");
     for (int64_t b0 = 0; b0 < batch; b0 += plan.batch_per_launch) {
         const int64_t bc = batch - b0 < plan.batch_per_launch ? batch - b0 : plan.batch_per_launch;
         if (once) {
@@ -523,8 +559,10 @@ xq_status run_matvec(OpInfo op, const void *W, const int8_t *table, const void *
         }
         a.y = dots ? nullptr : static_cast<float *>(out) + b0 * rows;
         a.dots = dots ? static_cast<int32_t *>(out) + b0 * rows * nb * 8 : nullptr;
-        cudaError_t e = launch_fmt(op.fmt, a, (int)bc, kind, grid, block,
-                                   (size_t)plan.smem_bytes, s);
+        cudaError_t e = plan.tensor ? launch_matvec_q4k_tc(a, (int)bc, grid, block,
+                                                          (size_t)plan.smem_bytes, s)
+                                    : launch_fmt(op.fmt, a, (int)bc, kind, grid, block,
+                                                 (size_t)plan.smem_bytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "mat-vec launch");
         g_counts[op.count].fetch_add(1, std::memory_order_relaxed);
         if (once) g_counts[XQ_COUNT_QUANTISE_ONCE].fetch_add(1, std::memory_order_relaxed);
@@ -896,6 +934,10 @@ int32_t xq_overlap_launches(void) { return g_overlap.load(); }
 
 void xq_set_quantise_once_override(int32_t mode) {
     g_override_quantise_once.store(mode < 0 || mode > 2 ? 0 : mode);
+}
+
+void xq_set_tensor_override(int32_t mode) {
+    g_override_tensor.store(mode < 0 || mode > 2 ? 0 : mode);
 }
 
 int32_t xq_codebook_split_table(const int8_t *table, uint32_t *out) {

@@ -49,6 +49,30 @@ constexpr int kVpWarps = 16;
 constexpr int kVpStages = 2;
 constexpr int kVpScratchBytes = (2 * 4 + 1) * 8 * 32;
 constexpr int kMaxStages = 8;
+// Tensor-core form (xq_tc.cuh): Q4_K rows of 16 chunks, 5..8 vectors on q8
+// blocks.  A CTA of four decoding, eight epilogue and one issuing warp owns
+// tiles of 128 rows; shared memory: the activation as the f16 B operand (16 chunks x
+// 16 slices x 256 bytes), the q8 scales and split sums per (chunk, vector),
+// each lane quarter's weight stages (32 rows x one chunk), the tensor-memory
+// address and six mbarriers; tensor memory (all 512 columns): A twice in 128
+// columns, the eight sub-block accumulators (16 columns each) twice in 128.
+constexpr int kTcWorkWarps = 12;
+// registers a thread: four of the 13 warps on one scheduler share its 16384
+constexpr int kTcMaxRegs = 128;
+constexpr int kTcThreads = (kTcWorkWarps + 1) * 32;
+constexpr int kTcRows = 128;
+constexpr int kTcChunks = 16;
+constexpr int kTcTmemCols = 512;
+constexpr int kTcXsAt = kTcChunks * 16 * 256;
+constexpr int kTcSplitAt = kTcXsAt + kTcChunks * 8 * 4;
+constexpr int kTcStagesAt = kTcSplitAt + kTcChunks * 8 * 16;
+constexpr int kTcQStageBytes = 32 * kChunkBytes;
+constexpr int kTcStageBytes = 4 * kTcQStageBytes;  // the four quarters' stages of one step
+constexpr int kTcStages = 3;
+constexpr uint32_t kTcSpinLimit = 1u << 20;
+// shared memory of a launch with S stages (1024 bytes of alignment slack)
+constexpr int64_t tc_smem_bytes(int S) { return (int64_t)kTcStagesAt + (int64_t)S * kTcStageBytes + 64 + 1024; }
+static_assert(kTcStagesAt % 128 == 0 && kTcStageBytes % 128 == 0, "128-byte aligned regions");
 
 // kCB4R: codebook blocks in resident rows (scale prefix, then 16-byte
 // payloads).  A 256-weight chunk is then 16 bytes of scales in the prefix and
@@ -87,6 +111,7 @@ struct MatvecArgs {
     int32_t stages;         // shared-memory stages per warp (2..8)
     int32_t row_block;      // row groups a warp works on at once (1, or 2 for Q4_K at batch >= 2)
     int32_t vector_pairs;   // 1: warp pairs share each unit, half of the vectors each
+    int32_t tensor;         // 1: the tensor-core kernel (xq_tc.cuh)
     uint32_t kv[4];         // codebook bytes kv[0..15], little-endian words (or, with
                             // kv_split, the two lookup tables whose sum is kv)
     int32_t kv_split;       // 1: kv holds the split tables (one-vector launches)
@@ -125,6 +150,7 @@ inline cudaError_t launch_kernel(void (*kern)(P...), dim3 grid, dim3 block, size
 
 // Status word bits (see xq_device_status).
 constexpr uint32_t kStatusBadExpertId = 2u;
+constexpr uint32_t kStatusTensorTimeout = 4u;
 
 // Launch entry points implemented per format (xq_matvec_q4k.cu / _cb4.cu).
 // kind: 0 = mat-vec on q8 blocks, 1 = the same with the exact dots,
@@ -143,5 +169,10 @@ cudaError_t configure_matvec_q4k_rb2(int smem_optin);
 cudaError_t launch_matvec_cb4r(const MatvecArgs &a, int batch, int kind, dim3 grid, dim3 block,
                                size_t smem, cudaStream_t s);
 cudaError_t configure_matvec_cb4r(int smem_optin);
+// The tensor-core Q4_K mat-vec on q8 blocks (xq_matvec_q4k_tc.cu): rows of 16
+// chunks, batch 5..8.
+cudaError_t launch_matvec_q4k_tc(const MatvecArgs &a, int batch, dim3 grid, dim3 block,
+                                 size_t smem, cudaStream_t s);
+cudaError_t configure_matvec_q4k_tc(int smem_optin);
 
 }  // namespace xq

@@ -292,6 +292,35 @@ def test_codebook_split_table(raw):
     assert ok == 1  # the seeded workload's table takes the split decode
 
 
+def test_tensor_plan(lib):
+    """The tensor-core plan: forced on, for the Q4_K mat-vec on q8 blocks with
+    rows of 16 chunks at 5..8 vectors only; one CTA of thirteen warps an SM
+    on 128-row tiles, three stages unless a stage override sizes it."""
+    act = 16 * 16 * 256 + 16 * 8 * 4 + 16 * 8 * 16
+    try:
+        lib.set_tensor_override(2)
+        p = lib.plan_matvec(128256, 4096, 8)
+        assert p["tensor"] == 1 and (p["warps"], p["stages"], p["grid"]) == (13, 3, 152)
+        assert (p["groups"], p["rows_per_group"], p["segments"], p["row_block"]) == (1002, 128, 16, 1)
+        assert p["smem_bytes"] == act + 3 * 128 * 144 + 64 + 1024
+        assert lib.plan_matvec(300, 4096, 5)["grid"] == 3
+        for rows, cols, batch, fmt in ((14336, 4096, 4, "q4k"), (4096, 14336, 8, "q4k"),
+                                       (11008, 4096, 8, "cb4"), (128256, 4096, 1, "q4k")):
+            assert lib.plan_matvec(rows, cols, batch, fmt=fmt)["tensor"] == 0
+        lib.set_plan_override(stages=5)
+        p = lib.plan_matvec(14336, 4096, 6)
+        assert p["tensor"] == 1 and (p["warps"], p["stages"]) == (13, 5)
+        assert p["smem_bytes"] == act + 5 * 128 * 144 + 64 + 1024
+        lib.set_plan_override(stages=1)  # below two: the default three
+        assert lib.plan_matvec(14336, 4096, 6)["stages"] == 3
+        lib.set_tensor_override(1)
+        lib.set_plan_override(0, 0)
+        assert lib.plan_matvec(128256, 4096, 8)["tensor"] == 0
+    finally:
+        lib.set_tensor_override(0)
+        lib.set_plan_override(0, 0)
+
+
 def test_plan_override_is_clamped(lib):
     try:
         lib.set_plan_override(warps=32, stages=64)
@@ -332,6 +361,7 @@ def test_no_kernel_spills(lib):
     # the split-table batch-1 codebook builds (2 formats x (plain, dots, fused
     # quantise, fused RMSNorm, grouped, and the 3 whole-row forms))
     assert len(matvec) == 3 * 8 * 4 + 3 + 7 * 4 * 2 + 2 * 3 + 1 + 2 * 8, len(matvec)
+    assert len([n for n in rep if "xq_tc_q4k_kernel" in n]) == 4  # tensor cores, batch 5..8
     for helper in ("q8_quantize_kernel", "rmsnorm_q8_kernel", "repack_cb4_kernel"):
         assert any(helper in n for n in rep), helper
     for name, r in rep.items():

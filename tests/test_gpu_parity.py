@@ -626,6 +626,57 @@ def test_vector_pairs_are_bit_identical(xq, orc, rows, batch):
     check_y(out[0][0], orc.matvec_q4k(W, orc.quantize_q8(x), rows, cols, batch), "warp pairs")
 
 
+# ---------------------------------------------------------------- tensor cores
+@pytest.mark.parametrize("rows,batch,kind", [(1, 8, "random"), (15, 5, "random"), (129, 6, "random"),
+                                             (77, 8, "random"), (1000, 7, "random"),
+                                             (4099, 8, "random"), (40000, 6, "random"),
+                                             (300, 8, "extreme+"), (130, 5, "extreme-"),
+                                             (33, 8, "zeros")])
+def test_tensor_cores_are_bit_identical(xq, orc, rows, batch, kind):
+    """The tensor-core kernel (tcgen05: 128-row tiles, f16 codes in tensor
+    memory, the activation by shared-memory descriptor, exact f32 accumulation
+    of each sub-block) gives the dp4a kernel's y bits, with two stages or
+    more, on the mat-vec and on the decode step: ragged last tiles, CTAs with
+    no tile, and the largest sums the route can form (all codes 15, all
+    scales and mins 63, activations all +127 or all -127) included."""
+    cols = 4096
+    W = synthetic.q4k_weights(rows, cols, 5 * rows + batch)
+    if kind == "random":
+        x = synthetic.activations(batch, cols, rows + 13, outlier_frac=0.001)
+    elif kind == "zeros":
+        x = np.zeros((batch, cols), np.float32)
+    else:
+        W.reshape(rows, -1, 144)[:, :, 4:] = 0xFF
+        x = np.full((batch, cols), 127.0 if kind == "extreme+" else -127.0, np.float32)
+    xq_dev = run_quantize(xq, x)
+    Wd, xd = dev(W), dev(x)
+    ws = torch.empty(xq.linear_workspace_bytes(cols, batch), dtype=torch.uint8, device="cuda")
+    out = []
+    try:
+        for tc, stages in ((1, 0), (2, 0), (2, 2), (2, 5)):
+            xq.set_tensor_override(tc)
+            xq.set_plan_override(0, stages)
+            y = run_matvec(xq, "q4k", W, None, xq_dev, rows, cols, batch)
+            p = xq.last_plan()
+            assert p["tensor"] == (tc == 2)
+            if tc == 2:
+                assert p["warps"] == 13 and p["stages"] == (stages or 3)
+            y_ws = xq.linear_ws("q4k", xd, Wd, rows, cols, ws).cpu().numpy()
+            assert xq.last_plan()["tensor"] == (tc == 2)
+            out.append((y, y_ws))
+    finally:
+        xq.set_tensor_override(0)
+        xq.set_plan_override(0, 0)
+    assert xq.device_status(clear=True) == 0
+    for y, y_ws in out:
+        assert np.array_equal(y, out[0][0]) and np.array_equal(y_ws, out[0][0])
+    y_ref = orc.matvec_q4k(W, orc.quantize_q8(x), rows, cols, batch)
+    if kind == "zeros":
+        assert np.all(out[0][0] == 0.0)
+    else:
+        check_y(out[0][0], y_ref, "tensor cores")
+
+
 # ---------------------------------------------------------------- codebook table forms
 @pytest.mark.parametrize("fmt", ["cb4", "cb4r"])
 @pytest.mark.parametrize("table", ["seeded", "unsplit", "random0", "random1", "extremes"])
