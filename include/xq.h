@@ -298,7 +298,7 @@ enum { XQ_FORMAT_Q4K = 0, XQ_FORMAT_CB4 = 1, XQ_FORMAT_CB4R = 2 };
  * warps = 16 by default, stages counts the stages of a pair, and smem_bytes
  * includes each warp's reduction scratch).  tensor: 1 if the dots are
  * taken on the tensor cores (tcgen05; the Q4_K mat-vec on q8 blocks with
- * rows of 16 chunks at 5..8 vectors): one CTA of thirteen warps an SM then
+ * rows of 16 chunks at 5..8 vectors): one CTA of seventeen warps an SM then
  * owns tiles of 128 rows (groups = tiles, rows_per_group = 128, segments =
  * 16 chunks a tile), and smem_bytes includes the activation staged as
  * f16. */

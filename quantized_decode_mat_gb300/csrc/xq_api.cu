@@ -361,7 +361,7 @@ xq_status make_plan(int fmt, int64_t rows, int64_t cols, int64_t batch, int32_t 
         }
     }
     // The tensor-core kernel: the Q4_K mat-vec on q8 blocks for rows of 16
-    // chunks at 5..8 vectors; one CTA of thirteen warps an SM on tiles of 128
+    // chunks at 5..8 vectors; one CTA of seventeen warps an SM on tiles of 128
     // rows (it holds all 512 columns of tensor memory), three stages.  Forced
     // on (override 2), a stage override (two or more) sizes it.
     const int32_t otc = g_override_tensor.load();

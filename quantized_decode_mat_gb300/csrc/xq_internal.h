@@ -50,15 +50,15 @@ constexpr int kVpStages = 2;
 constexpr int kVpScratchBytes = (2 * 4 + 1) * 8 * 32;
 constexpr int kMaxStages = 8;
 // Tensor-core form (xq_tc.cuh): Q4_K rows of 16 chunks, 5..8 vectors on q8
-// blocks.  A CTA of four decoding, eight epilogue and one issuing warp owns
+// blocks.  A CTA of eight decoding, eight epilogue and one issuing warp owns
 // tiles of 128 rows; shared memory: the activation as the f16 B operand (16 chunks x
 // 16 slices x 256 bytes), the q8 scales and split sums per (chunk, vector),
 // each lane quarter's weight stages (32 rows x one chunk), the tensor-memory
 // address and six mbarriers; tensor memory (all 512 columns): A twice in 128
 // columns, the eight sub-block accumulators (16 columns each) twice in 128.
-constexpr int kTcWorkWarps = 12;
-// registers a thread: four of the 13 warps on one scheduler share its 16384
-constexpr int kTcMaxRegs = 128;
+constexpr int kTcWorkWarps = 16;
+// registers a thread: five of the 17 warps on one scheduler share its 16384
+constexpr int kTcMaxRegs = 96;
 constexpr int kTcThreads = (kTcWorkWarps + 1) * 32;
 constexpr int kTcRows = 128;
 constexpr int kTcChunks = 16;

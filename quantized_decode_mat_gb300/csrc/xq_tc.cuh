@@ -5,33 +5,36 @@
 // quantised values, scale once per super-block) are a dense product of the
 // 4-bit codes with the int8 activations, so at 5..8 vectors they are taken by
 // tcgen05.mma (kind::f16, f32 accumulators in tensor memory) instead of dp4a.
-// They stay exact integers: a code q enters as the f16 value 1024 + q (a
-// high nibble as 1024 + 16q; a mask and an OR put the nibble under the f16
-// exponent of 1024), an activation value as itself, and each 32-value
-// sub-block has an accumulator of its own whose every partial sum is an
-// integer below 2^23, so f32 holds it exactly and cvt.rni reads it back.
-// Subtracting 1024 * (the sub-block's activation sum) leaves the dot (x16 for
-// a high nibble); from there the arithmetic is the dp4a kernel's: the same
-// integers S1 and S2, the same epilogue, and the same pairing tree over a
-// row's 16 chunk terms, so y has the same bits.
+// They stay exact integers: a code q is made the f16 value 1024 + q (a high
+// nibble 1024 + 16q: a mask and an OR put the nibble under the f16 exponent
+// of 1024), then one fused multiply-add by the sub-block's six-bit scale sc
+// and -1024 * sc (sc/16 and -64 * sc) gives the exact f16 q * sc (at most
+// 945); an activation value enters as itself.  Sub-blocks 0..3 and 4..7 each
+// accumulate in one f32 accumulator, whose partial sums are integers below
+// 4 * 32 * 945 * 127 < 2^24, so f32 holds them exactly and cvt.rni reads
+// them back: their sum is S1.  From there the arithmetic is the dp4a
+// kernel's: the same integers S1 and S2, the same epilogue, and the same
+// pairing tree over a row's 16 chunk terms, so y has the same bits.
 //
-// A CTA of thirteen warps owns tiles of 128 rows (one tensor-memory lane a
+// A CTA of seventeen warps owns tiles of 128 rows (one tensor-memory lane a
 // row; the warps of a quarter share lanes 32(w%4) .. 32(w%4)+31 and their 32
 // rows).  The roles run side by side, paced only by mbarriers:
-//   - decoders (warps 0-3, one a quarter): warp w stages its 32 rows'
-//     144-byte chunks by cp.async (three stages), unpacks their codes to f16
-//     pairs and writes them to tensor memory (tcgen05.st, the A operand, 128
-//     x 256), then arrives on A-full;
-//   - the issuer (warp 12) waits for A-full and for the accumulators to be
-//     free, issues 16 tcgen05.mma (per sub-block two K=16 slices into that
-//     sub-block's accumulator, M = 128, N = 16: the 8 vectors twice, the B
-//     descriptor's N-group stride being 0) and commits to D-full;
-//   - epilogue warps (4-11, two a quarter): warp w waits for D-full, reads
-//     vectors 4((w-4)/4) .. +3 of its rows' eight accumulators (tcgen05.ld),
+//   - decoders (warps 0-7, two a quarter): the quarter's two stage its 32
+//     rows' 144-byte chunks by cp.async (three stages) and meet on a named
+//     barrier; warp w unpacks groups 2(w/4), 2(w/4)+1 of its rows' codes to
+//     f16 pairs and writes them to tensor memory (tcgen05.st, the A operand,
+//     128 x 256), then arrives on A-full;
+//   - the issuer (warp 16) waits for A-full and for the accumulators to be
+//     free, issues 16 tcgen05.mma (two K=16 slices a sub-block, sub-blocks
+//     0..3 into one accumulator and 4..7 into another, M = 128, N = 16: the
+//     8 vectors twice, the B descriptor's N-group stride being 0) and
+//     commits to D-full;
+//   - epilogue warps (8-15, two a quarter): warp w waits for D-full, reads
+//     vectors 4((w-8)/4) .. +3 of its rows' two accumulators (tcgen05.ld),
 //     arrives on D-empty and forms the chunk's terms, with the rows' scales
 //     read from global memory one step ahead.
-// A and the accumulators are double-buffered (all 512 columns of tensor
-// memory).
+// A and the accumulators are double-buffered (A in columns 0..255, the
+// accumulators in 256..319 of the 512 allocated).
 // The activation is the B operand, staged once per CTA as f16 in the
 // canonical K-major layout without swizzle: core matrices of 8 vectors x 8
 // values (16 bytes a vector), the next 8 values of K 128 bytes on.
@@ -149,6 +152,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t mbar, uint32_t parity
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
 }
+// named barrier of a quarter's two decoder warps (ids 1..4; 0 is __syncthreads)
+__device__ __forceinline__ void decoder_barrier(int quarter) {
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+}
 
 template <int B>
 __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
@@ -159,9 +166,10 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const bool issuer = warp == kTcWorkWarps;  // warp 12: issues the products
-    const bool decoder = warp < 4;             // warps 0-3; 4-11 the epilogue
-    const int quarter = warp & 3, half = ((warp - 4) >> 2) & 1;  // lanes 32*quarter..; vectors 4half..
+    const bool issuer = warp == kTcWorkWarps;  // warp 16: issues the products
+    const bool decoder = warp < 8;             // warps 0-7; 8-15 the epilogue
+    const int quarter = warp & 3, half = (warp >> 2) & 1;  // lanes 32*quarter..; groups / vectors
+    const int qtid = half * 32 + lane;  // 0..63 among the quarter's decoders
     const int S = a.stages;
     const int64_t rows = a.rows;
     const int64_t ntiles = (rows + kTcRows - 1) / kTcRows;
@@ -175,13 +183,13 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
     uint8_t *qstage0 = smem + kTcStagesAt + (size_t)quarter * S * kTcQStageBytes;
     const uint32_t qstage0_u32 = smem_u32(qstage0);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTcStagesAt + 4 * S * kTcQStageBytes);
-    // a give-up flag, then mbarriers: A-full[2] (4 decoder arrivals), D-full[2]
+    // a give-up flag, then mbarriers: A-full[2] (8 decoder arrivals), D-full[2]
     // (the commit), D-empty[2] (8 epilogue arrivals)
     volatile uint32_t *abort_flag = tmem_slot + 1;
     const uint32_t bar0 = smem_u32(tmem_slot + 2);
     const uint32_t a_full = bar0, d_full = bar0 + 16, d_empty = bar0 + 32;
 
-    if (warp == 0) {  // tensor memory: A0 0..127, A1 128..255, D0 256..383, D1 384..511
+    if (warp == 0) {  // tensor memory: A0 0..127, A1 128..255, D0 256..287, D1 288..319
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
                      "r"((uint32_t)kTcTmemCols)
@@ -191,16 +199,16 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
     if (tid == 0) {
         *abort_flag = 0u;
         for (int b = 0; b < 2; ++b) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a_full + 8 * b), "r"(4u) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a_full + 8 * b), "r"(8u) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(d_full + 8 * b), "r"(1u) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(d_empty + 8 * b), "r"(8u) : "memory");
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
 
-    // producer (each quarter's decoder for its 32 rows): step ps of tile pt
-    // into stage p_stage; piece p = lane + 32k (< 288) is byte 16(p % 9) of the
-    // chunk of row p / 9 (rows past the end zero-filled)
+    // producer (each quarter's two decoders for its 32 rows): step ps of tile
+    // pt into stage p_stage; piece p = qtid + 64k (< 288) is byte 16(p % 9) of
+    // the chunk of row p / 9 (rows past the end zero-filled)
     int64_t pt = blockIdx.x;
     int ps = 0, p_stage = 0, issued = 0;
     auto issue_next = [&]() {
@@ -210,11 +218,13 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
         const int64_t rows_left = rows - row0;
         const uint32_t dst = qstage0_u32 + (uint32_t)p_stage * kTcQStageBytes;
 #pragma unroll
-        for (int k = 0; k < 9; ++k) {
-            const int p = lane + 32 * k;
-            const int r = p / 9, q = p - 9 * r;
-            const bool in = r < rows_left;
-            cp_async_16_zfill(dst + 16u * p, in ? base + r * kRowBytes + 16 * q : a.W, in ? 16u : 0u);
+        for (int k = 0; k < 5; ++k) {
+            const int p = qtid + 64 * k;
+            if (p < 32 * 9) {
+                const int r = p / 9, q = p - 9 * r;
+                const bool in = r < rows_left;
+                cp_async_16_zfill(dst + 16u * p, in ? base + r * kRowBytes + 16 * q : a.W, in ? 16u : 0u);
+            }
         }
         if (++ps == nb) {
             ps = 0;
@@ -297,12 +307,14 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
                 }
                 tc_fence_after();
                 const int c = tc_step_chunk(u % nb);
-                const uint32_t a_t = tmem + b * 128u, d_t = tmem + 256u + b * 128u;
+                const uint32_t a_t = tmem + b * 128u, d_t = tmem + 256u + b * 32u;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {  // sub-block j = 2gq + part: slices gq*4 + part*2 + {0, 1}
+                    // sub-blocks 0..3 into the first accumulator, 4..7 into the second
                     const int s0 = (j >> 1) * 4 + (j & 1) * 2;
-                    tc_mma_f16_ts(d_t + 16 * j, a_t + 8 * s0, tc_act_desc(act_u32, c, s0), kTcIdesc, 0u);
-                    tc_mma_f16_ts(d_t + 16 * j, a_t + 8 * (s0 + 1), tc_act_desc(act_u32, c, s0 + 1), kTcIdesc, 1u);
+                    const uint32_t acc = d_t + 16u * (uint32_t)(j >> 2);
+                    tc_mma_f16_ts(acc, a_t + 8 * s0, tc_act_desc(act_u32, c, s0), kTcIdesc, (j & 3) ? 1u : 0u);
+                    tc_mma_f16_ts(acc, a_t + 8 * (s0 + 1), tc_act_desc(act_u32, c, s0 + 1), kTcIdesc, 1u);
                 }
                 tc_commit(d_full + 8 * b);
             }
@@ -310,13 +322,13 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
         __syncwarp();
     } else if (decoder) {
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;  // this warp's 32 lanes
-        // the step's stage: this lane's copies, then the warp's
+        // the step's stage: this thread's copies, then the quarter decoders'
         auto stage_ready = [&]() {
             cp_async_wait_pending(S - 2);
-            __syncwarp();
+            decoder_barrier(quarter);
         };
         for (int g = 0; g < nitems; ++g) {
-            stage_ready();  // step g landed; the warp is past step g - 1
+            stage_ready();  // step g landed; both decoders are past step g - 1
             // step g + S - 1 into the stage of step g - 1
             if (issued < nitems) issue_next();
             cp_async_commit();
@@ -326,21 +338,36 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
                                                                          (uint32_t)((g - 2) >> 1) & 1u));
                 if (!ok && lane == 0) give_up();
             }
-            const uint8_t *row_chunk = qstage0 + (g % S) * kTcQStageBytes + lane * kChunkBytes + 16;
+            const uint8_t *row_chunk = qstage0 + (g % S) * kTcQStageBytes + lane * kChunkBytes;
+            const uint4 h = *reinterpret_cast<const uint4 *>(row_chunk);
+            const uint32_t sc_lo = h.y & 0x3F3F3F3Fu;  // six-bit scales of sub-blocks 0..3, 4..7
+            const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
             const uint32_t a_cols = tmem + lane_base + (uint32_t)(g & 1) * 128u;
 #pragma unroll
-            for (int gq = 0; gq < 4; ++gq) {  // group gq: slices 4gq + h (low), 4gq + 2 + h (high)
-                const uint4 u0 = *reinterpret_cast<const uint4 *>(row_chunk + 32 * gq);
-                const uint4 u1 = *reinterpret_cast<const uint4 *>(row_chunk + 32 * gq + 16);
+            for (int gg = 0; gg < 2; ++gg) {  // group gq: slices 4gq + h (low), 4gq + 2 + h (high)
+                const int gq = 2 * half + gg;
+                const uint4 u0 = *reinterpret_cast<const uint4 *>(row_chunk + 16 + 32 * gq);
+                const uint4 u1 = *reinterpret_cast<const uint4 *>(row_chunk + 32 + 32 * gq);
                 const uint32_t q[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                const uint32_t scw = gq < 2 ? sc_lo : sc_hi;
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
+                    // sub-block 2gq + part: (1024 + q) * sc - 1024 * sc, or for a
+                    // high nibble (1024 + 16q) * sc/16 - 64 * sc: the exact f16
+                    // q * sc (<= 945) by one fused multiply-add
+                    const float sc = (float)byte_of(scw, 2 * (gq & 1) + part);
+                    const __half2 mul = __float2half2_rn(part ? sc * 0.0625f : sc);
+                    const __half2 add = __float2half2_rn(part ? -64.0f * sc : -1024.0f * sc);
                     const uint32_t mask = part ? 0x00F000F0u : 0x000F000Fu;
                     uint32_t f[16];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        f[2 * i] = (q[i] & mask) | 0x64006400u;
-                        f[2 * i + 1] = ((q[i] >> 8) & mask) | 0x64006400u;
+                        const uint32_t b0 = (q[i] & mask) | 0x64006400u;
+                        const uint32_t b1 = ((q[i] >> 8) & mask) | 0x64006400u;
+                        const __half2 r0 = __hfma2(*reinterpret_cast<const __half2 *>(&b0), mul, add);
+                        const __half2 r1 = __hfma2(*reinterpret_cast<const __half2 *>(&b1), mul, add);
+                        f[2 * i] = *reinterpret_cast<const uint32_t *>(&r0);
+                        f[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&r1);
                     }
                     tc_st16(a_cols + 32u * gq + 16u * part, f);
                 }
@@ -351,7 +378,7 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
             if (lane == 0) mbar_arrive(a_full + 8 * (uint32_t)(g & 1));
         }
     } else {
-        // epilogue warps: vectors 4half .. 4half + 3 of this warp's 32 rows
+        // epilogue warps (8-15): vectors 4half .. 4half + 3 of this warp's 32 rows
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         float xh[4][4], xl[4][4];  // the binary counter of the pairing tree, four vectors
         // this row's 16-byte header of step g, from global memory
@@ -375,12 +402,12 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
                 ok = __all_sync(0xffffffffu, ok);  // warp-uniform: tcgen05.ld is warp-wide
                 if (!ok && lane == 0) give_up();
                 tc_fence_after();
-                uint32_t dv[8][4];
-                const uint32_t d_t = tmem + lane_base + 256u + b * 128u + 4u * half;
+                uint32_t dv[2][4];
+                const uint32_t d_t = tmem + lane_base + 256u + b * 32u + 4u * half;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    dv[j][0] = dv[j][1] = dv[j][2] = dv[j][3] = 0u;
-                    if (ok) tc_ld4(d_t + 16 * j, dv[j]);
+                for (int k = 0; k < 2; ++k) {
+                    dv[k][0] = dv[k][1] = dv[k][2] = dv[k][3] = 0u;
+                    if (ok) tc_ld4(d_t + 16 * k, dv[k]);
                 }
                 tc_wait_ld();
                 tc_fence_before();
@@ -389,34 +416,20 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
                 const int c = tc_step_chunk(s);
                 const float d = f16_bits_to_f32(h.x);
                 const float dmin = f16_bits_to_f32(h.x >> 16);
-                const uint32_t sc_lo = h.y & 0x3F3F3F3Fu;
                 const uint32_t m_lo = h.z & 0x3F3F3F3Fu;
-                const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
                 const uint32_t m_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
-                const uint32_t sce_lo = sc_lo & 0x00FF00FFu, sco_lo = sc_lo & 0xFF00FF00u;
-                const uint32_t sce_hi = sc_hi & 0x00FF00FFu, sco_hi = sc_hi & 0xFF00FF00u;
 #pragma unroll
                 for (int vv = 0; vv < 4; ++vv) {
                     const int v = 4 * half + vv;
-                    // 16 * S1 (mod 2^32: the terms carry 1024 * sub-block sum,
-                    // removed below; the result fits)
-                    uint32_t S16 = 0u;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t scw = j < 4 ? sc_lo : sc_hi;
-                        const uint32_t sc = (uint32_t)byte_of(scw, j & 3) << ((j & 1) ? 0 : 4);
-                        S16 += sc * (uint32_t)__float2int_rn(__uint_as_float(dv[j][vv]));
-                    }
+                    // S1 = sum of sc * dot over the eight sub-blocks: the two
+                    // accumulators' exact integers
+                    const int S1 = __float2int_rn(__uint_as_float(dv[0][vv])) +
+                                   __float2int_rn(__uint_as_float(dv[1][vv]));
                     const uint4 sp = split_tab[c * 8 + v];
-                    const int te = dp4a_uu(sce_hi, sp.y, dp4a_uu(sce_lo, sp.x, 0)) +
-                                   256 * dp4a_us(sce_hi, sp.w, dp4a_us(sce_lo, sp.z, 0));
-                    const int to = dp4a_uu(sco_hi, sp.y, dp4a_uu(sco_lo, sp.x, 0)) +
-                                   256 * dp4a_us(sco_hi, sp.w, dp4a_us(sco_lo, sp.z, 0));
-                    S16 -= 1024u * (16u * (uint32_t)te + (uint32_t)to);
                     const int S2 = dp4a_uu(m_hi, sp.y, dp4a_uu(m_lo, sp.x, 0)) +
                                    256 * dp4a_us(m_hi, sp.w, dp4a_us(m_lo, sp.z, 0));
                     float th, tl;
-                    q4k_epilogue(xs_tab[c * 8 + v], d, dmin, (int)S16 >> 4, S2, th, tl, true);
+                    q4k_epilogue(xs_tab[c * 8 + v], d, dmin, S1, S2, th, tl, true);
                     // the binary counter: level l pending after step s iff bit l of s is 0
 #pragma unroll
                     for (int l = 0; l < 4; ++l) {

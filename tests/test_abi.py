@@ -294,13 +294,13 @@ def test_codebook_split_table(raw):
 
 def test_tensor_plan(lib):
     """The tensor-core plan: forced on, for the Q4_K mat-vec on q8 blocks with
-    rows of 16 chunks at 5..8 vectors only; one CTA of thirteen warps an SM
+    rows of 16 chunks at 5..8 vectors only; one CTA of seventeen warps an SM
     on 128-row tiles, three stages unless a stage override sizes it."""
     act = 16 * 16 * 256 + 16 * 8 * 4 + 16 * 8 * 16
     try:
         lib.set_tensor_override(2)
         p = lib.plan_matvec(128256, 4096, 8)
-        assert p["tensor"] == 1 and (p["warps"], p["stages"], p["grid"]) == (13, 3, 152)
+        assert p["tensor"] == 1 and (p["warps"], p["stages"], p["grid"]) == (17, 3, 152)
         assert (p["groups"], p["rows_per_group"], p["segments"], p["row_block"]) == (1002, 128, 16, 1)
         assert p["smem_bytes"] == act + 3 * 128 * 144 + 64 + 1024
         assert lib.plan_matvec(300, 4096, 5)["grid"] == 3
@@ -309,7 +309,7 @@ def test_tensor_plan(lib):
             assert lib.plan_matvec(rows, cols, batch, fmt=fmt)["tensor"] == 0
         lib.set_plan_override(stages=5)
         p = lib.plan_matvec(14336, 4096, 6)
-        assert p["tensor"] == 1 and (p["warps"], p["stages"]) == (13, 5)
+        assert p["tensor"] == 1 and (p["warps"], p["stages"]) == (17, 5)
         assert p["smem_bytes"] == act + 5 * 128 * 144 + 64 + 1024
         lib.set_plan_override(stages=1)  # below two: the default three
         assert lib.plan_matvec(14336, 4096, 6)["stages"] == 3

@@ -660,7 +660,7 @@ def test_tensor_cores_are_bit_identical(xq, orc, rows, batch, kind):
             p = xq.last_plan()
             assert p["tensor"] == (tc == 2)
             if tc == 2:
-                assert p["warps"] == 13 and p["stages"] == (stages or 3)
+                assert p["warps"] == 17 and p["stages"] == (stages or 3)
             y_ws = xq.linear_ws("q4k", xd, Wd, rows, cols, ws).cpu().numpy()
             assert xq.last_plan()["tensor"] == (tc == 2)
             out.append((y, y_ws))
