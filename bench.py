@@ -107,7 +107,7 @@ def measured_peak() -> tuple[float, str]:
 
 
 def traffic_per_launch(kernel: str, case_name: str):
-    """DRAM bytes per launch of a kernel ("linear" or "matvec") on a case, from
+    """DRAM bytes per launch of a kernel ("linear", "matvec" or "matvec_tc") on a case, from
     a committed ncu capture; None unless the kernel sources are unchanged
     since that capture."""
     try:
@@ -389,6 +389,9 @@ def run_ours(args, c):
     dist = dist_init(world, "nccl")
     import quantized_decode_mat_gb300 as xq
 
+    # opt-in: the batch 5-8 Q4_K mat-vec on the tensor cores (tcgen05) where
+    # it applies; the planner's own choice otherwise
+    xq.set_tensor_override(2 if args.tensor == "on" else 0)
     dev = torch.device("cuda", local)
     W = torch.from_numpy(c.weights()).to(dev)
     if c.fmt == "cb4r":  # resident rows, repacked once at bind time (not timed)
@@ -653,6 +656,7 @@ def run_ours(args, c):
     # launch), or with the quantise-once plan the mat-vec on the q8 blocks;
     # either way the median of its rounds, timed on its launching stream
     once = bool(step_plan["quantise_once"])
+    tensor = bool(step_plan["tensor"])
     kernel_ms = mv_ms if once else step_ms
     achieved = gbs(kernel_ms)
     peak, peak_kind = measured_peak()
@@ -667,11 +671,15 @@ def run_ours(args, c):
     if large:
         config["l2"] = (f"inputs larger than L2: W {c.w_bytes / 1e6:.1f} MB > 129 MB, held "
                         "twice, consecutive steps alternate between the copies; no flush")
+    if tensor:
+        config["tensor"] = "tcgen05 (opt-in, --tensor on)"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
         "us_per_matvec": step_ms * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8 dp4a (int32 sums) + f32 epilogue",
+        "vs_baseline": None,
+        "dtype": ("f16 codes x f16 activations on tcgen05 (exact f32 sub-block sums) + f32 "
+                  "epilogue" if tensor else "int8 dp4a (int32 sums) + f32 epilogue"),
         "data": "synthetic (seeded, shapes and distributions of the decode workloads)",
         "config": config,
         "bytes": {"formula": BYTES_FORMULA, "per_step": B, "weights": nbytes["weights"],
@@ -685,15 +693,19 @@ def run_ours(args, c):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy (burst)",
                      "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
-                     "traffic": traffic_per_launch("matvec" if once else "linear", c.name),
-                     "kernel": (f"xq_matvec_kernel<{fmt}, batch {c.batch}> on q8 blocks (after "
+                     "traffic": traffic_per_launch(
+                         "matvec_tc" if tensor else "matvec" if once else "linear", c.name),
+                     "kernel": (f"xq_tc_q4k_kernel<batch {c.batch}> on q8 blocks (tcgen05, after "
+                                f"the quantise launch)" if tensor else
+                                f"xq_matvec_kernel<{fmt}, batch {c.batch}> on q8 blocks (after "
                                 f"the quantise launch)" if once else
                                 f"xq_matvec_kernel<{fmt}, batch {c.batch}, fused quantise>"),
                      "kernel_us": kernel_ms * 1e3,
                      "algorithmic_bytes_per_launch": B,
                      "timing": "median of the rounds, CUDA events on the launching stream"},
         "plan": {k: step_plan[k] for k in ("warps", "stages", "grid", "rows_per_group",
-                                            "segments", "row_block", "quantise_once")},
+                                            "segments", "row_block", "quantise_once",
+                                            "vector_pairs", "tensor")},
         "breakdown": {
             **({"step_one_buffer": {"us": one_ms * 1e3, "GBs": gbs(one_ms),
                                     "how": "every step on the same copy of W"}}
@@ -752,6 +764,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
     ap.add_argument("--overlap", choices=["on", "off"], default="on",
                     help="overlapped launches for the timed step (the weights are constant)")
+    ap.add_argument("--tensor", choices=["on", "off"], default="off",
+                    help="the batch 5-8 Q4_K mat-vec on the tensor cores (tcgen05), where it "
+                         "applies; off: the planner's choice")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -55,6 +55,20 @@ def test_bench_line_contract():
     assert d["device_status"] == 0
 
 
+def test_bench_line_tensor_opt_in():
+    """--tensor on times the tcgen05 form of the batch-8 mat-vec and says so;
+    the planner's line names the dp4a kernel."""
+    d = _run("--case", "c3_q4k_up_14336x4096_b8", "--steps", "100", "--warmup", "5",
+             "--rounds", "2", "--cpu-seconds", "0.1", "--tensor", "on")
+    assert d["plan"]["tensor"] == 1 and d["config"]["tensor"].startswith("tcgen05")
+    assert "xq_tc_q4k_kernel" in d["roofline"]["kernel"] and "tcgen05" in d["dtype"]
+    assert d["device_status"] == 0
+    d = _run("--case", "c3_q4k_up_14336x4096_b8", "--steps", "100", "--warmup", "5",
+             "--rounds", "2", "--cpu-seconds", "0.1")
+    assert d["plan"]["tensor"] == 0 and "tensor" not in d["config"]
+    assert "xq_matvec_kernel" in d["roofline"]["kernel"] and "dp4a" in d["dtype"]
+
+
 def test_reference_arm_line():
     d = _run("--impl", "reference", "--case", "c1_q4k_256x1024_b1", "--steps", "3",
              "--warmup", "3")
