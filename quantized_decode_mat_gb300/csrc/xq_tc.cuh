@@ -289,7 +289,9 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     // A wait that runs out sets the flag and the status bit; from then on no
-    // warp waits or issues products; every warp still runs to the end.
+    // warp waits or issues products (the issuer waits, bounded, for the
+    // products it already issued); every warp still runs to the end, where
+    // the copies are drained and the tensor memory freed.
     auto give_up = [&]() {
         *abort_flag = 1u;
         atomicOr(a.status, kStatusTensorTimeout);
@@ -298,6 +300,7 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
     if (issuer) {
         // warp 16: the products of every step, in order
         if (lane == 0) {
+            int last = -1;  // the last step whose products were issued
             for (int u = 0; u < nitems && *abort_flag == 0u; ++u) {
                 const uint32_t b = (uint32_t)(u & 1), par = (uint32_t)(u >> 1) & 1u;
                 if (!mbar_wait_bounded(a_full + 8 * b, par) ||
@@ -317,7 +320,12 @@ __global__ void __maxnreg__(kTcMaxRegs) xq_tc_q4k_kernel(const MatvecArgs a) {
                     tc_mma_f16_ts(acc, a_t + 8 * (s0 + 1), tc_act_desc(act_u32, c, s0 + 1), kTcIdesc, 1u);
                 }
                 tc_commit(d_full + 8 * b);
+                last = u;
             }
+            // after a give-up nobody may wait for the last products: wait for
+            // them here (bounded) so the tensor memory is not freed under them
+            if (last >= 0 && *abort_flag != 0u)
+                (void)mbar_wait_bounded(d_full + 8 * (uint32_t)(last & 1), (uint32_t)(last >> 1) & 1u);
         }
         __syncwarp();
     } else if (decoder) {
