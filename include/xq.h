@@ -129,12 +129,12 @@ xq_status xq_linear_cb4(const float *x, const void *W, const int8_t *table, floa
  * (xq_plan.quantise_once):
  *   - small activations: the one fused launch, where every CTA quantises the
  *     activation into its own shared memory (the workspace is not touched);
- *   - wide or batched activations (at least 32 q8 blocks a launch): the
+ *   - wide or batched activations (more than 32 q8 blocks a launch): the
  *     activation is quantised once, by xq_quantize_q8's kernel, into the
  *     workspace, and the mat-vec reads those q8 blocks.  Every CTA
  *     re-quantising the whole activation costs more than the second launch
- *     there (measured on GB300: 4096 x 14336 at batch 8, 58.4 us fused against
- *     34.9 us).
+ *     there (measured on GB300: 4096 x 14336 at batch 4, 16.8 us fused against
+ *     13.9 us).
  * ws: DEVICE scratch of at least xq_linear_workspace_bytes(cols, batch) bytes
  * (= xq_q8_bytes(cols, batch)), 16-byte aligned, not overlapping x, W or y;
  * its contents on entry do not matter; on return it holds the q8 blocks of

@@ -146,9 +146,12 @@ std::atomic<int32_t> g_override_tensor{0};
 std::atomic<int32_t> g_overlap{0};
 // The decode step with a workspace quantises the activation once, in a
 // launch of its own, when a launch's batch has at least this many q8 blocks;
-// below that every CTA of the one fused launch quantises it for itself
-// (measured crossover on GB300).
-constexpr int64_t kQuantOnceMinBlocks = 32;
+// below that every CTA of the one fused launch quantises it for itself.
+// Measured on GB300 over Q4_K and codebook rows of 4096 and 14336 and 2048 to
+// 14336 columns at batch 1 to 8: up to 32 blocks the fused launch was faster
+// in 21 of 24 shapes (by up to a third; the others by at most 2.4 %), from 48
+// blocks the launch of its own in most.
+constexpr int64_t kQuantOnceMinBlocks = 33;
 // Whether the planner picks warp pairs by itself (the override can force
 // them either way).
 constexpr bool kVectorPairsAuto = true;

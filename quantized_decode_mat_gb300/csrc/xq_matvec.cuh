@@ -453,6 +453,12 @@ __device__ __forceinline__ void cb4r_chunk(const uint8_t *__restrict__ stage, in
 // B/2 + B/4 + ... values a lane instead of B*log2(width).  On return,
 // h[i], l[i] (i < nlive) hold vector base + i of the row, complete in the
 // lanes whose bits below `keep` are zero.
+// a compile-time int as a value (for generic lambdas)
+template <int N>
+struct IntTag {
+    static constexpr int value = N;
+};
+
 template <int B>
 struct Pow2Ceil {
     static constexpr int v = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8;
@@ -835,6 +841,10 @@ __global__ void __launch_bounds__(VP ? kVpWarps * 32 : bound_threads<FMT, B, FUS
         // of them is processed: one L2 round trip per group.
         const int nblk = B * nb;
         constexpr int QG = B >= 2 ? 2 * kQuantGroup : kQuantGroup;
+        // blocks quantised together (a divisor of QG; two for the codebook
+        // forms, whose builds have fewer registers to spare)
+        constexpr int QN = FMT == kQ4K ? 4 : 2;
+        static_assert(QG % QN == 0, "whole sub-groups");
         float4 u[QG], v[QG];
         auto load_group = [&](int k0) {
 #pragma unroll
@@ -871,46 +881,75 @@ __global__ void __launch_bounds__(VP ? kVpWarps * 32 : bound_threads<FMT, B, FUS
             }
             __syncthreads();
         }
-        for (int k0 = warp; k0 < nblk; k0 += QG * W) {
-            if (k0 != warp) load_group(k0);
+        // The round's blocks are quantised QN at a time (q8_quantize_lanes:
+        // their steps interleaved, one division pass); a round with one block
+        // for this warp takes the one-block form.  Values, sums and scale go to
+        // the staged block; the Q4_K split sums are formed afterwards from the
+        // staged sums, one block a thread.
+        auto quantise_round = [&](int k0, int j0, auto tag) {
+            constexpr int N = decltype(tag)::value;
+            float vals[N][8];
 #pragma unroll
-            for (int j = 0; j < QG; ++j) {
-                const int blk = k0 + j * W;
-                if (blk >= nblk) break;  // warp-uniform
-                float vals[8] = {u[j].x, u[j].y, u[j].z, u[j].w, v[j].x, v[j].y, v[j].z, v[j].w};
-                if (FUSE == 2) {
+            for (int jj = 0; jj < N; ++jj) {
+                const int j = j0 + jj, blk = k0 + j * W;
+                const bool in = blk < nblk;  // warp-uniform
+                vals[jj][0] = in ? u[j].x : 0.0f;
+                vals[jj][1] = in ? u[j].y : 0.0f;
+                vals[jj][2] = in ? u[j].z : 0.0f;
+                vals[jj][3] = in ? u[j].w : 0.0f;
+                vals[jj][4] = in ? v[j].x : 0.0f;
+                vals[jj][5] = in ? v[j].y : 0.0f;
+                vals[jj][6] = in ? v[j].z : 0.0f;
+                vals[jj][7] = in ? v[j].w : 0.0f;
+                if (FUSE == 2 && in) {
                     const int b = blk / nb;
                     const float ns = *reinterpret_cast<const float *>(act + b * act_bstride + kActNormAt);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) vals[i] = __fmul_rn(vals[i], ns);
+                    for (int i = 0; i < 8; ++i) vals[jj][i] = __fmul_rn(vals[jj][i], ns);
                 }
-                const Q8Lane r = q8_quantize_lane(vals);
+            }
+            Q8Lane r[N];
+            q8_quantize_lanes<N>(vals, r, lane);
+#pragma unroll
+            for (int jj = 0; jj < N; ++jj) {
+                const int blk = k0 + (j0 + jj) * W;
+                if (blk >= nblk) break;  // warp-uniform
                 uint8_t *dst = act + blk * kActStride;
+                const Q8Lane &q = r[jj];
                 if (FMT == kQ4K) {
-                    *reinterpret_cast<uint2 *>(dst + lane * 8) = make_uint2(r.w0, r.w1);
+                    *reinterpret_cast<uint2 *>(dst + lane * 8) = make_uint2(q.w0, q.w1);
                 } else {
-                    // interleaved order: lane 4k+j writes words 2j, 2j+1 of
-                    // sub-block k, made of its words j and j+4 (lanes 4k + j/2
-                    // and 4k + 2 + j/2 hold them)
-                    const int j = lane & 3, src = (lane & ~3) + (j >> 1);
-                    const uint32_t v0 = __shfl_sync(0xffffffffu, r.w0, src);
-                    const uint32_t v1 = __shfl_sync(0xffffffffu, r.w1, src);
-                    const uint32_t u0 = __shfl_sync(0xffffffffu, r.w0, src + 2);
-                    const uint32_t u1 = __shfl_sync(0xffffffffu, r.w1, src + 2);
-                    const uint32_t wa = (j & 1) ? v1 : v0, wb = (j & 1) ? u1 : u0;
+                    // interleaved order: lane 4k+i writes words 2i, 2i+1 of
+                    // sub-block k, made of its words i and i+4 (lanes 4k + i/2
+                    // and 4k + 2 + i/2 hold them)
+                    const int i = lane & 3, src = (lane & ~3) + (i >> 1);
+                    const uint32_t v0 = __shfl_sync(0xffffffffu, q.w0, src);
+                    const uint32_t v1 = __shfl_sync(0xffffffffu, q.w1, src);
+                    const uint32_t u0 = __shfl_sync(0xffffffffu, q.w0, src + 2);
+                    const uint32_t u1 = __shfl_sync(0xffffffffu, q.w1, src + 2);
+                    const uint32_t wa = (i & 1) ? v1 : v0, wb = (i & 1) ? u1 : u0;
                     *reinterpret_cast<uint2 *>(dst + lane * 8) =
                         make_uint2(interleave_lo(wa, wb), interleave_hi(wa, wb));
                 }
-                if ((lane & 3) == 0) *reinterpret_cast<int *>(dst + kQ8SumAt + (lane >> 2) * 4) = r.sum;
-                uint32_t sums[8];
+                if ((lane & 3) == 0) *reinterpret_cast<int *>(dst + kQ8SumAt + (lane >> 2) * 4) = q.sum;
+                if (lane == 0) *reinterpret_cast<float *>(dst + kQ8ScaleAt) = q.d;
+            }
+        };
+        for (int k0 = warp; k0 < nblk; k0 += QG * W) {
+            if (k0 != warp) load_group(k0);
+            if (k0 + W >= nblk) {
+                quantise_round(k0, 0, IntTag<1>{});
+            } else {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) sums[q] = (uint32_t)__shfl_sync(0xffffffffu, r.sum, 4 * q);
-                if (lane == 0) {
-                    *reinterpret_cast<float *>(dst + kQ8ScaleAt) = r.d;
-                    *reinterpret_cast<uint4 *>(dst + kActSplitAt) =
-                        split_sums(make_uint4(sums[0], sums[1], sums[2], sums[3]),
-                                   make_uint4(sums[4], sums[5], sums[6], sums[7]));
-                }
+                for (int j0 = 0; j0 < QG; j0 += QN)
+                    if (k0 + j0 * W < nblk) quantise_round(k0, j0, IntTag<QN>{});  // warp-uniform
+            }
+        }
+        if (FMT == kQ4K) {
+            __syncthreads();  // every block's sums are staged
+            for (int blk = threadIdx.x; blk < nblk; blk += blockDim.x) {
+                const uint4 *sums = reinterpret_cast<const uint4 *>(act + blk * kActStride + kQ8SumAt);
+                *reinterpret_cast<uint4 *>(act + blk * kActStride + kActSplitAt) = split_sums(sums[0], sums[1]);
             }
         }
     } else if (FMT == kQ4K && nvec * nb >= kStageAsyncBlocks) {

@@ -20,55 +20,80 @@ struct Q8Lane {
     float d;          // the block scale, in every lane
 };
 
-// vals: values 8*lane .. 8*lane+7 of the block.  All 32 lanes must call.
-__device__ __forceinline__ Q8Lane q8_quantize_lane(const float (&vals)[8]) {
-    float amax = 0.0f;
+// N blocks at once, one warp: vals[j] holds values 8*lane .. 8*lane+7 of
+// block j.  All 32 lanes must call.  The steps of the N blocks are
+// interleaved and nothing branches: an all-zero block (amax = 0) gets
+// iscale = 127/0 = inf, so each of its products is 0*inf = NaN and quantises
+// to 0, and d = 0/127 = 0, as the rule asks.  A product is clamped to
+// [-127, 127] before it is rounded (so an iscale that overflowed to inf on a
+// tiny amax still gives +-127), and a NaN product gives 0.  With N >= 2 lane j
+// takes block j's two divisions and the others read them by shuffle: one
+// division pass for all N blocks.
+template <int N>
+__device__ __forceinline__ void q8_quantize_lanes(const float (&vals)[N][8], Q8Lane (&out)[N],
+                                                  int lane) {
+    static_assert(N >= 1 && N <= 32, "one block a lane at most");
+    float amax[N];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float t = fabsf(vals[i]);
-        amax = t > amax ? t : amax;
+    for (int j = 0; j < N; ++j) {
+        amax[j] = 0.0f;  // fmaxf keeps the non-NaN operand: NaN values do not count
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax[j] = fmaxf(amax[j], fabsf(vals[j][i]));
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, amax, off);
-        amax = o > amax ? o : amax;
-    }
-    int q[8];
-    if (amax == 0.0f) {
+    for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = 0;
+        for (int j = 0; j < N; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], off));
+    float iscale[N], d[N];
+    if constexpr (N == 1) {
+        iscale[0] = __fdiv_rn(127.0f, amax[0]);
+        d[0] = __fdiv_rn(amax[0], 127.0f);
     } else {
-        const float iscale = __fdiv_rn(127.0f, amax);
+        float a = amax[0];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float t = __fmul_rn(vals[i], iscale);
-            int r;
-            if (t != t)
-                r = 0;
-            else if (t >= 127.0f)
-                r = 127;
-            else if (t <= -127.0f)
-                r = -127;
-            else
-                r = __float2int_rn(t);  // round half to even
-            q[i] = r;
+        for (int j = 1; j < N; ++j) a = lane == j ? amax[j] : a;
+        const float is = __fdiv_rn(127.0f, a), dd = __fdiv_rn(a, 127.0f);
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            iscale[j] = __shfl_sync(0xffffffffu, is, j);
+            d[j] = __shfl_sync(0xffffffffu, dd, j);
         }
     }
-    Q8Lane out;
-    out.w0 = out.w1 = 0;
-    int sum = 0;
+    int sum[N];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        out.w0 |= (uint32_t)(q[i] & 0xFF) << (8 * i);
-        out.w1 |= (uint32_t)(q[4 + i] & 0xFF) << (8 * i);
+    for (int j = 0; j < N; ++j) {
+        int q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float t = __fmul_rn(vals[j][i], iscale[j]);
+            const int r = __float2int_rn(fminf(fmaxf(t, -127.0f), 127.0f));  // round half to even
+            q[i] = t != t ? 0 : r;
+        }
+        out[j].w0 = __byte_perm(__byte_perm((uint32_t)q[0], (uint32_t)q[1], 0x0040u),
+                                __byte_perm((uint32_t)q[2], (uint32_t)q[3], 0x0040u), 0x5410u);
+        out[j].w1 = __byte_perm(__byte_perm((uint32_t)q[4], (uint32_t)q[5], 0x0040u),
+                                __byte_perm((uint32_t)q[6], (uint32_t)q[7], 0x0040u), 0x5410u);
+        sum[j] = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum[j] += q[i];
+        out[j].d = d[j];
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sum += q[i];
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    out.sum = sum;
-    out.d = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, 127.0f);
-    return out;
+    for (int off = 1; off <= 2; off <<= 1)
+#pragma unroll
+        for (int j = 0; j < N; ++j) sum[j] += __shfl_xor_sync(0xffffffffu, sum[j], off);
+#pragma unroll
+    for (int j = 0; j < N; ++j) out[j].sum = sum[j];
+}
+
+// One block: vals holds values 8*lane .. 8*lane+7.  All 32 lanes must call.
+__device__ __forceinline__ Q8Lane q8_quantize_lane(const float (&vals)[8]) {
+    float v[1][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[0][i] = vals[i];
+    Q8Lane out[1];
+    q8_quantize_lanes<1>(v, out, 0);
+    return out[0];
 }
 
 }  // namespace xq

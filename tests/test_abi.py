@@ -457,7 +457,9 @@ def test_linear_ws_argument_checks(raw, lib):
 def test_plan_reports_the_workspace_choice(lib):
     assert lib.plan_matvec(128256, 4096, 1)["quantise_once"] == 0   # 16 blocks: per CTA
     assert lib.plan_matvec(4096, 14336, 1)["quantise_once"] == 1    # 56 blocks: once
-    assert lib.plan_matvec(14336, 4096, 2)["quantise_once"] == 1    # 32 blocks: once
+    assert lib.plan_matvec(14336, 4096, 2)["quantise_once"] == 0    # 32 blocks: per CTA
+    assert lib.plan_matvec(14336, 4096, 3)["quantise_once"] == 1    # 48 blocks: once
+    assert lib.plan_matvec(4096, 8448, 1)["quantise_once"] == 1     # 33 blocks: once
     assert lib.plan_matvec(4096, 7936, 1)["quantise_once"] == 0     # 31 blocks: per CTA
     assert lib.plan_matvec(14336, 4096, 8)["quantise_once"] == 1    # 128 blocks
     try:

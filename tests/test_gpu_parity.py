@@ -104,11 +104,39 @@ def _x_kind(kind, batch, cols, seed):
         x = (rng.integers(-254, 255, size=(batch, cols)) / 2.0).astype(np.float32)
         x.reshape(batch, -1, 256)[:, :, 0] = 127.0
         return x
+    if kind == "subnormal":
+        # blocks scaled into and around the subnormal range: where amax is
+        # below 127 / FLT_MAX, iscale = 127/amax overflows to inf and every
+        # nonzero value must still land on +-127 (zeros on 0)
+        x = synthetic.activations(batch, cols, seed).reshape(batch, -1, 256)
+        scales = np.array([1e-45, 1e-41, 1e-39, 3e-38, 1e-37, 1e-36], np.float32)
+        for k in range(x.shape[1]):
+            x[:, k] *= scales[k % len(scales)]
+        x[:, ::7, 3] = 0.0
+        return x.reshape(batch, cols)
+    if kind == "nonfinite":
+        # NaN values do not count towards amax and quantise to 0; an inf
+        # makes amax inf, iscale 0, the finite values 0 and the inf itself
+        # 0 * inf = NaN -> 0
+        x = synthetic.activations(batch, cols, seed).reshape(batch, -1, 256)
+        nb = x.shape[1]
+        x[:, 0, 5] = np.nan
+        if nb > 1:
+            x[:, 1, 17] = np.inf
+        if nb > 2:
+            x[:, 2, 200] = -np.inf
+            x[:, 2, 201] = np.nan
+        if nb > 3:
+            x[:, 3, :] = np.nan
+        if nb > 4:
+            x[:, 4, :] = 0.0
+            x[:, 4, 9] = np.nan
+        return x.reshape(batch, cols)
     raise ValueError(kind)
 
 
 @pytest.mark.parametrize("kind", ["normal", "outliers", "fixture", "zeros", "tiny", "huge",
-                                  "ties"])
+                                  "ties", "subnormal", "nonfinite"])
 @pytest.mark.parametrize("cols,batch", [(256, 1), (1024, 3), (4096, 8), (14336, 2)])
 def test_quantize_bit_exact(xq, orc, kind, cols, batch):
     x = _x_kind(kind, batch, cols, 1000 + cols + batch)
@@ -355,6 +383,33 @@ def test_linear_is_the_two_call_path(xq, orc, fmt, rows, cols, batch):
     y_ref = (orc.matvec_q4k(W, xq_ref, rows, cols, batch) if fmt == "q4k"
              else orc.matvec_cb4(W, kv, xq_ref, rows, cols, batch))
     check_y(y1, y_ref, f"linear {fmt} {rows}x{cols} b{batch}")
+
+
+@pytest.mark.parametrize("kind", ["zeros", "tiny", "huge", "ties", "subnormal", "nonfinite"])
+@pytest.mark.parametrize("fmt", ["q4k", "cb4"])
+@pytest.mark.parametrize("rows,cols,batch", [(5, 1024, 2), (37, 4096, 8), (65, 14336, 3),
+                                             (16, 65536, 1)])
+def test_linear_quantises_edge_inputs_like_the_quantiser(xq, orc, kind, fmt, rows, cols, batch):
+    """The fused launch quantises several blocks a warp at once; on inputs
+    that reach every branch of the rule (all-zero blocks, an iscale that
+    overflows, NaN and inf values) y has the bits of xq_quantize_q8 followed
+    by the mat-vec (NaN where both have NaN)."""
+    seed = 3 * rows + cols + batch
+    W = _weights(fmt, rows, cols, seed)
+    kv = synthetic.cb4_table()
+    x = _x_kind(kind, batch, cols, seed + 1)
+    xq_dev = run_quantize(xq, x)
+    assert np.array_equal(xq_dev.cpu().numpy(), orc.quantize_q8(x))
+    y2 = run_matvec(xq, fmt, W, kv, xq_dev, rows, cols, batch)
+    out = Guarded((batch, rows), torch.float32)
+    if fmt == "q4k":
+        xq.linear_q4k(dev(x), dev(W), rows, cols, out=out.t)
+    else:
+        xq.linear_cb4(dev(x), dev(W), kv, rows, cols, out=out.t)
+    torch.cuda.synchronize()
+    out.check_guard()
+    y1 = out.t.cpu().numpy()
+    assert np.array_equal(y1, y2, equal_nan=True)
 
 
 # ---------------------------------------------------------------- RMSNorm + q8 pack

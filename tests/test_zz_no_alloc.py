@@ -53,7 +53,8 @@ def call_static(fn, x, W, y, rows, cols, batch):
 
 
 # (rows, cols, batch, whether the plan quantises once into the scratch)
-CASES = [(4096, 14336, 4, 1), (300, 4096, 2, 1), (77, 4096, 1, 0), (1000, 25600, 8, 1),
+CASES = [(4096, 14336, 4, 1), (300, 4096, 3, 1), (300, 4096, 2, 0), (77, 4096, 1, 0),
+         (1000, 25600, 8, 1),
          (64, 69888, 3, 1)]  # the last: 3 * 273 = 819 q8 blocks, the whole array
 
 
