@@ -40,10 +40,11 @@ __device__ __forceinline__ void q8_quantize_lanes(const float (&vals)[N][8], Q8L
 #pragma unroll
         for (int i = 0; i < 8; ++i) amax[j] = fmaxf(amax[j], fabsf(vals[j][i]));
     }
+    // across the warp: a non-negative float (never NaN here) orders as its
+    // bits do, so one integer max reduction gives the block's amax exactly
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-        for (int j = 0; j < N; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], off));
+    for (int j = 0; j < N; ++j)
+        amax[j] = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax[j])));
     float iscale[N], d[N];
     if constexpr (N == 1) {
         iscale[0] = __fdiv_rn(127.0f, amax[0]);
