@@ -841,9 +841,11 @@ __global__ void __launch_bounds__(VP ? kVpWarps * 32 : bound_threads<FMT, B, FUS
         // of them is processed: one L2 round trip per group.
         const int nblk = B * nb;
         constexpr int QG = B >= 2 ? 2 * kQuantGroup : kQuantGroup;
-        // blocks quantised together (a divisor of QG; two for the codebook
-        // forms, whose builds have fewer registers to spare)
-        constexpr int QN = FMT == kQ4K ? 4 : 2;
+        // blocks quantised together (a divisor of QG).  The codebook forms
+        // take one at a time: the grouped form's registers cost their main
+        // loop more than it saves here (128256 x 4096 resident rows: 47.0
+        // against 45.7 us a step)
+        constexpr int QN = FMT == kQ4K ? 4 : 1;
         static_assert(QG % QN == 0, "whole sub-groups");
         float4 u[QG], v[QG];
         auto load_group = [&](int k0) {
