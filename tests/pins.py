@@ -104,6 +104,45 @@ def pin_q8_invariants(o):
         _q8_invariants(x, o.quantize_q8(x))
 
 
+def pin_q8_nonfinite_and_tiny(o):
+    """The rule's edge cases, in closed form: a NaN value does not count
+    towards amax and quantises to 0, so the block's bytes are those of the
+    same block with 0 there; an inf makes amax inf, so iscale = 127/inf = 0,
+    every finite value quantises to 0 and the inf to 0*inf = NaN -> 0, and
+    d = inf; an all-NaN block is an all-zero block; and an amax so small that
+    127/amax overflows to inf sends every nonzero value to +-127 (0 stays 0:
+    0*inf = NaN -> 0) while d = amax/127 rounds to 0."""
+    rng = np.random.Generator(np.random.PCG64(77))
+    base = rng.standard_normal(256).astype(np.float32)
+    # NaN at a few places == 0 at those places, byte for byte
+    xn, xz = base.copy(), base.copy()
+    xn[[3, 100, 255]] = np.nan
+    xz[[3, 100, 255]] = 0.0
+    assert np.array_equal(o.quantize_q8(xn[None, :]), o.quantize_q8(xz[None, :]))
+    # an inf: all zeros, d = +inf
+    xi = base.copy()
+    xi[17] = -np.inf
+    blk = o.quantize_q8(xi[None, :])[0, 0]
+    assert not blk[:288].any()
+    assert int(blk[288:292].view("<u4")[0]) == 0x7F800000
+    # all NaN: the zero block
+    blk = o.quantize_q8(np.full((1, 256), np.nan, np.float32))[0, 0]
+    assert not blk.any()
+    # amax of two smallest subnormals: 127/amax = inf
+    xt = np.zeros(256, np.float32)
+    tiny = np.float32(np.ldexp(1.0, -149))  # the smallest positive subnormal
+    xt[0], xt[1], xt[40] = tiny, -2 * tiny, tiny
+    with np.errstate(over="ignore"):
+        assert np.isinf(np.float32(127.0) / np.float32(2 * tiny))
+    blk = o.quantize_q8(xt[None, :])[0, 0]
+    q = blk[:256].view(np.int8).astype(np.int64)
+    want = np.zeros(256, np.int64)
+    want[0], want[1], want[40] = 127, -127, 127
+    assert np.array_equal(q, want)
+    assert list(_i32(blk[256:288])) == [0, 127, 0, 0, 0, 0, 0, 0]
+    assert int(blk[288:292].view("<u4")[0]) == 0  # 2^-148 / 127 rounds to +0
+
+
 # ---------------------------------------------------------------- Q4_K
 def pin_q4k_scale_pack(o):
     g = _golden("q4k_scale_pack.json")
@@ -394,7 +433,8 @@ def pin_cb4r_chunks_and_weights(o):
                               o.dequant_cb4(W, kv, rows, cols)), (rows, cols)
 
 
-ALL_PINS = [pin_f16_all_patterns, pin_q8_hand_cases, pin_q8_invariants, pin_q4k_scale_pack,
+ALL_PINS = [pin_f16_all_patterns, pin_q8_hand_cases, pin_q8_invariants, pin_q8_nonfinite_and_tiny,
+            pin_q4k_scale_pack,
             pin_q4k_roundtrip, pin_q4k_block_y, pin_q4k_bruteforce, pin_q4k_gemv_special,
             pin_q4k_min_term, pin_cb4_block_y, pin_cb4_bruteforce, pin_cb4_gemv_special,
             pin_rmsnorm_order, pin_rmsnorm_hand, pin_rmsnorm_constant, pin_rmsnorm_bound,
