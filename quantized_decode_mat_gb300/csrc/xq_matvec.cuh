@@ -911,7 +911,7 @@ __global__ void __launch_bounds__(VP ? kVpWarps * 32 : bound_threads<FMT, B, FUS
                 }
             }
             Q8Lane r[N];
-            q8_quantize_lanes<N>(vals, r, lane);
+            q8_quantize_lanes<N, FMT == kQ4K>(vals, r, lane);  // the codebook builds: the clamp form
 #pragma unroll
             for (int jj = 0; jj < N; ++jj) {
                 const int blk = k0 + (j0 + jj) * W;

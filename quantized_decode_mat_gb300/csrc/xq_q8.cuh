@@ -24,12 +24,16 @@ struct Q8Lane {
 // block j.  All 32 lanes must call.  The steps of the N blocks are
 // interleaved and nothing branches: an all-zero block (amax = 0) gets
 // iscale = 127/0 = inf, so each of its products is 0*inf = NaN and quantises
-// to 0, and d = 0/127 = 0, as the rule asks.  A product is clamped to
-// [-127, 127] before it is rounded (so an iscale that overflowed to inf on a
-// tiny amax still gives +-127), and a NaN product gives 0.  With N >= 2 lane j
+// to 0, and d = 0/127 = 0, as the rule asks.  A product is rounded by one
+// saturating conversion (NaN -> 0, +-inf -> 127 / -128) and raised to -127:
+// a finite product stays below 127.5 in magnitude, and an iscale that
+// overflowed to inf on a tiny amax still gives +-127.  With N >= 2 lane j
 // takes block j's two divisions and the others read them by shuffle: one
 // division pass for all N blocks.
-template <int N>
+// SAT: each product rounded by one saturating conversion (below); false: by
+// an explicit clamp, a rounding and a NaN select (the same bytes; the form
+// the raw codebook kernel's register assignment measured faster with).
+template <int N, bool SAT = true>
 __device__ __forceinline__ void q8_quantize_lanes(const float (&vals)[N][8], Q8Lane (&out)[N],
                                                   int lane) {
     static_assert(N >= 1 && N <= 32, "one block a lane at most");
@@ -66,17 +70,30 @@ __device__ __forceinline__ void q8_quantize_lanes(const float (&vals)[N][8], Q8L
         int q[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
+            // round half to even, saturating to [-128, 127] with NaN -> 0;
+            // a finite product is below 127.5 in magnitude (|x| <= amax), so
+            // only -inf (iscale overflowed) reaches -128, raised to -127
             const float t = __fmul_rn(vals[j][i], iscale[j]);
-            const int r = __float2int_rn(fminf(fmaxf(t, -127.0f), 127.0f));  // round half to even
-            q[i] = t != t ? 0 : r;
+            if constexpr (SAT) {
+                int r;
+                asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(r) : "f"(t));
+                q[i] = max(r, -127);
+            } else {
+                const int r = __float2int_rn(fminf(fmaxf(t, -127.0f), 127.0f));
+                q[i] = t != t ? 0 : r;
+            }
         }
         out[j].w0 = __byte_perm(__byte_perm((uint32_t)q[0], (uint32_t)q[1], 0x0040u),
                                 __byte_perm((uint32_t)q[2], (uint32_t)q[3], 0x0040u), 0x5410u);
         out[j].w1 = __byte_perm(__byte_perm((uint32_t)q[4], (uint32_t)q[5], 0x0040u),
                                 __byte_perm((uint32_t)q[6], (uint32_t)q[7], 0x0040u), 0x5410u);
-        sum[j] = 0;
+        if constexpr (SAT) {  // the lane's sum: its eight signed bytes dotted with ones
+            sum[j] = __dp4a((int)out[j].w1, 0x01010101, __dp4a((int)out[j].w0, 0x01010101, 0));
+        } else {
+            sum[j] = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sum[j] += q[i];
+            for (int i = 0; i < 8; ++i) sum[j] += q[i];
+        }
         out[j].d = d[j];
     }
 #pragma unroll
