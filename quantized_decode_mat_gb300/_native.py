@@ -310,7 +310,9 @@ def overlap_launches() -> bool:
 
 
 def set_quantise_once_override(mode: int = 0) -> None:
-    """1: every CTA quantises; 2: quantise once across the grid; 0: automatic."""
+    """The decode step's choice (xq_plan.quantise_once): 1 every CTA of the one
+    fused launch quantises x; 2 x is quantised once, by a launch of its own,
+    into the workspace; 0 automatic (once from 33 q8 blocks a launch)."""
     _set_qonce(mode)
 
 
